@@ -1,0 +1,29 @@
+"""Layer glue without reductions (test infrastructure only): embedding gather,
+residual add, SwiGLU.  None of these sums across elements, so each is
+batch-invariant by construction; they are here because the decoder step needs
+them.  SwiGLU: a = silu(g) * u with silu(g) = g / (1 + e^-g)."""
+from __future__ import annotations
+
+import numpy as np
+
+from . import bf16
+
+
+def embed(table_bits: np.ndarray, ids) -> np.ndarray:
+    return table_bits[np.asarray(ids, dtype=np.int64)].copy()
+
+
+def add(x_bits, y_bits) -> np.ndarray:
+    return bf16.from_f64(bf16.to_f64(x_bits) + bf16.to_f64(y_bits))
+
+
+def silu(g: np.ndarray) -> np.ndarray:
+    return g / (1.0 + np.exp(-g))
+
+
+def swiglu(gu_bits: np.ndarray) -> np.ndarray:
+    """gu [M][2F] holds gate in columns [0, F) and up in [F, 2F)."""
+    gu = bf16.to_f64(gu_bits)
+    f = gu.shape[-1] // 2
+    with np.errstate(over="ignore"):
+        return bf16.from_f64(silu(gu[..., :f]) * gu[..., f:])

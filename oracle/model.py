@@ -1,0 +1,95 @@
+"""The pre-norm decoder layer and the decode / prefill step (test
+infrastructure only).
+
+The pages name the three batch-invariant kernels (RMSNorm, matmul, attention,
+"Deterministic and bit-exact inference", *technical*) and the sampler settings
+(Kinetic "Receipts", *Making a receipt*) but not the block they sit in.  The
+plainest reading is the standard pre-norm decoder block of Llama/Qwen-style
+models, which is what the workloads describe (RMSNorm eps 1e-6, RoPE, SwiGLU
+FFN, grouped-query attention):
+
+    h  = RMSNorm(x) ; [q k v] = h . Wqkv^T
+    q, k = RoPE(QKnorm(q)), RoPE(QKnorm(k))   (QK-norm optional)
+    cache[pos] <- k, v ; a = Attention(q, cache)
+    x2 = x + a . Wo^T ; h2 = RMSNorm(x2)
+    [g u] = h2 . Wgu^T ; x3 = x2 + (silu(g) * u) . Wdown^T
+
+bf16 rounding happens at each stored tensor, the same boundaries as the GPU
+path.  Weights are bf16 bit arrays; the dictionaries below name them.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import attention, bf16, glue
+from .gemm import gemm
+from .rmsnorm import rmsnorm
+from .rope import rope
+from .sampler import sample
+
+
+@dataclass
+class Shape:
+    d_model: int
+    n_q: int
+    n_kv: int
+    head_dim: int
+    ffn: int
+    vocab: int = 0
+    n_layers: int = 1
+    eps: float = 1e-6
+    rope_base: float = 1e4
+    qk_norm: bool = False
+
+
+def layer_step(x_bits, lw: dict, k_cache, v_cache, pos, shape: Shape):
+    """One decoder layer for rows x [M][d].  Row m belongs to sequence seq[m]
+    at absolute position pos[m]; ``k_cache``/``v_cache`` are
+    [B][Lmax][Hkv][D] bf16 arrays updated in place.  ``pos`` is a list of
+    (seq, position) pairs in row order; rows of one sequence must be in
+    ascending position order, and attention for a row sees keys 0..position.
+    """
+    hq, hk, dh = shape.n_q, shape.n_kv, shape.head_dim
+    m = x_bits.shape[0]
+    h = rmsnorm(x_bits, lw["attn_norm"], shape.eps)
+    qkv = gemm(h, lw["w_qkv"]).reshape(m, hq + 2 * hk, dh)
+    positions = np.array([p for _, p in pos], dtype=np.int64)
+    qn = lw.get("q_norm") if shape.qk_norm else None
+    kn = lw.get("k_norm") if shape.qk_norm else None
+    q = rope(qkv[:, :hq], positions, shape.rope_base, qn, shape.eps)
+    k = rope(qkv[:, hq: hq + hk], positions, shape.rope_base, kn, shape.eps)
+    v = qkv[:, hq + hk:]
+    for i, (b, p) in enumerate(pos):
+        k_cache[b, p] = k[i]
+        v_cache[b, p] = v[i]
+    a = np.zeros_like(q)
+    for i, (b, p) in enumerate(pos):
+        a[i] = attention.decode(q[i: i + 1], k_cache[b: b + 1], v_cache[b: b + 1], [p + 1])[0]
+    o = gemm(a.reshape(m, hq * dh), lw["w_o"])
+    h2, x2 = rmsnorm(o, lw["ffn_norm"], shape.eps, residual_bits=x_bits)
+    act = glue.swiglu(gemm(h2, lw["w_gu"]))
+    return glue.add(x2, gemm(act, lw["w_down"]))
+
+
+def decode_step(tokens, model: dict, k_caches, v_caches, lengths, shape: Shape,
+                histories=None, steps=None, params=None, sample_tokens=True):
+    """Full model, one new token per sequence b at position lengths[b].
+    Returns (logits f32 [B][V], sampled ids or None, near-tie flags or None)."""
+    x = glue.embed(model["embed"], tokens)
+    pos = [(b, int(lengths[b])) for b in range(len(tokens))]
+    for li, lw in enumerate(model["layers"]):
+        x = layer_step(x, lw, k_caches[li], v_caches[li], pos, shape)
+    h = rmsnorm(x, model["final_norm"], shape.eps)
+    logits = gemm(h, model["lm_head"], out="f32")
+    if not sample_tokens:
+        return logits, None, None
+    toks, ties = sample(logits, histories, steps, params)
+    return logits, toks, ties
+
+
+def prefill_chunk(x_bits, lw: dict, k_cache, v_cache, seq: int, p0: int, shape: Shape):
+    """One layer over a chunk of T tokens of sequence ``seq`` at p0..p0+T-1."""
+    pos = [(seq, p0 + t) for t in range(x_bits.shape[0])]
+    return layer_step(x_bits, lw, k_cache, v_cache, pos, shape)

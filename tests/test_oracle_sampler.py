@@ -1,0 +1,137 @@
+"""Pins for Philox4x32-10 and the sampler oracle."""
+import ctypes
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import stats
+
+from oracle import philox
+from oracle.sampler import SamplingParams, penalize, sample_row
+
+
+def test_philox_two_restatements_agree():
+    rng = np.random.default_rng(0)
+    c = rng.integers(0, 2 ** 32, (200, 4), dtype=np.uint64)
+    k = rng.integers(0, 2 ** 32, (200, 2), dtype=np.uint64)
+    vec = philox.philox4x32_10_np(c[:, 0], c[:, 1], c[:, 2], c[:, 3], k[:, 0], k[:, 1])
+    for i in range(200):
+        ref = philox.philox4x32_10(tuple(int(x) for x in c[i]), tuple(int(x) for x in k[i]))
+        assert tuple(int(v[i]) for v in vec) == ref
+
+
+def _curand():
+    for path in ("/usr/local/cuda/lib64/libcurand.so", "libcurand.so", "libcurand.so.10"):
+        try:
+            return ctypes.CDLL(path)
+        except OSError:
+            continue
+    return None
+
+
+def test_philox_matches_curand_host_generator():
+    """cuRAND's host Philox4_32_10 generator (a library routine) seeded with s
+    emits, at offset 0, block j = Philox(counter=(0, 0, j, 0), key=(s_lo, s_hi))."""
+    lib = _curand()
+    if lib is None:
+        pytest.skip("libcurand not available")
+    gen = ctypes.c_void_p()
+    assert lib.curandCreateGeneratorHost(ctypes.byref(gen), 161) == 0
+    try:
+        for seed in (0, 42, 0x0123456789ABCDEF, 2 ** 64 - 1):
+            assert lib.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
+            assert lib.curandSetGeneratorOffset(gen, ctypes.c_ulonglong(0)) == 0
+            buf = (ctypes.c_uint * 64)()
+            assert lib.curandGenerate(gen, buf, ctypes.c_size_t(64)) == 0
+            for j in range(16):
+                mine = philox.philox4x32_10((0, 0, j, 0), (seed & 0xFFFFFFFF, seed >> 32))
+                assert tuple(buf[4 * j: 4 * j + 4]) == mine
+    finally:
+        lib.curandDestroyGenerator(gen)
+
+
+def test_philox_uniformity():
+    w = philox.philox4x32_10_np(np.arange(1 << 15), 0, 0, 0, 42, 0)
+    u = (w[0] >> 8).astype(np.float64) / 2 ** 24
+    assert stats.kstest(u, "uniform").pvalue > 1e-3
+    counts = np.bincount((w[1] >> 28).astype(np.int64), minlength=16)
+    assert stats.chisquare(counts).pvalue > 1e-3
+
+
+def _greedy_params(**kw):
+    p = SamplingParams(temperature=1.0, top_k=0, top_p=1.0, min_p=0.0, repeat_penalty=1.0,
+                       repeat_last_n=0, seed=7)
+    for a, b in kw.items():
+        setattr(p, a, b)
+    return p
+
+
+def test_greedy_and_degenerate_filters_give_argmax():
+    rng = np.random.default_rng(1)
+    z = rng.standard_normal(1000).astype(np.float32)
+    am = int(np.argmax(z))
+    for p in (_greedy_params(temperature=0.0), _greedy_params(top_k=1),
+              _greedy_params(top_k=50, top_p=1e-6), _greedy_params(top_k=50, min_p=1.0)):
+        for step in range(20):
+            assert sample_row(z, [], step, p)[0] == am
+    z2 = np.zeros(10, np.float32)
+    z2[[3, 7]] = 5.0                     # tie: lowest id wins
+    assert sample_row(z2, [], 0, _greedy_params(temperature=0.0))[0] == 3
+    assert sample_row(z2, [], 0, _greedy_params(top_k=1))[0] == 3
+
+
+def test_repeat_penalty_closed_form():
+    z = np.array([2.0, -2.0, 1.0, 0.0, 3.0], np.float32)
+    p = _greedy_params(repeat_penalty=2.0, repeat_last_n=3)
+    got = penalize(z, [4, 0, 1, 1, 0], p)      # last 3 = {1, 0}; id 4 is outside the window
+    assert np.array_equal(got, np.array([1.0, -4.0, 1.0, 0.0, 3.0], np.float32))
+    assert np.array_equal(penalize(z, [0, 1], _greedy_params(repeat_penalty=2.0, repeat_last_n=-1)),
+                          np.array([1.0, -4.0, 1.0, 0.0, 3.0], np.float32))
+    assert np.array_equal(penalize(z, [0, 1], _greedy_params(repeat_penalty=2.0, repeat_last_n=0)), z)
+
+
+def _freq(z, p, n, hist=()):
+    toks = [sample_row(z, list(hist), s, p)[0] for s in range(n)]
+    return np.bincount(toks, minlength=len(z))
+
+
+def test_frequencies_match_softmax_chi2():
+    z = np.array([0.5, -1.0, 2.0, 0.0, 1.0, -0.5, 0.25, 1.5], np.float32)
+    n = 40000
+    p = _greedy_params(temperature=1.0)
+    f = _freq(z, p, n)
+    pr = np.exp(z.astype(np.float64) - z.max())
+    pr /= pr.sum()
+    assert stats.chisquare(f, pr * n).pvalue > 1e-4
+    # temperature 0.5 and top-k 3: softmax(2z) over the three largest
+    p = _greedy_params(temperature=0.5, top_k=3)
+    f = _freq(z, p, n)
+    top = [2, 7, 4]
+    assert f.sum() == f[top].sum()
+    pr = np.exp(2 * (z[top].astype(np.float64) - z.max()))
+    pr /= pr.sum()
+    assert stats.chisquare(f[top], pr * n).pvalue > 1e-4
+
+
+def test_top_p_and_min_p_hand_built():
+    # probabilities 0.5, 0.3, 0.15, 0.05 (ids 1, 3, 0, 2)
+    pr = np.array([0.15, 0.5, 0.05, 0.3])
+    z = np.log(pr).astype(np.float32)
+    n = 20000
+    f = _freq(z, _greedy_params(top_p=0.75), n)      # keeps 0.5 and 0.3 (0.8 >= 0.75)
+    assert f[0] == 0 and f[2] == 0
+    assert stats.chisquare(f[[1, 3]], np.array([5, 3]) / 8 * n).pvalue > 1e-4
+    f = _freq(z, _greedy_params(min_p=0.2), n)       # keeps p >= 0.1: ids 1, 3, 0
+    assert f[2] == 0
+    assert stats.chisquare(f[[1, 3, 0]], np.array([0.5, 0.3, 0.15]) / 0.95 * n).pvalue > 1e-4
+
+
+def test_draw_uses_request_step_not_slot():
+    z = np.random.default_rng(3).standard_normal(500).astype(np.float32)
+    p = SamplingParams()
+    a = [sample_row(z, [], s, p)[0] for s in range(50)]
+    b = [sample_row(z, [], s, p)[0] for s in range(50)]
+    assert a == b
+    u = [philox.sampler_uniform(42, s) for s in range(3)]
+    assert len(set(u)) == 3 and all(0 <= x < 1 for x in u)
