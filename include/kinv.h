@@ -1,0 +1,244 @@
+/*
+ * kinv.h -- C ABI of libkinv, a batch-invariant LLM forward step for NVIDIA
+ * GB300 (sm_103a).
+ *
+ * What "batch-invariant" means here ("Deterministic and bit-exact inference",
+ * trustbutveri.fyi record M-0002, *technical* and *How it works*): every
+ * kernel fixes the reduction order of each output element whatever the batch
+ * size, so the bits of row i (request b) depend only on row i's own inputs --
+ * not on how many rows share the call, which rows they are, where row i sits
+ * in the batch, or how a prompt was chunked.  The three reductions the pages
+ * name are RMSNorm, matrix multiplication and attention; attention splits the
+ * key/value dimension by a FIXED SPLIT SIZE, not a fixed number of splits.
+ * The promise holds within one device class and one build (Kinetic
+ * "Receipts", *What a receipt proves*: bits are promised only within one class
+ * and one build); kinv_device_class() and kinv_build_id() name both.
+ *
+ * Conventions for every call below:
+ *  - Pointers marked "device" are CUDA device pointers owned by the caller.
+ *    The library never allocates, frees or synchronises on these paths; each
+ *    call enqueues its kernels on `stream` (NULL = the legacy default stream)
+ *    and returns.  Scratch space is passed in by the caller (`workspace`,
+ *    sized by the matching *_workspace() query).
+ *  - bf16 tensors are IEEE bfloat16 bit patterns, row-major, with the leading
+ *    dimension (`ld*`, in elements) given.  fp32 accumulation throughout.
+ *  - Errors are returned, never thrown, and nothing is launched when a call
+ *    returns an error.  Shape, alignment and workspace checks happen on the
+ *    host before any launch.  Launch failures return KINV_ERR_CUDA.  A device
+ *    wait that runs out of time (every spin in the kernels is bounded) records
+ *    a code in a device status word that kinv_last_device_status() reports.
+ *  - Calls are thread-safe; the only global state is per-device attributes.
+ */
+#ifndef KINV_H
+#define KINV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kinv_stream; /* same type as cudaStream_t */
+
+typedef enum {
+  KINV_OK = 0,
+  KINV_ERR_INVALID_ARG = -1, /* null pointer, negative size, bad enum */
+  KINV_ERR_UNSUPPORTED = -2, /* a shape or setting outside the supported set */
+  KINV_ERR_ALIGNMENT = -3,   /* base or leading dimension not 16-byte aligned */
+  KINV_ERR_WORKSPACE = -4,   /* workspace missing or smaller than the query */
+  KINV_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed */
+  KINV_ERR_TIMEOUT = -6      /* a bounded device-side wait gave up */
+} kinv_status;
+
+typedef enum { KINV_BF16 = 0, KINV_F32 = 1 } kinv_dtype;
+
+/* Human-readable name of a status code (static string). */
+const char* kinv_status_string(int status);
+
+/* Device class whose bits this build promises: "cuda-sm103a". */
+const char* kinv_device_class(void);
+
+/* Build id: 16 hex digits identifying this build of the kernels (a hash of
+ * the sources and compile flags, fixed at build time).  Kinetic "Receipts",
+ * *Making a receipt*: the receipt's build field pins every compiled kernel. */
+const char* kinv_build_id(void);
+
+/* Synchronises `stream`, then returns and clears the device status word of the
+ * current device: KINV_OK, or KINV_ERR_TIMEOUT if a bounded wait gave up since
+ * the last call.  Returns KINV_ERR_CUDA if the synchronisation itself fails. */
+int kinv_last_device_status(kinv_stream stream);
+
+/* ------------------------------------------------------------------ GEMM
+ * C[M][N] = A[M][K] . W[N][K]^T   ("Deterministic and bit-exact inference",
+ * *technical*: batch-invariant matrix multiplication).
+ *
+ * A, W: device bf16, row-major, leading dimensions lda, ldw (elements).
+ * C: device, bf16 (c_dtype = KINV_BF16) or fp32 (KINV_F32), leading dim ldc.
+ * Arithmetic: bf16 products, fp32 accumulation on the tensor cores, one
+ * rounding at the store.  The tile shape, the K order (ascending blocks of 64)
+ * and the constant split of K (summed in fixed rank order) are chosen from
+ * (N, K) alone, never from M: row i's bits are the same for every M.
+ * Requirements: K % 64 == 0, N % 16 == 0, M >= 0; A, W, C 16-byte aligned;
+ * lda, ldw multiples of 8; ldc a multiple of 8 (bf16) or 4 (fp32).
+ * Errors: KINV_ERR_UNSUPPORTED / KINV_ERR_ALIGNMENT / KINV_ERR_INVALID_ARG.
+ * M == 0 returns KINV_OK and launches nothing. */
+kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int64_t ldw,
+                      void* C, int64_t ldc, kinv_dtype c_dtype,
+                      int M, int N, int K, kinv_stream stream);
+
+/* --------------------------------------------------------------- RMSNorm
+ * y[r][i] = x[r][i] / sqrt(mean_j x[r][j]^2 + eps) * w[i]
+ * ("Deterministic and bit-exact inference", *technical*: batch-invariant
+ * RMSNorm).  One thread block per row; the sum of squares is taken in a fixed
+ * per-thread order, then a fixed shuffle tree, then a fixed cross-warp order,
+ * so a row's bits do not depend on `rows`.
+ * residual (nullable): when given, s = bf16(x + residual) is formed first,
+ * written back into `x` (the new residual stream), and y = RMSNorm(s).
+ * x, residual, y: device bf16 [rows][dim] with leading dims ldx, ldx, ldy.
+ * w: device bf16 [dim].  Requirements: dim % 8 == 0, 8 <= dim <= 16384,
+ * 16-byte aligned bases, ldx and ldy multiples of 8.  `x` may be const when
+ * residual is NULL (it is not written). */
+kinv_status kinv_rmsnorm(void* x, int64_t ldx, const void* residual,
+                         const void* w, void* y, int64_t ldy,
+                         int rows, int dim, float eps, kinv_stream stream);
+
+/* ------------------------------------------------------ decode attention
+ * out[b][h] = sum_{j < L_b} softmax_j(scale * q[b][h] . k[b][j][g]) v[b][j][g],
+ * g = h / (Hq / Hkv)  ("Deterministic and bit-exact inference", *technical*:
+ * batch-invariant attention with a fixed split size of the key/value
+ * dimension rather than a fixed number of splits).
+ *
+ * Keys of sequence b are cut into splits of `split_len` keys at absolute
+ * offsets 0, split_len, 2 split_len, ...; each split yields an fp32 partial
+ * (max, sum of exponentials, unnormalised output) and the partials are folded
+ * in ascending split order.  The cut depends only on L_b, so a sequence's bits
+ * do not depend on its batch-mates or their lengths.  L_b == 0 gives zeros.
+ *
+ * q, out: device bf16 [B][Hq][D] (contiguous).  k_cache, v_cache: device bf16;
+ *   element (b, j, g, d) is at b*seq_stride + j*tok_stride + g*D + d
+ *   (elements); e.g. a contiguous [B][Lmax][Hkv][D] cache has
+ *   seq_stride = Lmax*Hkv*D, tok_stride = Hkv*D.
+ * kv_len: device int32 [B], each in [0, Lmax].
+ * workspace: device, at least kinv_attn_decode_workspace(B, Hq, D, Lmax,
+ *   split_len) bytes, 16-byte aligned.
+ * Requirements: D in {64, 128}; Hq % Hkv == 0; Hq / Hkv in {1, 2, 4, 8};
+ * split_len == 256; strides multiples of 8.  scale <= 0 means 1/sqrt(D). */
+size_t kinv_attn_decode_workspace(int B, int Hq, int D, int Lmax, int split_len);
+kinv_status kinv_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                             int64_t seq_stride, int64_t tok_stride,
+                             const int32_t* kv_len, void* out,
+                             int B, int Hq, int Hkv, int D, int Lmax, int split_len,
+                             float scale, void* workspace, size_t workspace_bytes,
+                             kinv_stream stream);
+
+/* ----------------------------------------------------- prefill attention
+ * Causal attention for chunks of new query rows against the cache (which
+ * must already hold their keys).  Sequence b contributes q_len[b] rows,
+ * stored at rows q_offset[b] .. q_offset[b] + q_len[b] - 1 of q/out, at
+ * absolute positions q_start[b] .. q_start[b] + q_len[b] - 1; the row at
+ * position p attends to keys 0..p of sequence b.
+ * Each row is computed with exactly the arithmetic of kinv_attn_decode for a
+ * sequence of length p + 1 (same splits at absolute offsets, same fold), so a
+ * row's bits do not depend on the chunking, on p0, on the other rows, and a
+ * decode step equals a one-row prefill bit for bit.
+ * q, out: device bf16 [total_rows][Hq][D].  q_start, q_len, q_offset: device
+ * int32 [B].  Caches and strides as for decode.  max_q_len bounds q_len[b],
+ * max_kv bounds q_start[b] + q_len[b] (both used to size the grid and the
+ * workspace).  Requirements as for decode. */
+size_t kinv_attn_prefill_workspace(int total_rows, int Hq, int D, int max_kv, int split_len);
+kinv_status kinv_attn_prefill(const void* q, const void* k_cache, const void* v_cache,
+                              int64_t seq_stride, int64_t tok_stride,
+                              const int32_t* q_start, const int32_t* q_len,
+                              const int32_t* q_offset, void* out,
+                              int B, int total_rows, int max_q_len, int max_kv,
+                              int Hq, int Hkv, int D, int split_len, float scale,
+                              void* workspace, size_t workspace_bytes,
+                              kinv_stream stream);
+
+/* --------------------------------------------------------------- sampler
+ * Seeded sampler with the settings a Kinetic receipt records (Kinetic
+ * "Receipts", *Making a receipt*, the `sampling` object).  Per row b, in this
+ * order: repeat penalty over the distinct ids among the last repeat_last_n
+ * history tokens (z/r if z > 0 else z*r; n < 0: all, n == 0: none);
+ * temperature <= 0 -> greedy argmax (lowest id on ties); otherwise the top_k
+ * candidates ordered by (z desc, id asc); s = z / temperature;
+ * e_i = exp(s_i - s_0); top-p keeps the shortest prefix whose sum of e reaches
+ * top_p * sum(e) (skipped when top_p >= 1); min-p keeps e_i >= min_p (skipped
+ * when min_p <= 0); then u = (Philox4x32-10(counter = (step lo, step hi, 0, 0),
+ * key = (seed lo, seed hi)).word0 >> 8) * 2^-24 picks the first kept candidate
+ * whose running sum of e exceeds u * (sum of kept e).  The counter is the
+ * request's own step, never its batch slot: the drawn token depends only on
+ * the row's logits, history, settings and step.  One thread block per row;
+ * ranking and thresholds are compare-only on fp32 values; sums in fixed order.
+ *
+ * logits: device fp32 [B][ld]; params: device kinv_sampling_params [B];
+ * history: device int32 [B][hist_ld], row b holding hist_len[b] ids, oldest
+ * first; step: device int64 [B]; out_tokens: device int32 [B].
+ * Requirements: 1 <= V; ld >= V; top_k in [1, 1024] unless temperature <= 0;
+ * hist_len[b] <= hist_ld.  Rows whose settings are outside this set get token
+ * -1 and the device status word records KINV_ERR_UNSUPPORTED. */
+typedef struct {
+  float temperature;
+  float top_p;
+  float min_p;
+  float repeat_penalty;
+  int32_t top_k;
+  int32_t repeat_last_n;
+  uint64_t seed;
+} kinv_sampling_params;
+
+size_t kinv_sample_workspace(int B, int V);
+kinv_status kinv_sample(const float* logits, int64_t ld, int B, int V,
+                        const kinv_sampling_params* params,
+                        const int32_t* history, int hist_ld, const int32_t* hist_len,
+                        const int64_t* step, int32_t* out_tokens,
+                        void* workspace, size_t workspace_bytes, kinv_stream stream);
+
+/* ------------------------------------------------------------ layer glue
+ * Element-wise steps of the decoder block.  None of them sums across
+ * elements, so each is batch-invariant by construction. */
+
+/* out[r] = table[ids[r]] for r < rows; table bf16 [vocab][dim] (ld = dim),
+ * ids device int32 [rows] (ids outside [0, vocab) give zeros), dim % 8 == 0. */
+kinv_status kinv_embed(const void* table, int vocab, int dim, const int32_t* ids,
+                       void* out, int rows, kinv_stream stream);
+
+/* out = bf16(x + y), n elements, bf16, n % 8 == 0, 16-byte aligned. */
+kinv_status kinv_add(const void* x, const void* y, void* out, int64_t n, kinv_stream stream);
+
+/* out[r][i] = bf16(silu(gu[r][i]) * gu[r][F + i]), silu(g) = g / (1 + e^-g);
+ * gu bf16 [rows][2F] (ld_gu), out bf16 [rows][F] (ld_out); F % 8 == 0. */
+kinv_status kinv_swiglu(const void* gu, int64_t ld_gu, void* out, int64_t ld_out,
+                        int rows, int F, kinv_stream stream);
+
+/* Rotary embedding (rotate-half pairs (i, i + D/2), theta_i = p * base^(-2i/D))
+ * with optional per-head RMSNorm first (q_norm / k_norm nullable, gains [D]),
+ * then the key/value append: for row r of sequence seq[r] at absolute position
+ * pos[r]:
+ *   q_out[r][h]                = bf16(RoPE(norm(q)))        h < Hq
+ *   k_cache[seq][pos][g]       = bf16(RoPE(norm(k)))        g < Hkv
+ *   v_cache[seq][pos][g]       = v                           (copied bits)
+ * qkv: device bf16 [rows][(Hq + 2 Hkv) D] (ld_qkv), q, k, v heads in that
+ * order.  q_out: bf16 [rows][Hq][D].  seq, pos: device int32 [rows].
+ * Requirements: D in {64, 128}; strides multiples of 8; 16-byte alignment. */
+kinv_status kinv_rope_append(const void* qkv, int64_t ld_qkv, void* q_out,
+                             void* k_cache, void* v_cache, int64_t seq_stride,
+                             int64_t tok_stride, const int32_t* seq, const int32_t* pos,
+                             const void* q_norm, const void* k_norm, float eps,
+                             int rows, int Hq, int Hkv, int D, float rope_base,
+                             kinv_stream stream);
+
+/* One decode iteration's bookkeeping, per request b < B: append
+ * tokens[b] to history row b (shifting out the oldest id once hist_len ==
+ * hist_ld), hist_len[b] = min(hist_len[b] + 1, hist_ld), step[b] += 1, and
+ * pos[b] += 1, kv_len[b] += 1 for whichever of pos / kv_len is not NULL.
+ * All device pointers. */
+kinv_status kinv_decode_advance(const int32_t* tokens, int32_t* history, int hist_ld,
+                                int32_t* hist_len, int64_t* step, int32_t* pos,
+                                int32_t* kv_len, int B, kinv_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KINV_H */

@@ -1,0 +1,447 @@
+// Batch-invariant split-KV attention for decode and prefill
+// ("Deterministic and bit-exact inference", *technical*: attention made
+// batch-invariant "with a fixed split size for the key-value dimension rather
+// than a fixed number of splits").
+//
+// A query row with L visible keys cuts them into splits of 256 keys at
+// absolute offsets 0, 256, 512, ...; the cut depends only on L.  Split kernel:
+// one thread block per (split, kv head, group of query rows of one sequence).
+// Thread t owns key t of the split.  For every query row r and query head i of
+// the kv head's group:
+//   s_t  = (q . k_t) * scale          fp32 fused multiply-adds over d ascending
+//   m    = max_t s_t                  (max is exact in any order)
+//   e_t  = exp(s_t - m)
+//   l    = sum_t e_t                  butterfly in each warp (lane 0), then the
+//                                     8 warp sums in ascending warp order
+//   o[d] = sum_t e_t v_t[d]           fused multiply-adds over t ascending
+// and (m, l, o) is stored as the split's fp32 partial.  Keys a row cannot see
+// (t >= its count) contribute e_t = 0 to the butterfly and are skipped in the
+// o sum, so a row's arithmetic is the same whichever rows share the block.
+// Merge kernel: per (row, query head), fold the partials in ascending split
+// order with the log-sum-exp update, then o / l -> bf16.
+//
+// Decode is the case of one row per block with L = kv_len[b]; prefill groups
+// up to 32 / (Hq/Hkv) consecutive rows of one sequence per block (they share
+// the split's K and V tiles in shared memory) with L = position + 1.  Both run
+// the same compiled kernels, so a decode step equals a one-row prefill bit for
+// bit, and a prompt's rows have the same bits for every chunking.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace kinv {
+namespace {
+
+constexpr int kSplit = 256;      // keys per split (the fixed split size)
+constexpr int kThreads = 256;    // one thread per key of a split
+constexpr int kMaxRG = 32;       // rows x query heads handled by one block
+constexpr int kMaxG = 8;         // query heads per kv head
+
+struct AttnParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  int64_t seq_stride, tok_stride;
+  const int32_t* kv_len;    // decode
+  const int32_t* q_start;   // prefill
+  const int32_t* q_len;
+  const int32_t* q_offset;
+  __nv_bfloat16* out;
+  float* ws_o;              // [rows][Hq][S][D]
+  float* ws_ml;             // [rows][Hq][S][2]
+  int prefill;
+  int Hq, Hkv, G, R;
+  int S;                    // splits per row in the workspace
+  int groups_per_seq;       // prefill: ceil(max_q_len / R)
+  int rg_cap;               // R * G: sizes the query and weight buffers
+  float scale;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Rows handled by this block: their q/out row indices and visible key counts.
+struct RowSet {
+  int nrows;
+  int seq;
+  int row0;     // q/out row of the first row (rows are consecutive)
+  int len0;     // visible keys of the first row (row r sees len0 + r)
+};
+
+__device__ __forceinline__ bool block_rows(const AttnParams& p, RowSet& rs) {
+  if (!p.prefill) {
+    const int b = blockIdx.z;
+    rs.nrows = 1;
+    rs.seq = b;
+    rs.row0 = b;
+    rs.len0 = p.kv_len[b];
+    return rs.len0 > 0;
+  }
+  const int b = blockIdx.z / p.groups_per_seq;
+  const int j = blockIdx.z % p.groups_per_seq;
+  const int first = j * p.R;
+  const int n = p.q_len[b];
+  if (first >= n) return false;
+  rs.nrows = min(p.R, n - first);
+  rs.seq = b;
+  rs.row0 = p.q_offset[b] + first;
+  rs.len0 = p.q_start[b] + first + 1;
+  return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p) {
+  constexpr int C8 = D / 8;                // 16-byte chunks per key row
+  // K (then V) tile [256][D] bf16; chunk c of key row t is stored at chunk
+  // c ^ (t & 7) of that row, so that both the per-key reads of the scores and
+  // the per-column reads of the o sum are free of bank conflicts.
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(smem_raw);
+  float* qs = reinterpret_cast<float*>(smem_raw + kSplit * D * 2);        // [rg_cap][D]
+  float* es = qs + p.rg_cap * D;                                          // [rg_cap][256]
+  __shared__ float red[kThreads / 32][kMaxRG];
+  __shared__ float mrow[kMaxRG];
+  __shared__ float lrow[kMaxRG];
+
+  RowSet rs;
+  if (!block_rows(p, rs)) return;
+  const int s = blockIdx.x;
+  const int g = blockIdx.y;
+  const int k0 = s * kSplit;
+  const int lenmax = rs.len0 + rs.nrows - 1;           // the last row sees the most keys
+  const int nmax = min(kSplit, lenmax - k0);
+  if (nmax <= 0) return;
+  const int G = p.G;
+  const int RG = rs.nrows * G;
+  const int t = threadIdx.x;
+  const int lane = t & 31, warp = t >> 5;
+
+  // --- K tile (and the queries) into shared memory
+  const __nv_bfloat16* kbase = p.k + rs.seq * p.seq_stride + static_cast<int64_t>(k0) * p.tok_stride + g * D;
+  for (int idx = t; idx < nmax * C8; idx += kThreads) {
+    const int row = idx / C8, c = idx % C8;
+    cp_async16(smem_addr(kv + row * D + ((c ^ (row & 7)) * 8)), kbase + row * p.tok_stride + c * 8);
+  }
+  cp_async_commit();
+  for (int idx = t; idx < RG * D; idx += kThreads) {
+    const int rg = idx / D, d = idx % D;
+    const int r = rg / G, i = rg % G;
+    qs[idx] = __bfloat162float(p.q[(static_cast<int64_t>(rs.row0 + r) * p.Hq + g * G + i) * D + d]);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // --- scores: thread t against key t, every (row, head)
+  float acc[kMaxRG];
+#pragma unroll
+  for (int j = 0; j < kMaxRG; ++j) acc[j] = 0.f;
+  if (t < nmax) {
+    const __nv_bfloat16* kr = kv + t * D;
+#pragma unroll 2
+    for (int c = 0; c < C8; ++c) {
+      const uint4 u = *reinterpret_cast<const uint4*>(kr + ((c ^ (t & 7)) * 8));
+      float kf[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                     bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+#pragma unroll
+      for (int j = 0; j < kMaxRG; ++j) {
+        if (j < RG) {
+          const float4 qa = *reinterpret_cast<const float4*>(qs + j * D + c * 8);
+          const float4 qb = *reinterpret_cast<const float4*>(qs + j * D + c * 8 + 4);
+          float a = acc[j];
+          a = fmaf(qa.x, kf[0], a); a = fmaf(qa.y, kf[1], a);
+          a = fmaf(qa.z, kf[2], a); a = fmaf(qa.w, kf[3], a);
+          a = fmaf(qb.x, kf[4], a); a = fmaf(qb.y, kf[5], a);
+          a = fmaf(qb.z, kf[6], a); a = fmaf(qb.w, kf[7], a);
+          acc[j] = a;
+        }
+      }
+    }
+  }
+  __syncthreads();  // every thread is done with the K tile
+
+  // --- V tile load overlaps the softmax statistics
+  const __nv_bfloat16* vbase = p.v + rs.seq * p.seq_stride + static_cast<int64_t>(k0) * p.tok_stride + g * D;
+  for (int idx = t; idx < nmax * C8; idx += kThreads) {
+    const int row = idx / C8, c = idx % C8;
+    cp_async16(smem_addr(kv + row * D + ((c ^ (row & 7)) * 8)), vbase + row * p.tok_stride + c * 8);
+  }
+  cp_async_commit();
+
+  // scaled scores; keys a row cannot see are -inf for the max
+#pragma unroll
+  for (int j = 0; j < kMaxRG; ++j) {
+    if (j < RG) {
+      const int nr = min(kSplit, rs.len0 + j / G - k0);
+      acc[j] = t < nr ? __fmul_rn(acc[j], p.scale) : -INFINITY;
+    }
+  }
+  // row maxima (max is exact, so the tree shape does not matter)
+#pragma unroll
+  for (int j = 0; j < kMaxRG; ++j) {
+    if (j < RG) {
+      float m = acc[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) red[warp][j] = m;
+    }
+  }
+  __syncthreads();
+  if (t < RG) {
+    float m = red[0][t];
+    for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, red[w][t]);
+    mrow[t] = m;
+  }
+  __syncthreads();
+  // exponentials and their sums: butterfly per warp (lane 0), warps in order
+#pragma unroll
+  for (int j = 0; j < kMaxRG; ++j) {
+    if (j < RG) {
+      const int nr = min(kSplit, rs.len0 + j / G - k0);
+      const float e = t < nr ? expf(__fsub_rn(acc[j], mrow[j])) : 0.f;
+      es[j * kSplit + t] = e;
+      float l = e;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, o));
+      if (lane == 0) red[warp][j] = l;
+    }
+  }
+  __syncthreads();
+  if (t < RG) {
+    float l = red[0][t];
+    for (int w = 1; w < kThreads / 32; ++w) l = __fadd_rn(l, red[w][t]);
+    lrow[t] = l;
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // --- o = sum_t e_t v_t: thread -> (d pair, a slot of (row, head) pairs)
+  constexpr int DP = D / 2;
+  constexpr int SLOTS = kThreads / DP;       // 4 (D = 128) or 8 (D = 64)
+  constexpr int PER = kMaxRG / SLOTS;        // (row, head) pairs per thread at most
+  const int dp = t % DP;
+  const int slot = t / DP;
+  float2 o[PER];
+  int cnt[PER];
+#pragma unroll
+  for (int c = 0; c < PER; ++c) {
+    o[c] = make_float2(0.f, 0.f);
+    const int j = slot + c * SLOTS;
+    cnt[c] = j < RG ? min(kSplit, rs.len0 + j / G - k0) : 0;
+  }
+  for (int key = 0; key < nmax; ++key) {
+    const uint32_t vv = *reinterpret_cast<const uint32_t*>(
+        kv + key * D + ((((2 * dp) >> 3) ^ (key & 7)) << 3) + ((2 * dp) & 7));
+    const float v0 = bf16_lo(vv), v1 = bf16_hi(vv);
+#pragma unroll
+    for (int c = 0; c < PER; ++c) {
+      if (key < cnt[c]) {
+        const float e = es[(slot + c * SLOTS) * kSplit + key];
+        o[c].x = fmaf(e, v0, o[c].x);
+        o[c].y = fmaf(e, v1, o[c].y);
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < PER; ++c) {
+    const int j = slot + c * SLOTS;
+    if (j < RG && cnt[c] > 0) {
+      const int r = j / G, i = j % G;
+      const int64_t base = (static_cast<int64_t>(rs.row0 + r) * p.Hq + g * G + i) * p.S + s;
+      *reinterpret_cast<float2*>(p.ws_o + base * D + 2 * dp) = o[c];
+      if (dp == 0) {
+        p.ws_ml[base * 2 + 0] = mrow[j];
+        p.ws_ml[base * 2 + 1] = lrow[j];
+      }
+    }
+  }
+}
+
+// One block per (query head, row); thread d folds column d.
+template <int D>
+__global__ void attn_merge_kernel(const AttnParams p) {
+  int row, len;
+  if (!p.prefill) {
+    row = blockIdx.y;
+    len = p.kv_len[row];
+  } else {
+    const int b = blockIdx.z;
+    const int i = blockIdx.y;
+    if (i >= p.q_len[b]) return;
+    row = p.q_offset[b] + i;
+    len = p.q_start[b] + i + 1;
+  }
+  const int h = blockIdx.x;
+  const int d = threadIdx.x;
+  __nv_bfloat16* dst = p.out + (static_cast<int64_t>(row) * p.Hq + h) * D + d;
+  if (len <= 0) {
+    *dst = __float2bfloat16_rn(0.f);
+    return;
+  }
+  const int ns = (len + kSplit - 1) / kSplit;
+  const int64_t base = (static_cast<int64_t>(row) * p.Hq + h) * p.S;
+  float m_acc = -INFINITY, l_acc = 0.f, o_acc = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float m_s = p.ws_ml[(base + s) * 2 + 0];
+    const float l_s = p.ws_ml[(base + s) * 2 + 1];
+    const float o_s = p.ws_o[(base + s) * D + d];
+    const float m_new = fmaxf(m_acc, m_s);
+    const float a = expf(__fsub_rn(m_acc, m_new));
+    const float c = expf(__fsub_rn(m_s, m_new));
+    l_acc = __fadd_rn(__fmul_rn(l_acc, a), __fmul_rn(l_s, c));
+    o_acc = __fadd_rn(__fmul_rn(o_acc, a), __fmul_rn(o_s, c));
+    m_acc = m_new;
+  }
+  *dst = __float2bfloat16_rn(__fdiv_rn(o_acc, l_acc));
+}
+
+template <int D>
+size_t split_smem_bytes(int rg_cap) {
+  return static_cast<size_t>(kSplit) * D * 2 + static_cast<size_t>(rg_cap) * D * 4 +
+         static_cast<size_t>(rg_cap) * kSplit * 4;
+}
+
+template <int D>
+kinv_status launch(const AttnParams& p, dim3 split_grid, dim3 merge_grid, cudaStream_t stream) {
+  const size_t smem = split_smem_bytes<D>(p.rg_cap);
+  static bool configured[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KINV_ERR_CUDA;
+  if (dev < 64 && !configured[dev]) {
+    if (cudaFuncSetAttribute(attn_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(split_smem_bytes<D>(kMaxRG))) != cudaSuccess)
+      return KINV_ERR_CUDA;
+    configured[dev] = true;
+  }
+  attn_split_kernel<D><<<split_grid, kThreads, smem, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return KINV_ERR_CUDA;
+  attn_merge_kernel<D><<<merge_grid, D, 0, stream>>>(p);
+  return launch_status();
+}
+
+kinv_status check_common(const void* q, const void* k, const void* v, int64_t seq_stride,
+                         int64_t tok_stride, const void* out, int Hq, int Hkv, int D,
+                         int split_len, const void* ws) {
+  if (!q || !k || !v || !out || !ws) return KINV_ERR_INVALID_ARG;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv) return KINV_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != kMaxG) return KINV_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return KINV_ERR_UNSUPPORTED;
+  if (split_len != kSplit) return KINV_ERR_UNSUPPORTED;
+  if (tok_stride < static_cast<int64_t>(Hkv) * D || seq_stride < 0) return KINV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(ws) ||
+      seq_stride % 8 || tok_stride % 8)
+    return KINV_ERR_ALIGNMENT;
+  return KINV_OK;
+}
+
+size_t workspace_bytes(int64_t rows, int Hq, int D, int S) {
+  const size_t o = static_cast<size_t>(rows) * Hq * S * D * 4;
+  const size_t ml = static_cast<size_t>(rows) * Hq * S * 2 * 4;
+  return ((o + 255) / 256) * 256 + ml;
+}
+
+}  // namespace
+}  // namespace kinv
+
+using namespace kinv;
+
+extern "C" size_t kinv_attn_decode_workspace(int B, int Hq, int D, int Lmax, int split_len) {
+  if (B <= 0 || Hq <= 0 || D <= 0 || Lmax <= 0 || split_len <= 0) return 0;
+  return workspace_bytes(B, Hq, D, (Lmax + split_len - 1) / split_len);
+}
+
+extern "C" kinv_status kinv_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                                        int64_t seq_stride, int64_t tok_stride,
+                                        const int32_t* kv_len, void* out, int B, int Hq, int Hkv,
+                                        int D, int Lmax, int split_len, float scale,
+                                        void* workspace, size_t ws_bytes, kinv_stream stream) {
+  if (B < 0 || Lmax < 0) return KINV_ERR_INVALID_ARG;
+  if (B == 0) return KINV_OK;
+  if (!kv_len) return KINV_ERR_INVALID_ARG;
+  kinv_status st = check_common(q, k_cache, v_cache, seq_stride, tok_stride, out, Hq, Hkv, D,
+                                split_len, workspace);
+  if (st != KINV_OK) return st;
+  if (B > 65535) return KINV_ERR_UNSUPPORTED;
+  const int S = Lmax > 0 ? (Lmax + kSplit - 1) / kSplit : 1;
+  if (ws_bytes < workspace_bytes(B, Hq, D, S)) return KINV_ERR_WORKSPACE;
+  AttnParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k_cache);
+  p.v = static_cast<const __nv_bfloat16*>(v_cache);
+  p.seq_stride = seq_stride;
+  p.tok_stride = tok_stride;
+  p.kv_len = kv_len;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.ws_o = static_cast<float*>(workspace);
+  const size_t o_bytes = static_cast<size_t>(B) * Hq * S * D * 4;
+  p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
+  p.prefill = 0;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.R = 1;
+  p.S = S;
+  p.groups_per_seq = 1;
+  p.rg_cap = p.G;
+  p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
+  const dim3 split_grid(S, Hkv, B), merge_grid(Hq, B, 1);
+  return D == 128 ? launch<128>(p, split_grid, merge_grid, stream)
+                  : launch<64>(p, split_grid, merge_grid, stream);
+}
+
+extern "C" size_t kinv_attn_prefill_workspace(int total_rows, int Hq, int D, int max_kv,
+                                              int split_len) {
+  if (total_rows <= 0 || Hq <= 0 || D <= 0 || max_kv <= 0 || split_len <= 0) return 0;
+  return workspace_bytes(total_rows, Hq, D, (max_kv + split_len - 1) / split_len);
+}
+
+extern "C" kinv_status kinv_attn_prefill(const void* q, const void* k_cache, const void* v_cache,
+                                         int64_t seq_stride, int64_t tok_stride,
+                                         const int32_t* q_start, const int32_t* q_len,
+                                         const int32_t* q_offset, void* out, int B,
+                                         int total_rows, int max_q_len, int max_kv, int Hq,
+                                         int Hkv, int D, int split_len, float scale,
+                                         void* workspace, size_t ws_bytes, kinv_stream stream) {
+  if (B < 0 || total_rows < 0 || max_q_len < 0 || max_kv < 0) return KINV_ERR_INVALID_ARG;
+  if (B == 0 || total_rows == 0 || max_q_len == 0) return KINV_OK;
+  if (!q_start || !q_len || !q_offset || max_kv <= 0) return KINV_ERR_INVALID_ARG;
+  kinv_status st = check_common(q, k_cache, v_cache, seq_stride, tok_stride, out, Hq, Hkv, D,
+                                split_len, workspace);
+  if (st != KINV_OK) return st;
+  const int S = (max_kv + kSplit - 1) / kSplit;
+  if (ws_bytes < workspace_bytes(total_rows, Hq, D, S)) return KINV_ERR_WORKSPACE;
+  AttnParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k_cache);
+  p.v = static_cast<const __nv_bfloat16*>(v_cache);
+  p.seq_stride = seq_stride;
+  p.tok_stride = tok_stride;
+  p.q_start = q_start;
+  p.q_len = q_len;
+  p.q_offset = q_offset;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.ws_o = static_cast<float*>(workspace);
+  const size_t o_bytes = static_cast<size_t>(total_rows) * Hq * S * D * 4;
+  p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
+  p.prefill = 1;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.R = kMaxRG / p.G < 8 ? kMaxRG / p.G : 8;
+  p.S = S;
+  p.groups_per_seq = (max_q_len + p.R - 1) / p.R;
+  p.rg_cap = p.R * p.G;
+  p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
+  const int64_t groups = static_cast<int64_t>(B) * p.groups_per_seq;
+  if (groups > 65535 || max_q_len > 65535 || B > 65535) return KINV_ERR_UNSUPPORTED;
+  const dim3 split_grid(S, Hkv, static_cast<unsigned>(groups)), merge_grid(Hq, max_q_len, B);
+  return D == 128 ? launch<128>(p, split_grid, merge_grid, stream)
+                  : launch<64>(p, split_grid, merge_grid, stream);
+}

@@ -1,0 +1,370 @@
+// Batch-invariant GEMM on the 5th-generation tensor cores
+// ("Deterministic and bit-exact inference", *technical*: matrix
+// multiplication made batch-invariant by fixing each output element's
+// reduction order regardless of batch size).
+//
+// C[M][N] = A[M][K] . W[N][K]^T, bf16 inputs, fp32 accumulation in tensor
+// memory (TMEM), one rounding at the store.
+//
+// Per output element the arithmetic is fixed by (N, K) alone:
+//  * every tile is 128 rows of A by BN rows of W; each K step is one
+//    tcgen05.mma of shape 128 x BN x 16 (kind::f16, bf16 in, fp32 accumulate),
+//    four per 64-wide K block, K blocks in ascending order;
+//  * K is cut into `splits` equal, contiguous ranges (splits depends on N and
+//    K only); the CTAs of one cluster compute one range each, and the partial
+//    sums are added in rank order p0 + p1 + ... through distributed shared
+//    memory -- no atomics, no batch-dependent split;
+//  * rows of A beyond M are zero-filled by TMA and never stored.
+// Row i therefore meets the same instructions in the same order for every M,
+// at whichever lane of the tile it lands.
+//
+// Roles inside a 128-thread CTA: thread 0 issues TMA loads into a ring of
+// shared-memory stages (mbarrier full/empty pairs), thread 32 issues the MMAs
+// and commits each stage back to the producer, and all four warps read the
+// accumulator out of TMEM (warp w owns TMEM lanes 32w..32w+31 = tile rows).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace kinv {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // one 128-byte swizzle row of bf16
+constexpr int kGemmThreads = 128;
+constexpr int A_STAGE = BM * BK * 2;
+
+// tcgen05 instruction descriptor, kind::f16: fp32 accumulate (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major, N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+template <int BN>
+__device__ constexpr uint32_t instr_desc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+         (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor for a K-major tile written by TMA with
+// 128-byte swizzling: start address >> 4, leading offset 1 (unused for this
+// layout), stride between 8-row groups 1024 bytes, descriptor version 1,
+// layout type 2 (128-byte swizzle).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (1ull << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+struct GemmArgs {
+  void* C;
+  int64_t ldc;
+  int M, N;
+  int k_tiles;  // 64-wide K blocks per split
+  int c_f32;
+  int stages;
+  int splits;
+  int* status;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                const GemmArgs args) {
+  constexpr int W_STAGE = BN * BK * 2;
+  constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int stages = args.stages;
+  unsigned char* a_st = base;
+  unsigned char* w_st = base + stages * A_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(w_st + stages * W_STAGE);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto full_bar = [&](int s) { return smem_addr(bars + s); };
+  auto empty_bar = [&](int s) { return smem_addr(bars + stages + s); };
+  const uint32_t done_bar = smem_addr(bars + 2 * stages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int splits = args.splits;
+  const int rank = splits > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int n0 = blockIdx.y * BN;
+  const int m0 = blockIdx.z * BM;
+  const int k_tiles = args.k_tiles;
+  const int kt0 = rank * k_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  int issued = 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+      const uint64_t pol_a = l2_policy_evict_last();   // A is re-read by every N tile
+      const uint64_t pol_w = l2_policy_evict_first();  // each W tile is read once
+      for (int kt = 0; kt < k_tiles; ++kt) {
+        const int s = kt % stages;
+        const uint32_t ph = (kt / stages) & 1u;
+        if (*abort_flag ||
+            !mbar_wait_bounded(empty_bar(s), ph ^ 1u, args.status, DEV_TIMEOUT_GEMM_PRODUCER)) {
+          *abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(full_bar(s), A_STAGE + W_STAGE);
+        const int kx = (kt0 + kt) * BK;
+        tma_load_2d(smem_addr(a_st + s * A_STAGE), &tmA, kx, m0, full_bar(s), pol_a);
+        tma_load_2d(smem_addr(w_st + s * W_STAGE), &tmW, kx, n0, full_bar(s), pol_w);
+        ++issued;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = instr_desc<BN>();
+      for (int kt = 0; kt < k_tiles; ++kt) {
+        const int s = kt % stages;
+        const uint32_t ph = (kt / stages) & 1u;
+        if (*abort_flag ||
+            !mbar_wait_bounded(full_bar(s), ph, args.status, DEV_TIMEOUT_GEMM_MMA)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = smem_addr(a_st + s * A_STAGE);
+        const uint32_t w_addr = smem_addr(w_st + s * W_STAGE);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          umma_bf16(tmem, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(w_addr + kk * 32), idesc,
+                    (kt | kk) != 0 ? 1u : 0u);
+        }
+        umma_commit(empty_bar(s));  // the stage is free once these MMAs have read it
+      }
+      umma_commit(done_bar);
+    }
+    __syncwarp();
+  }
+
+  // ---- epilogue
+  const bool ok = mbar_wait_bounded(done_bar, 0, args.status, DEV_TIMEOUT_GEMM_EPILOGUE);
+  __syncwarp();
+  tc_fence_after();
+  const int row_local = warp * 32 + lane;
+  const int m = m0 + row_local;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const bool good = ok && !*abort_flag && k_tiles > 0;
+
+  if (splits == 1) {
+    if (good) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + c0, r);
+        if (m < args.M) {
+          if (args.c_f32) {
+            float* crow = static_cast<float*>(args.C) + m * args.ldc + n0 + c0;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              if (n0 + c0 + j < args.N)
+                *reinterpret_cast<uint4*>(crow + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+            }
+          } else {
+            __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(args.C) + m * args.ldc + n0 + c0;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              if (n0 + c0 + j < args.N) {
+                uint4 o;
+                o.x = pack_bf16(__uint_as_float(r[j + 0]), __uint_as_float(r[j + 1]));
+                o.y = pack_bf16(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+                o.z = pack_bf16(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
+                o.w = pack_bf16(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
+                *reinterpret_cast<uint4*>(crow + j) = o;
+              }
+            }
+          }
+        }
+      }
+    }
+  } else {
+    // Constant split-K: park this CTA's fp32 partial tile in its own shared
+    // memory (the stage ring is idle now), then rank q reduces rows
+    // [q * 128 / splits, (q + 1) * 128 / splits) over all ranks in rank order.
+    constexpr int LDR = BN + 1;
+    float* red = reinterpret_cast<float*>(base);
+    if (good) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(lane_base + c0, r);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) red[row_local * LDR + c0 + j] = __uint_as_float(r[j]);
+      }
+    }
+    cluster_sync();
+    const int rows_per = BM / splits;
+    const int rbase = rank * rows_per;
+    if (good) {
+      for (int idx = threadIdx.x; idx < rows_per * BN; idx += kGemmThreads) {
+        const int rl = rbase + idx / BN;
+        const int col = idx % BN;
+        const int mm = m0 + rl, nn = n0 + col;
+        if (mm >= args.M || nn >= args.N) continue;
+        const uint32_t local = smem_addr(red + rl * LDR + col);
+        float acc = ld_dsmem_f32(map_to_rank(local, 0));
+        for (int q = 1; q < splits; ++q) acc = __fadd_rn(acc, ld_dsmem_f32(map_to_rank(local, q)));
+        if (args.c_f32)
+          static_cast<float*>(args.C)[mm * args.ldc + nn] = acc;
+        else
+          static_cast<__nv_bfloat16*>(args.C)[mm * args.ldc + nn] = __float2bfloat16_rn(acc);
+      }
+    }
+    cluster_sync();  // no CTA leaves while another still reads its partial
+  }
+
+  // ---- teardown
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // give loads still in flight a bounded chance to land before the block exits
+    for (int kt = issued - stages > 0 ? issued - stages : 0; kt < issued; ++kt)
+      mbar_wait_bounded(full_bar(kt % stages), (kt / stages) & 1u, nullptr, 0);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+              int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Plan {
+  int bn, splits, stages;
+};
+
+// The tile width and the K split depend on (N, K) only -- never on M -- so
+// every row meets the same reduction order whatever the batch.  They are
+// chosen to put at least two CTAs per SM in flight for a skinny (decode) M.
+Plan plan_for(int N, int K) {
+  const int kt = K / BK;
+  const int target = 2 * 148;
+  Plan p{64, 1, 4};
+  if (N / 128 >= target) p = Plan{128, 1, 3};
+  const int tiles = (N + p.bn - 1) / p.bn;
+  int s = 1;
+  while (s < 8 && tiles * s < target && kt % (2 * s) == 0 && kt / (2 * s) >= 4) s *= 2;
+  p.splits = s;
+  return p;
+}
+
+template <int BN>
+size_t smem_bytes(int stages) {
+  return 1024 + static_cast<size_t>(stages) * (A_STAGE + BN * BK * 2) + (2 * stages + 1) * 8 + 16;
+}
+
+template <int BN>
+kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, const GemmArgs& a, int grid_y,
+                        int grid_z, cudaStream_t stream) {
+  const size_t smem = smem_bytes<BN>(a.stages);
+  if (a.splits > 1 && static_cast<size_t>(BM) * (BN + 1) * 4 > static_cast<size_t>(a.stages) * (A_STAGE + BN * BK * 2))
+    return KINV_ERR_UNSUPPORTED;
+  static bool configured[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KINV_ERR_CUDA;
+  if (dev < 64 && !configured[dev]) {
+    if (cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes<BN>(8))) != cudaSuccess)
+      return KINV_ERR_CUDA;
+    configured[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.splits, grid_y, grid_z);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.splits > 1 ? 1 : 0;
+  return cuda_status(cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, ta, tw, a));
+}
+
+}  // namespace
+}  // namespace kinv
+
+using namespace kinv;
+
+extern "C" kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int64_t ldw, void* C,
+                                 int64_t ldc, kinv_dtype c_dtype, int M, int N, int K,
+                                 kinv_stream stream) {
+  if (M < 0 || N <= 0 || K <= 0) return KINV_ERR_INVALID_ARG;
+  if (c_dtype != KINV_BF16 && c_dtype != KINV_F32) return KINV_ERR_INVALID_ARG;
+  if (M == 0) return KINV_OK;
+  if (!A || !W || !C) return KINV_ERR_INVALID_ARG;
+  if (K % BK || N % 16) return KINV_ERR_UNSUPPORTED;
+  if (lda < K || ldw < K || ldc < N) return KINV_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(C) || lda % 8 || ldw % 8 ||
+      (c_dtype == KINV_BF16 ? ldc % 8 : ldc % 4))
+    return KINV_ERR_ALIGNMENT;
+  const Plan p = plan_for(N, K);
+  const int grid_y = (N + p.bn - 1) / p.bn;
+  const int grid_z = (M + BM - 1) / BM;
+  if (grid_y > 65535 || grid_z > 65535) return KINV_ERR_UNSUPPORTED;
+  CUtensorMap ta, tw;
+  if (!make_map(&ta, A, M, K, lda, BM) || !make_map(&tw, W, N, K, ldw, p.bn)) return KINV_ERR_CUDA;
+  GemmArgs a;
+  a.C = C;
+  a.ldc = ldc;
+  a.M = M;
+  a.N = N;
+  a.k_tiles = K / BK / p.splits;
+  a.c_f32 = c_dtype == KINV_F32;
+  a.stages = p.stages;
+  a.splits = p.splits;
+  a.status = device_status_word();
+  switch (p.bn) {
+    case 64: return launch_gemm<64>(ta, tw, a, grid_y, grid_z, stream);
+    case 128: return launch_gemm<128>(ta, tw, a, grid_y, grid_z, stream);
+    default: return KINV_ERR_UNSUPPORTED;
+  }
+}

@@ -1,0 +1,246 @@
+// Element-wise glue of the decoder block: embedding gather, residual add,
+// SwiGLU, rotary embedding with the key/value append, and the per-step
+// bookkeeping of a decode loop.  None of these sums across elements except
+// the optional per-head RMSNorm in kinv_rope_append, whose order is fixed
+// per head exactly as in kinv_rmsnorm's scheme (per-lane, butterfly, lane 0).
+#include <math.h>
+
+#include "common.cuh"
+
+namespace kinv {
+namespace {
+
+__global__ void embed_kernel(const uint4* __restrict__ table, int vocab, int dim8,
+                             const int32_t* __restrict__ ids, uint4* __restrict__ out) {
+  const int r = blockIdx.x;
+  const int id = ids[r];
+  for (int c = threadIdx.x; c < dim8; c += blockDim.x) {
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (id >= 0 && id < vocab) v = table[static_cast<int64_t>(id) * dim8 + c];
+    out[static_cast<int64_t>(r) * dim8 + c] = v;
+  }
+}
+
+// out may alias x or y: each element is read before it is written, by the
+// same thread.
+__global__ void add_kernel(const uint4* x, const uint4* y, uint4* out, int64_t n8) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 a = x[i], b = y[i];
+    uint4 o;
+    o.x = pack_bf16(bf16_lo(a.x) + bf16_lo(b.x), bf16_hi(a.x) + bf16_hi(b.x));
+    o.y = pack_bf16(bf16_lo(a.y) + bf16_lo(b.y), bf16_hi(a.y) + bf16_hi(b.y));
+    o.z = pack_bf16(bf16_lo(a.z) + bf16_lo(b.z), bf16_hi(a.z) + bf16_hi(b.z));
+    o.w = pack_bf16(bf16_lo(a.w) + bf16_lo(b.w), bf16_hi(a.w) + bf16_hi(b.w));
+    out[i] = o;
+  }
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+__global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ gu, int64_t ld_gu,
+                              __nv_bfloat16* __restrict__ out, int64_t ld_out, int F) {
+  const int r = blockIdx.y;
+  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
+  if (c >= F) return;
+  const uint4 g = *reinterpret_cast<const uint4*>(gu + r * ld_gu + c);
+  const uint4 u = *reinterpret_cast<const uint4*>(gu + r * ld_gu + F + c);
+  uint4 o;
+  o.x = pack_bf16(silu_mul(bf16_lo(g.x), bf16_lo(u.x)), silu_mul(bf16_hi(g.x), bf16_hi(u.x)));
+  o.y = pack_bf16(silu_mul(bf16_lo(g.y), bf16_lo(u.y)), silu_mul(bf16_hi(g.y), bf16_hi(u.y)));
+  o.z = pack_bf16(silu_mul(bf16_lo(g.z), bf16_lo(u.z)), silu_mul(bf16_hi(g.z), bf16_hi(u.z)));
+  o.w = pack_bf16(silu_mul(bf16_lo(g.w), bf16_lo(u.w)), silu_mul(bf16_hi(g.w), bf16_hi(u.w)));
+  *reinterpret_cast<uint4*>(out + r * ld_out + c) = o;
+}
+
+// One block per row.  The first D/2 threads compute this row's rotation
+// angles in fp64 (theta_i = p * base^(-2i/D)) into shared memory; then each
+// warp takes whole heads.  Lane l of a warp holds the pairs
+// (i, i + D/2) for i in {l * P .. l * P + P - 1}, P = D / 64.
+template <int D>
+__global__ void rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int64_t ld_qkv,
+                                   __nv_bfloat16* __restrict__ q_out,
+                                   __nv_bfloat16* __restrict__ k_cache,
+                                   __nv_bfloat16* __restrict__ v_cache, int64_t seq_stride,
+                                   int64_t tok_stride, const int32_t* __restrict__ seq,
+                                   const int32_t* __restrict__ pos,
+                                   const __nv_bfloat16* __restrict__ q_norm,
+                                   const __nv_bfloat16* __restrict__ k_norm, float eps, int Hq,
+                                   int Hkv, double rope_base) {
+  constexpr int HALF = D / 2;
+  constexpr int P = D / 64;  // pairs per lane
+  __shared__ float cs[HALF], sn[HALF];
+  const int r = blockIdx.x;
+  const int p = pos[r];
+  const int s = seq[r];
+  for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
+    const double inv_freq = pow(rope_base, -2.0 * i / D);
+    double sv, cv;
+    sincos(static_cast<double>(p) * inv_freq, &sv, &cv);
+    cs[i] = static_cast<float>(cv);
+    sn[i] = static_cast<float>(sv);
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const __nv_bfloat16* row = qkv + r * ld_qkv;
+  __nv_bfloat16* kdst_row = k_cache + s * seq_stride + p * tok_stride;
+  __nv_bfloat16* vdst_row = v_cache + s * seq_stride + p * tok_stride;
+  const int heads = Hq + 2 * Hkv;
+  for (int h = warp; h < heads; h += nwarps) {
+    const __nv_bfloat16* src = row + h * D;
+    if (h >= Hq + Hkv) {  // value head: copy bits
+      const int g = h - Hq - Hkv;
+      for (int c = lane; c < D / 8; c += 32)
+        reinterpret_cast<uint4*>(vdst_row + g * D)[c] = reinterpret_cast<const uint4*>(src)[c];
+      continue;
+    }
+    float a[P], b[P];
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+      a[j] = __bfloat162float(src[lane * P + j]);
+      b[j] = __bfloat162float(src[HALF + lane * P + j]);
+    }
+    const __nv_bfloat16* nw = h < Hq ? q_norm : k_norm;
+    if (nw) {
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < P; ++j) acc = fmaf(a[j], a[j], acc);
+#pragma unroll
+      for (int j = 0; j < P; ++j) acc = fmaf(b[j], b[j], acc);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      acc = __shfl_sync(0xffffffffu, acc, 0);
+      const float inv = 1.0f / sqrtf(acc / static_cast<float>(D) + eps);
+#pragma unroll
+      for (int j = 0; j < P; ++j) {
+        a[j] = a[j] * inv * __bfloat162float(nw[lane * P + j]);
+        b[j] = b[j] * inv * __bfloat162float(nw[HALF + lane * P + j]);
+      }
+    }
+    __nv_bfloat16* dst = h < Hq ? q_out + (static_cast<int64_t>(r) * Hq + h) * D
+                                : kdst_row + (h - Hq) * D;
+#pragma unroll
+    for (int j = 0; j < P; ++j) {
+      const int i = lane * P + j;
+      const float c = cs[i], sv = sn[i];
+      dst[i] = __float2bfloat16_rn(a[j] * c - b[j] * sv);
+      dst[HALF + i] = __float2bfloat16_rn(b[j] * c + a[j] * sv);
+    }
+  }
+}
+
+__global__ void decode_advance_kernel(const int32_t* __restrict__ tokens, int32_t* history,
+                                      int hist_ld, int32_t* hist_len, int64_t* step, int32_t* pos,
+                                      int32_t* kv_len, int B) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  int32_t* h = history + static_cast<int64_t>(b) * hist_ld;
+  int n = hist_len[b];
+  if (n >= hist_ld) {
+    for (int i = 1; i < hist_ld; ++i) h[i - 1] = h[i];
+    n = hist_ld - 1;
+  }
+  h[n] = tokens[b];
+  hist_len[b] = n + 1;
+  step[b] += 1;
+  if (pos) pos[b] += 1;
+  if (kv_len) kv_len[b] += 1;
+}
+
+}  // namespace
+}  // namespace kinv
+
+using namespace kinv;
+
+extern "C" kinv_status kinv_embed(const void* table, int vocab, int dim, const int32_t* ids,
+                                  void* out, int rows, kinv_stream stream) {
+  if (rows < 0 || vocab <= 0 || dim <= 0) return KINV_ERR_INVALID_ARG;
+  if (rows == 0) return KINV_OK;
+  if (!table || !ids || !out) return KINV_ERR_INVALID_ARG;
+  if (dim % 8) return KINV_ERR_UNSUPPORTED;
+  if (!aligned16(table) || !aligned16(out)) return KINV_ERR_ALIGNMENT;
+  const int dim8 = dim / 8;
+  embed_kernel<<<rows, dim8 < 256 ? 32 * ((dim8 + 31) / 32) : 256, 0, stream>>>(
+      static_cast<const uint4*>(table), vocab, dim8, ids, static_cast<uint4*>(out));
+  return launch_status();
+}
+
+extern "C" kinv_status kinv_add(const void* x, const void* y, void* out, int64_t n,
+                                kinv_stream stream) {
+  if (n < 0) return KINV_ERR_INVALID_ARG;
+  if (n == 0) return KINV_OK;
+  if (!x || !y || !out) return KINV_ERR_INVALID_ARG;
+  if (n % 8) return KINV_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(out)) return KINV_ERR_ALIGNMENT;
+  const int64_t n8 = n / 8;
+  const int64_t blocks = (n8 + 255) / 256;
+  const int grid = static_cast<int>(blocks < 4096 ? blocks : 4096);
+  add_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), static_cast<const uint4*>(y),
+                                       static_cast<uint4*>(out), n8);
+  return launch_status();
+}
+
+extern "C" kinv_status kinv_swiglu(const void* gu, int64_t ld_gu, void* out, int64_t ld_out,
+                                   int rows, int F, kinv_stream stream) {
+  if (rows < 0 || F <= 0) return KINV_ERR_INVALID_ARG;
+  if (rows == 0) return KINV_OK;
+  if (!gu || !out) return KINV_ERR_INVALID_ARG;
+  if (F % 8) return KINV_ERR_UNSUPPORTED;
+  if (ld_gu < 2 * static_cast<int64_t>(F) || ld_out < F) return KINV_ERR_INVALID_ARG;
+  if (!aligned16(gu) || !aligned16(out) || ld_gu % 8 || ld_out % 8) return KINV_ERR_ALIGNMENT;
+  if (rows > 65535) return KINV_ERR_UNSUPPORTED;
+  dim3 grid((F / 8 + 127) / 128, rows);
+  swiglu_kernel<<<grid, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(gu), ld_gu,
+                                          static_cast<__nv_bfloat16*>(out), ld_out, F);
+  return launch_status();
+}
+
+extern "C" kinv_status kinv_rope_append(const void* qkv, int64_t ld_qkv, void* q_out,
+                                        void* k_cache, void* v_cache, int64_t seq_stride,
+                                        int64_t tok_stride, const int32_t* seq,
+                                        const int32_t* pos, const void* q_norm,
+                                        const void* k_norm, float eps, int rows, int Hq, int Hkv,
+                                        int D, float rope_base, kinv_stream stream) {
+  if (rows < 0 || Hq <= 0 || Hkv <= 0 || !(rope_base > 0.f) || !(eps >= 0.f))
+    return KINV_ERR_INVALID_ARG;
+  if (rows == 0) return KINV_OK;
+  if (!qkv || !q_out || !k_cache || !v_cache || !seq || !pos) return KINV_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return KINV_ERR_UNSUPPORTED;
+  if (ld_qkv < static_cast<int64_t>(Hq + 2 * Hkv) * D || tok_stride < static_cast<int64_t>(Hkv) * D ||
+      seq_stride < 0)
+    return KINV_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(q_out) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      ld_qkv % 8 || seq_stride % 8 || tok_stride % 8)
+    return KINV_ERR_ALIGNMENT;
+  const int heads = Hq + 2 * Hkv;
+  int threads = 32 * (heads < 8 ? heads : 8);
+  if (threads < 64) threads = 64;
+  auto* k = static_cast<__nv_bfloat16*>(k_cache);
+  auto* v = static_cast<__nv_bfloat16*>(v_cache);
+  auto* src = static_cast<const __nv_bfloat16*>(qkv);
+  auto* qo = static_cast<__nv_bfloat16*>(q_out);
+  auto* qn = static_cast<const __nv_bfloat16*>(q_norm);
+  auto* kn = static_cast<const __nv_bfloat16*>(k_norm);
+  if (D == 128)
+    rope_append_kernel<128><<<rows, threads, 0, stream>>>(src, ld_qkv, qo, k, v, seq_stride,
+                                                         tok_stride, seq, pos, qn, kn, eps, Hq,
+                                                         Hkv, static_cast<double>(rope_base));
+  else
+    rope_append_kernel<64><<<rows, threads, 0, stream>>>(src, ld_qkv, qo, k, v, seq_stride,
+                                                        tok_stride, seq, pos, qn, kn, eps, Hq, Hkv,
+                                                        static_cast<double>(rope_base));
+  return launch_status();
+}
+
+extern "C" kinv_status kinv_decode_advance(const int32_t* tokens, int32_t* history, int hist_ld,
+                                           int32_t* hist_len, int64_t* step, int32_t* pos,
+                                           int32_t* kv_len, int B, kinv_stream stream) {
+  if (B < 0 || hist_ld <= 0) return KINV_ERR_INVALID_ARG;
+  if (B == 0) return KINV_OK;
+  if (!tokens || !history || !hist_len || !step) return KINV_ERR_INVALID_ARG;
+  decode_advance_kernel<<<(B + 127) / 128, 128, 0, stream>>>(tokens, history, hist_ld, hist_len,
+                                                             step, pos, kv_len, B);
+  return launch_status();
+}

@@ -1,0 +1,200 @@
+"""Decoder drivers over the kinv C ABI: a pre-norm decoder (RMSNorm, QKV GEMM,
+RoPE + KV append, split-KV attention, O GEMM, residual RMSNorm, gate/up GEMM,
+SwiGLU, down GEMM), an untied LM head and the seeded sampler.
+
+Every arithmetic step is a kinv kernel; this module only owns buffers and
+issues the calls in order on the current CUDA stream, so a whole decode step
+can be captured into a CUDA graph.  The residual add that closes one layer is
+fused into the RMSNorm that opens the next (and into the final norm).
+
+Layouts (all bf16 unless noted):
+  embed, lm_head [V][d]; per layer w_qkv [(Hq + 2 Hkv) D][d], w_o [d][Hq D],
+  w_gu [2F][d] (gate rows then up rows), w_down [d][F], norm gains [d] / [D];
+  KV cache [layers][2][B][Lmax][Hkv][D] (k then v), token-major per sequence.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+from . import kinv, synth
+
+
+@dataclass
+class ModelShape:
+    d_model: int
+    n_q: int
+    n_kv: int
+    head_dim: int
+    ffn: int
+    vocab: int
+    n_layers: int
+    eps: float = 1e-6
+    rope_base: float = 1e4
+    qk_norm: bool = False
+
+    @property
+    def qkv_dim(self) -> int:
+        return (self.n_q + 2 * self.n_kv) * self.head_dim
+
+
+TINY = ModelShape(d_model=256, n_q=4, n_kv=2, head_dim=64, ffn=512, vocab=512, n_layers=1,
+                  rope_base=1e4, qk_norm=False)
+# Qwen3-8B-shaped: 36 layers, d 4096, 32 query / 8 kv heads of 128, FFN 12288,
+# vocab 151936; QK-norm on; RoPE base 1e6.
+QWEN3_8B = ModelShape(d_model=4096, n_q=32, n_kv=8, head_dim=128, ffn=12288, vocab=151936,
+                      n_layers=36, rope_base=1e6, qk_norm=True)
+
+
+def random_weights(shape: ModelShape, seed: int = synth.SEED_WEIGHTS, device="cuda",
+                   with_head: bool = True) -> dict:
+    """Projections ~N(0, 0.02) bf16, gains 1 (drawn with seeded generators on
+    ``device``)."""
+    w = {"layers": [synth.layer_weights(shape.d_model, shape.n_q, shape.n_kv, shape.head_dim,
+                                        shape.ffn, seed * 1000 + li, shape.qk_norm, device)
+                    for li in range(shape.n_layers)]}
+    if with_head:
+        w["embed"] = synth.normal_bf16((shape.vocab, shape.d_model), 0.02, seed * 1000 + 997, device)
+        w["lm_head"] = synth.normal_bf16((shape.vocab, shape.d_model), 0.02, seed * 1000 + 998, device)
+        w["final_norm"] = torch.ones(shape.d_model, dtype=torch.bfloat16, device=device)
+    return w
+
+
+class Decoder:
+    """Owns weights, the KV cache and every activation buffer for up to
+    ``max_batch`` sequences of up to ``max_len`` tokens (and prefill chunks of
+    up to ``max_chunk`` rows)."""
+
+    def __init__(self, shape: ModelShape, weights: dict, max_batch: int, max_len: int,
+                 max_chunk: int = 0, device="cuda"):
+        self.s = shape
+        self.w = weights
+        self.B = max_batch
+        self.Lmax = max_len
+        self.dev = torch.device(device)
+        s = shape
+        rows = max(max_batch, max_chunk)
+        self.max_rows = rows
+        bf = dict(dtype=torch.bfloat16, device=self.dev)
+        self.kv = torch.zeros(s.n_layers, 2, max_batch, max_len, s.n_kv, s.head_dim, **bf)
+        self.x = torch.zeros(rows, s.d_model, **bf)
+        self.h = torch.zeros(rows, s.d_model, **bf)
+        self.qkv = torch.zeros(rows, s.qkv_dim, **bf)
+        self.q = torch.zeros(rows, s.n_q, s.head_dim, **bf)
+        self.attn = torch.zeros(rows, s.n_q, s.head_dim, **bf)
+        self.o = torch.zeros(rows, s.d_model, **bf)
+        self.gu = torch.zeros(rows, 2 * s.ffn, **bf)
+        self.act = torch.zeros(rows, s.ffn, **bf)
+        self.delta = torch.zeros(rows, s.d_model, **bf)
+        ws = kinv.attn_decode_workspace(max_batch, s.n_q, s.head_dim, max_len)
+        if max_chunk:
+            ws = max(ws, kinv.attn_prefill_workspace(max_chunk, s.n_q, s.head_dim, max_len))
+        self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=self.dev)
+        i32 = dict(dtype=torch.int32, device=self.dev)
+        # decode state: row b is sequence b at position pos[b]; attention sees pos[b] + 1 keys
+        self.seq = torch.arange(max_batch, **i32)
+        self.pos = torch.zeros(max_batch, **i32)
+        self.kv_len = torch.ones(max_batch, **i32)
+        if "lm_head" in weights:
+            self.logits = torch.zeros(max_batch, s.vocab, dtype=torch.float32, device=self.dev)
+        self.tokens = torch.zeros(max_batch, **i32)
+        self.hist_ld = 64
+        self.history = torch.zeros(max_batch, self.hist_ld, **i32)
+        self.hist_len = torch.zeros(max_batch, **i32)
+        self.step = torch.zeros(max_batch, dtype=torch.int64, device=self.dev)
+        self.params = torch.zeros(max_batch * 32, dtype=torch.uint8, device=self.dev)
+
+    # ------------------------------------------------------------ state setup
+    def set_sampling(self, params_list) -> None:
+        packed = synth.sampling_struct(params_list)
+        self.params[: packed.nbytes].copy_(torch.from_numpy(packed.view(np.uint8)))
+
+    def set_positions(self, pos) -> None:
+        """pos[b]: index of the token to decode next (= tokens already cached)."""
+        p = torch.as_tensor(pos, dtype=torch.int32)
+        self.pos[: len(p)].copy_(p)
+        self.kv_len[: len(p)].copy_(p + 1)
+
+    def set_history(self, hist_rows) -> None:
+        """hist_rows[b]: the request's tokens so far (prompt and output)."""
+        for b, row in enumerate(hist_rows):
+            tail = list(row)[-self.hist_ld:]
+            self.history[b, : len(tail)] = torch.tensor(tail, dtype=torch.int32)
+            self.hist_len[b] = len(tail)
+
+    # --------------------------------------------------------------- a layer
+    def layer(self, li: int, rows: int, first: bool, attention) -> None:
+        """One decoder layer on rows [0, rows) of the activation buffers.
+        ``x`` holds the residual stream and ``delta`` the previous layer's
+        FFN output (not yet added unless ``first``)."""
+        s, lw = self.s, self.w["layers"][li]
+        x, h = self.x[:rows], self.h[:rows]
+        kinv.rmsnorm(x, lw["attn_norm"], s.eps, residual=None if first else self.delta[:rows], out=h)
+        kinv.gemm(h, lw["w_qkv"], out=self.qkv[:rows])
+        kc, vc = self.kv[li, 0], self.kv[li, 1]
+        attention(li, rows, kc, vc)
+        kinv.gemm(self.attn[:rows].view(rows, -1), lw["w_o"], out=self.o[:rows])
+        kinv.rmsnorm(x, lw["ffn_norm"], s.eps, residual=self.o[:rows], out=h)
+        kinv.gemm(h, lw["w_gu"], out=self.gu[:rows])
+        kinv.swiglu(self.gu[:rows], out=self.act[:rows])
+        kinv.gemm(self.act[:rows], lw["w_down"], out=self.delta[:rows])
+
+    def _rope(self, li, rows, kc, vc, seq, pos):
+        s, lw = self.s, self.w["layers"][li]
+        kinv.rope_append(self.qkv[:rows], self.q[:rows], kc, vc, seq, pos, s.n_q, s.n_kv,
+                         s.head_dim, s.rope_base, lw.get("q_norm") if s.qk_norm else None,
+                         lw.get("k_norm") if s.qk_norm else None, s.eps)
+
+    # ---------------------------------------------------------------- decode
+    def decode_layers(self, bsz: int) -> None:
+        """All layers for one new token of sequences 0..bsz-1 (rows = bsz);
+        the token's hidden state must be in x; leaves the final residual
+        pieces in x and delta."""
+        def attention(li, rows, kc, vc):
+            self._rope(li, rows, kc, vc, self.seq[:rows], self.pos[:rows])
+            kinv.attn_decode(self.q[:rows], kc[:rows], vc[:rows], self.kv_len[:rows],
+                             out=self.attn[:rows], workspace=self.ws)
+        for li in range(self.s.n_layers):
+            self.layer(li, bsz, li == 0, attention)
+
+    def decode_step(self, bsz: int, sample: bool = True) -> None:
+        """Embed tokens[:bsz], run every layer, the final norm, the LM head
+        and (optionally) the sampler, then advance positions and histories.
+        The sampled ids land in ``tokens`` (they are the next step's input)."""
+        s = self.s
+        kinv.embed(self.w["embed"], self.tokens[:bsz], out=self.x[:bsz])
+        self.decode_layers(bsz)
+        kinv.rmsnorm(self.x[:bsz], self.w["final_norm"], s.eps, residual=self.delta[:bsz],
+                     out=self.h[:bsz])
+        kinv.gemm(self.h[:bsz], self.w["lm_head"], out=self.logits[:bsz])
+        if sample:
+            kinv.sample(self.logits[:bsz], self.params, self.history[:bsz], self.hist_len[:bsz],
+                        self.step[:bsz], out=self.tokens[:bsz])
+            kinv.decode_advance(self.tokens[:bsz], self.history[:bsz], self.hist_len[:bsz],
+                                self.step[:bsz], pos=self.pos[:bsz], kv_len=self.kv_len[:bsz])
+
+    # --------------------------------------------------------------- prefill
+    def prefill_chunk(self, seq: int, p0: int, rows: int) -> None:
+        """All layers for rows [0, rows) of x, which hold tokens p0..p0+rows-1
+        of sequence ``seq``; their keys and values go into the cache."""
+        i32 = dict(dtype=torch.int32, device=self.dev)
+        seq_t = torch.full((rows,), seq, **i32)
+        pos_t = torch.arange(p0, p0 + rows, **i32)
+        q_start = torch.tensor([p0], **i32)
+        q_len = torch.tensor([rows], **i32)
+        q_off = torch.zeros(1, **i32)
+
+        def attention(li, n, kc, vc):
+            self._rope(li, n, kc, vc, seq_t, pos_t)
+            # a one-sequence view of the cache keeps the sequence index at 0
+            kinv.attn_prefill(self.q[:n], kc[seq: seq + 1], vc[seq: seq + 1], q_start, q_len,
+                              q_off, n, p0 + n, out=self.attn[:n], workspace=self.ws)
+        for li in range(self.s.n_layers):
+            self.layer(li, rows, li == 0, attention)
+
+    def close_residual(self, rows: int) -> torch.Tensor:
+        """x <- bf16(x + delta) for rows [0, rows): the last layer's output."""
+        kinv.add(self.x[:rows], self.delta[:rows], out=self.x[:rows])
+        return self.x[:rows]

@@ -1,0 +1,120 @@
+"""kinv_gemm on the GPU: exactness, oracle parity and batch invariance."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import assert_close, assert_same_bits, ensure_lib, f64, gpu, synth
+from oracle import bf16 as obf
+from oracle.gemm import gemm as ogemm, gemm_f64_rows
+
+pytestmark = gpu
+
+
+@pytest.fixture(scope="module")
+def kinv():
+    return ensure_lib()
+
+
+def _int_bf16(shape, seed, lo=-8, hi=8):
+    return synth.int_bf16(shape, lo, hi, seed).cuda()
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 64, 64), (7, 80, 256), (130, 128, 512), (300, 208, 1024),
+                                   (5, 4096, 4096), (129, 6144, 4096), (3, 4096, 12288)])
+def test_integer_inputs_are_exact(kinv, m, n, k):
+    """Integer inputs in [-8, 8]: every partial sum is an integer below 2^24,
+    so fp32 accumulation is exact in any order and the result must equal the
+    exact product (fp32 out) or its bf16 rounding (bf16 out)."""
+    a = _int_bf16((m, k), 1)
+    w = _int_bf16((n, k), 2)
+    exact = ogemm(synth.bits(a), synth.bits(w), out="f64")
+    c32 = kinv.gemm(a, w, out_dtype=torch.float32)
+    assert np.array_equal(f64(c32), exact)
+    c16 = kinv.gemm(a, w)
+    assert np.array_equal(synth.bits(c16), obf.from_f64(exact))
+    assert kinv.last_device_status() == 0
+
+
+def test_identity_weights_copy_rows(kinv):
+    a = synth.normal_bf16((33, 256), 1.0, 3).cuda()
+    eye = torch.eye(256, dtype=torch.bfloat16, device="cuda")
+    assert_same_bits(kinv.gemm(a, eye), a, "A . I")
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 512, 256), (4, 256, 512), (37, 1024, 256), (200, 96, 640)])
+def test_parity_random(kinv, m, n, k):
+    a = synth.normal_bf16((m, k), 1.0, 4).cuda()
+    w = synth.normal_bf16((n, k), 0.02, 5).cuda()
+    got = kinv.gemm(a, w)
+    ref = ogemm(synth.bits(a), synth.bits(w))
+    assert_close(f64(got), obf.to_f64(ref), f"gemm {m}x{n}x{k}")
+    got32 = kinv.gemm(a, w, out_dtype=torch.float32)
+    assert_close(f64(got32), ogemm(synth.bits(a), synth.bits(w), out="f64"), "gemm f32 out")
+
+
+# Qwen3-8B-shaped projections: (N, K)
+SHAPES_8B = [(6144, 4096), (4096, 4096), (24576, 4096), (4096, 12288)]
+MS = [1, 7, 16, 64, 128, 256]
+
+
+@pytest.mark.parametrize("n,k", SHAPES_8B)
+def test_8b_shapes_row_bits_independent_of_m(kinv, n, k):
+    """Row i's bits are the same for M in {1, 7, 16, 64, 128, 256} and for any
+    co-batched rows; sampled outputs match the oracle."""
+    w = synth.normal_bf16((n, k), 0.02, 6).cuda()
+    a = synth.normal_bf16((256, k), 1.0, 7).cuda()
+    full = kinv.gemm(a, w)
+    for m in MS:
+        part = kinv.gemm(a[:m].contiguous(), w)
+        assert_same_bits(part, full[:m], f"N={n} K={k} M={m}")
+    # the same rows among different batch-mates, at other positions
+    other = synth.normal_bf16((256, k), 1.0, 8).cuda()
+    perm = torch.randperm(256, generator=synth.gen(9))
+    mixed = other.clone()
+    mixed[perm[:64]] = a[:64]
+    got = kinv.gemm(mixed, w)
+    assert_same_bits(got[perm[:64]], full[:64], "rows among other batch-mates")
+    # oracle on sampled rows and columns
+    rows = [0, 1, 6, 15, 63, 127, 128, 255]
+    cols = torch.randint(0, n, (64,), generator=synth.gen(10)).numpy()
+    ref = gemm_f64_rows(synth.bits(a), synth.bits(w), rows, cols)
+    assert_close(f64(full)[rows][:, cols], obf.round_f64(ref), f"oracle N={n} K={k}")
+    assert kinv.last_device_status() == 0
+
+
+def test_lm_head_fp32_row_invariance(kinv):
+    n, k = 151936, 4096
+    w = synth.normal_bf16((n, k), 0.02, 11).cuda()
+    a = synth.normal_bf16((16, k), 1.0, 12).cuda()
+    full = kinv.gemm(a, w, out_dtype=torch.float32)
+    one = kinv.gemm(a[3:4].contiguous(), w, out_dtype=torch.float32)
+    assert_same_bits(one, full[3:4], "LM head row 3")
+    cols = torch.randint(0, n, (128,), generator=synth.gen(13)).numpy()
+    ref = gemm_f64_rows(synth.bits(a), synth.bits(w), [0, 3, 15], cols)
+    assert_close(f64(full)[[0, 3, 15]][:, cols], ref, "LM head vs oracle", atol=1e-4, rtol=1e-4)
+
+
+def test_prefill_sized_m(kinv):
+    """M up to 4096 (prefill chunks) keeps the same row bits."""
+    n, k = 4096, 4096
+    w = synth.normal_bf16((n, k), 0.02, 14).cuda()
+    a = synth.normal_bf16((4096, k), 1.0, 15).cuda()
+    full = kinv.gemm(a, w)
+    for m0, m in [(0, 1), (4095, 1), (512, 512), (1000, 64)]:
+        part = kinv.gemm(a[m0: m0 + m].contiguous(), w)
+        assert_same_bits(part, full[m0: m0 + m], f"rows {m0}..{m0 + m}")
+
+
+def test_errors_before_launch(kinv):
+    a = torch.zeros(4, 100, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(64, 100, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(kinv.KinvError) as e:
+        kinv.gemm(a, w)
+    assert e.value.status == kinv.ERR_UNSUPPORTED
+    a = torch.zeros(4, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(24, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(kinv.KinvError):
+        kinv.gemm(a, w)
+    m0 = kinv.gemm(torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda"),
+                   torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda"))
+    assert m0.shape == (0, 64)

@@ -1,0 +1,144 @@
+"""kinv_sample on the GPU: token parity with the oracle, bit-exactness across
+batch composition, ties, greedy and the unsupported-settings path."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import ensure_lib, gpu, synth
+from oracle.sampler import SamplingParams as OParams, sample_row
+
+pytestmark = gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "receipt_sampling.json")
+
+
+@pytest.fixture(scope="module")
+def kinv():
+    return ensure_lib()
+
+
+def _receipt_params():
+    with open(GOLDEN) as fh:
+        g = json.load(fh)
+    return dict(temperature=g["temperature"], top_k=g["top_k"], top_p=g["top_p"],
+                min_p=g["min_p"], repeat_penalty=g["repeat_penalty"],
+                repeat_last_n=g["repeat_last_n"], seed=g["seed"])
+
+
+def _run(kinv, logits, plist, hists, steps, hist_ld=64):
+    bsz = logits.shape[0]
+    packed = synth.sampling_struct(plist)
+    pdev = torch.from_numpy(packed.view(np.uint8).copy()).cuda()
+    hist = torch.zeros(bsz, hist_ld, dtype=torch.int32)
+    hl = torch.zeros(bsz, dtype=torch.int32)
+    for b, h in enumerate(hists):
+        h = list(h)[-hist_ld:]
+        hist[b, : len(h)] = torch.tensor(h, dtype=torch.int32)
+        hl[b] = len(h)
+    st = torch.tensor(steps, dtype=torch.int64)
+    return kinv.sample(logits, pdev, hist.cuda(), hl.cuda(), st.cuda()).cpu().numpy()
+
+
+def _oracle(logits, plist, hists, steps):
+    z = logits.cpu().numpy()
+    toks, ties = [], []
+    for b in range(z.shape[0]):
+        p = OParams(**{k: getattr(plist[b], k) for k in OParams.__dataclass_fields__})
+        t, n = sample_row(z[b], list(hists[b])[-64:], steps[b], p)
+        toks.append(t)
+        ties.append(n)
+    return np.array(toks), np.array(ties)
+
+
+@pytest.mark.parametrize("sigma", [1.3, 5.0])
+def test_token_parity_receipt_settings(kinv, sigma):
+    bsz, vocab = 64, 151936
+    g = synth.gen(70)
+    logits = (torch.randn(bsz, vocab, generator=g) * sigma).cuda()
+    base = _receipt_params()
+    plist = [kinv.SamplingParams(**{**base, "seed": 1000 + b}) for b in range(bsz)]
+    hists = [torch.randint(0, vocab, (int(torch.randint(0, 100, (1,), generator=g)),), generator=g).tolist()
+             for _ in range(bsz)]
+    # make the penalty matter: put some history ids at the top
+    for b in range(0, bsz, 4):
+        top = torch.topk(logits[b], 3).indices.cpu().tolist()
+        hists[b] = hists[b] + top
+    steps = [int(s) for s in torch.randint(0, 10 ** 6, (bsz,), generator=g)]
+    got = _run(kinv, logits, plist, hists, steps)
+    ref, ties = _oracle(logits, plist, hists, steps)
+    ok = ~ties
+    assert ties.sum() <= 2, f"{ties.sum()} near ties"
+    assert np.array_equal(got[ok], ref[ok]), np.nonzero(got != ref)
+    assert kinv.last_device_status() == 0
+
+
+def test_setting_variants(kinv):
+    vocab = 151936
+    g = synth.gen(71)
+    variants = [
+        dict(temperature=0.0, top_k=50, top_p=0.95, min_p=0.05, repeat_penalty=1.1, repeat_last_n=64),
+        dict(temperature=1.0, top_k=1, top_p=1.0, min_p=0.0, repeat_penalty=1.0, repeat_last_n=0),
+        dict(temperature=1.5, top_k=1024, top_p=1.0, min_p=0.0, repeat_penalty=1.3, repeat_last_n=-1),
+        dict(temperature=0.7, top_k=200, top_p=0.5, min_p=0.0, repeat_penalty=1.0, repeat_last_n=64),
+        dict(temperature=0.7, top_k=200, top_p=1.0, min_p=0.2, repeat_penalty=0.9, repeat_last_n=8),
+        dict(temperature=2.0, top_k=vocab + 5, top_p=1.0, min_p=0.0, repeat_penalty=1.0, repeat_last_n=0),
+    ]
+    plist, hists, steps = [], [], []
+    for i, v in enumerate(variants):
+        for j in range(4):
+            plist.append(kinv.SamplingParams(**v, seed=17 * i + j))
+            hists.append(torch.randint(0, 500, (70,), generator=g).tolist())
+            steps.append(i * 100 + j)
+    logits = (torch.randn(len(plist), vocab, generator=g) * 2).cuda()
+    logits[:, :500] += 3.0   # the history ids are among the top candidates
+    # the last variant keeps the whole vocabulary only when V <= 1024: shrink it
+    small = logits[-4:, :1000].contiguous()
+    got = _run(kinv, logits[:-4].contiguous(), plist[:-4], hists[:-4], steps[:-4])
+    ref, ties = _oracle(logits[:-4], plist[:-4], hists[:-4], steps[:-4])
+    assert np.array_equal(got[~ties], ref[~ties])
+    got2 = _run(kinv, small, plist[-4:], hists[-4:], steps[-4:])
+    ref2, ties2 = _oracle(small, plist[-4:], hists[-4:], steps[-4:])
+    assert np.array_equal(got2[~ties2], ref2[~ties2])
+
+
+def test_exact_ties_take_lowest_ids(kinv):
+    vocab = 151936
+    logits = torch.zeros(3, vocab, device="cuda")
+    logits[1, 7] = 1.0
+    p = [kinv.SamplingParams(temperature=1.0, top_k=50, top_p=1.0, min_p=0.0, repeat_penalty=1.0,
+                             repeat_last_n=0, seed=s) for s in range(3)]
+    p[2].temperature = 0.0
+    steps = [0, 1, 2]
+    got = _run(kinv, logits, p, [[], [], []], steps)
+    ref, ties = _oracle(logits, p, [[], [], []], steps)
+    assert np.array_equal(got, ref)
+    assert got[0] < 50 and got[2] == 0
+
+
+def test_row_bits_independent_of_batch(kinv):
+    vocab = 151936
+    g = synth.gen(72)
+    logits = (torch.randn(32, vocab, generator=g) * 1.3).cuda()
+    base = _receipt_params()
+    plist = [kinv.SamplingParams(**{**base, "seed": 5000 + b}) for b in range(32)]
+    hists = [list(range(b, b + 40)) for b in range(32)]
+    steps = list(range(100, 132))
+    full = _run(kinv, logits, plist, hists, steps)
+    for b in (0, 13, 31):
+        one = _run(kinv, logits[b: b + 1].contiguous(), plist[b: b + 1], hists[b: b + 1], steps[b: b + 1])
+        assert one[0] == full[b]
+    perm = torch.randperm(32, generator=g).tolist()
+    got = _run(kinv, logits[perm].contiguous(), [plist[i] for i in perm], [hists[i] for i in perm],
+               [steps[i] for i in perm])
+    assert np.array_equal(got, full[perm])
+
+
+def test_unsupported_top_k_reports_status(kinv):
+    logits = torch.randn(2, 5000, device="cuda")
+    p = [kinv.SamplingParams(top_k=2000, seed=1), kinv.SamplingParams(top_k=10, seed=2)]
+    got = _run(kinv, logits, p, [[], []], [0, 0])
+    assert got[0] == -1 and got[1] >= 0
+    assert kinv.last_device_status() == kinv.ERR_UNSUPPORTED
+    assert kinv.last_device_status() == 0
