@@ -305,14 +305,19 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, const Gemm
   const size_t smem = smem_bytes<BN>(a.stages);
   if (a.splits > 1 && static_cast<size_t>(BM) * (BN + 1) * 4 > static_cast<size_t>(a.stages) * (A_STAGE + BN * BK * 2))
     return KINV_ERR_UNSUPPORTED;
-  static bool configured[64] = {};
+  // the opt-in limit is raised once per device to the largest request seen
+  static size_t configured[64] = {};
+  static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return KINV_ERR_CUDA;
-  if (dev < 64 && !configured[dev]) {
-    if (cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<BN>(8))) != cudaSuccess)
-      return KINV_ERR_CUDA;
-    configured[dev] = true;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return KINV_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (configured[dev] < smem) {
+      if (cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem)) != cudaSuccess)
+        return KINV_ERR_CUDA;
+      configured[dev] = smem;
+    }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.splits, grid_y, grid_z);
