@@ -14,7 +14,8 @@ Layouts (all bf16 unless noted):
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+import contextlib
+from dataclasses import dataclass
 
 import numpy as np
 import torch
@@ -105,6 +106,15 @@ class Decoder:
         self.hist_len = torch.zeros(max_batch, **i32)
         self.step = torch.zeros(max_batch, dtype=torch.int64, device=self.dev)
         self.params = torch.zeros(max_batch * 32, dtype=torch.uint8, device=self.dev)
+        # optional per-call timing: name -> list of (start, end) CUDA events
+        self.timer = None
+
+    def _t(self, name: str):
+        """Brackets one kernel call with CUDA events on the current stream
+        when a timer dict is installed (used by the benchmark only)."""
+        if self.timer is None:
+            return contextlib.nullcontext()
+        return _EventPair(self.timer, name)
 
     # ------------------------------------------------------------ state setup
     def set_sampling(self, params_list) -> None:
@@ -131,15 +141,23 @@ class Decoder:
         FFN output (not yet added unless ``first``)."""
         s, lw = self.s, self.w["layers"][li]
         x, h = self.x[:rows], self.h[:rows]
-        kinv.rmsnorm(x, lw["attn_norm"], s.eps, residual=None if first else self.delta[:rows], out=h)
-        kinv.gemm(h, lw["w_qkv"], out=self.qkv[:rows])
+        with self._t("rmsnorm"):
+            kinv.rmsnorm(x, lw["attn_norm"], s.eps, residual=None if first else self.delta[:rows],
+                         out=h)
+        with self._t("gemm_qkv"):
+            kinv.gemm(h, lw["w_qkv"], out=self.qkv[:rows])
         kc, vc = self.kv[li, 0], self.kv[li, 1]
         attention(li, rows, kc, vc)
-        kinv.gemm(self.attn[:rows].view(rows, -1), lw["w_o"], out=self.o[:rows])
-        kinv.rmsnorm(x, lw["ffn_norm"], s.eps, residual=self.o[:rows], out=h)
-        kinv.gemm(h, lw["w_gu"], out=self.gu[:rows])
-        kinv.swiglu(self.gu[:rows], out=self.act[:rows])
-        kinv.gemm(self.act[:rows], lw["w_down"], out=self.delta[:rows])
+        with self._t("gemm_o"):
+            kinv.gemm(self.attn[:rows].view(rows, -1), lw["w_o"], out=self.o[:rows])
+        with self._t("rmsnorm"):
+            kinv.rmsnorm(x, lw["ffn_norm"], s.eps, residual=self.o[:rows], out=h)
+        with self._t("gemm_gate_up"):
+            kinv.gemm(h, lw["w_gu"], out=self.gu[:rows])
+        with self._t("swiglu"):
+            kinv.swiglu(self.gu[:rows], out=self.act[:rows])
+        with self._t("gemm_down"):
+            kinv.gemm(self.act[:rows], lw["w_down"], out=self.delta[:rows])
 
     def _rope(self, li, rows, kc, vc, seq, pos):
         s, lw = self.s, self.w["layers"][li]
@@ -153,9 +171,11 @@ class Decoder:
         the token's hidden state must be in x; leaves the final residual
         pieces in x and delta."""
         def attention(li, rows, kc, vc):
-            self._rope(li, rows, kc, vc, self.seq[:rows], self.pos[:rows])
-            kinv.attn_decode(self.q[:rows], kc[:rows], vc[:rows], self.kv_len[:rows],
-                             out=self.attn[:rows], workspace=self.ws)
+            with self._t("rope_append"):
+                self._rope(li, rows, kc, vc, self.seq[:rows], self.pos[:rows])
+            with self._t("attn_decode"):
+                kinv.attn_decode(self.q[:rows], kc[:rows], vc[:rows], self.kv_len[:rows],
+                                 out=self.attn[:rows], workspace=self.ws)
         for li in range(self.s.n_layers):
             self.layer(li, bsz, li == 0, attention)
 
@@ -164,16 +184,21 @@ class Decoder:
         and (optionally) the sampler, then advance positions and histories.
         The sampled ids land in ``tokens`` (they are the next step's input)."""
         s = self.s
-        kinv.embed(self.w["embed"], self.tokens[:bsz], out=self.x[:bsz])
+        with self._t("embed"):
+            kinv.embed(self.w["embed"], self.tokens[:bsz], out=self.x[:bsz])
         self.decode_layers(bsz)
-        kinv.rmsnorm(self.x[:bsz], self.w["final_norm"], s.eps, residual=self.delta[:bsz],
-                     out=self.h[:bsz])
-        kinv.gemm(self.h[:bsz], self.w["lm_head"], out=self.logits[:bsz])
+        with self._t("rmsnorm"):
+            kinv.rmsnorm(self.x[:bsz], self.w["final_norm"], s.eps, residual=self.delta[:bsz],
+                         out=self.h[:bsz])
+        with self._t("gemm_lm_head"):
+            kinv.gemm(self.h[:bsz], self.w["lm_head"], out=self.logits[:bsz])
         if sample:
-            kinv.sample(self.logits[:bsz], self.params, self.history[:bsz], self.hist_len[:bsz],
-                        self.step[:bsz], out=self.tokens[:bsz])
-            kinv.decode_advance(self.tokens[:bsz], self.history[:bsz], self.hist_len[:bsz],
-                                self.step[:bsz], pos=self.pos[:bsz], kv_len=self.kv_len[:bsz])
+            with self._t("sample"):
+                kinv.sample(self.logits[:bsz], self.params, self.history[:bsz],
+                            self.hist_len[:bsz], self.step[:bsz], out=self.tokens[:bsz])
+            with self._t("decode_advance"):
+                kinv.decode_advance(self.tokens[:bsz], self.history[:bsz], self.hist_len[:bsz],
+                                    self.step[:bsz], pos=self.pos[:bsz], kv_len=self.kv_len[:bsz])
 
     # --------------------------------------------------------------- prefill
     def prefill_chunk(self, seq: int, p0: int, rows: int) -> None:
@@ -198,3 +223,19 @@ class Decoder:
         """x <- bf16(x + delta) for rows [0, rows): the last layer's output."""
         kinv.add(self.x[:rows], self.delta[:rows], out=self.x[:rows])
         return self.x[:rows]
+
+
+class _EventPair:
+    def __init__(self, timer: dict, name: str):
+        self.timer, self.name = timer, name
+
+    def __enter__(self):
+        self.a = torch.cuda.Event(enable_timing=True)
+        self.b = torch.cuda.Event(enable_timing=True)
+        self.a.record()
+        return self
+
+    def __exit__(self, *exc):
+        self.b.record()
+        self.timer.setdefault(self.name, []).append((self.a, self.b))
+        return False

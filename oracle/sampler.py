@@ -29,8 +29,11 @@ integers (which ids survive, in which order), so they are taken in fp32 with
 correctly rounded division and multiplication, as the kernel takes them; those
 decisions are then identical on both sides.  The exponentials and sums are
 fp64 here and fp32 on the GPU, so a draw or a top-p / min-p cut that falls
-within ``TIE_TOL`` (relative) of a boundary is reported as a near tie, and
-token parity is not asserted for such a row.
+within a margin of a boundary is reported as a near tie, and token parity is
+not asserted for such a row.  The margin (relative to the sum) bounds the
+kernel's fp32 error: a sequential sum of k terms below 1 is off by at most
+k * 2^-24 relative, and each exponential by a few units in the last place, so
+``tie_tol(k) = 1e-5 + k * 6e-8``.
 """
 from __future__ import annotations
 
@@ -40,7 +43,9 @@ import numpy as np
 
 from .philox import sampler_uniform
 
-TIE_TOL = 1e-4
+
+def tie_tol(k: int) -> float:
+    return 1e-5 + k * 6e-8
 
 
 @dataclass
@@ -81,6 +86,7 @@ def sample_row(logits_f32: np.ndarray, history, step: int, p: SamplingParams):
         order = order[:k]
     s = (z[order] / t).astype(np.float64)          # fp32 division, widened exactly
     e = np.exp(s - s[0])
+    tol = tie_tol(len(order))
     near = False
     keep = len(order)
     if p.top_p < 1.0:
@@ -88,23 +94,25 @@ def sample_row(logits_f32: np.ndarray, history, step: int, p: SamplingParams):
         target = float(np.float32(p.top_p)) * cum[-1]
         keep = int(np.searchsorted(cum, target, side="left")) + 1
         keep = max(1, min(keep, len(order)))
-        lo = max(0, keep - 2)
-        if np.any(np.abs(cum[lo: keep + 1] - target) <= TIE_TOL * cum[-1]):
+        # the cut moves if cum[keep-1] or cum[keep-2] sits at the target
+        if np.any(np.abs(cum[max(0, keep - 2): keep] - target) <= tol * cum[-1]):
             near = True
     if p.min_p > 0.0:
         mp = float(np.float32(p.min_p))
         ok = e[:keep] >= mp
-        keep = max(1, int(np.count_nonzero(ok)))
-        if np.any(np.abs(e[: keep + 1] - mp) <= TIE_TOL):
+        n_ok = int(np.count_nonzero(ok))
+        # the cut moves if the last kept or the first dropped e sits at min_p
+        if np.any(np.abs(e[max(0, n_ok - 1): min(n_ok + 1, keep)] - mp) <= tol):
             near = True
+        keep = max(1, n_ok)
     e = e[:keep]
     cum = np.cumsum(e)
     u = sampler_uniform(p.seed, step)
     target = u * cum[-1]
     idx = int(np.searchsorted(cum, target, side="right"))
     idx = min(idx, keep - 1)
-    lo = max(0, idx - 1)
-    if np.any(np.abs(cum[lo: idx + 1] - target) <= TIE_TOL * cum[-1]):
+    # the pick moves if cum[idx] or cum[idx-1] sits at the target
+    if np.any(np.abs(cum[max(0, idx - 1): idx + 1] - target) <= tol * cum[-1]):
         near = True
     return int(order[idx]), near
 

@@ -69,7 +69,7 @@ def test_token_parity_receipt_settings(kinv, sigma):
     got = _run(kinv, logits, plist, hists, steps)
     ref, ties = _oracle(logits, plist, hists, steps)
     ok = ~ties
-    assert ties.sum() <= 2, f"{ties.sum()} near ties"
+    assert ties.sum() <= max(2, bsz // 16), f"{ties.sum()} near ties"
     assert np.array_equal(got[ok], ref[ok]), np.nonzero(got != ref)
     assert kinv.last_device_status() == 0
 
