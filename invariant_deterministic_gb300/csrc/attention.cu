@@ -63,8 +63,9 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Rows handled by this block: their q/out row indices and visible key counts.
@@ -98,15 +99,17 @@ __device__ __forceinline__ bool block_rows(const AttnParams& p, RowSet& rs) {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p) {
-  constexpr int C8 = D / 8;                // 16-byte chunks per key row
-  // K (then V) tile [256][D] bf16; chunk c of key row t is stored at chunk
-  // c ^ (t & 7) of that row, so that both the per-key reads of the scores and
-  // the per-column reads of the o sum are free of bank conflicts.
+  constexpr int C8 = D / 8;               // 16-byte chunks per key row
+  constexpr int SUB = 64;                 // keys per pipeline stage
+  constexpr int NSUB = kSplit / SUB;      // 4 stages: the ring holds the whole split
+  // Ring of NSUB stages, each [SUB][D] bf16.  Chunk c of key row k sits at
+  // chunk c ^ (4 * (k & 1)) of its row: the score phase's quads (two keys x
+  // four chunk lanes per 8-thread phase) and the o phase's row-wide reads both
+  // hit distinct bank groups.
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(smem_raw);
+  __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem_raw);
   float* qs = reinterpret_cast<float*>(smem_raw + kSplit * D * 2);        // [rg_cap][D]
   float* es = qs + p.rg_cap * D;                                          // [rg_cap][256]
-  __shared__ float red[kThreads / 32][kMaxRG];
   __shared__ float mrow[kMaxRG];
   __shared__ float lrow[kMaxRG];
 
@@ -122,106 +125,113 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   const int RG = rs.nrows * G;
   const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
+  const int64_t seq_off = rs.seq * p.seq_stride + static_cast<int64_t>(k0) * p.tok_stride + g * D;
 
-  // --- K tile (and the queries) into shared memory
-  const __nv_bfloat16* kbase = p.k + rs.seq * p.seq_stride + static_cast<int64_t>(k0) * p.tok_stride + g * D;
-  for (int idx = t; idx < nmax * C8; idx += kThreads) {
-    const int row = idx / C8, c = idx % C8;
-    cp_async16(smem_addr(kv + row * D + ((c ^ (row & 7)) * 8)), kbase + row * p.tok_stride + c * 8);
-  }
-  cp_async_commit();
+  // Issue the loads of sub-tile j of `src` (K or V) into stage j (an empty
+  // commit group when the sub-tile holds no key, to keep the group count).
+  auto load_sub = [&](const __nv_bfloat16* src, int j) {
+    const int rows = min(SUB, nmax - j * SUB);
+    __nv_bfloat16* dst = ring + j * SUB * D;
+    for (int idx = t; idx < rows * C8; idx += kThreads) {
+      const int r = idx / C8, c = idx % C8;
+      const int key = j * SUB + r;
+      cp_async16(smem_addr(dst + r * D + ((c ^ ((key & 1) << 2)) << 3)),
+                 src + seq_off + static_cast<int64_t>(key) * p.tok_stride + c * 8);
+    }
+    cp_async_commit();
+  };
+
+#pragma unroll
+  for (int j = 0; j < NSUB; ++j) load_sub(p.k, j);
   for (int idx = t; idx < RG * D; idx += kThreads) {
     const int rg = idx / D, d = idx % D;
     const int r = rg / G, i = rg % G;
     qs[idx] = __bfloat162float(p.q[(static_cast<int64_t>(rs.row0 + r) * p.Hq + g * G + i) * D + d]);
   }
-  cp_async_wait_all();
-  __syncthreads();
 
-  // --- scores: thread t against key t, every (row, head)
-  float acc[kMaxRG];
+  // --- scores.  Four threads per key; lane q of a quad sums chunks q, q+4,
+  // q+8, ... of d with FMAs, then two xor-shuffles add the quad's partials
+  // (the same bits in all four lanes).
+  const int kq = t >> 2, q4 = t & 3;
 #pragma unroll
-  for (int j = 0; j < kMaxRG; ++j) acc[j] = 0.f;
-  if (t < nmax) {
-    const __nv_bfloat16* kr = kv + t * D;
-#pragma unroll 2
-    for (int c = 0; c < C8; ++c) {
-      const uint4 u = *reinterpret_cast<const uint4*>(kr + ((c ^ (t & 7)) * 8));
-      float kf[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
-                     bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+  for (int j = 0; j < NSUB; ++j) {
+    cp_async_wait<3>();  // groups after K_j: K_{j+1..3} and V_{0..j-1}, three in all
+    __syncthreads();
+    const int key = j * SUB + kq;
+    if (j * SUB < nmax) {
+      const __nv_bfloat16* kr = ring + j * SUB * D + kq * D;
+      float acc[kMaxRG];
 #pragma unroll
-      for (int j = 0; j < kMaxRG; ++j) {
-        if (j < RG) {
-          const float4 qa = *reinterpret_cast<const float4*>(qs + j * D + c * 8);
-          const float4 qb = *reinterpret_cast<const float4*>(qs + j * D + c * 8 + 4);
-          float a = acc[j];
-          a = fmaf(qa.x, kf[0], a); a = fmaf(qa.y, kf[1], a);
-          a = fmaf(qa.z, kf[2], a); a = fmaf(qa.w, kf[3], a);
-          a = fmaf(qb.x, kf[4], a); a = fmaf(qb.y, kf[5], a);
-          a = fmaf(qb.z, kf[6], a); a = fmaf(qb.w, kf[7], a);
-          acc[j] = a;
+      for (int r = 0; r < kMaxRG; ++r) acc[r] = 0.f;
+#pragma unroll
+      for (int m = 0; m < C8 / 4; ++m) {
+        const int c = q4 + 4 * m;
+        const uint4 u = *reinterpret_cast<const uint4*>(kr + ((c ^ ((key & 1) << 2)) << 3));
+        const float kf[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                             bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+#pragma unroll
+        for (int r = 0; r < kMaxRG; ++r) {
+          if (r < RG) {
+            const float4 qa = *reinterpret_cast<const float4*>(qs + r * D + c * 8);
+            const float4 qb = *reinterpret_cast<const float4*>(qs + r * D + c * 8 + 4);
+            float a = acc[r];
+            a = fmaf(qa.x, kf[0], a); a = fmaf(qa.y, kf[1], a);
+            a = fmaf(qa.z, kf[2], a); a = fmaf(qa.w, kf[3], a);
+            a = fmaf(qb.x, kf[4], a); a = fmaf(qb.y, kf[5], a);
+            a = fmaf(qb.z, kf[6], a); a = fmaf(qb.w, kf[7], a);
+            acc[r] = a;
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kMaxRG; ++r) {
+        if (r < RG) {
+          float a = acc[r];
+          a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
+          a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 2));
+          if (q4 == 0) {
+            const int nr = min(kSplit, rs.len0 + r / G - k0);
+            es[r * kSplit + key] = key < nr ? __fmul_rn(a, p.scale) : -INFINITY;
+          }
         }
       }
     }
+    __syncthreads();           // stage j is free
+    if (j * SUB < nmax) load_sub(p.v, j);
+    else cp_async_commit();
   }
-  __syncthreads();  // every thread is done with the K tile
 
-  // --- V tile load overlaps the softmax statistics
-  const __nv_bfloat16* vbase = p.v + rs.seq * p.seq_stride + static_cast<int64_t>(k0) * p.tok_stride + g * D;
-  for (int idx = t; idx < nmax * C8; idx += kThreads) {
-    const int row = idx / C8, c = idx % C8;
-    cp_async16(smem_addr(kv + row * D + ((c ^ (row & 7)) * 8)), vbase + row * p.tok_stride + c * 8);
-  }
-  cp_async_commit();
-
-  // scaled scores; keys a row cannot see are -inf for the max
+  // --- softmax statistics: warp w takes (row, head) pairs w, w + 8, ...;
+  // lane l owns keys l, l + 32, ..., l + 224 (sequential), then a butterfly.
+  for (int r = warp; r < RG; r += kThreads / 32) {
+    const int nr = min(kSplit, rs.len0 + r / G - k0);
+    float* e = es + r * kSplit;
+    float m = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < kMaxRG; ++j) {
-    if (j < RG) {
-      const int nr = min(kSplit, rs.len0 + j / G - k0);
-      acc[j] = t < nr ? __fmul_rn(acc[j], p.scale) : -INFINITY;
+    for (int i = 0; i < kSplit / 32; ++i) {
+      const int key = lane + 32 * i;
+      if (key < nr) m = fmaxf(m, e[key]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float l = 0.f;
+#pragma unroll
+    for (int i = 0; i < kSplit / 32; ++i) {
+      const int key = lane + 32 * i;
+      const float x = key < nr ? expf(__fsub_rn(e[key], m)) : 0.f;
+      e[key] = x;
+      l = __fadd_rn(l, x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, o));
+    if (lane == 0) {
+      mrow[r] = m;
+      lrow[r] = l;
     }
   }
-  // row maxima (max is exact, so the tree shape does not matter)
-#pragma unroll
-  for (int j = 0; j < kMaxRG; ++j) {
-    if (j < RG) {
-      float m = acc[j];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) red[warp][j] = m;
-    }
-  }
-  __syncthreads();
-  if (t < RG) {
-    float m = red[0][t];
-    for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, red[w][t]);
-    mrow[t] = m;
-  }
-  __syncthreads();
-  // exponentials and their sums: butterfly per warp (lane 0), warps in order
-#pragma unroll
-  for (int j = 0; j < kMaxRG; ++j) {
-    if (j < RG) {
-      const int nr = min(kSplit, rs.len0 + j / G - k0);
-      const float e = t < nr ? expf(__fsub_rn(acc[j], mrow[j])) : 0.f;
-      es[j * kSplit + t] = e;
-      float l = e;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, o));
-      if (lane == 0) red[warp][j] = l;
-    }
-  }
-  __syncthreads();
-  if (t < RG) {
-    float l = red[0][t];
-    for (int w = 1; w < kThreads / 32; ++w) l = __fadd_rn(l, red[w][t]);
-    lrow[t] = l;
-  }
-  cp_async_wait_all();
-  __syncthreads();
 
-  // --- o = sum_t e_t v_t: thread -> (d pair, a slot of (row, head) pairs)
+  // --- o = sum_t e_t v_t: thread -> (d pair, a slot of (row, head) pairs),
+  // keys ascending across the four V sub-tiles.
   constexpr int DP = D / 2;
   constexpr int SLOTS = kThreads / DP;       // 4 (D = 128) or 8 (D = 64)
   constexpr int PER = kMaxRG / SLOTS;        // (row, head) pairs per thread at most
@@ -235,16 +245,28 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
     const int j = slot + c * SLOTS;
     cnt[c] = j < RG ? min(kSplit, rs.len0 + j / G - k0) : 0;
   }
-  for (int key = 0; key < nmax; ++key) {
-    const uint32_t vv = *reinterpret_cast<const uint32_t*>(
-        kv + key * D + ((((2 * dp) >> 3) ^ (key & 7)) << 3) + ((2 * dp) & 7));
-    const float v0 = bf16_lo(vv), v1 = bf16_hi(vv);
+  const int col = 2 * dp;
 #pragma unroll
-    for (int c = 0; c < PER; ++c) {
-      if (key < cnt[c]) {
-        const float e = es[(slot + c * SLOTS) * kSplit + key];
-        o[c].x = fmaf(e, v0, o[c].x);
-        o[c].y = fmaf(e, v1, o[c].y);
+  for (int j = 0; j < NSUB; ++j) {
+    if (j == 0) cp_async_wait<3>();
+    else if (j == 1) cp_async_wait<2>();
+    else if (j == 2) cp_async_wait<1>();
+    else cp_async_wait<0>();
+    __syncthreads();
+    const int kend = min(SUB, nmax - j * SUB);
+    const __nv_bfloat16* vt = ring + j * SUB * D;
+    for (int kk = 0; kk < kend; ++kk) {
+      const int key = j * SUB + kk;
+      const uint32_t vv = *reinterpret_cast<const uint32_t*>(
+          vt + kk * D + ((((col >> 3) ^ ((key & 1) << 2))) << 3) + (col & 7));
+      const float v0 = bf16_lo(vv), v1 = bf16_hi(vv);
+#pragma unroll
+      for (int c = 0; c < PER; ++c) {
+        if (key < cnt[c]) {
+          const float e = es[(slot + c * SLOTS) * kSplit + key];
+          o[c].x = fmaf(e, v0, o[c].x);
+          o[c].y = fmaf(e, v1, o[c].y);
+        }
       }
     }
   }
@@ -254,7 +276,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
     if (j < RG && cnt[c] > 0) {
       const int r = j / G, i = j % G;
       const int64_t base = (static_cast<int64_t>(rs.row0 + r) * p.Hq + g * G + i) * p.S + s;
-      *reinterpret_cast<float2*>(p.ws_o + base * D + 2 * dp) = o[c];
+      *reinterpret_cast<float2*>(p.ws_o + base * D + col) = o[c];
       if (dp == 0) {
         p.ws_ml[base * 2 + 0] = mrow[j];
         p.ws_ml[base * 2 + 1] = lrow[j];

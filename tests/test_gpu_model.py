@@ -121,7 +121,79 @@ def test_full_depth_alone_vs_cobatched(M):
     assert_same_bits(l[2], alone_l[0], "logits at full depth")
 
 
+def test_every_stage_of_the_step_matches_the_oracle(M):
+    """Each kernel of a 2-layer 8B-shaped decode step, fed the GPU's own
+    inputs for that stage, matches the oracle within the tolerance."""
+    from oracle import attention as oattn, glue as oglue
+    from oracle.gemm import gemm as og
+    from oracle.rmsnorm import rmsnorm as orms
+    from oracle.rope import rope as orope
+    kinv = M.kinv
+    shape = _shape(M, 2)
+    w = M.random_weights(shape, device="cuda")
+    B, L = 3, [16, 300, 1]
+    dec = M.Decoder(shape, w, max_batch=B, max_len=512)
+    for r in range(B):
+        dec.kv[:, :, r, : L[r]].copy_(synth.normal_bf16((2, 2, L[r], 8, 128), 1.0, 5000 + r, "cuda"))
+    dec.set_positions(L)
+    dec.tokens[:B] = torch.tensor([5, 77, 151935], dtype=torch.int32, device="cuda")
+    b = synth.bits
+    kinv.embed(w["embed"], dec.tokens[:B], out=dec.x[:B])
+    assert np.array_equal(b(dec.x[:B]), oglue.embed(b(w["embed"]), [5, 77, 151935]))
+    for li in range(2):
+        lw = w["layers"][li]
+        x0, d0 = b(dec.x[:B]), b(dec.delta[:B])
+        kinv.rmsnorm(dec.x[:B], lw["attn_norm"], 1e-6, residual=None if li == 0 else dec.delta[:B],
+                     out=dec.h[:B])
+        if li == 0:
+            assert_close(f64(dec.h[:B]), obf.to_f64(orms(x0, b(lw["attn_norm"]), 1e-6)), "attn norm")
+        else:
+            y, s = orms(x0, b(lw["attn_norm"]), 1e-6, residual_bits=d0)
+            assert_close(f64(dec.x[:B]), obf.to_f64(s), "residual")
+            assert_close(f64(dec.h[:B]), obf.to_f64(y), "attn norm")
+        kinv.gemm(dec.h[:B], lw["w_qkv"], out=dec.qkv[:B])
+        assert_close(f64(dec.qkv[:B]), obf.to_f64(og(b(dec.h[:B]), b(lw["w_qkv"]))), "qkv")
+        qkv = b(dec.qkv[:B]).reshape(B, 48, 128)
+        kc, vc = dec.kv[li, 0], dec.kv[li, 1]
+        kinv.rope_append(dec.qkv[:B], dec.q[:B], kc, vc, dec.seq[:B], dec.pos[:B], 32, 8, 128, 1e6,
+                         lw["q_norm"], lw["k_norm"], 1e-6)
+        pos = np.array(L)
+        assert_close(f64(dec.q[:B]), obf.to_f64(orope(qkv[:, :32], pos, 1e6, b(lw["q_norm"]))), "rope q")
+        rk = orope(qkv[:, 32:40], pos, 1e6, b(lw["k_norm"]))
+        for r in range(B):
+            assert_close(f64(kc[r, L[r]]), obf.to_f64(rk[r]), "rope k")
+            assert np.array_equal(b(vc[r, L[r]]), qkv[r, 40:])
+        kinv.attn_decode(dec.q[:B], kc[:B], vc[:B], dec.kv_len[:B], out=dec.attn[:B], workspace=dec.ws)
+        ref = oattn.decode(b(dec.q[:B]), b(kc[:B]), b(vc[:B]), [n + 1 for n in L])
+        assert_close(f64(dec.attn[:B]), obf.to_f64(ref), "attention")
+        kinv.gemm(dec.attn[:B].view(B, -1), lw["w_o"], out=dec.o[:B])
+        assert_close(f64(dec.o[:B]), obf.to_f64(og(b(dec.attn[:B]).reshape(B, -1), b(lw["w_o"]))), "o")
+        x1, o1 = b(dec.x[:B]), b(dec.o[:B])
+        kinv.rmsnorm(dec.x[:B], lw["ffn_norm"], 1e-6, residual=dec.o[:B], out=dec.h[:B])
+        y, s = orms(x1, b(lw["ffn_norm"]), 1e-6, residual_bits=o1)
+        assert_close(f64(dec.x[:B]), obf.to_f64(s), "x2")
+        assert_close(f64(dec.h[:B]), obf.to_f64(y), "ffn norm")
+        kinv.gemm(dec.h[:B], lw["w_gu"], out=dec.gu[:B])
+        assert_close(f64(dec.gu[:B]), obf.to_f64(og(b(dec.h[:B]), b(lw["w_gu"]))), "gate/up")
+        kinv.swiglu(dec.gu[:B], out=dec.act[:B])
+        assert_close(f64(dec.act[:B]), obf.to_f64(oglue.swiglu(b(dec.gu[:B]))), "swiglu")
+        kinv.gemm(dec.act[:B], lw["w_down"], out=dec.delta[:B])
+        assert_close(f64(dec.delta[:B]), obf.to_f64(og(b(dec.act[:B]), b(lw["w_down"]))), "down")
+    x1, d1 = b(dec.x[:B]), b(dec.delta[:B])
+    kinv.rmsnorm(dec.x[:B], w["final_norm"], 1e-6, residual=dec.delta[:B], out=dec.h[:B])
+    y, s = orms(x1, b(w["final_norm"]), 1e-6, residual_bits=d1)
+    assert_close(f64(dec.h[:B]), obf.to_f64(y), "final norm")
+    kinv.gemm(dec.h[:B], w["lm_head"], out=dec.logits[:B])
+    assert_close(f64(dec.logits[:B]), og(b(dec.h[:B]), b(w["lm_head"]), out="f64"), "logits",
+                 atol=1e-4, rtol=1e-4)
+    assert kinv.last_device_status() == 0
+
+
 def test_first_step_logits_match_oracle(M):
+    """End to end over two layers: bf16 roundings that differ by one unit in a
+    few elements compound through the layers, so this end-to-end check uses
+    the norm-relative criterion and a 99% per-element share; the per-stage
+    test above holds every kernel to the per-element tolerance."""
     shape = _shape(M, 2)
     w = M.random_weights(shape, device="cuda")
     lengths = [16, 16]
@@ -144,8 +216,9 @@ def test_first_step_logits_match_oracle(M):
     params = [OParams(seed=1000 + r) for r in range(2)]
     ologits, otoks, ties = odecode(tokens, om, kc, vc, lengths, oshape, histories=hist,
                                    steps=[0, 0], params=params)
-    assert_close(f64(logits[:, 0]), ologits.astype(np.float64), "first-step logits",
-                 atol=2e-2, rtol=1e-2)
+    g, r = f64(logits[:, 0]), ologits.astype(np.float64)
+    assert np.linalg.norm(g - r) / np.linalg.norm(r) <= 1e-2
+    assert np.mean(np.abs(g - r) <= 2e-2 + 1e-2 * np.abs(r)) >= 0.99
     for r in range(2):
         if not ties[r]:
             # the kernel's logits differ from the oracle's in low bits, so
