@@ -113,6 +113,8 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   __shared__ float mrow[kMaxRG];
   __shared__ float lrow[kMaxRG];
 
+  pdl_launch_dependents();
+  pdl_wait();
   RowSet rs;
   if (!block_rows(p, rs)) return;
   const int s = blockIdx.x;
@@ -288,6 +290,8 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
 // One block per (query head, row); thread d folds column d.
 template <int D>
 __global__ void attn_merge_kernel(const AttnParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   int row, len;
   if (!p.prefill) {
     row = blockIdx.y;
@@ -309,16 +313,29 @@ __global__ void attn_merge_kernel(const AttnParams p) {
   const int ns = (len + kSplit - 1) / kSplit;
   const int64_t base = (static_cast<int64_t>(row) * p.Hq + h) * p.S;
   float m_acc = -INFINITY, l_acc = 0.f, o_acc = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float m_s = p.ws_ml[(base + s) * 2 + 0];
-    const float l_s = p.ws_ml[(base + s) * 2 + 1];
-    const float o_s = p.ws_o[(base + s) * D + d];
-    const float m_new = fmaxf(m_acc, m_s);
-    const float a = expf(__fsub_rn(m_acc, m_new));
-    const float c = expf(__fsub_rn(m_s, m_new));
-    l_acc = __fadd_rn(__fmul_rn(l_acc, a), __fmul_rn(l_s, c));
-    o_acc = __fadd_rn(__fmul_rn(o_acc, a), __fmul_rn(o_s, c));
-    m_acc = m_new;
+  constexpr int CH = 8;  // partials loaded ahead of the (sequential) fold
+  for (int s0 = 0; s0 < ns; s0 += CH) {
+    float mv[CH], lv[CH], ov[CH];
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      if (s0 + i < ns) {
+        const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + (base + s0 + i) * 2);
+        mv[i] = ml.x;
+        lv[i] = ml.y;
+        ov[i] = p.ws_o[(base + s0 + i) * D + d];
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+      if (s0 + i < ns) {
+        const float m_new = fmaxf(m_acc, mv[i]);
+        const float a = expf(__fsub_rn(m_acc, m_new));
+        const float c = expf(__fsub_rn(mv[i], m_new));
+        l_acc = __fadd_rn(__fmul_rn(l_acc, a), __fmul_rn(lv[i], c));
+        o_acc = __fadd_rn(__fmul_rn(o_acc, a), __fmul_rn(ov[i], c));
+        m_acc = m_new;
+      }
+    }
   }
   *dst = __float2bfloat16_rn(__fdiv_rn(o_acc, l_acc));
 }
@@ -341,10 +358,9 @@ kinv_status launch(const AttnParams& p, dim3 split_grid, dim3 merge_grid, cudaSt
       return KINV_ERR_CUDA;
     configured[dev] = true;
   }
-  attn_split_kernel<D><<<split_grid, kThreads, smem, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return KINV_ERR_CUDA;
-  attn_merge_kernel<D><<<merge_grid, D, 0, stream>>>(p);
-  return launch_status();
+  const kinv_status st = launch_kernel(attn_split_kernel<D>, split_grid, dim3(kThreads), smem, stream, 1, p);
+  if (st != KINV_OK) return st;
+  return launch_kernel(attn_merge_kernel<D>, merge_grid, dim3(D), 0, stream, 1, p);
 }
 
 kinv_status check_common(const void* q, const void* k, const void* v, int64_t seq_stride,

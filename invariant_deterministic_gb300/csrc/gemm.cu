@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int k_tiles = args.k_tiles;
   const int kt0 = rank * k_tiles;
 
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full_bar(s), 1);
@@ -115,7 +116,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
       const uint64_t pol_a = l2_policy_evict_last();   // A is re-read by every N tile
       const uint64_t pol_w = l2_policy_evict_first();  // each W tile is read once
-      for (int kt = 0; kt < k_tiles; ++kt) {
+      // The weights do not depend on the kernel before this one: the first
+      // ring's worth of W tiles is requested before waiting for it; A (its
+      // output) only after.  Fresh stages need no empty-barrier wait.
+      const int pre = k_tiles < stages ? k_tiles : stages;
+      for (int kt = 0; kt < pre; ++kt) {
+        mbar_arrive_expect_tx(full_bar(kt), A_STAGE + W_STAGE);
+        tma_load_2d(smem_addr(w_st + kt * W_STAGE), &tmW, (kt0 + kt) * BK, n0, full_bar(kt), pol_w);
+      }
+      pdl_wait();
+      for (int kt = 0; kt < pre; ++kt)
+        tma_load_2d(smem_addr(a_st + kt * A_STAGE), &tmA, (kt0 + kt) * BK, m0, full_bar(kt), pol_a);
+      issued = pre;
+      for (int kt = pre; kt < k_tiles; ++kt) {
         const int s = kt % stages;
         const uint32_t ph = (kt / stages) & 1u;
         if (*abort_flag ||
@@ -319,19 +332,8 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, const Gemm
       configured[dev] = smem;
     }
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.splits, grid_y, grid_z);
-  cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = a.splits;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = a.splits > 1 ? 1 : 0;
-  return cuda_status(cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, ta, tw, a));
+  return launch_kernel(gemm_kernel<BN>, dim3(a.splits, grid_y, grid_z), dim3(kGemmThreads), smem,
+                       stream, static_cast<unsigned>(a.splits), ta, tw, a);
 }
 
 }  // namespace

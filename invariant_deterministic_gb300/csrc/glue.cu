@@ -12,6 +12,8 @@ namespace {
 
 __global__ void embed_kernel(const uint4* __restrict__ table, int vocab, int dim8,
                              const int32_t* __restrict__ ids, uint4* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int r = blockIdx.x;
   const int id = ids[r];
   for (int c = threadIdx.x; c < dim8; c += blockDim.x) {
@@ -24,6 +26,8 @@ __global__ void embed_kernel(const uint4* __restrict__ table, int vocab, int dim
 // out may alias x or y: each element is read before it is written, by the
 // same thread.
 __global__ void add_kernel(const uint4* x, const uint4* y, uint4* out, int64_t n8) {
+  pdl_launch_dependents();
+  pdl_wait();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint4 a = x[i], b = y[i];
@@ -40,6 +44,8 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f +
 
 __global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ gu, int64_t ld_gu,
                               __nv_bfloat16* __restrict__ out, int64_t ld_out, int F) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int r = blockIdx.y;
   const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 8;
   if (c >= F) return;
@@ -70,6 +76,8 @@ __global__ void rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int64_
   constexpr int HALF = D / 2;
   constexpr int P = D / 64;  // pairs per lane
   __shared__ float cs[HALF], sn[HALF];
+  pdl_launch_dependents();
+  pdl_wait();
   const int r = blockIdx.x;
   const int p = pos[r];
   const int s = seq[r];
@@ -134,19 +142,31 @@ __global__ void rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int64_
 __global__ void decode_advance_kernel(const int32_t* __restrict__ tokens, int32_t* history,
                                       int hist_ld, int32_t* hist_len, int64_t* step, int32_t* pos,
                                       int32_t* kv_len, int B) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
+  // one warp per request: the warp shifts the history row in chunks of 32
+  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
   if (b >= B) return;
   int32_t* h = history + static_cast<int64_t>(b) * hist_ld;
   int n = hist_len[b];
   if (n >= hist_ld) {
-    for (int i = 1; i < hist_ld; ++i) h[i - 1] = h[i];
+    for (int i0 = 1; i0 < hist_ld; i0 += 32) {
+      const int i = i0 + lane;
+      const int32_t v = i < hist_ld ? h[i] : 0;
+      __syncwarp();
+      if (i < hist_ld) h[i - 1] = v;
+      __syncwarp();
+    }
     n = hist_ld - 1;
   }
-  h[n] = tokens[b];
-  hist_len[b] = n + 1;
-  step[b] += 1;
-  if (pos) pos[b] += 1;
-  if (kv_len) kv_len[b] += 1;
+  if (lane == 0) {
+    h[n] = tokens[b];
+    hist_len[b] = n + 1;
+    step[b] += 1;
+    if (pos) pos[b] += 1;
+    if (kv_len) kv_len[b] += 1;
+  }
 }
 
 }  // namespace
@@ -162,9 +182,9 @@ extern "C" kinv_status kinv_embed(const void* table, int vocab, int dim, const i
   if (dim % 8) return KINV_ERR_UNSUPPORTED;
   if (!aligned16(table) || !aligned16(out)) return KINV_ERR_ALIGNMENT;
   const int dim8 = dim / 8;
-  embed_kernel<<<rows, dim8 < 256 ? 32 * ((dim8 + 31) / 32) : 256, 0, stream>>>(
-      static_cast<const uint4*>(table), vocab, dim8, ids, static_cast<uint4*>(out));
-  return launch_status();
+  return launch_kernel(embed_kernel, dim3(rows), dim3(dim8 < 256 ? 32 * ((dim8 + 31) / 32) : 256), 0,
+                       stream, 1, static_cast<const uint4*>(table), vocab, dim8, ids,
+                       static_cast<uint4*>(out));
 }
 
 extern "C" kinv_status kinv_add(const void* x, const void* y, void* out, int64_t n,
@@ -177,9 +197,8 @@ extern "C" kinv_status kinv_add(const void* x, const void* y, void* out, int64_t
   const int64_t n8 = n / 8;
   const int64_t blocks = (n8 + 255) / 256;
   const int grid = static_cast<int>(blocks < 4096 ? blocks : 4096);
-  add_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), static_cast<const uint4*>(y),
-                                       static_cast<uint4*>(out), n8);
-  return launch_status();
+  return launch_kernel(add_kernel, dim3(grid), dim3(256), 0, stream, 1, static_cast<const uint4*>(x),
+                       static_cast<const uint4*>(y), static_cast<uint4*>(out), n8);
 }
 
 extern "C" kinv_status kinv_swiglu(const void* gu, int64_t ld_gu, void* out, int64_t ld_out,
@@ -192,9 +211,9 @@ extern "C" kinv_status kinv_swiglu(const void* gu, int64_t ld_gu, void* out, int
   if (!aligned16(gu) || !aligned16(out) || ld_gu % 8 || ld_out % 8) return KINV_ERR_ALIGNMENT;
   if (rows > 65535) return KINV_ERR_UNSUPPORTED;
   dim3 grid((F / 8 + 127) / 128, rows);
-  swiglu_kernel<<<grid, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(gu), ld_gu,
-                                          static_cast<__nv_bfloat16*>(out), ld_out, F);
-  return launch_status();
+  return launch_kernel(swiglu_kernel, grid, dim3(128), 0, stream, 1,
+                       static_cast<const __nv_bfloat16*>(gu), ld_gu, static_cast<__nv_bfloat16*>(out),
+                       ld_out, F);
 }
 
 extern "C" kinv_status kinv_rope_append(const void* qkv, int64_t ld_qkv, void* q_out,
@@ -224,14 +243,12 @@ extern "C" kinv_status kinv_rope_append(const void* qkv, int64_t ld_qkv, void* q
   auto* qn = static_cast<const __nv_bfloat16*>(q_norm);
   auto* kn = static_cast<const __nv_bfloat16*>(k_norm);
   if (D == 128)
-    rope_append_kernel<128><<<rows, threads, 0, stream>>>(src, ld_qkv, qo, k, v, seq_stride,
-                                                         tok_stride, seq, pos, qn, kn, eps, Hq,
-                                                         Hkv, static_cast<double>(rope_base));
-  else
-    rope_append_kernel<64><<<rows, threads, 0, stream>>>(src, ld_qkv, qo, k, v, seq_stride,
-                                                        tok_stride, seq, pos, qn, kn, eps, Hq, Hkv,
-                                                        static_cast<double>(rope_base));
-  return launch_status();
+    return launch_kernel(rope_append_kernel<128>, dim3(rows), dim3(threads), 0, stream, 1, src,
+                         ld_qkv, qo, k, v, seq_stride, tok_stride, seq, pos, qn, kn, eps, Hq, Hkv,
+                         static_cast<double>(rope_base));
+  return launch_kernel(rope_append_kernel<64>, dim3(rows), dim3(threads), 0, stream, 1, src, ld_qkv,
+                       qo, k, v, seq_stride, tok_stride, seq, pos, qn, kn, eps, Hq, Hkv,
+                       static_cast<double>(rope_base));
 }
 
 extern "C" kinv_status kinv_decode_advance(const int32_t* tokens, int32_t* history, int hist_ld,
@@ -240,7 +257,6 @@ extern "C" kinv_status kinv_decode_advance(const int32_t* tokens, int32_t* histo
   if (B < 0 || hist_ld <= 0) return KINV_ERR_INVALID_ARG;
   if (B == 0) return KINV_OK;
   if (!tokens || !history || !hist_len || !step) return KINV_ERR_INVALID_ARG;
-  decode_advance_kernel<<<(B + 127) / 128, 128, 0, stream>>>(tokens, history, hist_ld, hist_len,
-                                                             step, pos, kv_len, B);
-  return launch_status();
+  return launch_kernel(decode_advance_kernel, dim3((B + 3) / 4), dim3(128), 0, stream, 1, tokens,
+                       history, hist_ld, hist_len, step, pos, kv_len, B);
 }

@@ -28,6 +28,8 @@ __global__ void rmsnorm_kernel(__nv_bfloat16* __restrict__ x, int64_t ldx,
                                __nv_bfloat16* __restrict__ y, int64_t ldy, int dim, float eps) {
   __shared__ float warp_sums[8];
   __shared__ float row_inv;
+  pdl_launch_dependents();
+  pdl_wait();
   const int row = blockIdx.x;
   const int t = threadIdx.x;
   const int T = blockDim.x;
@@ -106,8 +108,8 @@ extern "C" kinv_status kinv_rmsnorm(void* x, int64_t ldx, const void* residual, 
     return KINV_ERR_ALIGNMENT;
   const int chunks = dim / 8;
   int threads = chunks < 256 ? ((chunks + 31) / 32) * 32 : 256;
-  rmsnorm_kernel<<<rows, threads, 0, stream>>>(
-      static_cast<__nv_bfloat16*>(x), ldx, static_cast<const __nv_bfloat16*>(residual),
-      static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(y), ldy, dim, eps);
-  return launch_status();
+  return launch_kernel(rmsnorm_kernel, dim3(rows), dim3(threads), 0, stream, 1,
+                       static_cast<__nv_bfloat16*>(x), ldx, static_cast<const __nv_bfloat16*>(residual),
+                       static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(y), ldy, dim,
+                       eps);
 }

@@ -112,6 +112,8 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + sizeof(Smem));
+  pdl_launch_dependents();
+  pdl_wait();
   const int b = blockIdx.x;
   const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
@@ -346,7 +348,6 @@ extern "C" kinv_status kinv_sample(const float* logits, int64_t ld, int B, int V
       return KINV_ERR_CUDA;
     configured[dev] = true;
   }
-  sample_kernel<<<B, kThreadsS, smem, stream>>>(logits, ld, V, params, history, hist_ld, hist_len,
-                                                step, out_tokens, device_status_word());
-  return launch_status();
+  return launch_kernel(sample_kernel, dim3(B), dim3(kThreadsS), smem, stream, 1, logits, ld, V, params,
+                       history, hist_ld, hist_len, step, out_tokens, device_status_word());
 }
