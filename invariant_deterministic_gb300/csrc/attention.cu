@@ -103,13 +103,13 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   constexpr int SUB = 64;                 // keys per pipeline stage
   constexpr int NSUB = kSplit / SUB;      // 4 stages: the ring holds the whole split
   // Ring of NSUB stages, each [SUB][D] bf16.  Chunk c of key row k sits at
-  // chunk c ^ (4 * (k & 1)) of its row: the score phase's quads (two keys x
-  // four chunk lanes per 8-thread phase) and the o phase's row-wide reads both
-  // hit distinct bank groups.
+  // chunk c ^ swz(k), swz(k) = 4 (k & 1) | (k & 2): the score phase (two keys
+  // x four chunk lanes per 8-thread phase) and the o phase (four keys x eight
+  // column pairs per warp) both hit distinct bank groups.
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem_raw);
   float* qs = reinterpret_cast<float*>(smem_raw + kSplit * D * 2);        // [rg_cap][D]
-  float* es = qs + p.rg_cap * D;                                          // [rg_cap][256]
+  float* es = qs + p.rg_cap * D;                                          // [rg_cap/4][256][4]
   __shared__ float mrow[kMaxRG];
   __shared__ float lrow[kMaxRG];
 
@@ -124,58 +124,65 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   const int nmax = min(kSplit, lenmax - k0);
   if (nmax <= 0) return;
   const int G = p.G;
-  const int RG = rs.nrows * G;
+  const int RG = rs.nrows * G;                         // (row, head) pairs of this block
+  const int RB = (RG + 3) >> 2;                        // handled in blocks of four
   const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
   const int64_t seq_off = rs.seq * p.seq_stride + static_cast<int64_t>(k0) * p.tok_stride + g * D;
+  auto swz = [](int key) { return ((key & 1) << 2) | (key & 2); };
+  // keys visible to (row, head) pair r (rows of one block see consecutive lengths)
+  auto count = [&](int r) { return r < RG ? min(kSplit, rs.len0 + r / G - k0) : 0; };
 
-  // Issue the loads of sub-tile j of `src` (K or V) into stage j (an empty
-  // commit group when the sub-tile holds no key, to keep the group count).
   auto load_sub = [&](const __nv_bfloat16* src, int j) {
     const int rows = min(SUB, nmax - j * SUB);
     __nv_bfloat16* dst = ring + j * SUB * D;
     for (int idx = t; idx < rows * C8; idx += kThreads) {
       const int r = idx / C8, c = idx % C8;
       const int key = j * SUB + r;
-      cp_async16(smem_addr(dst + r * D + ((c ^ ((key & 1) << 2)) << 3)),
+      cp_async16(smem_addr(dst + r * D + ((c ^ swz(key)) << 3)),
                  src + seq_off + static_cast<int64_t>(key) * p.tok_stride + c * 8);
     }
-    cp_async_commit();
+    cp_async_commit();  // an empty group when the sub-tile holds no key keeps the count
   };
 
 #pragma unroll
   for (int j = 0; j < NSUB; ++j) load_sub(p.k, j);
-  for (int idx = t; idx < RG * D; idx += kThreads) {
+  for (int idx = t; idx < RB * 4 * D; idx += kThreads) {
     const int rg = idx / D, d = idx % D;
-    const int r = rg / G, i = rg % G;
-    qs[idx] = __bfloat162float(p.q[(static_cast<int64_t>(rs.row0 + r) * p.Hq + g * G + i) * D + d]);
+    float v = 0.f;
+    if (rg < RG) {
+      const int r = rg / G, i = rg % G;
+      v = __bfloat162float(p.q[(static_cast<int64_t>(rs.row0 + r) * p.Hq + g * G + i) * D + d]);
+    }
+    qs[idx] = v;
   }
 
-  // --- scores.  Four threads per key; lane q of a quad sums chunks q, q+4,
-  // q+8, ... of d with FMAs, then two xor-shuffles add the quad's partials
-  // (the same bits in all four lanes).
+  // --- scores.  Four threads per key; lane q4 of a quad sums chunks q4,
+  // q4 + 4, ... of d with FMAs, then two xor-shuffles add the quad's partials
+  // (the same bits in all four lanes); lane q4 stores pair q4 of the block.
   const int kq = t >> 2, q4 = t & 3;
 #pragma unroll
   for (int j = 0; j < NSUB; ++j) {
     cp_async_wait<3>();  // groups after K_j: K_{j+1..3} and V_{0..j-1}, three in all
     __syncthreads();
-    const int key = j * SUB + kq;
     if (j * SUB < nmax) {
+      const int key = j * SUB + kq;
       const __nv_bfloat16* kr = ring + j * SUB * D + kq * D;
-      float acc[kMaxRG];
+      uint4 kc[C8 / 4];
 #pragma unroll
-      for (int r = 0; r < kMaxRG; ++r) acc[r] = 0.f;
+      for (int m = 0; m < C8 / 4; ++m)
+        kc[m] = *reinterpret_cast<const uint4*>(kr + (((q4 + 4 * m) ^ swz(key)) << 3));
+      for (int rb = 0; rb < RB; ++rb) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int m = 0; m < C8 / 4; ++m) {
-        const int c = q4 + 4 * m;
-        const uint4 u = *reinterpret_cast<const uint4*>(kr + ((c ^ ((key & 1) << 2)) << 3));
-        const float kf[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
-                             bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
+        for (int m = 0; m < C8 / 4; ++m) {
+          const int c = q4 + 4 * m;
+          const float kf[8] = {bf16_lo(kc[m].x), bf16_hi(kc[m].x), bf16_lo(kc[m].y), bf16_hi(kc[m].y),
+                               bf16_lo(kc[m].z), bf16_hi(kc[m].z), bf16_lo(kc[m].w), bf16_hi(kc[m].w)};
 #pragma unroll
-        for (int r = 0; r < kMaxRG; ++r) {
-          if (r < RG) {
-            const float4 qa = *reinterpret_cast<const float4*>(qs + r * D + c * 8);
-            const float4 qb = *reinterpret_cast<const float4*>(qs + r * D + c * 8 + 4);
+          for (int r = 0; r < 4; ++r) {
+            const float4 qa = *reinterpret_cast<const float4*>(qs + (rb * 4 + r) * D + c * 8);
+            const float4 qb = *reinterpret_cast<const float4*>(qs + (rb * 4 + r) * D + c * 8 + 4);
             float a = acc[r];
             a = fmaf(qa.x, kf[0], a); a = fmaf(qa.y, kf[1], a);
             a = fmaf(qa.z, kf[2], a); a = fmaf(qa.w, kf[3], a);
@@ -184,18 +191,16 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
             acc[r] = a;
           }
         }
-      }
+        float mine = 0.f;
 #pragma unroll
-      for (int r = 0; r < kMaxRG; ++r) {
-        if (r < RG) {
+        for (int r = 0; r < 4; ++r) {
           float a = acc[r];
           a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
           a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 2));
-          if (q4 == 0) {
-            const int nr = min(kSplit, rs.len0 + r / G - k0);
-            es[r * kSplit + key] = key < nr ? __fmul_rn(a, p.scale) : -INFINITY;
-          }
+          if (r == q4) mine = a;
         }
+        const int pr = rb * 4 + q4;
+        es[(rb * kSplit + key) * 4 + q4] = key < count(pr) ? __fmul_rn(mine, p.scale) : -INFINITY;
       }
     }
     __syncthreads();           // stage j is free
@@ -203,85 +208,111 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
     else cp_async_commit();
   }
 
-  // --- softmax statistics: warp w takes (row, head) pairs w, w + 8, ...;
-  // lane l owns keys l, l + 32, ..., l + 224 (sequential), then a butterfly.
-  for (int r = warp; r < RG; r += kThreads / 32) {
-    const int nr = min(kSplit, rs.len0 + r / G - k0);
-    float* e = es + r * kSplit;
-    float m = -INFINITY;
+  // --- softmax statistics: warp w takes block w (four pairs); lane l owns
+  // keys l, l + 32, ..., l + 224 (sequential), then a butterfly per pair.
+  for (int rb = warp; rb < RB; rb += kThreads / 32) {
+    float4* e4 = reinterpret_cast<float4*>(es) + rb * kSplit;
+    int cnt[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) cnt[r] = count(rb * 4 + r);
+    float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int i = 0; i < kSplit / 32; ++i) {
       const int key = lane + 32 * i;
-      if (key < nr) m = fmaxf(m, e[key]);
+      const float4 x = e4[key];
+      const float xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        if (key < cnt[r]) m[r] = fmaxf(m[r], xv[r]);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float l = 0.f;
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m[r] = fmaxf(m[r], __shfl_xor_sync(0xffffffffu, m[r], o));
+    float l[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < kSplit / 32; ++i) {
       const int key = lane + 32 * i;
-      const float x = key < nr ? expf(__fsub_rn(e[key], m)) : 0.f;
-      e[key] = x;
-      l = __fadd_rn(l, x);
+      const float4 x = e4[key];
+      float xv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        xv[r] = key < cnt[r] ? expf(__fsub_rn(xv[r], m[r])) : 0.f;
+        l[r] = __fadd_rn(l[r], xv[r]);
+      }
+      e4[key] = make_float4(xv[0], xv[1], xv[2], xv[3]);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, o));
-    if (lane == 0) {
-      mrow[r] = m;
-      lrow[r] = l;
-    }
-  }
-
-  // --- o = sum_t e_t v_t: thread -> (d pair, a slot of (row, head) pairs),
-  // keys ascending across the four V sub-tiles.
-  constexpr int DP = D / 2;
-  constexpr int SLOTS = kThreads / DP;       // 4 (D = 128) or 8 (D = 64)
-  constexpr int PER = kMaxRG / SLOTS;        // (row, head) pairs per thread at most
-  const int dp = t % DP;
-  const int slot = t / DP;
-  float2 o[PER];
-  int cnt[PER];
+    for (int r = 0; r < 4; ++r) {
 #pragma unroll
-  for (int c = 0; c < PER; ++c) {
-    o[c] = make_float2(0.f, 0.f);
-    const int j = slot + c * SLOTS;
-    cnt[c] = j < RG ? min(kSplit, rs.len0 + j / G - k0) : 0;
-  }
-  const int col = 2 * dp;
-#pragma unroll
-  for (int j = 0; j < NSUB; ++j) {
-    if (j == 0) cp_async_wait<3>();
-    else if (j == 1) cp_async_wait<2>();
-    else if (j == 2) cp_async_wait<1>();
-    else cp_async_wait<0>();
-    __syncthreads();
-    const int kend = min(SUB, nmax - j * SUB);
-    const __nv_bfloat16* vt = ring + j * SUB * D;
-    for (int kk = 0; kk < kend; ++kk) {
-      const int key = j * SUB + kk;
-      const uint32_t vv = *reinterpret_cast<const uint32_t*>(
-          vt + kk * D + ((((col >> 3) ^ ((key & 1) << 2))) << 3) + (col & 7));
-      const float v0 = bf16_lo(vv), v1 = bf16_hi(vv);
-#pragma unroll
-      for (int c = 0; c < PER; ++c) {
-        if (key < cnt[c]) {
-          const float e = es[(slot + c * SLOTS) * kSplit + key];
-          o[c].x = fmaf(e, v0, o[c].x);
-          o[c].y = fmaf(e, v1, o[c].y);
-        }
+      for (int o = 16; o > 0; o >>= 1) l[r] = __fadd_rn(l[r], __shfl_xor_sync(0xffffffffu, l[r], o));
+      if (lane == 0) {
+        mrow[rb * 4 + r] = m[r];
+        lrow[rb * 4 + r] = l[r];
       }
     }
   }
+
+  // --- o = sum_t e_t v_t.  Warp w owns column pairs dp = 8w .. 8w + 7; lane
+  // = 8 kg + (dp - 8w): key group kg sums keys kg, kg + 4, ... ascending with
+  // FMAs, and a butterfly over the four key groups (xor 8, 16) adds them.
+  constexpr int DP_WARPS = D / 16;
+  const int kg = lane >> 3;
+  const int dp = warp * 8 + (lane & 7);
+  const int col = 2 * dp;
+  for (int rb = 0; rb < RB; ++rb) {
+    int cnt[4];
 #pragma unroll
-  for (int c = 0; c < PER; ++c) {
-    const int j = slot + c * SLOTS;
-    if (j < RG && cnt[c] > 0) {
-      const int r = j / G, i = j % G;
-      const int64_t base = (static_cast<int64_t>(rs.row0 + r) * p.Hq + g * G + i) * p.S + s;
-      *reinterpret_cast<float2*>(p.ws_o + base * D + col) = o[c];
-      if (dp == 0) {
-        p.ws_ml[base * 2 + 0] = mrow[j];
-        p.ws_ml[base * 2 + 1] = lrow[j];
+    for (int r = 0; r < 4; ++r) cnt[r] = count(rb * 4 + r);
+    float2 o[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                   make_float2(0.f, 0.f)};
+    const float4* e4 = reinterpret_cast<const float4*>(es) + rb * kSplit;
+#pragma unroll
+    for (int j = 0; j < NSUB; ++j) {
+      if (rb == 0) {
+        if (j == 0) cp_async_wait<3>();
+        else if (j == 1) cp_async_wait<2>();
+        else if (j == 2) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        __syncthreads();
+      }
+      if (warp < DP_WARPS) {
+        const int kend = min(SUB, nmax - j * SUB);
+        const __nv_bfloat16* vt = ring + j * SUB * D;
+        for (int kk = kg; kk < kend; kk += 4) {
+          const int key = j * SUB + kk;
+          const uint32_t vv = *reinterpret_cast<const uint32_t*>(
+              vt + kk * D + (((col >> 3) ^ swz(key)) << 3) + (col & 7));
+          const float v0 = bf16_lo(vv), v1 = bf16_hi(vv);
+          const float4 e = e4[key];
+          const float ev[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            if (key < cnt[r]) {
+              o[r].x = fmaf(ev[r], v0, o[r].x);
+              o[r].y = fmaf(ev[r], v1, o[r].y);
+            }
+          }
+        }
+      }
+    }
+    if (warp < DP_WARPS) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        o[r].x = __fadd_rn(o[r].x, __shfl_xor_sync(0xffffffffu, o[r].x, 8));
+        o[r].y = __fadd_rn(o[r].y, __shfl_xor_sync(0xffffffffu, o[r].y, 8));
+        o[r].x = __fadd_rn(o[r].x, __shfl_xor_sync(0xffffffffu, o[r].x, 16));
+        o[r].y = __fadd_rn(o[r].y, __shfl_xor_sync(0xffffffffu, o[r].y, 16));
+        const int pr = rb * 4 + r;
+        if (kg == 0 && pr < RG && cnt[r] > 0) {
+          const int row = pr / G, i = pr % G;
+          const int64_t base = (static_cast<int64_t>(rs.row0 + row) * p.Hq + g * G + i) * p.S + s;
+          *reinterpret_cast<float2*>(p.ws_o + base * D + col) = o[r];
+          if (dp == 0) {
+            p.ws_ml[base * 2 + 0] = mrow[pr];
+            p.ws_ml[base * 2 + 1] = lrow[pr];
+          }
+        }
       }
     }
   }
@@ -427,7 +458,7 @@ extern "C" kinv_status kinv_attn_decode(const void* q, const void* k_cache, cons
   p.R = 1;
   p.S = S;
   p.groups_per_seq = 1;
-  p.rg_cap = p.G;
+  p.rg_cap = ((p.G + 3) / 4) * 4;
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   const dim3 split_grid(S, Hkv, B), merge_grid(Hq, B, 1);
   return D == 128 ? launch<128>(p, split_grid, merge_grid, stream)
@@ -475,7 +506,7 @@ extern "C" kinv_status kinv_attn_prefill(const void* q, const void* k_cache, con
   p.R = kMaxRG / p.G < 8 ? kMaxRG / p.G : 8;
   p.S = S;
   p.groups_per_seq = (max_q_len + p.R - 1) / p.R;
-  p.rg_cap = p.R * p.G;
+  p.rg_cap = ((p.R * p.G + 3) / 4) * 4;
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   const int64_t groups = static_cast<int64_t>(B) * p.groups_per_seq;
   if (groups > 65535 || max_q_len > 65535 || B > 65535) return KINV_ERR_UNSUPPORTED;

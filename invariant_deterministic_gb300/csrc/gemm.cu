@@ -60,6 +60,7 @@ struct GemmArgs {
   int64_t ldc;
   int M, N;
   int k_tiles;  // 64-wide K blocks per split
+  int a_rows;   // rows of A that TMA brings in per tile (the rest of the 128 are never stored)
   int c_f32;
   int stages;
   int splits;
@@ -88,8 +89,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int splits = args.splits;
   const int rank = splits > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int n0 = blockIdx.y * BN;
-  const int m0 = blockIdx.z * BM;
+  const int m0 = blockIdx.y * BM;  // M tiles of one N tile are launch neighbours: W is read once
+  const int n0 = blockIdx.z * BN;
+  const uint32_t stage_bytes = static_cast<uint32_t>(args.a_rows * BK * 2 + W_STAGE);
   const int k_tiles = args.k_tiles;
   const int kt0 = rank * k_tiles;
 
@@ -121,7 +123,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // output) only after.  Fresh stages need no empty-barrier wait.
       const int pre = k_tiles < stages ? k_tiles : stages;
       for (int kt = 0; kt < pre; ++kt) {
-        mbar_arrive_expect_tx(full_bar(kt), A_STAGE + W_STAGE);
+        mbar_arrive_expect_tx(full_bar(kt), stage_bytes);
         tma_load_2d(smem_addr(w_st + kt * W_STAGE), &tmW, (kt0 + kt) * BK, n0, full_bar(kt), pol_w);
       }
       pdl_wait();
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           *abort_flag = 1;
           break;
         }
-        mbar_arrive_expect_tx(full_bar(s), A_STAGE + W_STAGE);
+        mbar_arrive_expect_tx(full_bar(s), stage_bytes);
         const int kx = (kt0 + kt) * BK;
         tma_load_2d(smem_addr(a_st + s * A_STAGE), &tmA, kx, m0, full_bar(s), pol_a);
         tma_load_2d(smem_addr(w_st + s * W_STAGE), &tmW, kx, n0, full_bar(s), pol_w);
@@ -293,16 +295,18 @@ struct Plan {
 };
 
 // The tile width and the K split depend on (N, K) only -- never on M -- so
-// every row meets the same reduction order whatever the batch.  They are
-// chosen to put at least two CTAs per SM in flight for a skinny (decode) M.
+// every row meets the same reduction order whatever the batch.  Measured on
+// the decode shapes: three 24 KB stages (three CTAs per SM) beat deeper rings,
+// and a split of K into up to four ranks that brings the CTA count to about
+// 256 beats both no split and eight ranks.  Wide outputs (the LM head) take
+// 128-wide tiles and no split.
 Plan plan_for(int N, int K) {
   const int kt = K / BK;
-  const int target = 2 * 148;
-  Plan p{64, 1, 4};
-  if (N / 128 >= target) p = Plan{128, 1, 3};
+  Plan p{64, 1, 3};
+  if (N >= 37888) p = Plan{128, 1, 3};
   const int tiles = (N + p.bn - 1) / p.bn;
   int s = 1;
-  while (s < 8 && tiles * s < target && kt % (2 * s) == 0 && kt / (2 * s) >= 4) s *= 2;
+  while (s < 4 && tiles * s < 256 && kt % (2 * s) == 0 && kt / (2 * s) >= 4) s *= 2;
   p.splits = s;
   return p;
 }
@@ -354,17 +358,22 @@ extern "C" kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int6
       (c_dtype == KINV_BF16 ? ldc % 8 : ldc % 4))
     return KINV_ERR_ALIGNMENT;
   const Plan p = plan_for(N, K);
-  const int grid_y = (N + p.bn - 1) / p.bn;
-  const int grid_z = (M + BM - 1) / BM;
+  const int grid_y = (M + BM - 1) / BM;
+  const int grid_z = (N + p.bn - 1) / p.bn;
   if (grid_y > 65535 || grid_z > 65535) return KINV_ERR_UNSUPPORTED;
+  // A tiles carry only the rows that exist (a multiple of 8 up to 128): zero
+  // fill of a mostly empty box is slow, and the tile rows beyond M feed only
+  // accumulator rows that are never stored.
+  const int a_rows = M >= BM ? BM : ((M + 7) / 8) * 8;
   CUtensorMap ta, tw;
-  if (!make_map(&ta, A, M, K, lda, BM) || !make_map(&tw, W, N, K, ldw, p.bn)) return KINV_ERR_CUDA;
+  if (!make_map(&ta, A, M, K, lda, a_rows) || !make_map(&tw, W, N, K, ldw, p.bn)) return KINV_ERR_CUDA;
   GemmArgs a;
   a.C = C;
   a.ldc = ldc;
   a.M = M;
   a.N = N;
   a.k_tiles = K / BK / p.splits;
+  a.a_rows = a_rows;
   a.c_f32 = c_dtype == KINV_F32;
   a.stages = p.stages;
   a.splits = p.splits;
