@@ -5,18 +5,22 @@
 //
 // A query row with L visible keys cuts them into splits of 256 keys at
 // absolute offsets 0, 256, 512, ...; the cut depends only on L.  Split kernel:
-// one thread block per (split, kv head, group of query rows of one sequence).
-// Thread t owns key t of the split.  For every query row r and query head i of
-// the kv head's group:
-//   s_t  = (q . k_t) * scale          fp32 fused multiply-adds over d ascending
-//   m    = max_t s_t                  (max is exact in any order)
+// one thread block per (split, kv head, group of query rows of one sequence);
+// K and then V stream through a ring of four 64-key stages (cp.async), so
+// loads stay in flight while the scores are formed.  For every query row r and
+// query head i of the kv head's group (a "pair"):
+//   s_t  = (q . k_t) * scale   four partial dot products over interleaved
+//                              16-byte chunks of d (fp32 FMAs, chunks
+//                              ascending), added by a fixed two-step butterfly
+//   m    = max_t s_t           (max is exact in any order)
 //   e_t  = exp(s_t - m)
-//   l    = sum_t e_t                  butterfly in each warp (lane 0), then the
-//                                     8 warp sums in ascending warp order
-//   o[d] = sum_t e_t v_t[d]           fused multiply-adds over t ascending
-// and (m, l, o) is stored as the split's fp32 partial.  Keys a row cannot see
-// (t >= its count) contribute e_t = 0 to the butterfly and are skipped in the
-// o sum, so a row's arithmetic is the same whichever rows share the block.
+//   l    = sum_t e_t           lane l sums keys l, l+32, ..., l+224 in order,
+//                              then a fixed butterfly over the 32 lanes
+//   o[d] = sum_t e_t v_t[d]    four key groups (t mod 4) each summed with FMAs
+//                              over t ascending, then a fixed butterfly
+// and (m, l, o) is stored as the split's fp32 partial.  A key a row cannot see
+// (beyond its count) gets e_t = 0 in l and is skipped in o, so a row's
+// arithmetic is the same whichever rows share the block.
 // Merge kernel: per (row, query head), fold the partials in ascending split
 // order with the log-sum-exp update, then o / l -> bf16.
 //
@@ -33,7 +37,7 @@ namespace kinv {
 namespace {
 
 constexpr int kSplit = 256;      // keys per split (the fixed split size)
-constexpr int kThreads = 256;    // one thread per key of a split
+constexpr int kThreads = 256;    // four per key of a 64-key stage
 constexpr int kMaxRG = 32;       // rows x query heads handled by one block
 constexpr int kMaxG = 8;         // query heads per kv head
 

@@ -14,7 +14,8 @@
 //    K only); the CTAs of one cluster compute one range each, and the partial
 //    sums are added in rank order p0 + p1 + ... through distributed shared
 //    memory -- no atomics, no batch-dependent split;
-//  * rows of A beyond M are zero-filled by TMA and never stored.
+//  * TMA brings in the rows of A that exist (M rounded up to 8, at most 128);
+//    the tile rows beyond them feed accumulator rows that are never stored.
 // Row i therefore meets the same instructions in the same order for every M,
 // at whichever lane of the tile it lands.
 //
