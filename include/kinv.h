@@ -90,9 +90,9 @@ kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int64_t ldw,
 /* --------------------------------------------------------------- RMSNorm
  * y[r][i] = x[r][i] / sqrt(mean_j x[r][j]^2 + eps) * w[i]
  * ("Deterministic and bit-exact inference", *technical*: batch-invariant
- * RMSNorm).  One thread block per row; the sum of squares is taken in a fixed
- * per-thread order, then a fixed shuffle tree, then a fixed cross-warp order,
- * so a row's bits do not depend on `rows`.
+ * RMSNorm).  One warp per row; each lane sums the squares of its chunks in a
+ * fixed order, then a fixed xor butterfly adds the 32 lane sums, so a row's
+ * bits do not depend on `rows` or on which rows share a thread block.
  * residual (nullable): when given, s = bf16(x + residual) is formed first,
  * written back into `x` (the new residual stream), and y = RMSNorm(s).
  * x, residual, y: device bf16 [rows][dim] with leading dims ldx, ldx, ldy.

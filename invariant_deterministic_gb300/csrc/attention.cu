@@ -121,8 +121,10 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   pdl_wait();
   RowSet rs;
   if (!block_rows(p, rs)) return;
-  const int s = blockIdx.x;
-  const int g = blockIdx.y;
+  // kv heads are the fastest grid index: the blocks reading the 256-byte
+  // slices of the same token rows run side by side
+  const int g = blockIdx.x;
+  const int s = blockIdx.y;
   const int k0 = s * kSplit;
   const int lenmax = rs.len0 + rs.nrows - 1;           // the last row sees the most keys
   const int nmax = min(kSplit, lenmax - k0);
@@ -464,7 +466,7 @@ extern "C" kinv_status kinv_attn_decode(const void* q, const void* k_cache, cons
   p.groups_per_seq = 1;
   p.rg_cap = ((p.G + 3) / 4) * 4;
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
-  const dim3 split_grid(S, Hkv, B), merge_grid(Hq, B, 1);
+  const dim3 split_grid(Hkv, S, B), merge_grid(Hq, B, 1);
   return D == 128 ? launch<128>(p, split_grid, merge_grid, stream)
                   : launch<64>(p, split_grid, merge_grid, stream);
 }
@@ -514,7 +516,7 @@ extern "C" kinv_status kinv_attn_prefill(const void* q, const void* k_cache, con
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   const int64_t groups = static_cast<int64_t>(B) * p.groups_per_seq;
   if (groups > 65535 || max_q_len > 65535 || B > 65535) return KINV_ERR_UNSUPPORTED;
-  const dim3 split_grid(S, Hkv, static_cast<unsigned>(groups)), merge_grid(Hq, max_q_len, B);
+  const dim3 split_grid(Hkv, S, static_cast<unsigned>(groups)), merge_grid(Hq, max_q_len, B);
   return D == 128 ? launch<128>(p, split_grid, merge_grid, stream)
                   : launch<64>(p, split_grid, merge_grid, stream);
 }

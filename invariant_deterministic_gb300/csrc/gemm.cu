@@ -62,6 +62,7 @@ struct GemmArgs {
   int M, N;
   int k_tiles;  // 64-wide K blocks per split
   int a_rows;   // rows of A that TMA brings in per tile (the rest of the 128 are never stored)
+  int a_stride; // bytes between A stages (a_rows * 128)
   int c_f32;
   int stages;
   int splits;
@@ -78,8 +79,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int stages = args.stages;
+  // A stages first, then W stages.  An MMA reads 128 rows (16 KB) from the
+  // start of an A stage; when a stage holds fewer rows the extra rows come
+  // from the following stages (inside this block's shared memory) and only
+  // feed accumulator rows that are never stored.
+  const int a_stride = args.a_stride;
   unsigned char* a_st = base;
-  unsigned char* w_st = base + stages * A_STAGE;
+  unsigned char* w_st = base + stages * a_stride;
   uint64_t* bars = reinterpret_cast<uint64_t*>(w_st + stages * W_STAGE);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -129,7 +135,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       pdl_wait();
       for (int kt = 0; kt < pre; ++kt)
-        tma_load_2d(smem_addr(a_st + kt * A_STAGE), &tmA, (kt0 + kt) * BK, m0, full_bar(kt), pol_a);
+        tma_load_2d(smem_addr(a_st + kt * a_stride), &tmA, (kt0 + kt) * BK, m0, full_bar(kt), pol_a);
       issued = pre;
       for (int kt = pre; kt < k_tiles; ++kt) {
         const int s = kt % stages;
@@ -141,7 +147,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         mbar_arrive_expect_tx(full_bar(s), stage_bytes);
         const int kx = (kt0 + kt) * BK;
-        tma_load_2d(smem_addr(a_st + s * A_STAGE), &tmA, kx, m0, full_bar(s), pol_a);
+        tma_load_2d(smem_addr(a_st + s * a_stride), &tmA, kx, m0, full_bar(s), pol_a);
         tma_load_2d(smem_addr(w_st + s * W_STAGE), &tmW, kx, n0, full_bar(s), pol_w);
         ++issued;
       }
@@ -159,7 +165,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a_addr = smem_addr(a_st + s * A_STAGE);
+        const uint32_t a_addr = smem_addr(a_st + s * a_stride);
         const uint32_t w_addr = smem_addr(w_st + s * W_STAGE);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
@@ -292,7 +298,8 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int
 }
 
 struct Plan {
-  int bn, splits, stages;
+  int bn, splits;
+  int smem_budget;  // bytes of stage ring per block (sets blocks per SM)
 };
 
 // The tile width and the K split depend on (N, K) only -- never on M -- so
@@ -303,8 +310,8 @@ struct Plan {
 // 128-wide tiles and no split.
 Plan plan_for(int N, int K) {
   const int kt = K / BK;
-  Plan p{64, 1, 3};
-  if (N >= 37888) p = Plan{128, 1, 3};
+  Plan p{64, 1, 72 * 1024};
+  if (N >= 37888) p = Plan{128, 1, 96 * 1024};
   const int tiles = (N + p.bn - 1) / p.bn;
   int s = 1;
   while (s < 4 && tiles * s < 256 && kt % (2 * s) == 0 && kt / (2 * s) >= 4) s *= 2;
@@ -313,16 +320,25 @@ Plan plan_for(int N, int K) {
 }
 
 template <int BN>
-size_t smem_bytes(int stages) {
-  return 1024 + static_cast<size_t>(stages) * (A_STAGE + BN * BK * 2) + (2 * stages + 1) * 8 + 16;
+size_t smem_bytes(int stages, int a_stride) {
+  return 1024 + static_cast<size_t>(stages) * (a_stride + BN * BK * 2) + (2 * stages + 1) * 8 + 16;
 }
 
 template <int BN>
-kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, const GemmArgs& a, int grid_y,
-                        int grid_z, cudaStream_t stream) {
-  const size_t smem = smem_bytes<BN>(a.stages);
-  if (a.splits > 1 && static_cast<size_t>(BM) * (BN + 1) * 4 > static_cast<size_t>(a.stages) * (A_STAGE + BN * BK * 2))
-    return KINV_ERR_UNSUPPORTED;
+kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a, int budget,
+                        int grid_y, int grid_z, cudaStream_t stream) {
+  // As many stages as the budget holds (2..8): small M leaves room for more
+  // weight tiles in flight.  The ring must also hold the split-K partial tile
+  // and the 128 rows one MMA reads from the start of the last A stage.
+  const int stage = a.a_stride + BN * BK * 2;
+  int stages = budget / stage;
+  stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
+  while (static_cast<size_t>(stages) * stage < static_cast<size_t>(BM) * (BN + 1) * 4 ||
+         (stages - 1) * a.a_stride + A_STAGE > stages * stage)
+    ++stages;
+  a.stages = stages;
+  const size_t smem = smem_bytes<BN>(stages, a.a_stride);
+  if (smem > static_cast<size_t>(max_smem_optin())) return KINV_ERR_UNSUPPORTED;
   // the opt-in limit is raised once per device to the largest request seen
   static size_t configured[64] = {};
   static std::mutex mu;
@@ -375,13 +391,14 @@ extern "C" kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int6
   a.N = N;
   a.k_tiles = K / BK / p.splits;
   a.a_rows = a_rows;
+  a.a_stride = a_rows * BK * 2;
   a.c_f32 = c_dtype == KINV_F32;
-  a.stages = p.stages;
+  a.stages = 0;
   a.splits = p.splits;
   a.status = device_status_word();
   switch (p.bn) {
-    case 64: return launch_gemm<64>(ta, tw, a, grid_y, grid_z, stream);
-    case 128: return launch_gemm<128>(ta, tw, a, grid_y, grid_z, stream);
+    case 64: return launch_gemm<64>(ta, tw, a, p.smem_budget, grid_y, grid_z, stream);
+    case 128: return launch_gemm<128>(ta, tw, a, p.smem_budget, grid_y, grid_z, stream);
     default: return KINV_ERR_UNSUPPORTED;
   }
 }

@@ -5,6 +5,8 @@
 // per head exactly as in kinv_rmsnorm's scheme (per-lane, butterfly, lane 0).
 #include <math.h>
 
+#include <cmath>
+
 #include "common.cuh"
 
 namespace kinv {
@@ -59,9 +61,14 @@ __global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ gu, int64_t ld_g
   *reinterpret_cast<uint4*>(out + r * ld_out + c) = o;
 }
 
+// Inverse frequencies base^(-2i/D), formed once per call on the host in fp64.
+struct RopeFreqs {
+  double inv_freq[64];
+};
+
 // One block per row.  The first D/2 threads compute this row's rotation
-// angles in fp64 (theta_i = p * base^(-2i/D)) into shared memory; then each
-// warp takes whole heads.  Lane l of a warp holds the pairs
+// angles in fp64 (theta_i = p * inv_freq_i, then sin and cos) into shared
+// memory; then each warp takes whole heads.  Lane l of a warp holds the pairs
 // (i, i + D/2) for i in {l * P .. l * P + P - 1}, P = D / 64.
 template <int D>
 __global__ void rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int64_t ld_qkv,
@@ -72,7 +79,7 @@ __global__ void rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int64_
                                    const int32_t* __restrict__ pos,
                                    const __nv_bfloat16* __restrict__ q_norm,
                                    const __nv_bfloat16* __restrict__ k_norm, float eps, int Hq,
-                                   int Hkv, double rope_base) {
+                                   int Hkv, const RopeFreqs freqs) {
   constexpr int HALF = D / 2;
   constexpr int P = D / 64;  // pairs per lane
   __shared__ float cs[HALF], sn[HALF];
@@ -82,9 +89,8 @@ __global__ void rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int64_
   const int p = pos[r];
   const int s = seq[r];
   for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
-    const double inv_freq = pow(rope_base, -2.0 * i / D);
     double sv, cv;
-    sincos(static_cast<double>(p) * inv_freq, &sv, &cv);
+    sincos(static_cast<double>(p) * freqs.inv_freq[i], &sv, &cv);
     cs[i] = static_cast<float>(cv);
     sn[i] = static_cast<float>(sv);
   }
@@ -233,6 +239,8 @@ extern "C" kinv_status kinv_rope_append(const void* qkv, int64_t ld_qkv, void* q
   if (!aligned16(qkv) || !aligned16(q_out) || !aligned16(k_cache) || !aligned16(v_cache) ||
       ld_qkv % 8 || seq_stride % 8 || tok_stride % 8)
     return KINV_ERR_ALIGNMENT;
+  RopeFreqs freqs;
+  for (int i = 0; i < D / 2; ++i) freqs.inv_freq[i] = std::pow(static_cast<double>(rope_base), -2.0 * i / D);
   const int heads = Hq + 2 * Hkv;
   int threads = 32 * (heads < 8 ? heads : 8);
   if (threads < 64) threads = 64;
@@ -245,10 +253,10 @@ extern "C" kinv_status kinv_rope_append(const void* qkv, int64_t ld_qkv, void* q
   if (D == 128)
     return launch_kernel(rope_append_kernel<128>, dim3(rows), dim3(threads), 0, stream, 1, src,
                          ld_qkv, qo, k, v, seq_stride, tok_stride, seq, pos, qn, kn, eps, Hq, Hkv,
-                         static_cast<double>(rope_base));
+                         freqs);
   return launch_kernel(rope_append_kernel<64>, dim3(rows), dim3(threads), 0, stream, 1, src, ld_qkv,
                        qo, k, v, seq_stride, tok_stride, seq, pos, qn, kn, eps, Hq, Hkv,
-                       static_cast<double>(rope_base));
+                       freqs);
 }
 
 extern "C" kinv_status kinv_decode_advance(const int32_t* tokens, int32_t* history, int hist_ld,
