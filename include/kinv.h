@@ -90,9 +90,10 @@ kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int64_t ldw,
 /* --------------------------------------------------------------- RMSNorm
  * y[r][i] = x[r][i] / sqrt(mean_j x[r][j]^2 + eps) * w[i]
  * ("Deterministic and bit-exact inference", *technical*: batch-invariant
- * RMSNorm).  One warp per row; each lane sums the squares of its chunks in a
- * fixed order, then a fixed xor butterfly adds the 32 lane sums, so a row's
- * bits do not depend on `rows` or on which rows share a thread block.
+ * RMSNorm).  One thread block per row, its size a function of `dim`; each
+ * thread sums the squares of its chunks in a fixed order, a fixed xor
+ * butterfly adds the lanes of a warp, and the warp sums are added in
+ * ascending order, so a row's bits do not depend on `rows`.
  * residual (nullable): when given, s = bf16(x + residual) is formed first,
  * written back into `x` (the new residual stream), and y = RMSNorm(s).
  * x, residual, y: device bf16 [rows][dim] with leading dims ldx, ldx, ldy.

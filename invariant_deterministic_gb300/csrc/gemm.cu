@@ -313,9 +313,14 @@ Plan plan_for(int N, int K) {
   Plan p{64, 1, 72 * 1024};
   if (N >= 37888) p = Plan{128, 1, 96 * 1024};
   const int tiles = (N + p.bn - 1) / p.bn;
+  // a long K (the down projection) takes up to eight ranks and a 48 KB ring
+  const bool long_k = K >= 8192;
+  const int max_s = long_k ? 8 : 4;
+  const int want = long_k ? 512 : 256;
   int s = 1;
-  while (s < 4 && tiles * s < 256 && kt % (2 * s) == 0 && kt / (2 * s) >= 4) s *= 2;
+  while (s < max_s && tiles * s < want && kt % (2 * s) == 0 && kt / (2 * s) >= 4) s *= 2;
   p.splits = s;
+  if (s == 8) p.smem_budget = 48 * 1024;
   return p;
 }
 

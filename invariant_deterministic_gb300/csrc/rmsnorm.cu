@@ -2,20 +2,18 @@
 // *technical*: RMSNorm made batch-invariant by fixing each row's reduction
 // order).
 //
-// One warp per row (eight rows per 256-thread block; which block a row lands
-// in does not touch its arithmetic).  Lane l owns the 8-element chunks
-// l, l + 32, l + 64, ... of the row and sums their squares in that order with
-// fused multiply-adds; a fixed xor butterfly over the 32 lanes adds the lane
-// sums (every lane ends with the same bits).  Nothing depends on the number
-// of rows, so a row's bits are the same in any batch.  With a residual, the
-// first pass also forms and stores s = bf16(x + r); the second pass re-reads
-// the lane's own chunks of s (written by the same lane).
+// One thread block per row.  The block size depends only on `dim`; thread t
+// owns the 8-element chunks t, t + T, t + 2T, ... (all loaded up front) and
+// sums their squares in that order with fused multiply-adds; a fixed xor
+// butterfly adds the 32 lane sums of a warp (every lane ends with the same
+// bits); the warp sums are added in ascending warp order.  Nothing depends on
+// the number of rows, so a row's bits are the same in any batch.
 #include "common.cuh"
 
 namespace kinv {
 namespace {
 
-constexpr int kRowsPerBlock = 8;
+constexpr int kMaxChunksPerThread = 8;  // dim <= 256 threads * 8 chunks * 8
 
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
   f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x);
@@ -33,44 +31,68 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   return o;
 }
 
-__global__ void __launch_bounds__(32 * kRowsPerBlock)
+__global__ void __launch_bounds__(256)
     rmsnorm_kernel(__nv_bfloat16* x, int64_t ldx, const __nv_bfloat16* __restrict__ residual,
                    const __nv_bfloat16* __restrict__ w, __nv_bfloat16* __restrict__ y, int64_t ldy,
-                   int rows, int dim, float eps) {
+                   int dim, float eps) {
+  __shared__ float warp_sums[8];
   pdl_launch_dependents();
   pdl_wait();
-  const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
+  const int row = blockIdx.x;
+  const int t = threadIdx.x;
+  const int T = blockDim.x;
+  const int lane = t & 31;
   const int chunks = dim >> 3;
   __nv_bfloat16* xr = x + row * ldx;
   const __nv_bfloat16* rr = residual ? residual + row * ldx : nullptr;
 
-  float acc = 0.f;
-  for (int c = lane; c < chunks; c += 32) {
-    float v[8];
-    unpack8(*reinterpret_cast<const uint4*>(xr + c * 8), v);
-    if (rr) {
-      float r8[8];
-      unpack8(*reinterpret_cast<const uint4*>(rr + c * 8), r8);
+  uint4 raw[kMaxChunksPerThread];
+  uint4 rraw[kMaxChunksPerThread];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = __bfloat162float(__float2bfloat16_rn(v[e] + r8[e]));
-      *reinterpret_cast<uint4*>(xr + c * 8) = pack8(v);
+  for (int i = 0; i < kMaxChunksPerThread; ++i) {
+    const int c = t + i * T;
+    if (c < chunks) {
+      raw[i] = *reinterpret_cast<const uint4*>(xr + c * 8);
+      if (rr) rraw[i] = *reinterpret_cast<const uint4*>(rr + c * 8);
     }
+  }
+  float v[kMaxChunksPerThread][8];
+  float acc = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc = fmaf(v[e], v[e], acc);
+  for (int i = 0; i < kMaxChunksPerThread; ++i) {
+    const int c = t + i * T;
+    if (c < chunks) {
+      unpack8(raw[i], v[i]);
+      if (rr) {
+        float r8[8];
+        unpack8(rraw[i], r8);
+        // the new residual stream s = bf16(x + r), kept as bf16 values
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[i][e] = __bfloat162float(__float2bfloat16_rn(v[i][e] + r8[e]));
+        *reinterpret_cast<uint4*>(xr + c * 8) = pack8(v[i]);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc = fmaf(v[i][e], v[i][e], acc);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
-  const float inv = 1.0f / sqrtf(acc / static_cast<float>(dim) + eps);
+  if (lane == 0) warp_sums[t >> 5] = acc;
+  __syncthreads();
+  float ss = warp_sums[0];
+  for (int i = 1; i < (T >> 5); ++i) ss = __fadd_rn(ss, warp_sums[i]);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(dim) + eps);
   __nv_bfloat16* yr = y + row * ldy;
-  for (int c = lane; c < chunks; c += 32) {
-    float v[8], g[8];
-    unpack8(*reinterpret_cast<const uint4*>(xr + c * 8), v);
-    unpack8(*reinterpret_cast<const uint4*>(w + c * 8), g);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = v[e] * inv * g[e];
-    *reinterpret_cast<uint4*>(yr + c * 8) = pack8(v);
+  for (int i = 0; i < kMaxChunksPerThread; ++i) {
+    const int c = t + i * T;
+    if (c < chunks) {
+      float g[8];
+      unpack8(*reinterpret_cast<const uint4*>(w + c * 8), g);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[i][e] = v[i][e] * inv * g[e];
+      *reinterpret_cast<uint4*>(yr + c * 8) = pack8(v[i]);
+    }
   }
 }
 
@@ -84,14 +106,16 @@ extern "C" kinv_status kinv_rmsnorm(void* x, int64_t ldx, const void* residual, 
   if (rows < 0 || dim <= 0 || !(eps >= 0.f)) return KINV_ERR_INVALID_ARG;
   if (rows == 0) return KINV_OK;
   if (!x || !w || !y) return KINV_ERR_INVALID_ARG;
-  if (dim % 8 != 0 || dim > 16384) return KINV_ERR_UNSUPPORTED;
+  if (dim % 8 != 0 || dim > 256 * 8 * kMaxChunksPerThread) return KINV_ERR_UNSUPPORTED;
   if (ldx < dim || ldy < dim) return KINV_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (residual && !aligned16(residual)) ||
       ldx % 8 || ldy % 8)
     return KINV_ERR_ALIGNMENT;
-  const int blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
-  return launch_kernel(rmsnorm_kernel, dim3(blocks), dim3(32 * kRowsPerBlock), 0, stream, 1,
+  if (rows > 2147483647 / 2) return KINV_ERR_UNSUPPORTED;
+  const int chunks = dim / 8;
+  const int threads = chunks < 256 ? ((chunks + 31) / 32) * 32 : 256;
+  return launch_kernel(rmsnorm_kernel, dim3(rows), dim3(threads), 0, stream, 1,
                        static_cast<__nv_bfloat16*>(x), ldx, static_cast<const __nv_bfloat16*>(residual),
-                       static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(y), ldy, rows,
-                       dim, eps);
+                       static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(y), ldy, dim,
+                       eps);
 }
