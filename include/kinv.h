@@ -133,6 +133,34 @@ kinv_status kinv_attn_decode(const void* q, const void* k_cache, const void* v_c
                              float scale, void* workspace, size_t workspace_bytes,
                              kinv_stream stream);
 
+/* --------------------------------------- decode attention, no allocation
+ * The pages have no counterpart to this call: it exists for callers that
+ * cannot allocate device memory.  Some code cannot call cudaMalloc -- a plug-in
+ * whose host program owns every byte of device memory through its own pool, a
+ * real-time loop that must not take the allocator's implicit device-wide
+ * synchronisation, or a binding with no device allocator at all -- and so
+ * cannot provide the scratch that kinv_attn_decode takes as `workspace`.
+ *
+ * Same arguments, arithmetic and output bits as kinv_attn_decode, minus the
+ * workspace: the split partials live in a scratch array compiled into the
+ * library (KINV_NOALLOC_SCRATCH_BYTES bytes on every GPU that loads it, held
+ * until the process exits).  Nothing is allocated or freed.
+ *  - A call whose partials need more than KINV_NOALLOC_SCRATCH_BYTES (that is,
+ *    kinv_attn_decode_workspace(B, Hq, D, Lmax, split_len) is larger) returns
+ *    KINV_ERR_WORKSPACE and launches nothing.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array, which keeps whatever the
+ *    last call left in it (each call writes every partial it later reads, so
+ *    nothing needs clearing).  Calls that overlap on the GPU -- on two streams,
+ *    or from two threads -- race on it: serialise them. */
+#define KINV_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+kinv_status kinv_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                     int64_t seq_stride, int64_t tok_stride,
+                                     const int32_t* kv_len, void* out,
+                                     int B, int Hq, int Hkv, int D, int Lmax, int split_len,
+                                     float scale, kinv_stream stream);
+
 /* ----------------------------------------------------- prefill attention
  * Causal attention for chunks of new query rows against the cache (which
  * must already hold their keys).  Sequence b contributes q_len[b] rows,

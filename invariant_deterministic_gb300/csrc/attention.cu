@@ -520,3 +520,82 @@ extern "C" kinv_status kinv_attn_prefill(const void* q, const void* k_cache, con
   return D == 128 ? launch<128>(p, split_grid, merge_grid, stream)
                   : launch<64>(p, split_grid, merge_grid, stream);
 }
+
+// ---------------------------------------------------------------------------
+// kinv_attn_decode_noalloc: decode attention for callers that cannot allocate
+// device memory.  The split partials go to a scratch array compiled into the
+// library instead of a caller-provided workspace.
+
+#include <mutex>
+
+// Scratch shared by every kinv_attn_decode_noalloc call on a device (held by
+// each GPU that loads the library until the process exits).
+static __device__ __align__(256) unsigned char kinv_noalloc_scratch[KINV_NOALLOC_SCRATCH_BYTES];
+
+namespace kinv {
+namespace {
+
+// In host code the array's name is a host-side stand-in, not a device
+// address: the device address is looked up once per device, with that device
+// current, and cached.
+void* noalloc_scratch_address() {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, kinv_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace kinv
+
+extern "C" kinv_status kinv_attn_decode_noalloc(const void* q, const void* k_cache,
+                                                const void* v_cache, int64_t seq_stride,
+                                                int64_t tok_stride, const int32_t* kv_len,
+                                                void* out, int B, int Hq, int Hkv, int D, int Lmax,
+                                                int split_len, float scale, kinv_stream stream) {
+  if (B < 0 || Lmax < 0) return KINV_ERR_INVALID_ARG;
+  if (B == 0) return KINV_OK;
+  if (!kv_len || Hq <= 0 || D <= 0) return KINV_ERR_INVALID_ARG;
+  if (B > 65535) return KINV_ERR_UNSUPPORTED;
+  if (split_len != kSplit) return KINV_ERR_UNSUPPORTED;
+  const int S = Lmax > 0 ? (Lmax + kSplit - 1) / kSplit : 1;
+  const size_t need = workspace_bytes(B, Hq, D, S);
+  if (need > static_cast<size_t>(KINV_NOALLOC_SCRATCH_BYTES)) return KINV_ERR_WORKSPACE;
+  // shape and alignment checks first (no CUDA call), with a stand-in pointer
+  const void* aligned_placeholder = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+  kinv_status st = check_common(q, k_cache, v_cache, seq_stride, tok_stride, out, Hq, Hkv, D,
+                                split_len, aligned_placeholder);
+  if (st != KINV_OK) return st;
+  void* scratch = noalloc_scratch_address();
+  if (!scratch) return KINV_ERR_CUDA;
+  AttnParams p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k_cache);
+  p.v = static_cast<const __nv_bfloat16*>(v_cache);
+  p.seq_stride = seq_stride;
+  p.tok_stride = tok_stride;
+  p.kv_len = kv_len;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.ws_o = static_cast<float*>(scratch);
+  const size_t o_bytes = static_cast<size_t>(B) * Hq * S * D * 4;
+  p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + ((o_bytes + 255) / 256) * 256);
+  p.prefill = 0;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.R = 1;
+  p.S = S;
+  p.groups_per_seq = 1;
+  p.rg_cap = ((p.G + 3) / 4) * 4;
+  p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
+  const dim3 split_grid(Hkv, S, B), merge_grid(Hq, B, 1);
+  return D == 128 ? launch<128>(p, split_grid, merge_grid, stream)
+                  : launch<64>(p, split_grid, merge_grid, stream);
+}

@@ -43,6 +43,8 @@ SIGNATURES = {
     "kinv_attn_decode_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "kinv_attn_decode": (_i32, [_c_p, _c_p, _c_p, _i64, _i64, _c_p, _c_p, _i32, _i32, _i32, _i32,
                                 _i32, _i32, _f32, _c_p, _sz, _c_p]),
+    "kinv_attn_decode_noalloc": (_i32, [_c_p, _c_p, _c_p, _i64, _i64, _c_p, _c_p, _i32, _i32, _i32,
+                                        _i32, _i32, _i32, _f32, _c_p]),
     "kinv_attn_prefill_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "kinv_attn_prefill": (_i32, [_c_p, _c_p, _c_p, _i64, _i64, _c_p, _c_p, _c_p, _c_p, _i32, _i32,
                                  _i32, _i32, _i32, _i32, _i32, _i32, _f32, _c_p, _sz, _c_p]),
@@ -175,6 +177,26 @@ def attn_decode(q, k_cache, v_cache, kv_len, out=None, workspace=None, split_len
                                   k_cache.stride(1), _ptr(kv_len), _ptr(out), bsz, hq, hkv, d, lmax,
                                   split_len, float(scale), _ptr(workspace), workspace.numel(),
                                   _stream(stream)), "kinv_attn_decode")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def attn_decode_noalloc(q, k_cache, v_cache, kv_len, out, split_len=SPLIT_LEN, scale: float = 0.0,
+                        stream=None):
+    """Decode attention for callers that cannot allocate device memory: the
+    library's own scratch array holds the partials (up to
+    NOALLOC_SCRATCH_BYTES; calls sharing a device must not overlap on the GPU).
+    ``out`` must be given, since this path allocates nothing."""
+    _need(q, torch.bfloat16, "q")
+    _need(kv_len, torch.int32, "kv_len")
+    bsz, hq, d = q.shape
+    lmax, hkv = k_cache.shape[1], k_cache.shape[2]
+    _check(lib().kinv_attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.stride(0),
+                                          k_cache.stride(1), _ptr(kv_len), _ptr(out), bsz, hq, hkv,
+                                          d, lmax, split_len, float(scale), _stream(stream)),
+           "kinv_attn_decode_noalloc")
     return out
 
 
