@@ -48,6 +48,18 @@ def build_id() -> str:
     return h.hexdigest()[:16]
 
 
+def source_hash(names) -> str:
+    """16 hex digits over the named csrc files (plus the shared header): a
+    measurement taken on a kernel stays valid while this value is unchanged."""
+    h = hashlib.sha256()
+    for name in sorted(set(list(names) + ["common.cuh"])):
+        with open(os.path.join(CSRC, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
+    h.update(" ".join(ARCH + FLAGS).encode())
+    return h.hexdigest()[:16]
+
+
 def build(verbose: bool = False, force: bool = False) -> str:
     """Compile (if needed) and return the path of libkinv.so."""
     bid = build_id()

@@ -221,11 +221,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // Constant split-K: park this CTA's fp32 partial tile in its own shared
-    // memory (the stage ring is idle now), then rank q reduces rows
-    // [q * 128 / splits, (q + 1) * 128 / splits) over all ranks in rank order.
+    // memory (the stage ring is idle now), then rank q reduces columns
+    // [q * BN / splits, (q + 1) * BN / splits) of every row present, over all
+    // ranks in rank order p0 + p1 + ...
     constexpr int LDR = BN + 1;
     float* red = reinterpret_cast<float*>(base);
-    if (good) {
+    const int rows_here = args.M - m0 < BM ? args.M - m0 : BM;
+    if (good && warp * 32 < rows_here) {
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t r[32];
@@ -235,17 +237,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
     cluster_sync();
-    const int rows_per = BM / splits;
-    const int rbase = rank * rows_per;
+    const int cols_per = BN / splits;
+    const int cbase = rank * cols_per;
     if (good) {
-      for (int idx = threadIdx.x; idx < rows_per * BN; idx += kGemmThreads) {
-        const int rl = rbase + idx / BN;
-        const int col = idx % BN;
+      for (int idx = threadIdx.x; idx < rows_here * cols_per; idx += kGemmThreads) {
+        const int rl = idx / cols_per;
+        const int col = cbase + idx % cols_per;
         const int mm = m0 + rl, nn = n0 + col;
-        if (mm >= args.M || nn >= args.N) continue;
+        if (nn >= args.N) continue;
         const uint32_t local = smem_addr(red + rl * LDR + col);
-        float acc = ld_dsmem_f32(map_to_rank(local, 0));
-        for (int q = 1; q < splits; ++q) acc = __fadd_rn(acc, ld_dsmem_f32(map_to_rank(local, q)));
+        float part[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < splits) part[q] = ld_dsmem_f32(map_to_rank(local, q));
+        float acc = part[0];
+#pragma unroll
+        for (int q = 1; q < 8; ++q)
+          if (q < splits) acc = __fadd_rn(acc, part[q]);
         if (args.c_f32)
           static_cast<float*>(args.C)[mm * args.ldc + nn] = acc;
         else

@@ -89,10 +89,16 @@ __global__ void rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int64_
   const int p = pos[r];
   const int s = seq[r];
   for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
-    double sv, cv;
-    sincos(static_cast<double>(p) * freqs.inv_freq[i], &sv, &cv);
-    cs[i] = static_cast<float>(cv);
-    sn[i] = static_cast<float>(sv);
+    // theta in fp64, reduced to [-pi, pi] in fp64 (2 pi split into a head
+    // and a tail), then sin and cos of the reduced angle in fp32
+    const double theta = static_cast<double>(p) * freqs.inv_freq[i];
+    const double k = rint(theta * 0.15915494309189535);  // 1 / (2 pi)
+    double r = fma(-k, 6.283185307179586, theta);
+    r = fma(-k, 2.4492935982947064e-16, r);
+    float sv, cv;
+    sincosf(static_cast<float>(r), &sv, &cv);
+    cs[i] = cv;
+    sn[i] = sv;
   }
   __syncthreads();
   const int lane = threadIdx.x & 31;
