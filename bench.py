@@ -27,6 +27,16 @@ sys.path.insert(0, ROOT)
 METRIC = "decode tokens/s (8B-shaped, batch 1-256) and % of HBM / tensor-core roofline"
 UNIT = "tokens/s"
 
+# DRAM bytes (read + write) per launch of each GEMM projection at batch 16,
+# from one `ncu --set full` capture (profiles/gemm_kernel_qwen3_8b_decode_b16.md).
+# Reported only while the GEMM's sources still hash to `src`.
+NCU_GEMM_TRAFFIC = {
+    "src": "fc4cfa6b2326b09e",
+    "batch": 16,
+    "bytes": {"gemm_qkv": 50.504e6, "gemm_o": 33.719e6, "gemm_gate_up": 204.304e6,
+              "gemm_down": 103.801e6, "gemm_lm_head": 1251.728e6},
+}
+
 
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -254,14 +264,23 @@ def run_kinv(args):
                           "gbs": gemm_b[k] / (kernel_ms[k] / 1e3) / 1e9,
                           "frac": gemm_b[k] / (kernel_ms[k] / 1e3) / 1e9 / hbm_peak}
                       for k in gemm_b if k in kernel_ms}
+        # per-launch DRAM bytes from the ncu capture, averaged like `achieved`
+        # (over the step's GEMM launches), while the GEMM sources are unchanged
         traffic = None
+        n_launch = sum(kernel_n.get(k, 0) for k in gemm_b)
+        if build.source_hash(["gemm.cu"]) == NCU_GEMM_TRAFFIC["src"] and bsz == NCU_GEMM_TRAFFIC["batch"]:
+            tb = NCU_GEMM_TRAFFIC["bytes"]
+            traffic = round(sum(tb[k] * kernel_n.get(k, 0) for k in tb) / n_launch)
+        alg_per_launch = round(gemm_bytes_step / n_launch)
     else:
         dom = "attn_split_kernel + attn_merge_kernel (split-KV decode attention)"
         achieved = attn_b / (kernel_ms["attn_decode"] / 1e3) / 1e9
         per_launch = {"attn_decode": {"bytes": attn_b, "ms": kernel_ms["attn_decode"]}}
         traffic = None
+        alg_per_launch = attn_b
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm_peak,
                 "unit": "GB/s", "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                "algorithmic_bytes_per_launch": alg_per_launch,
                 "peak_kind": f"{peak_kind} (copy bandwidth)", "per_launch": per_launch,
                 "step_share": {k: round(v / sum(total.values()), 4) for k, v in
                                sorted(total.items(), key=lambda kv: -kv[1])}}

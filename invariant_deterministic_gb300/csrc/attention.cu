@@ -5,22 +5,21 @@
 //
 // A query row with L visible keys cuts them into splits of 256 keys at
 // absolute offsets 0, 256, 512, ...; the cut depends only on L.  Split kernel:
-// one thread block per (split, kv head, group of query rows of one sequence);
-// K and then V stream through a ring of four 64-key stages (cp.async), so
-// loads stay in flight while the scores are formed.  For every query row r and
-// query head i of the kv head's group (a "pair"):
-//   s_t  = (q . k_t) * scale   four partial dot products over interleaved
-//                              16-byte chunks of d (fp32 FMAs, chunks
-//                              ascending), added by a fixed two-step butterfly
+// one thread block (eight warps) per (split, kv head, group of query rows of
+// one sequence); up to 16 (row, query head) pairs form the 16 rows of
+// warp-level tensor-core MMAs (m16n8k16, bf16 inputs, fp32 accumulation).
+// K, then V, arrive in shared memory through cp.async.  For every pair:
+//   s_t  = (q . k_t) * scale   warp w forms keys 32w..32w+31: eight 16-wide
+//                              k steps of d, ascending, accumulated in fp32
 //   m    = max_t s_t           (max is exact in any order)
-//   e_t  = exp(s_t - m)
-//   l    = sum_t e_t           lane l sums keys l, l+32, ..., l+224 in order,
-//                              then a fixed butterfly over the 32 lanes
-//   o[d] = sum_t e_t v_t[d]    four key groups (t mod 4) each summed with FMAs
-//                              over t ascending, then a fixed butterfly
-// and (m, l, o) is stored as the split's fp32 partial.  A key a row cannot see
-// (beyond its count) gets e_t = 0 in l and is skipped in o, so a row's
-// arithmetic is the same whichever rows share the block.
+//   p_t  = bf16(exp(s_t - m))  the weights are rounded to bf16 once
+//   l    = sum_t p_t           a lane's eight keys in order, a fixed
+//                              butterfly over four lanes, warps in order
+//   o[d] = sum_t p_t v_t[d]    sixteen 16-key k steps, ascending, in fp32
+// and (m, l, o) is stored as the split's fp32 partial.  A key a pair cannot
+// see (beyond its count) gets p_t = 0; keys past the split's end read zero V.
+// An MMA row depends only on its own q row and weights, so a pair's bits are
+// the same whichever pairs share the block.
 // Merge kernel: per (row, query head), fold the partials in ascending split
 // order with the log-sum-exp update, then o / l -> bf16.
 //
@@ -37,8 +36,8 @@ namespace kinv {
 namespace {
 
 constexpr int kSplit = 256;      // keys per split (the fixed split size)
-constexpr int kThreads = 256;    // four per key of a 64-key stage
-constexpr int kMaxRG = 32;       // rows x query heads handled by one block
+constexpr int kThreads = 256;    // eight warps, 32 keys each for the scores
+constexpr int kRowsMma = 16;     // (row, head) pairs of one block: the MMA's 16 rows
 constexpr int kMaxG = 8;         // query heads per kv head
 
 struct AttnParams {
@@ -101,21 +100,42 @@ __device__ __forceinline__ bool block_rows(const AttnParams& p, RowSet& rs) {
   return true;
 }
 
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// D = A . B + D, one 16 x 8 x 16 warp MMA, bf16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p) {
   constexpr int C8 = D / 8;               // 16-byte chunks per key row
-  constexpr int SUB = 64;                 // keys per pipeline stage
-  constexpr int NSUB = kSplit / SUB;      // 4 stages: the ring holds the whole split
-  // Ring of NSUB stages, each [SUB][D] bf16.  Chunk c of key row k sits at
-  // chunk c ^ swz(k), swz(k) = 4 (k & 1) | (k & 2): the score phase (two keys
-  // x four chunk lanes per 8-thread phase) and the o phase (four keys x eight
-  // column pairs per warp) both hit distinct bank groups.
+  constexpr int SUB = 64;                 // keys per load stage
+  constexpr int NSUB = kSplit / SUB;      // the K stages are reused for V
+  constexpr int KS = D / 16;              // 16-wide k steps of q . k
+  // Tiles in shared memory, rows of 16-byte chunks; chunk c of row r is
+  // stored at chunk c ^ (r & 7), so the eight row addresses of every ldmatrix
+  // phase fall in eight different bank groups.
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  __nv_bfloat16* ring = reinterpret_cast<__nv_bfloat16*>(smem_raw);
-  float* qs = reinterpret_cast<float*>(smem_raw + kSplit * D * 2);        // [rg_cap][D]
-  float* es = qs + p.rg_cap * D;                                          // [rg_cap/4][256][4]
-  __shared__ float mrow[kMaxRG];
-  __shared__ float lrow[kMaxRG];
+  __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(smem_raw);                 // [256][D]
+  __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(smem_raw + kSplit * D * 2);  // P [16][256]
+  __shared__ float wmax[kThreads / 32][kRowsMma];
+  __shared__ float wsum[kThreads / 32][kRowsMma];
 
   pdl_launch_dependents();
   pdl_wait();
@@ -130,194 +150,183 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   const int nmax = min(kSplit, lenmax - k0);
   if (nmax <= 0) return;
   const int G = p.G;
-  const int RG = rs.nrows * G;                         // (row, head) pairs of this block
-  const int RB = (RG + 3) >> 2;                        // handled in blocks of four
+  const int RG = rs.nrows * G;                         // (row, head) pairs: MMA rows 0..RG-1
   const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
+  const int gq = lane >> 2, tq = lane & 3;             // fragment row / column group
   const int64_t seq_off = rs.seq * p.seq_stride + static_cast<int64_t>(k0) * p.tok_stride + g * D;
-  auto swz = [](int key) { return ((key & 1) << 2) | (key & 2); };
-  // keys visible to (row, head) pair r (rows of one block see consecutive lengths)
+  const uint32_t kv_base = smem_addr(kv);
+  const uint32_t pt_base = smem_addr(pt);
   auto count = [&](int r) { return r < RG ? min(kSplit, rs.len0 + r / G - k0) : 0; };
 
   auto load_sub = [&](const __nv_bfloat16* src, int j) {
     const int rows = min(SUB, nmax - j * SUB);
-    __nv_bfloat16* dst = ring + j * SUB * D;
     for (int idx = t; idx < rows * C8; idx += kThreads) {
       const int r = idx / C8, c = idx % C8;
       const int key = j * SUB + r;
-      cp_async16(smem_addr(dst + r * D + ((c ^ swz(key)) << 3)),
+      cp_async16(kv_base + static_cast<uint32_t>(key * D * 2 + ((c ^ (key & 7)) << 4)),
                  src + seq_off + static_cast<int64_t>(key) * p.tok_stride + c * 8);
     }
-    cp_async_commit();  // an empty group when the sub-tile holds no key keeps the count
   };
-
 #pragma unroll
   for (int j = 0; j < NSUB; ++j) load_sub(p.k, j);
-  for (int idx = t; idx < RB * 4 * D; idx += kThreads) {
-    const int rg = idx / D, d = idx % D;
-    float v = 0.f;
-    if (rg < RG) {
-      const int r = rg / G, i = rg % G;
-      v = __bfloat162float(p.q[(static_cast<int64_t>(rs.row0 + r) * p.Hq + g * G + i) * D + d]);
-    }
-    qs[idx] = v;
-  }
+  cp_async_commit();
 
-  // --- scores.  Four threads per key; lane q4 of a quad sums chunks q4,
-  // q4 + 4, ... of d with FMAs, then two xor-shuffles add the quad's partials
-  // (the same bits in all four lanes); lane q4 stores pair q4 of the block.
-  const int kq = t >> 2, q4 = t & 3;
+  // q fragments (A operand, rows = (row, head) pairs), straight from global
+  uint32_t qa[KS][4];
+  {
+    const int r_lo = gq, r_hi = gq + 8;
+    const __nv_bfloat16* q_lo = r_lo < RG
+        ? p.q + (static_cast<int64_t>(rs.row0 + r_lo / G) * p.Hq + g * G + r_lo % G) * D : nullptr;
+    const __nv_bfloat16* q_hi = r_hi < RG
+        ? p.q + (static_cast<int64_t>(rs.row0 + r_hi / G) * p.Hq + g * G + r_hi % G) * D : nullptr;
 #pragma unroll
-  for (int j = 0; j < NSUB; ++j) {
-    cp_async_wait<3>();  // groups after K_j: K_{j+1..3} and V_{0..j-1}, three in all
-    __syncthreads();
-    if (j * SUB < nmax) {
-      const int key = j * SUB + kq;
-      const __nv_bfloat16* kr = ring + j * SUB * D + kq * D;
-      uint4 kc[C8 / 4];
-#pragma unroll
-      for (int m = 0; m < C8 / 4; ++m)
-        kc[m] = *reinterpret_cast<const uint4*>(kr + (((q4 + 4 * m) ^ swz(key)) << 3));
-      for (int rb = 0; rb < RB; ++rb) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int m = 0; m < C8 / 4; ++m) {
-          const int c = q4 + 4 * m;
-          const float kf[8] = {bf16_lo(kc[m].x), bf16_hi(kc[m].x), bf16_lo(kc[m].y), bf16_hi(kc[m].y),
-                               bf16_lo(kc[m].z), bf16_hi(kc[m].z), bf16_lo(kc[m].w), bf16_hi(kc[m].w)};
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const float4 qa = *reinterpret_cast<const float4*>(qs + (rb * 4 + r) * D + c * 8);
-            const float4 qb = *reinterpret_cast<const float4*>(qs + (rb * 4 + r) * D + c * 8 + 4);
-            float a = acc[r];
-            a = fmaf(qa.x, kf[0], a); a = fmaf(qa.y, kf[1], a);
-            a = fmaf(qa.z, kf[2], a); a = fmaf(qa.w, kf[3], a);
-            a = fmaf(qb.x, kf[4], a); a = fmaf(qb.y, kf[5], a);
-            a = fmaf(qb.z, kf[6], a); a = fmaf(qb.w, kf[7], a);
-            acc[r] = a;
-          }
-        }
-        float mine = 0.f;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          float a = acc[r];
-          a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
-          a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 2));
-          if (r == q4) mine = a;
-        }
-        const int pr = rb * 4 + q4;
-        es[(rb * kSplit + key) * 4 + q4] = key < count(pr) ? __fmul_rn(mine, p.scale) : -INFINITY;
-      }
-    }
-    __syncthreads();           // stage j is free
-    if (j * SUB < nmax) load_sub(p.v, j);
-    else cp_async_commit();
-  }
-
-  // --- softmax statistics: warp w takes block w (four pairs); lane l owns
-  // keys l, l + 32, ..., l + 224 (sequential), then a butterfly per pair.
-  for (int rb = warp; rb < RB; rb += kThreads / 32) {
-    float4* e4 = reinterpret_cast<float4*>(es) + rb * kSplit;
-    int cnt[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) cnt[r] = count(rb * 4 + r);
-    float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-    for (int i = 0; i < kSplit / 32; ++i) {
-      const int key = lane + 32 * i;
-      const float4 x = e4[key];
-      const float xv[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-        if (key < cnt[r]) m[r] = fmaxf(m[r], xv[r]);
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m[r] = fmaxf(m[r], __shfl_xor_sync(0xffffffffu, m[r], o));
-    float l[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < kSplit / 32; ++i) {
-      const int key = lane + 32 * i;
-      const float4 x = e4[key];
-      float xv[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        xv[r] = key < cnt[r] ? expf(__fsub_rn(xv[r], m[r])) : 0.f;
-        l[r] = __fadd_rn(l[r], xv[r]);
-      }
-      e4[key] = make_float4(xv[0], xv[1], xv[2], xv[3]);
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) l[r] = __fadd_rn(l[r], __shfl_xor_sync(0xffffffffu, l[r], o));
-      if (lane == 0) {
-        mrow[rb * 4 + r] = m[r];
-        lrow[rb * 4 + r] = l[r];
-      }
+    for (int ks = 0; ks < KS; ++ks) {
+      const int d0 = ks * 16 + 2 * tq;
+      qa[ks][0] = q_lo ? *reinterpret_cast<const uint32_t*>(q_lo + d0) : 0u;
+      qa[ks][1] = q_hi ? *reinterpret_cast<const uint32_t*>(q_hi + d0) : 0u;
+      qa[ks][2] = q_lo ? *reinterpret_cast<const uint32_t*>(q_lo + d0 + 8) : 0u;
+      qa[ks][3] = q_hi ? *reinterpret_cast<const uint32_t*>(q_hi + d0 + 8) : 0u;
     }
   }
+  cp_async_wait<0>();
+  __syncthreads();
 
-  // --- o = sum_t e_t v_t.  Warp w owns column pairs dp = 8w .. 8w + 7; lane
-  // = 8 kg + (dp - 8w): key group kg sums keys kg, kg + 4, ... ascending with
-  // FMAs, and a butterfly over the four key groups (xor 8, 16) adds them.
-  constexpr int DP_WARPS = D / 16;
-  const int kg = lane >> 3;
-  const int dp = warp * 8 + (lane & 7);
-  const int col = 2 * dp;
-  for (int rb = 0; rb < RB; ++rb) {
-    int cnt[4];
+  // --- scores: warp w owns keys 32w .. 32w + 31 (four 8-key n blocks)
+  float sc[4][4];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) cnt[r] = count(rb * 4 + r);
-    float2 o[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                   make_float2(0.f, 0.f)};
-    const float4* e4 = reinterpret_cast<const float4*>(es) + rb * kSplit;
+  for (int nb = 0; nb < 4; ++nb) {
 #pragma unroll
-    for (int j = 0; j < NSUB; ++j) {
-      if (rb == 0) {
-        if (j == 0) cp_async_wait<3>();
-        else if (j == 1) cp_async_wait<2>();
-        else if (j == 2) cp_async_wait<1>();
-        else cp_async_wait<0>();
-        __syncthreads();
-      }
-      if (warp < DP_WARPS) {
-        const int kend = min(SUB, nmax - j * SUB);
-        const __nv_bfloat16* vt = ring + j * SUB * D;
-        for (int kk = kg; kk < kend; kk += 4) {
-          const int key = j * SUB + kk;
-          const uint32_t vv = *reinterpret_cast<const uint32_t*>(
-              vt + kk * D + (((col >> 3) ^ swz(key)) << 3) + (col & 7));
-          const float v0 = bf16_lo(vv), v1 = bf16_hi(vv);
-          const float4 e = e4[key];
-          const float ev[4] = {e.x, e.y, e.z, e.w};
+    for (int i = 0; i < 4; ++i) sc[nb][i] = 0.f;
+    const int key = warp * 32 + nb * 8 + (lane & 7);
 #pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            if (key < cnt[r]) {
-              o[r].x = fmaf(ev[r], v0, o[r].x);
-              o[r].y = fmaf(ev[r], v1, o[r].y);
-            }
-          }
-        }
-      }
+    for (int kp = 0; kp < KS / 2; ++kp) {
+      const int c = kp * 4 + (lane >> 3);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kv_base + static_cast<uint32_t>(key * D * 2 + ((c ^ (key & 7)) << 4)), b0, b1, b2, b3);
+      mma_bf16_16816(sc[nb], qa[2 * kp], b0, b1);
+      mma_bf16_16816(sc[nb], qa[2 * kp + 1], b2, b3);
     }
-    if (warp < DP_WARPS) {
+  }
+  __syncthreads();  // every warp is done with K: the stages take V now
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        o[r].x = __fadd_rn(o[r].x, __shfl_xor_sync(0xffffffffu, o[r].x, 8));
-        o[r].y = __fadd_rn(o[r].y, __shfl_xor_sync(0xffffffffu, o[r].y, 8));
-        o[r].x = __fadd_rn(o[r].x, __shfl_xor_sync(0xffffffffu, o[r].x, 16));
-        o[r].y = __fadd_rn(o[r].y, __shfl_xor_sync(0xffffffffu, o[r].y, 16));
-        const int pr = rb * 4 + r;
-        if (kg == 0 && pr < RG && cnt[r] > 0) {
-          const int row = pr / G, i = pr % G;
-          const int64_t base = (static_cast<int64_t>(rs.row0 + row) * p.Hq + g * G + i) * p.S + s;
-          *reinterpret_cast<float2*>(p.ws_o + base * D + col) = o[r];
-          if (dp == 0) {
-            p.ws_ml[base * 2 + 0] = mrow[pr];
-            p.ws_ml[base * 2 + 1] = lrow[pr];
-          }
+  for (int j = 0; j < NSUB; ++j) load_sub(p.v, j);
+  // keys the split does not hold read as zero (their weights are zero, and a
+  // stale NaN times zero would not be)
+  for (int idx = t; idx < (kSplit - nmax) * C8; idx += kThreads) {
+    const int key = nmax + idx / C8, c = idx % C8;
+    *reinterpret_cast<uint4*>(kv + key * D + ((c ^ (key & 7)) << 3)) = make_uint4(0, 0, 0, 0);
+  }
+  cp_async_commit();
+
+  // --- softmax statistics.  A lane holds rows gq and gq + 8, keys
+  // 32w + 8nb + 2tq (+1).  Maxima: lane, then the four lanes of a row
+  // (exact), then the eight warps.  Weights are rounded to bf16 once; the sum
+  // adds the rounded weights: a lane's eight in (nb, pair) order, a fixed
+  // butterfly over the four lanes, the eight warps in ascending order.
+  const int cnt_lo = count(gq), cnt_hi = count(gq + 8);
+  float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+  for (int nb = 0; nb < 4; ++nb) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int key = warp * 32 + nb * 8 + 2 * tq + e;
+      sc[nb][e] = key < cnt_lo ? __fmul_rn(sc[nb][e], p.scale) : -INFINITY;
+      sc[nb][2 + e] = key < cnt_hi ? __fmul_rn(sc[nb][2 + e], p.scale) : -INFINITY;
+      mx_lo = fmaxf(mx_lo, sc[nb][e]);
+      mx_hi = fmaxf(mx_hi, sc[nb][2 + e]);
+    }
+  }
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, o));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, o));
+  }
+  if (tq == 0) {
+    wmax[warp][gq] = mx_lo;
+    wmax[warp][gq + 8] = mx_hi;
+  }
+  __syncthreads();
+  float m_lo = wmax[0][gq], m_hi = wmax[0][gq + 8];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) {
+    m_lo = fmaxf(m_lo, wmax[w][gq]);
+    m_hi = fmaxf(m_hi, wmax[w][gq + 8]);
+  }
+  float sum_lo = 0.f, sum_hi = 0.f;
+#pragma unroll
+  for (int nb = 0; nb < 4; ++nb) {
+    float e4[4];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float xl = sc[nb][e] == -INFINITY ? 0.f : expf(__fsub_rn(sc[nb][e], m_lo));
+      const float xh = sc[nb][2 + e] == -INFINITY ? 0.f : expf(__fsub_rn(sc[nb][2 + e], m_hi));
+      e4[e] = __bfloat162float(__float2bfloat16_rn(xl));
+      e4[2 + e] = __bfloat162float(__float2bfloat16_rn(xh));
+      sum_lo = __fadd_rn(sum_lo, e4[e]);
+      sum_hi = __fadd_rn(sum_hi, e4[2 + e]);
+    }
+    const int kc = warp * 4 + nb;                       // 8-key chunk of P
+    const uint32_t off_lo = static_cast<uint32_t>(gq * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
+    const uint32_t off_hi = static_cast<uint32_t>((gq + 8) * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_lo) = pack_bf16(e4[0], e4[1]);
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_hi) = pack_bf16(e4[2], e4[3]);
+  }
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    sum_lo = __fadd_rn(sum_lo, __shfl_xor_sync(0xffffffffu, sum_lo, o));
+    sum_hi = __fadd_rn(sum_hi, __shfl_xor_sync(0xffffffffu, sum_hi, o));
+  }
+  if (tq == 0) {
+    wsum[warp][gq] = sum_lo;
+    wsum[warp][gq + 8] = sum_hi;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // --- o = P . V: warp w owns columns 16w .. 16w + 15 (two 8-wide n
+  // blocks) over all 256 keys, sixteen k steps of 16 keys in ascending order.
+  if (warp < D / 16) {
+    float oc[2][4];
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) oc[nb][i] = 0.f;
+#pragma unroll 4
+    for (int kk = 0; kk < kSplit / 16; ++kk) {
+      uint32_t a[4];
+      {
+        const int prow = lane & 15;
+        const int kc = 2 * kk + (lane >> 4);
+        ldsm_x4(pt_base + static_cast<uint32_t>(prow * kSplit * 2 + ((kc ^ (prow & 7)) << 4)), a[0], a[1],
+                a[2], a[3]);
+      }
+      uint32_t b0, b1, b2, b3;
+      {
+        const int key = kk * 16 + (lane & 15);
+        const int c = warp * 2 + (lane >> 4);
+        ldsm_x4_t(kv_base + static_cast<uint32_t>(key * D * 2 + ((c ^ (key & 7)) << 4)), b0, b1, b2, b3);
+      }
+      mma_bf16_16816(oc[0], a, b0, b1);
+      mma_bf16_16816(oc[1], a, b2, b3);
+    }
+    // rows gq and gq + 8, columns 16w + 8nb + 2tq (+1)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int r = gq + 8 * h;
+      if (r < RG && count(r) > 0) {
+        const int row = r / G, i = r % G;
+        const int64_t base = (static_cast<int64_t>(rs.row0 + row) * p.Hq + g * G + i) * p.S + s;
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb)
+          *reinterpret_cast<float2*>(p.ws_o + base * D + warp * 16 + nb * 8 + 2 * tq) =
+              make_float2(oc[nb][2 * h], oc[nb][2 * h + 1]);
+        if (warp == 0 && tq == 0) {
+          float l = wsum[0][r];
+#pragma unroll
+          for (int w = 1; w < kThreads / 32; ++w) l = __fadd_rn(l, wsum[w][r]);
+          p.ws_ml[base * 2 + 0] = h ? m_hi : m_lo;
+          p.ws_ml[base * 2 + 1] = l;
         }
       }
     }
@@ -378,20 +387,19 @@ __global__ void attn_merge_kernel(const AttnParams p) {
 }
 
 template <int D>
-size_t split_smem_bytes(int rg_cap) {
-  return static_cast<size_t>(kSplit) * D * 2 + static_cast<size_t>(rg_cap) * D * 4 +
-         static_cast<size_t>(rg_cap) * kSplit * 4;
+size_t split_smem_bytes() {
+  return static_cast<size_t>(kSplit) * D * 2 + static_cast<size_t>(kRowsMma) * kSplit * 2;
 }
 
 template <int D>
 kinv_status launch(const AttnParams& p, dim3 split_grid, dim3 merge_grid, cudaStream_t stream) {
-  const size_t smem = split_smem_bytes<D>(p.rg_cap);
+  const size_t smem = split_smem_bytes<D>();
   static bool configured[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KINV_ERR_CUDA;
   if (dev < 64 && !configured[dev]) {
     if (cudaFuncSetAttribute(attn_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(split_smem_bytes<D>(kMaxRG))) != cudaSuccess)
+                             static_cast<int>(split_smem_bytes<D>())) != cudaSuccess)
       return KINV_ERR_CUDA;
     configured[dev] = true;
   }
@@ -509,7 +517,7 @@ extern "C" kinv_status kinv_attn_prefill(const void* q, const void* k_cache, con
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.G = Hq / Hkv;
-  p.R = kMaxRG / p.G < 8 ? kMaxRG / p.G : 8;
+  p.R = kRowsMma / p.G;
   p.S = S;
   p.groups_per_seq = (max_q_len + p.R - 1) / p.R;
   p.rg_cap = ((p.R * p.G + 3) / 4) * 4;
