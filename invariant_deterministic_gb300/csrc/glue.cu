@@ -68,7 +68,8 @@ struct RopeFreqs {
 
 // One block per row.  The first D/2 threads compute this row's rotation
 // angles in fp64 (theta_i = p * inv_freq_i, then sin and cos) into shared
-// memory; then each warp takes whole heads.  Lane l of a warp holds the pairs
+// memory; then each warp takes one head (grid.y picks eight of the row's
+// heads).  Lane l of a warp holds the pairs
 // (i, i + D/2) for i in {l * P .. l * P + P - 1}, P = D / 64.
 template <int D>
 __global__ void rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int64_t ld_qkv,
@@ -93,10 +94,10 @@ __global__ void rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int64_
     // and a tail), then sin and cos of the reduced angle in fp32
     const double theta = static_cast<double>(p) * freqs.inv_freq[i];
     const double k = rint(theta * 0.15915494309189535);  // 1 / (2 pi)
-    double r = fma(-k, 6.283185307179586, theta);
-    r = fma(-k, 2.4492935982947064e-16, r);
+    double red = fma(-k, 6.283185307179586, theta);
+    red = fma(-k, 2.4492935982947064e-16, red);
     float sv, cv;
-    sincosf(static_cast<float>(r), &sv, &cv);
+    sincosf(static_cast<float>(red), &sv, &cv);
     cs[i] = cv;
     sn[i] = sv;
   }
@@ -108,7 +109,8 @@ __global__ void rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int64_
   __nv_bfloat16* kdst_row = k_cache + s * seq_stride + p * tok_stride;
   __nv_bfloat16* vdst_row = v_cache + s * seq_stride + p * tok_stride;
   const int heads = Hq + 2 * Hkv;
-  for (int h = warp; h < heads; h += nwarps) {
+  // block y takes heads 8y .. 8y + 7 of the row, one per warp
+  for (int h = blockIdx.y * nwarps + warp; h < heads && h < (blockIdx.y + 1) * nwarps; h += nwarps) {
     const __nv_bfloat16* src = row + h * D;
     if (h >= Hq + Hkv) {  // value head: copy bits
       const int g = h - Hq - Hkv;
@@ -248,8 +250,8 @@ extern "C" kinv_status kinv_rope_append(const void* qkv, int64_t ld_qkv, void* q
   RopeFreqs freqs;
   for (int i = 0; i < D / 2; ++i) freqs.inv_freq[i] = std::pow(static_cast<double>(rope_base), -2.0 * i / D);
   const int heads = Hq + 2 * Hkv;
-  int threads = 32 * (heads < 8 ? heads : 8);
-  if (threads < 64) threads = 64;
+  const int threads = 256;  // eight warps: one head each, grid.y covers the heads
+  const dim3 grid(rows, (heads + 7) / 8);
   auto* k = static_cast<__nv_bfloat16*>(k_cache);
   auto* v = static_cast<__nv_bfloat16*>(v_cache);
   auto* src = static_cast<const __nv_bfloat16*>(qkv);
@@ -257,10 +259,10 @@ extern "C" kinv_status kinv_rope_append(const void* qkv, int64_t ld_qkv, void* q
   auto* qn = static_cast<const __nv_bfloat16*>(q_norm);
   auto* kn = static_cast<const __nv_bfloat16*>(k_norm);
   if (D == 128)
-    return launch_kernel(rope_append_kernel<128>, dim3(rows), dim3(threads), 0, stream, 1, src,
+    return launch_kernel(rope_append_kernel<128>, grid, dim3(threads), 0, stream, 1, src,
                          ld_qkv, qo, k, v, seq_stride, tok_stride, seq, pos, qn, kn, eps, Hq, Hkv,
                          freqs);
-  return launch_kernel(rope_append_kernel<64>, dim3(rows), dim3(threads), 0, stream, 1, src, ld_qkv,
+  return launch_kernel(rope_append_kernel<64>, grid, dim3(threads), 0, stream, 1, src, ld_qkv,
                        qo, k, v, seq_stride, tok_stride, seq, pos, qn, kn, eps, Hq, Hkv,
                        freqs);
 }

@@ -81,6 +81,47 @@ __device__ __forceinline__ float penalised(const float* __restrict__ row, int i,
   return z;
 }
 
+// Visits every id of the row once, in rounds in which each thread loads
+// four 16-byte vectors (16 logits) before using any of them, so a pass keeps
+// many loads in flight.  f(valid, id, key) sees the key of the penalised
+// logit; every lane runs the same number of rounds (f may use warp votes).
+template <typename F>
+__device__ __forceinline__ void for_each_key(const float* __restrict__ row, int V,
+                                             const uint32_t* bitmap, float r, F&& f) {
+  constexpr int U = 4;
+  const int t = threadIdx.x;
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  const int V4 = vec ? (V >> 2) : 0;
+  const float4* row4 = reinterpret_cast<const float4*>(row);
+  for (int base = 0; base < V4; base += kThreadsS * U) {
+    float4 x[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i4 = base + u * kThreadsS + t;
+      x[u] = i4 < V4 ? row4[i4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i4 = base + u * kThreadsS + t;
+      const bool valid = i4 < V4;
+      const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 4 * i4 + e;
+        float z = xv[e];
+        if (valid && ((bitmap[i >> 5] >> (i & 31)) & 1u)) z = z > 0.f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
+        f(valid, i, valid ? ordered_key(z) : 0u);
+      }
+    }
+  }
+  // the ids not covered by whole vectors, one per thread and round
+  for (int base = 4 * V4; base < V; base += kThreadsS) {
+    const int i = base + t;
+    const bool valid = i < V;
+    f(valid, i, valid ? ordered_key(penalised(row, i, bitmap, r)) : 0u);
+  }
+}
+
 __device__ __forceinline__ unsigned long long composite(uint32_t key, int id) {
   return (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(id));
 }
@@ -178,27 +219,43 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
     const int nb = 1 << w;
     for (int i = t; i < nb; i += kThreadsS) sm.hist[i] = 0u;
     __syncthreads();
-    for (int base = 0; base < V; base += kThreadsS) {  // same trip count in every lane
-      const int i = base + t;
-      const uint32_t key = i < V ? ordered_key(penalised(row, i, bitmap, r)) : 0u;
-      const bool in = i < V && (fixed == 0 || (key >> (32 - fixed)) == prefix);
+    for_each_key(row, V, bitmap, r, [&](bool valid, int, uint32_t key) {
+      const bool in = valid && (fixed == 0 || (key >> (32 - fixed)) == prefix);
       const uint32_t digit = in ? (key >> shift) & (nb - 1) : 0xFFFFFFFFu;
       const unsigned peers = __match_any_sync(0xffffffffu, digit);
       if (in && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[digit], __popc(peers));
-    }
+    });
     __syncthreads();
-    if (t == 0) {
-      int cum = 0, d = nb - 1;
-      for (; d > 0; --d) {
-        if (cum + static_cast<int>(sm.hist[d]) >= k_rem) break;
-        cum += sm.hist[d];
+    if (warp == 0) {
+      // lane l sums bins [nb - (l + 1) * nb / 32, nb - l * nb / 32) (lane 0 the
+      // top block); an exclusive scan from the top finds the block holding
+      // the k_rem-th id, whose lane then walks its bins downwards
+      const int per = nb / 32;
+      const int hi = nb - lane * per;
+      int bsum = 0;
+      for (int d = hi - 1; d >= hi - per; --d) bsum += static_cast<int>(sm.hist[d]);
+      int incl = bsum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
       }
-      // ids with digit > d are all in; ids with digit == d hold the k_rem-th
-      const int at_or_above = above + cum + static_cast<int>(sm.hist[d]);
-      sm.thresh = ((prefix << w) | static_cast<uint32_t>(d)) << shift;
-      sm.k_rem = k_rem - cum;
-      sm.ok = at_or_above <= kCap ? 1 : 0;
-      sm.warp_cnt[0] = static_cast<uint32_t>(above + cum);
+      const int excl = incl - bsum;
+      const unsigned hit = __ballot_sync(0xffffffffu, incl >= k_rem);
+      const int owner = hit ? __ffs(hit) - 1 : 31;
+      if (lane == owner) {
+        int cum = excl, d = hi - 1;
+        for (; d > hi - per; --d) {
+          if (cum + static_cast<int>(sm.hist[d]) >= k_rem) break;
+          cum += sm.hist[d];
+        }
+        // ids with digit > d are all in; ids with digit == d hold the k_rem-th
+        const int at_or_above = above + cum + static_cast<int>(sm.hist[d]);
+        sm.thresh = ((prefix << w) | static_cast<uint32_t>(d)) << shift;
+        sm.k_rem = k_rem - cum;
+        sm.ok = at_or_above <= kCap ? 1 : 0;
+        sm.warp_cnt[0] = static_cast<uint32_t>(above + cum);
+      }
     }
     __syncthreads();
     const uint32_t th = sm.thresh;
@@ -217,13 +274,12 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
   }
   __syncthreads();
   if (!exact_ties) {
-    for (int i = t; i < V; i += kThreadsS) {
-      const uint32_t key = ordered_key(penalised(row, i, bitmap, r));
-      if (key >= thresh) {
+    for_each_key(row, V, bitmap, r, [&](bool valid, int i, uint32_t key) {
+      if (valid && key >= thresh) {
         const uint32_t slot = atomicAdd(&sm.n_cand, 1u);  // parking slot only
         sm.cand[slot] = composite(key, i);
       }
-    }
+    });
   } else {
     // every id above the threshold, plus the lowest-id ties, in id order
     const int need_eq = k_rem;
