@@ -72,6 +72,11 @@ struct Smem {
   int k_rem;
   int ok;
   int result;
+  float wmax[32];
+  int wcnt[32][8];
+  int cnt[8];
+  float thresh_f;       // fast path: gather ids whose value >= thresh_f
+  int fast;
 };
 
 __device__ __forceinline__ float penalised(const float* __restrict__ row, int i,
@@ -86,8 +91,8 @@ __device__ __forceinline__ float penalised(const float* __restrict__ row, int i,
 // many loads in flight.  f(valid, id, key) sees the key of the penalised
 // logit; every lane runs the same number of rounds (f may use warp votes).
 template <typename F>
-__device__ __forceinline__ void for_each_key(const float* __restrict__ row, int V,
-                                             const uint32_t* bitmap, float r, F&& f) {
+__device__ __forceinline__ void for_each_value(const float* __restrict__ row, int V,
+                                               const uint32_t* bitmap, float r, F&& f) {
   constexpr int U = 4;
   const int t = threadIdx.x;
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
@@ -110,7 +115,7 @@ __device__ __forceinline__ void for_each_key(const float* __restrict__ row, int 
         const int i = 4 * i4 + e;
         float z = xv[e];
         if (valid && ((bitmap[i >> 5] >> (i & 31)) & 1u)) z = z > 0.f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
-        f(valid, i, valid ? ordered_key(z) : 0u);
+        f(valid, i, isnan(z) ? -INFINITY : z);
       }
     }
   }
@@ -118,8 +123,16 @@ __device__ __forceinline__ void for_each_key(const float* __restrict__ row, int 
   for (int base = 4 * V4; base < V; base += kThreadsS) {
     const int i = base + t;
     const bool valid = i < V;
-    f(valid, i, valid ? ordered_key(penalised(row, i, bitmap, r)) : 0u);
+    const float z = valid ? penalised(row, i, bitmap, r) : 0.f;
+    f(valid, i, isnan(z) ? -INFINITY : z);
   }
+}
+
+template <typename F>
+__device__ __forceinline__ void for_each_key(const float* __restrict__ row, int V,
+                                             const uint32_t* bitmap, float r, F&& f) {
+  for_each_value(row, V, bitmap, r,
+                 [&](bool valid, int i, float z) { f(valid, i, valid ? ordered_key(z) : 0u); });
 }
 
 __device__ __forceinline__ unsigned long long composite(uint32_t key, int id) {
@@ -206,14 +219,69 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
     return;
   }
 
-  // 2. radix narrowing of the threshold
+  // 2a. Fast path: the row maximum M, then how many ids have a value of at
+  // least M - delta for eight deltas (integer counts, exact maximum: nothing
+  // depends on the order of the sums).  The smallest delta that holds at
+  // least k ids, if it holds at most kCap, gives the gathering threshold; the
+  // set gathered is every id at or above it, which contains the top k.
+  constexpr float kDeltas[8] = {0.5f, 1.f, 2.f, 4.f, 8.f, 16.f, 32.f, 64.f};
+  {
+    float mx = -INFINITY;
+    for_each_value(row, V, bitmap, r, [&](bool valid, int, float z) {
+      if (valid) mx = fmaxf(mx, z);
+    });
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) sm.wmax[warp] = mx;
+    __syncthreads();
+    float m = sm.wmax[0];
+    for (int w = 1; w < kThreadsS / 32; ++w) m = fmaxf(m, sm.wmax[w]);
+    float th[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) th[j] = __fsub_rn(m, kDeltas[j]);
+    int c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for_each_value(row, V, bitmap, r, [&](bool valid, int, float z) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] += (valid && z >= th[j]) ? 1 : 0;
+    });
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) c[j] += __shfl_xor_sync(0xffffffffu, c[j], o);
+      if (lane == 0) sm.wcnt[warp][j] = c[j];
+    }
+    __syncthreads();
+    if (t < 8) {
+      int tot = 0;
+      for (int w = 0; w < kThreadsS / 32; ++w) tot += sm.wcnt[w][t];
+      sm.cnt[t] = tot;
+    }
+    __syncthreads();
+    if (t == 0) {
+      sm.fast = 0;
+      for (int j = 0; j < 8; ++j) {
+        if (sm.cnt[j] >= k) {
+          if (sm.cnt[j] <= kCap && m > -INFINITY) {
+            sm.fast = 1;
+            sm.thresh_f = th[j];
+          }
+          break;
+        }
+      }
+      sm.n_cand = 0;
+    }
+    __syncthreads();
+  }
+  const bool fast = sm.fast != 0;
+
+  // 2b. Otherwise, radix narrowing of the threshold
   uint32_t prefix = 0;  // fixed high bits of the threshold
   int fixed = 0;        // how many high bits are fixed
   int k_rem = k;        // how many ids are still needed at or below the prefix
   int above = 0;        // ids strictly above the prefix region (all taken)
   bool exact_ties = false;
   const int widths[3] = {11, 11, 10};
-  for (int pass = 0; pass < 3; ++pass) {
+  for (int pass = 0; pass < 3 && !fast; ++pass) {
     const int w = widths[pass];
     const int shift = 32 - fixed - w;
     const int nb = 1 << w;
@@ -273,7 +341,15 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
     sm.eq_taken = 0;
   }
   __syncthreads();
-  if (!exact_ties) {
+  if (fast) {
+    const float tf = sm.thresh_f;
+    for_each_value(row, V, bitmap, r, [&](bool valid, int i, float z) {
+      if (valid && z >= tf) {
+        const uint32_t slot = atomicAdd(&sm.n_cand, 1u);  // parking slot only
+        sm.cand[slot] = composite(ordered_key(z), i);
+      }
+    });
+  } else if (!exact_ties) {
     for_each_key(row, V, bitmap, r, [&](bool valid, int i, uint32_t key) {
       if (valid && key >= thresh) {
         const uint32_t slot = atomicAdd(&sm.n_cand, 1u);  // parking slot only
