@@ -56,6 +56,8 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
          (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+__device__ __forceinline__ float silu_times(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
 struct GemmArgs {
   void* C;
   int64_t ldc;
@@ -64,6 +66,7 @@ struct GemmArgs {
   int a_rows;   // rows of A that TMA brings in per tile (the rest of the 128 are never stored)
   int a_stride; // bytes between A stages (a_rows * 128)
   int c_f32;
+  int swiglu;   // output silu(gate) * up: tile columns [0, 32) gate, [32, 64) up
   int stages;
   int splits;
   int* status;
@@ -188,7 +191,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
   const bool good = ok && !*abort_flag && k_tiles > 0;
 
-  if (splits == 1) {
+  if (splits == 1 && args.swiglu) {
+    // columns [0, 32) of the tile are gate features n0/2 .. n0/2 + 31, columns
+    // [32, 64) the up features for the same ids
+    if (good) {
+      uint32_t gv[32], uv[32];
+      tmem_ld32(lane_base, gv);
+      tmem_ld32(lane_base + 32, uv);
+      if (m < args.M) {
+        __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(args.C) + m * args.ldc + n0 / 2;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          uint4 o;
+          o.x = pack_bf16(silu_times(__uint_as_float(gv[j + 0]), __uint_as_float(uv[j + 0])),
+                          silu_times(__uint_as_float(gv[j + 1]), __uint_as_float(uv[j + 1])));
+          o.y = pack_bf16(silu_times(__uint_as_float(gv[j + 2]), __uint_as_float(uv[j + 2])),
+                          silu_times(__uint_as_float(gv[j + 3]), __uint_as_float(uv[j + 3])));
+          o.z = pack_bf16(silu_times(__uint_as_float(gv[j + 4]), __uint_as_float(uv[j + 4])),
+                          silu_times(__uint_as_float(gv[j + 5]), __uint_as_float(uv[j + 5])));
+          o.w = pack_bf16(silu_times(__uint_as_float(gv[j + 6]), __uint_as_float(uv[j + 6])),
+                          silu_times(__uint_as_float(gv[j + 7]), __uint_as_float(uv[j + 7])));
+          *reinterpret_cast<uint4*>(crow + j) = o;
+        }
+      }
+    }
+  } else if (splits == 1) {
     if (good) {
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -239,7 +266,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     cluster_sync();
     const int cols_per = BN / splits;
     const int cbase = rank * cols_per;
-    if (good) {
+    if (good && args.swiglu) {
+      // rank q forms features [q * 32 / splits, (q + 1) * 32 / splits): their
+      // gate column f and up column 32 + f, each summed in rank order
+      const int feats_per = 32 / splits;
+      const int fbase = rank * feats_per;
+      for (int idx = threadIdx.x; idx < rows_here * feats_per; idx += kGemmThreads) {
+        const int rl = idx / feats_per;
+        const int f = fbase + idx % feats_per;
+        const int mm = m0 + rl;
+        const uint32_t lg = smem_addr(red + rl * LDR + f);
+        const uint32_t lu = smem_addr(red + rl * LDR + 32 + f);
+        float pg[8], pu[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < splits) {
+            pg[q] = ld_dsmem_f32(map_to_rank(lg, q));
+            pu[q] = ld_dsmem_f32(map_to_rank(lu, q));
+          }
+        float g = pg[0], u = pu[0];
+#pragma unroll
+        for (int q = 1; q < 8; ++q)
+          if (q < splits) {
+            g = __fadd_rn(g, pg[q]);
+            u = __fadd_rn(u, pu[q]);
+          }
+        static_cast<__nv_bfloat16*>(args.C)[mm * args.ldc + n0 / 2 + f] =
+            __float2bfloat16_rn(silu_times(g, u));
+      }
+    } else if (good) {
       for (int idx = threadIdx.x; idx < rows_here * cols_per; idx += kGemmThreads) {
         const int rl = idx / cols_per;
         const int col = cbase + idx % cols_per;
@@ -375,19 +430,21 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a
 
 using namespace kinv;
 
-extern "C" kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int64_t ldw, void* C,
-                                 int64_t ldc, kinv_dtype c_dtype, int M, int N, int K,
-                                 kinv_stream stream) {
+namespace kinv {
+namespace {
+kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, void* C, int64_t ldc,
+                      kinv_dtype c_dtype, int M, int N, int K, bool swiglu, cudaStream_t stream) {
   if (M < 0 || N <= 0 || K <= 0) return KINV_ERR_INVALID_ARG;
   if (c_dtype != KINV_BF16 && c_dtype != KINV_F32) return KINV_ERR_INVALID_ARG;
   if (M == 0) return KINV_OK;
   if (!A || !W || !C) return KINV_ERR_INVALID_ARG;
-  if (K % BK || N % 16) return KINV_ERR_UNSUPPORTED;
-  if (lda < K || ldw < K || ldc < N) return KINV_ERR_INVALID_ARG;
+  if (K % BK || N % 16 || (swiglu && (N % 64 || c_dtype != KINV_BF16))) return KINV_ERR_UNSUPPORTED;
+  if (lda < K || ldw < K || ldc < (swiglu ? N / 2 : N)) return KINV_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(W) || !aligned16(C) || lda % 8 || ldw % 8 ||
       (c_dtype == KINV_BF16 ? ldc % 8 : ldc % 4))
     return KINV_ERR_ALIGNMENT;
-  const Plan p = plan_for(N, K);
+  Plan p = plan_for(N, K);
+  if (swiglu) p.bn = 64;  // a tile holds 32 gate and the matching 32 up columns
   const int grid_y = (M + BM - 1) / BM;
   const int grid_z = (N + p.bn - 1) / p.bn;
   if (grid_y > 65535 || grid_z > 65535) return KINV_ERR_UNSUPPORTED;
@@ -406,6 +463,7 @@ extern "C" kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int6
   a.a_rows = a_rows;
   a.a_stride = a_rows * BK * 2;
   a.c_f32 = c_dtype == KINV_F32;
+  a.swiglu = swiglu ? 1 : 0;
   a.stages = 0;
   a.splits = p.splits;
   a.status = device_status_word();
@@ -414,4 +472,19 @@ extern "C" kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int6
     case 128: return launch_gemm<128>(ta, tw, a, p.smem_budget, grid_y, grid_z, stream);
     default: return KINV_ERR_UNSUPPORTED;
   }
+}
+}  // namespace
+}  // namespace kinv
+
+extern "C" kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int64_t ldw, void* C,
+                                 int64_t ldc, kinv_dtype c_dtype, int M, int N, int K,
+                                 kinv_stream stream) {
+  return kinv::gemm_impl(A, lda, W, ldw, C, ldc, c_dtype, M, N, K, false, stream);
+}
+
+extern "C" kinv_status kinv_gemm_swiglu(const void* A, int64_t lda, const void* W_gu, int64_t ldw,
+                                        void* act, int64_t ld_act, int M, int F, int K,
+                                        kinv_stream stream) {
+  if (F <= 0 || F % 32) return F <= 0 ? KINV_ERR_INVALID_ARG : KINV_ERR_UNSUPPORTED;
+  return kinv::gemm_impl(A, lda, W_gu, ldw, act, ld_act, KINV_BF16, M, 2 * F, K, true, stream);
 }

@@ -39,6 +39,7 @@ SIGNATURES = {
     "kinv_build_id": (ctypes.c_char_p, []),
     "kinv_last_device_status": (_i32, [_c_p]),
     "kinv_gemm": (_i32, [_c_p, _i64, _c_p, _i64, _c_p, _i64, _i32, _i32, _i32, _i32, _c_p]),
+    "kinv_gemm_swiglu": (_i32, [_c_p, _i64, _c_p, _i64, _c_p, _i64, _i32, _i32, _i32, _c_p]),
     "kinv_rmsnorm": (_i32, [_c_p, _i64, _c_p, _c_p, _c_p, _i64, _i32, _i32, _f32, _c_p]),
     "kinv_attn_decode_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "kinv_attn_decode": (_i32, [_c_p, _c_p, _c_p, _i64, _i64, _c_p, _c_p, _i32, _i32, _i32, _i32,
@@ -136,6 +137,29 @@ def gemm(a: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
     dt = F32 if out.dtype == torch.float32 else BF16
     _check(lib().kinv_gemm(_ptr(a), a.stride(0), _ptr(w), w.stride(0), _ptr(out), out.stride(0),
                            dt, m, n, k, _stream(stream)), "kinv_gemm")
+    return out
+
+
+def interleave_gate_up(w_gu: torch.Tensor) -> torch.Tensor:
+    """[gate rows; up rows] ([2F][K]) -> the block-of-32 interleaved layout
+    kinv_gemm_swiglu reads (a one-time weight layout change, a copy)."""
+    two_f, k = w_gu.shape
+    f = two_f // 2
+    return w_gu.view(2, f // 32, 32, k).permute(1, 0, 2, 3).reshape(two_f, k).contiguous()
+
+
+def gemm_swiglu(a: torch.Tensor, w_gu_il: torch.Tensor, out: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """act[M][F] = bf16(silu(a . Wgate^T) * (a . Wup^T)), W in the interleaved
+    layout of ``interleave_gate_up``."""
+    _need(a, torch.bfloat16, "a")
+    _need(w_gu_il, torch.bfloat16, "w_gu")
+    m, k = a.shape
+    f = w_gu_il.shape[0] // 2
+    if out is None:
+        out = torch.empty(m, f, dtype=torch.bfloat16, device=a.device)
+    _check(lib().kinv_gemm_swiglu(_ptr(a), a.stride(0), _ptr(w_gu_il), w_gu_il.stride(0), _ptr(out),
+                                  out.stride(0), m, f, k, _stream(stream)), "kinv_gemm_swiglu")
     return out
 
 

@@ -9,7 +9,9 @@ fused into the RMSNorm that opens the next (and into the final norm).
 
 Layouts (all bf16 unless noted):
   embed, lm_head [V][d]; per layer w_qkv [(Hq + 2 Hkv) D][d], w_o [d][Hq D],
-  w_gu [2F][d] (gate rows then up rows), w_down [d][F], norm gains [d] / [D];
+  w_gu [2F][d] (gate rows then up rows; the decoder keeps a copy interleaved
+  in blocks of 32 for the fused gate/up + SwiGLU GEMM), w_down [d][F], norm
+  gains [d] / [D];
   KV cache [layers][2][B][Lmax][Hkv][D] (k then v), token-major per sequence.
 """
 from __future__ import annotations
@@ -86,7 +88,8 @@ class Decoder:
         self.q = torch.zeros(rows, s.n_q, s.head_dim, **bf)
         self.attn = torch.zeros(rows, s.n_q, s.head_dim, **bf)
         self.o = torch.zeros(rows, s.d_model, **bf)
-        self.gu = torch.zeros(rows, 2 * s.ffn, **bf)
+        # gate/up weights in the interleaved layout of kinv_gemm_swiglu
+        self.w_gu_il = [kinv.interleave_gate_up(lw["w_gu"]) for lw in weights["layers"]]
         self.act = torch.zeros(rows, s.ffn, **bf)
         self.delta = torch.zeros(rows, s.d_model, **bf)
         ws = kinv.attn_decode_workspace(max_batch, s.n_q, s.head_dim, max_len)
@@ -153,9 +156,7 @@ class Decoder:
         with self._t("rmsnorm"):
             kinv.rmsnorm(x, lw["ffn_norm"], s.eps, residual=self.o[:rows], out=h)
         with self._t("gemm_gate_up"):
-            kinv.gemm(h, lw["w_gu"], out=self.gu[:rows])
-        with self._t("swiglu"):
-            kinv.swiglu(self.gu[:rows], out=self.act[:rows])
+            kinv.gemm_swiglu(h, self.w_gu_il[li], out=self.act[:rows])
         with self._t("gemm_down"):
             kinv.gemm(self.act[:rows], lw["w_down"], out=self.delta[:rows])
 

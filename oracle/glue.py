@@ -22,8 +22,13 @@ def silu(g: np.ndarray) -> np.ndarray:
 
 
 def swiglu(gu_bits: np.ndarray) -> np.ndarray:
-    """gu [M][2F] holds gate in columns [0, F) and up in [F, 2F)."""
-    gu = bf16.to_f64(gu_bits)
+    """gu [M][2F] holds gate in columns [0, F) and up in [F, 2F) (bf16)."""
+    return swiglu_f64(bf16.to_f64(gu_bits))
+
+
+def swiglu_f64(gu: np.ndarray) -> np.ndarray:
+    """The same on unrounded fp64 gate/up values (the fused gate/up GEMM keeps
+    g and u in its fp32 accumulators and rounds only the product)."""
     f = gu.shape[-1] // 2
     with np.errstate(over="ignore"):
         return bf16.from_f64(silu(gu[..., :f]) * gu[..., f:])

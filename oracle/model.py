@@ -15,7 +15,8 @@ FFN, grouped-query attention):
     [g u] = h2 . Wgu^T ; x3 = x2 + (silu(g) * u) . Wdown^T
 
 bf16 rounding happens at each stored tensor, the same boundaries as the GPU
-path.  Weights are bf16 bit arrays; the dictionaries below name them.
+path (g and u are not stored: the gate/up product and SwiGLU are one GPU
+step).  Weights are bf16 bit arrays; the dictionaries below name them.
 """
 from __future__ import annotations
 
@@ -69,7 +70,8 @@ def layer_step(x_bits, lw: dict, k_cache, v_cache, pos, shape: Shape):
         a[i] = attention.decode(q[i: i + 1], k_cache[b: b + 1], v_cache[b: b + 1], [p + 1])[0]
     o = gemm(a.reshape(m, hq * dh), lw["w_o"])
     h2, x2 = rmsnorm(o, lw["ffn_norm"], shape.eps, residual_bits=x_bits)
-    act = glue.swiglu(gemm(h2, lw["w_gu"]))
+    # gate/up and SwiGLU form one GPU kernel: g and u are not rounded to bf16
+    act = glue.swiglu_f64(gemm(h2, lw["w_gu"], out="f64"))
     return glue.add(x2, gemm(act, lw["w_down"]))
 
 

@@ -5,6 +5,7 @@ import torch
 
 from helpers import assert_close, assert_same_bits, ensure_lib, f64, gpu, synth
 from oracle import bf16 as obf
+from oracle import glue as oglue
 from oracle.gemm import gemm as ogemm, gemm_f64_rows
 
 pytestmark = gpu
@@ -118,3 +119,62 @@ def test_errors_before_launch(kinv):
     m0 = kinv.gemm(torch.zeros(0, 64, dtype=torch.bfloat16, device="cuda"),
                    torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda"))
     assert m0.shape == (0, 64)
+
+
+# ---------------------------------------------------------------- fused gate/up + SwiGLU
+def _swiglu_ref(a, w_gu):
+    """bf16(silu(g) * u) from unrounded fp64 g = a . Wgate^T, u = a . Wup^T."""
+    return oglue.swiglu_f64(ogemm(synth.bits(a), synth.bits(w_gu), out="f64"))
+
+
+@pytest.mark.parametrize("m,f,k", [(1, 32, 64), (5, 96, 256), (130, 160, 512), (33, 1024, 1024)])
+def test_gemm_swiglu_parity(kinv, m, f, k):
+    a = synth.normal_bf16((m, k), 1.0, 21).cuda()
+    w_gu = synth.normal_bf16((2 * f, k), 0.05, 22).cuda()
+    got = kinv.gemm_swiglu(a, kinv.interleave_gate_up(w_gu))
+    assert got.shape == (m, f)
+    assert_close(f64(got), obf.to_f64(_swiglu_ref(a, w_gu)), f"gemm_swiglu {m}x{f}x{k}")
+    assert kinv.last_device_status() == 0
+
+
+def test_gemm_swiglu_interleave_layout(kinv):
+    """Gate rows and up rows are told apart: swapping them changes the result
+    to silu(u) * g, which the oracle computes from the swapped weights."""
+    m, f, k = 9, 64, 128
+    a = synth.normal_bf16((m, k), 1.0, 23).cuda()
+    w_gu = synth.normal_bf16((2 * f, k), 0.1, 24).cuda()
+    swapped = torch.cat([w_gu[f:], w_gu[:f]])
+    got = kinv.gemm_swiglu(a, kinv.interleave_gate_up(swapped))
+    assert_close(f64(got), obf.to_f64(_swiglu_ref(a, swapped)), "swapped gate/up")
+    direct = kinv.gemm_swiglu(a, kinv.interleave_gate_up(w_gu))
+    assert not torch.equal(got, direct)
+
+
+def test_gemm_swiglu_8b_row_bits_independent_of_m(kinv):
+    """Qwen3-8B FFN (F=12288, K=4096): row bits do not depend on M or on the
+    batch-mates, and sampled features match the oracle."""
+    f, k = 12288, 4096
+    w_gu = synth.normal_bf16((2 * f, k), 0.02, 25).cuda()
+    w_il = kinv.interleave_gate_up(w_gu)
+    a = synth.normal_bf16((256, k), 1.0, 26).cuda()
+    full = kinv.gemm_swiglu(a, w_il)
+    for m in MS:
+        assert_same_bits(kinv.gemm_swiglu(a[:m].contiguous(), w_il), full[:m], f"swiglu M={m}")
+    other = synth.normal_bf16((256, k), 1.0, 27).cuda()
+    perm = torch.randperm(256, generator=synth.gen(28))
+    mixed = other.clone()
+    mixed[perm[:32]] = a[:32]
+    assert_same_bits(kinv.gemm_swiglu(mixed, w_il)[perm[:32]], full[:32], "swiglu batch-mates")
+    rows = [0, 5, 15, 127, 255]
+    cols = torch.randint(0, f, (48,), generator=synth.gen(29)).numpy()
+    gu = gemm_f64_rows(synth.bits(a), synth.bits(w_gu), rows, np.concatenate([cols, cols + f]))
+    ref = oglue.swiglu_f64(gu)
+    assert_close(f64(full)[rows][:, cols], obf.to_f64(ref), "swiglu 8B vs oracle")
+    assert kinv.last_device_status() == 0
+
+
+def test_gemm_swiglu_rejects_bad_f(kinv):
+    a = torch.zeros(2, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(2 * 48, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(kinv.KinvError):
+        kinv.gemm_swiglu(a, w)
