@@ -92,9 +92,9 @@ kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int64_t ldw,
  *   g = A[m] . Wgate[f],  u = A[m] . Wup[f]  (fp32 accumulators, never rounded)
  * with the same tile, K order and split as kinv_gemm for N = 2F (so a row's
  * bits do not depend on M).  W_gu holds the 2F weight rows interleaved in
- * blocks of 32: rows 64j .. 64j+31 are gate rows 32j .. 32j+31 and rows
- * 64j+32 .. 64j+63 are up rows 32j .. 32j+31.  act: bf16 [M][F], leading
- * dimension ld_act (a multiple of 8).  Requirements: F % 32 == 0, K % 64 == 0,
+ * blocks of 64: rows 128j .. 128j+63 are gate rows 64j .. 64j+63 and rows
+ * 128j+64 .. 128j+127 are up rows 64j .. 64j+63.  act: bf16 [M][F], leading
+ * dimension ld_act (a multiple of 8).  Requirements: F % 64 == 0, K % 64 == 0,
  * alignment as for kinv_gemm. */
 kinv_status kinv_gemm_swiglu(const void* A, int64_t lda, const void* W_gu, int64_t ldw,
                              void* act, int64_t ld_act, int M, int F, int K,

@@ -16,6 +16,8 @@ std::once_flag g_once[kMaxDevices];
 int* g_status_ptr[kMaxDevices];
 int g_sm_count[kMaxDevices];
 int g_smem_optin[kMaxDevices];
+int g_smem_per_sm[kMaxDevices];
+int g_smem_reserved[kMaxDevices];
 
 int current_device() {
   int dev = -1;
@@ -28,6 +30,8 @@ void init_device(int dev) {
   if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) g_status_ptr[dev] = static_cast<int*>(p);
   cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
   cudaDeviceGetAttribute(&g_smem_optin[dev], cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaDeviceGetAttribute(&g_smem_per_sm[dev], cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  cudaDeviceGetAttribute(&g_smem_reserved[dev], cudaDevAttrReservedSharedMemoryPerBlock, dev);
 }
 
 int ensure() {
@@ -49,6 +53,14 @@ int sm_count() {
 int max_smem_optin() {
   const int dev = ensure();
   return dev < 0 ? 0 : g_smem_optin[dev];
+}
+int smem_per_sm() {
+  const int dev = ensure();
+  return dev < 0 ? 0 : g_smem_per_sm[dev];
+}
+int smem_reserved_per_block() {
+  const int dev = ensure();
+  return dev < 0 ? 0 : g_smem_reserved[dev];
 }
 
 }  // namespace kinv

@@ -10,10 +10,15 @@
 //  * every tile is 128 rows of A by BN rows of W; each K step is one
 //    tcgen05.mma of shape 128 x BN x 16 (kind::f16, bf16 in, fp32 accumulate),
 //    four per 64-wide K block, K blocks in ascending order;
+//  * one pipeline stage carries j consecutive 64-wide K blocks of A and W,
+//    each brought by a single 3-D TMA copy (a CTA keeps only a few copies in
+//    flight, so each copy must be large for the weight stream to keep up);
 //  * K is cut into `splits` equal, contiguous ranges (splits depends on N and
-//    K only); the CTAs of one cluster compute one range each, and the partial
-//    sums are added in rank order p0 + p1 + ... through distributed shared
-//    memory -- no atomics, no batch-dependent split;
+//    K only); the CTAs of one cluster compute one range each.  Each rank
+//    pushes its fp32 partial rows into the shared memory of the rank that
+//    owns them (row m belongs to rank m % splits), and the owner adds the
+//    partials in rank order p0 + p1 + ... -- no atomics, no batch-dependent
+//    split;
 //  * TMA brings in the rows of A that exist (M rounded up to 8, at most 128);
 //    the tile rows beyond them feed accumulator rows that are never stored.
 // Row i therefore meets the same instructions in the same order for every M,
@@ -62,13 +67,15 @@ struct GemmArgs {
   void* C;
   int64_t ldc;
   int M, N;
-  int k_tiles;  // 64-wide K blocks per split
-  int a_rows;   // rows of A that TMA brings in per tile (the rest of the 128 are never stored)
-  int a_stride; // bytes between A stages (a_rows * 128)
+  int k_stages;  // pipeline stages per split (each j K blocks)
+  int j;         // 64-wide K blocks per stage
+  int a_rows;    // rows of A that TMA brings in per tile (the rest of the 128 are never stored)
+  int a_blk;     // bytes of one K block of A in shared memory (a_rows * 128)
   int c_f32;
-  int swiglu;   // output silu(gate) * up: tile columns [0, 32) gate, [32, 64) up
+  int swiglu;    // output silu(gate) * up: tile columns [0, BN/2) gate, [BN/2, BN) up
   int stages;
   int splits;
+  int own_rows;  // split-K: rows a rank owns at most (ceil(a_rows / splits))
   int* status;
 };
 
@@ -76,34 +83,43 @@ template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                 const GemmArgs args) {
-  constexpr int W_STAGE = BN * BK * 2;
+  constexpr int W_BLK = BN * BK * 2;  // one K block of W
   constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int stages = args.stages;
-  // A stages first, then W stages.  An MMA reads 128 rows (16 KB) from the
-  // start of an A stage; when a stage holds fewer rows the extra rows come
-  // from the following stages (inside this block's shared memory) and only
-  // feed accumulator rows that are never stored.
-  const int a_stride = args.a_stride;
+  const int jb = args.j;
+  const int W_STAGE = W_BLK * jb;
+  // A stages first, then W stages; a stage holds j K blocks back to back.
+  // An MMA reads 128 rows (16 KB) from the start of an A block; when a block
+  // holds fewer rows the extra rows come from the memory that follows
+  // (inside this block's shared memory) and only feed accumulator rows that
+  // are never stored.
+  const int a_blk = args.a_blk;
+  const int a_stride = a_blk * jb;
   unsigned char* a_st = base;
   unsigned char* w_st = base + stages * a_stride;
+  // split-K partials received from every rank, [splits][own_rows][BN] fp32,
+  // over the stage ring (idle by then in every rank of the cluster)
+  float* recv = reinterpret_cast<float*>(base);
   uint64_t* bars = reinterpret_cast<uint64_t*>(w_st + stages * W_STAGE);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   auto full_bar = [&](int s) { return smem_addr(bars + s); };
   auto empty_bar = [&](int s) { return smem_addr(bars + stages + s); };
   const uint32_t done_bar = smem_addr(bars + 2 * stages);
+  const uint32_t recv_bar = smem_addr(bars + 2 * stages + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int splits = args.splits;
   const int rank = splits > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const int m0 = blockIdx.y * BM;  // M tiles of one N tile are launch neighbours: W is read once
   const int n0 = blockIdx.z * BN;
-  const uint32_t stage_bytes = static_cast<uint32_t>(args.a_rows * BK * 2 + W_STAGE);
-  const int k_tiles = args.k_tiles;
-  const int kt0 = rank * k_tiles;
+  const int rows_here = args.M - m0 < BM ? args.M - m0 : BM;
+  const uint32_t stage_bytes = static_cast<uint32_t>(a_stride + W_STAGE);
+  const int k_stages = args.k_stages;
+  const int kb0 = rank * k_stages * jb;  // first K block of this split
 
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
@@ -112,8 +128,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(empty_bar(s), 1);
     }
     mbar_init(done_bar, 1);
+    mbar_init(recv_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    if (splits > 1) {
+      // the partial rows this rank owns arrive from every other rank
+      const int owned = rank < rows_here ? (rows_here - rank + splits - 1) / splits : 0;
+      mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>((splits - 1) * owned * BN * 4));
+    }
   }
   if (warp == 0) tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
   tc_fence_before();
@@ -131,16 +153,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // The weights do not depend on the kernel before this one: the first
       // ring's worth of W tiles is requested before waiting for it; A (its
       // output) only after.  Fresh stages need no empty-barrier wait.
-      const int pre = k_tiles < stages ? k_tiles : stages;
+      const int pre = k_stages < stages ? k_stages : stages;
       for (int kt = 0; kt < pre; ++kt) {
         mbar_arrive_expect_tx(full_bar(kt), stage_bytes);
-        tma_load_2d(smem_addr(w_st + kt * W_STAGE), &tmW, (kt0 + kt) * BK, n0, full_bar(kt), pol_w);
+        tma_load_3d(smem_addr(w_st + kt * W_STAGE), &tmW, 0, n0, kb0 + kt * jb, full_bar(kt), pol_w);
       }
       pdl_wait();
       for (int kt = 0; kt < pre; ++kt)
-        tma_load_2d(smem_addr(a_st + kt * a_stride), &tmA, (kt0 + kt) * BK, m0, full_bar(kt), pol_a);
+        tma_load_3d(smem_addr(a_st + kt * a_stride), &tmA, 0, m0, kb0 + kt * jb, full_bar(kt), pol_a);
       issued = pre;
-      for (int kt = pre; kt < k_tiles; ++kt) {
+      for (int kt = pre; kt < k_stages; ++kt) {
         const int s = kt % stages;
         const uint32_t ph = (kt / stages) & 1u;
         if (*abort_flag ||
@@ -149,9 +171,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(full_bar(s), stage_bytes);
-        const int kx = (kt0 + kt) * BK;
-        tma_load_2d(smem_addr(a_st + s * a_stride), &tmA, kx, m0, full_bar(s), pol_a);
-        tma_load_2d(smem_addr(w_st + s * W_STAGE), &tmW, kx, n0, full_bar(s), pol_w);
+        const int kb = kb0 + kt * jb;
+        tma_load_3d(smem_addr(a_st + s * a_stride), &tmA, 0, m0, kb, full_bar(s), pol_a);
+        tma_load_3d(smem_addr(w_st + s * W_STAGE), &tmW, 0, n0, kb, full_bar(s), pol_w);
         ++issued;
       }
     }
@@ -159,7 +181,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = instr_desc<BN>();
-      for (int kt = 0; kt < k_tiles; ++kt) {
+      for (int kt = 0; kt < k_stages; ++kt) {
         const int s = kt % stages;
         const uint32_t ph = (kt / stages) & 1u;
         if (*abort_flag ||
@@ -168,12 +190,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a_addr = smem_addr(a_st + s * a_stride);
-        const uint32_t w_addr = smem_addr(w_st + s * W_STAGE);
+#pragma unroll 1
+        for (int jj = 0; jj < jb; ++jj) {
+          const uint32_t a_addr = smem_addr(a_st + s * a_stride + jj * a_blk);
+          const uint32_t w_addr = smem_addr(w_st + s * W_STAGE + jj * W_BLK);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          umma_bf16(tmem, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(w_addr + kk * 32), idesc,
-                    (kt | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            umma_bf16(tmem, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(w_addr + kk * 32), idesc,
+                      (kt | jj | kk) != 0 ? 1u : 0u);
+          }
         }
         umma_commit(empty_bar(s));  // the stage is free once these MMAs have read it
       }
@@ -189,17 +214,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int row_local = warp * 32 + lane;
   const int m = m0 + row_local;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-  const bool good = ok && !*abort_flag && k_tiles > 0;
+  const bool good = ok && !*abort_flag && k_stages > 0;
+  constexpr int HALF = BN / 2;
 
   if (splits == 1 && args.swiglu) {
-    // columns [0, 32) of the tile are gate features n0/2 .. n0/2 + 31, columns
-    // [32, 64) the up features for the same ids
-    if (good) {
+    // columns [0, BN/2) of the tile are gate features n0/2 .. n0/2 + BN/2 - 1,
+    // columns [BN/2, BN) the up features for the same ids
+#pragma unroll 1
+    for (int c0 = 0; c0 < HALF && good; c0 += 32) {
       uint32_t gv[32], uv[32];
-      tmem_ld32(lane_base, gv);
-      tmem_ld32(lane_base + 32, uv);
+      tmem_ld32(lane_base + c0, gv);
+      tmem_ld32(lane_base + HALF + c0, uv);
       if (m < args.M) {
-        __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(args.C) + m * args.ldc + n0 / 2;
+        __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(args.C) + m * args.ldc + n0 / 2 + c0;
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
           uint4 o;
@@ -247,75 +274,69 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else {
-    // Constant split-K: park this CTA's fp32 partial tile in its own shared
-    // memory (the stage ring is idle now), then rank q reduces columns
-    // [q * BN / splits, (q + 1) * BN / splits) of every row present, over all
-    // ranks in rank order p0 + p1 + ...
-    constexpr int LDR = BN + 1;
-    float* red = reinterpret_cast<float*>(base);
-    const int rows_here = args.M - m0 < BM ? args.M - m0 : BM;
-    if (good && warp * 32 < rows_here) {
+    // Constant split-K.  Rank r pushes row m of its partial tile into slot r of
+    // the owner rank m % splits (row index m / splits there; the owner's own
+    // rows are plain local stores); once all slots of its rows are in, the
+    // owner adds them in rank order and stores.
+    // every rank's MMAs have drained its ring (and its receive barrier is set)
+    cluster_sync();
+    const int own_rows = args.own_rows;
+    if (warp * 32 < rows_here) {
+      const bool row_ok = row_local < rows_here;
+      const int owner = row_ok ? row_local % splits : rank;
+      float* dst_local = recv + (rank * own_rows + (row_ok ? row_local / splits : 0)) * BN;
+      const uint32_t dst_base = map_to_rank(smem_addr(dst_local), owner);
+      const uint32_t dst_bar = map_to_rank(recv_bar, owner);
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(lane_base + c0, r);
+        if (row_ok && owner == rank) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) red[row_local * LDR + c0 + j] = __uint_as_float(r[j]);
+          for (int q = 0; q < 32; q += 4)
+            *reinterpret_cast<uint4*>(dst_local + c0 + q) = make_uint4(r[q], r[q + 1], r[q + 2], r[q + 3]);
+        } else if (row_ok) {
+#pragma unroll
+          for (int q = 0; q < 32; q += 4)
+            st_async_v4(dst_base + (c0 + q) * 4, r[q], r[q + 1], r[q + 2], r[q + 3], dst_bar);
+        }
       }
     }
-    cluster_sync();
-    const int cols_per = BN / splits;
-    const int cbase = rank * cols_per;
-    if (good && args.swiglu) {
-      // rank q forms features [q * 32 / splits, (q + 1) * 32 / splits): their
-      // gate column f and up column 32 + f, each summed in rank order
-      const int feats_per = 32 / splits;
-      const int fbase = rank * feats_per;
-      for (int idx = threadIdx.x; idx < rows_here * feats_per; idx += kGemmThreads) {
-        const int rl = idx / feats_per;
-        const int f = fbase + idx % feats_per;
-        const int mm = m0 + rl;
-        const uint32_t lg = smem_addr(red + rl * LDR + f);
-        const uint32_t lu = smem_addr(red + rl * LDR + 32 + f);
-        float pg[8], pu[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q < splits) {
-            pg[q] = ld_dsmem_f32(map_to_rank(lg, q));
-            pu[q] = ld_dsmem_f32(map_to_rank(lu, q));
+    __syncthreads();  // this rank's own rows are in place
+    const int owned = rank < rows_here ? (rows_here - rank + splits - 1) / splits : 0;
+    const bool got = mbar_wait_bounded(recv_bar, 0, args.status, DEV_TIMEOUT_GEMM_EPILOGUE);
+    if (good && got) {
+      const int slot = own_rows * BN;
+      if (args.swiglu) {
+        // gate column f and up column HALF + f of each owned row
+        for (int idx = threadIdx.x; idx < owned * HALF; idx += kGemmThreads) {
+          const int i = idx / HALF, f = idx % HALF;
+          const float* src = recv + i * BN + f;
+          float g = src[0], u = src[HALF];
+          for (int q = 1; q < splits; ++q) {
+            g = __fadd_rn(g, src[q * slot]);
+            u = __fadd_rn(u, src[q * slot + HALF]);
           }
-        float g = pg[0], u = pu[0];
-#pragma unroll
-        for (int q = 1; q < 8; ++q)
-          if (q < splits) {
-            g = __fadd_rn(g, pg[q]);
-            u = __fadd_rn(u, pu[q]);
-          }
-        static_cast<__nv_bfloat16*>(args.C)[mm * args.ldc + n0 / 2 + f] =
-            __float2bfloat16_rn(silu_times(g, u));
-      }
-    } else if (good) {
-      for (int idx = threadIdx.x; idx < rows_here * cols_per; idx += kGemmThreads) {
-        const int rl = idx / cols_per;
-        const int col = cbase + idx % cols_per;
-        const int mm = m0 + rl, nn = n0 + col;
-        if (nn >= args.N) continue;
-        const uint32_t local = smem_addr(red + rl * LDR + col);
-        float part[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (q < splits) part[q] = ld_dsmem_f32(map_to_rank(local, q));
-        float acc = part[0];
-#pragma unroll
-        for (int q = 1; q < 8; ++q)
-          if (q < splits) acc = __fadd_rn(acc, part[q]);
-        if (args.c_f32)
-          static_cast<float*>(args.C)[mm * args.ldc + nn] = acc;
-        else
-          static_cast<__nv_bfloat16*>(args.C)[mm * args.ldc + nn] = __float2bfloat16_rn(acc);
+          const int mm = m0 + i * splits + rank;
+          static_cast<__nv_bfloat16*>(args.C)[mm * args.ldc + n0 / 2 + f] =
+              __float2bfloat16_rn(silu_times(g, u));
+        }
+      } else {
+        for (int idx = threadIdx.x; idx < owned * BN; idx += kGemmThreads) {
+          const int i = idx / BN, col = idx % BN;
+          const int nn = n0 + col;
+          if (nn >= args.N) continue;
+          const float* src = recv + i * BN + col;
+          float acc = src[0];
+          for (int q = 1; q < splits; ++q) acc = __fadd_rn(acc, src[q * slot]);
+          const int mm = m0 + i * splits + rank;
+          if (args.c_f32)
+            static_cast<float*>(args.C)[mm * args.ldc + nn] = acc;
+          else
+            static_cast<__nv_bfloat16*>(args.C)[mm * args.ldc + nn] = __float2bfloat16_rn(acc);
+        }
       }
     }
-    cluster_sync();  // no CTA leaves while another still reads its partial
   }
 
   // ---- teardown
@@ -347,65 +368,82 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// A row-major [rows][cols] bf16 matrix seen as 3-D (64 columns, rows,
+// cols / 64 K blocks): one box is box_rows rows by kblocks K blocks, landing
+// in shared memory as kblocks consecutive [box_rows][64] swizzled blocks.
 bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
-              int box_rows) {
+              int box_rows, int kblocks) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(cols / BK)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, BK * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows),
+                             static_cast<cuuint32_t>(kblocks)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct Plan {
   int bn, splits;
+  int j;            // K blocks per pipeline stage
   int smem_budget;  // bytes of stage ring per block (sets blocks per SM)
 };
 
 // The tile width and the K split depend on (N, K) only -- never on M -- so
-// every row meets the same reduction order whatever the batch.  Measured on
-// the decode shapes: three 24 KB stages (three CTAs per SM) beat deeper rings,
-// and a split of K into up to four ranks that brings the CTA count to about
-// 256 beats both no split and eight ranks.  Wide outputs (the LM head) take
-// 128-wide tiles and no split.
+// every row meets the same reduction order whatever the batch.  Decode GEMMs
+// stream the weights once and are bound by how many bytes are in flight: a
+// CTA keeps only a few TMA copies outstanding, so there are many CTAs (a K
+// split bringing the count to at least 256) and each copy carries two K
+// blocks (32 KB of W).  How many K blocks a copy carries and how deep the
+// ring is do not change the order of the MMAs; they are set per launch.
 Plan plan_for(int N, int K) {
-  const int kt = K / BK;
-  Plan p{64, 1, 72 * 1024};
-  if (N >= 37888) p = Plan{128, 1, 96 * 1024};
+  const int kb = K / BK;
+  Plan p{128, 1, 2, 112 * 1024};
   const int tiles = (N + p.bn - 1) / p.bn;
-  // a long K (the down projection) takes up to eight ranks and a 48 KB ring
-  const bool long_k = K >= 8192;
-  const int max_s = long_k ? 8 : 4;
-  const int want = long_k ? 512 : 256;
   int s = 1;
-  while (s < max_s && tiles * s < want && kt % (2 * s) == 0 && kt / (2 * s) >= 4) s *= 2;
+  while (s < 8 && tiles * s < 256 && kb % (4 * s) == 0) s *= 2;
   p.splits = s;
-  if (s == 8) p.smem_budget = 48 * 1024;
+  if ((kb / s) % 2) p.j = 1;
   return p;
 }
 
-template <int BN>
-size_t smem_bytes(int stages, int a_stride) {
-  return 1024 + static_cast<size_t>(stages) * (a_stride + BN * BK * 2) + (2 * stages + 1) * 8 + 16;
+// Shared memory a block may use so that `ctas` blocks are resident at once
+// (at most four per SM: four 128-column TMEM tiles).
+int ring_cap(long long ctas) {
+  const int sms = sm_count() > 0 ? sm_count() : 1;
+  long long per_sm = (ctas + sms - 1) / sms;
+  per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
+  return static_cast<int>(smem_per_sm() / per_sm) - smem_reserved_per_block() - 1024 - 256;
+}
+
+size_t smem_bytes(int stages, int stage_bytes) {
+  return 1024 + static_cast<size_t>(stages) * stage_bytes + (2 * stages + 2) * 8 + 16;
 }
 
 template <int BN>
 kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a, int budget,
                         int grid_y, int grid_z, cudaStream_t stream) {
-  // As many stages as the budget holds (2..8): small M leaves room for more
-  // weight tiles in flight.  The ring must also hold the split-K partial tile
-  // and the 128 rows one MMA reads from the start of the last A stage.
-  const int stage = a.a_stride + BN * BK * 2;
-  int stages = budget / stage;
+  // The ring is sized so that the whole grid is resident at once (a second
+  // wave would double the time of a weight stream): at most the SM's shared
+  // memory divided by the blocks each SM must hold, within the plan's budget
+  // and 2..8 stages.  It must also hold the split-K receive slots (they reuse
+  // it), and the 128 rows one MMA reads from the start of the last A block
+  // must stay inside the block's shared memory.
+  a.own_rows = (a.a_rows + a.splits - 1) / a.splits;
+  const int recv_bytes = a.splits > 1 ? a.splits * a.own_rows * BN * 4 : 0;
+  const int cap = ring_cap(static_cast<long long>(a.splits) * grid_y * grid_z);
+  const int limit = budget < cap ? budget : cap;
+  const int stage = a.a_blk * a.j + BN * BK * 2 * a.j;
+  int stages = limit / stage;
   stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
-  while (static_cast<size_t>(stages) * stage < static_cast<size_t>(BM) * (BN + 1) * 4 ||
-         (stages - 1) * a.a_stride + A_STAGE > stages * stage)
+  while (static_cast<long long>(stages) * stage < recv_bytes ||
+         (stages - 1) * a.a_blk * a.j + (a.j - 1) * a.a_blk + A_STAGE > stages * stage)
     ++stages;
   a.stages = stages;
-  const size_t smem = smem_bytes<BN>(stages, a.a_stride);
+  const size_t smem = smem_bytes(stages, stage);
   if (smem > static_cast<size_t>(max_smem_optin())) return KINV_ERR_UNSUPPORTED;
   // the opt-in limit is raised once per device to the largest request seen
   static size_t configured[64] = {};
@@ -438,13 +476,12 @@ kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, vo
   if (c_dtype != KINV_BF16 && c_dtype != KINV_F32) return KINV_ERR_INVALID_ARG;
   if (M == 0) return KINV_OK;
   if (!A || !W || !C) return KINV_ERR_INVALID_ARG;
-  if (K % BK || N % 16 || (swiglu && (N % 64 || c_dtype != KINV_BF16))) return KINV_ERR_UNSUPPORTED;
+  if (K % BK || N % 16 || (swiglu && (N % 128 || c_dtype != KINV_BF16))) return KINV_ERR_UNSUPPORTED;
   if (lda < K || ldw < K || ldc < (swiglu ? N / 2 : N)) return KINV_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(W) || !aligned16(C) || lda % 8 || ldw % 8 ||
       (c_dtype == KINV_BF16 ? ldc % 8 : ldc % 4))
     return KINV_ERR_ALIGNMENT;
-  Plan p = plan_for(N, K);
-  if (swiglu) p.bn = 64;  // a tile holds 32 gate and the matching 32 up columns
+  const Plan p = plan_for(N, K);  // 128-wide tiles: 64 gate and the matching 64 up columns
   const int grid_y = (M + BM - 1) / BM;
   const int grid_z = (N + p.bn - 1) / p.bn;
   if (grid_y > 65535 || grid_z > 65535) return KINV_ERR_UNSUPPORTED;
@@ -452,20 +489,28 @@ kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, vo
   // fill of a mostly empty box is slow, and the tile rows beyond M feed only
   // accumulator rows that are never stored.
   const int a_rows = M >= BM ? BM : ((M + 7) / 8) * 8;
+  // K blocks per stage only set how the loads are grouped, not the order of
+  // the MMAs: two per stage when two such stages fit the one-wave ring
+  const long long ctas = static_cast<long long>(p.splits) * grid_y * grid_z;
+  const int two_stages = 2 * (a_rows * BK * 2 + p.bn * BK * 2) * p.j;
+  const int j = two_stages <= ring_cap(ctas) && two_stages <= p.smem_budget ? p.j : 1;
   CUtensorMap ta, tw;
-  if (!make_map(&ta, A, M, K, lda, a_rows) || !make_map(&tw, W, N, K, ldw, p.bn)) return KINV_ERR_CUDA;
+  if (!make_map(&ta, A, M, K, lda, a_rows, j) || !make_map(&tw, W, N, K, ldw, p.bn, j))
+    return KINV_ERR_CUDA;
   GemmArgs a;
   a.C = C;
   a.ldc = ldc;
   a.M = M;
   a.N = N;
-  a.k_tiles = K / BK / p.splits;
+  a.k_stages = K / BK / p.splits / j;
+  a.j = j;
   a.a_rows = a_rows;
-  a.a_stride = a_rows * BK * 2;
+  a.a_blk = a_rows * BK * 2;
   a.c_f32 = c_dtype == KINV_F32;
   a.swiglu = swiglu ? 1 : 0;
   a.stages = 0;
   a.splits = p.splits;
+  a.own_rows = 0;
   a.status = device_status_word();
   switch (p.bn) {
     case 64: return launch_gemm<64>(ta, tw, a, p.smem_budget, grid_y, grid_z, stream);
@@ -485,6 +530,6 @@ extern "C" kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int6
 extern "C" kinv_status kinv_gemm_swiglu(const void* A, int64_t lda, const void* W_gu, int64_t ldw,
                                         void* act, int64_t ld_act, int M, int F, int K,
                                         kinv_stream stream) {
-  if (F <= 0 || F % 32) return F <= 0 ? KINV_ERR_INVALID_ARG : KINV_ERR_UNSUPPORTED;
+  if (F <= 0 || F % 64) return F <= 0 ? KINV_ERR_INVALID_ARG : KINV_ERR_UNSUPPORTED;
   return kinv::gemm_impl(A, lda, W_gu, ldw, act, ld_act, KINV_BF16, M, 2 * F, K, true, stream);
 }

@@ -141,11 +141,11 @@ def gemm(a: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
 
 
 def interleave_gate_up(w_gu: torch.Tensor) -> torch.Tensor:
-    """[gate rows; up rows] ([2F][K]) -> the block-of-32 interleaved layout
+    """[gate rows; up rows] ([2F][K]) -> the block-of-64 interleaved layout
     kinv_gemm_swiglu reads (a one-time weight layout change, a copy)."""
     two_f, k = w_gu.shape
     f = two_f // 2
-    return w_gu.view(2, f // 32, 32, k).permute(1, 0, 2, 3).reshape(two_f, k).contiguous()
+    return w_gu.view(2, f // 64, 64, k).permute(1, 0, 2, 3).reshape(two_f, k).contiguous()
 
 
 def gemm_swiglu(a: torch.Tensor, w_gu_il: torch.Tensor, out: torch.Tensor | None = None,

@@ -127,7 +127,7 @@ def _swiglu_ref(a, w_gu):
     return oglue.swiglu_f64(ogemm(synth.bits(a), synth.bits(w_gu), out="f64"))
 
 
-@pytest.mark.parametrize("m,f,k", [(1, 32, 64), (5, 96, 256), (130, 160, 512), (33, 1024, 1024)])
+@pytest.mark.parametrize("m,f,k", [(1, 64, 64), (5, 192, 256), (130, 320, 512), (33, 1024, 1024)])
 def test_gemm_swiglu_parity(kinv, m, f, k):
     a = synth.normal_bf16((m, k), 1.0, 21).cuda()
     w_gu = synth.normal_bf16((2 * f, k), 0.05, 22).cuda()
@@ -175,6 +175,6 @@ def test_gemm_swiglu_8b_row_bits_independent_of_m(kinv):
 
 def test_gemm_swiglu_rejects_bad_f(kinv):
     a = torch.zeros(2, 64, dtype=torch.bfloat16, device="cuda")
-    w = torch.zeros(2 * 48, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(2 * 96, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(kinv.KinvError):
         kinv.gemm_swiglu(a, w)
