@@ -32,10 +32,10 @@ UNIT = "tokens/s"
 # from one `ncu --set full` capture (profiles/gemm_kernel_qwen3_8b_decode_b16.md).
 # Reported only while the GEMM's sources still hash to `src`.
 NCU_GEMM_TRAFFIC = {
-    "src": "fc4cfa6b2326b09e",
+    "src": "e64befe941d13f2e",
     "batch": 16,
-    "bytes": {"gemm_qkv": 50.504e6, "gemm_o": 33.719e6, "gemm_gate_up": 204.304e6,
-              "gemm_down": 103.801e6, "gemm_lm_head": 1251.728e6},
+    "bytes": {"gemm_qkv": 50.572e6, "gemm_o": 33.744e6, "gemm_gate_up": 204.502e6,
+              "gemm_down": 103.970e6, "gemm_lm_head": 1250.961e6},
 }
 
 
@@ -126,14 +126,14 @@ class Clocks:
 
 
 # ----------------------------------------------------------------- workload
-def build_workload(max_batch, steps_total, n_layers, rank, device):
+def build_workload(max_batch, steps_total, n_layers, rank, device, max_chunk=0):
     import torch
     from invariant_deterministic_gb300 import kinv, model as M, synth
     shape = M.ModelShape(**{**M.QWEN3_8B.__dict__, "n_layers": n_layers})
     w = M.random_weights(shape, seed=synth.SEED_WEIGHTS, device=device)
     lens = replica_lengths(max_batch, rank)
     lmax = 4096 + steps_total + 8
-    dec = M.Decoder(shape, w, max_batch=max_batch, max_len=lmax, device=device)
+    dec = M.Decoder(shape, w, max_batch=max_batch, max_len=lmax, max_chunk=max_chunk, device=device)
     g = synth.gen(synth.SEED_ACT + 100 * rank, device)
     for li in range(n_layers):
         dec.kv[li].normal_(generator=g)   # prompt KV ~N(0, 1)
@@ -162,8 +162,62 @@ def step_bytes(shape, bsz, lens_now):
     return weights + kv + logits
 
 
+def workload_name(layers, bsz):
+    return (f"Qwen3-8B-shaped decode step ({layers} layers, d 4096, 32/8 heads of 128, FFN 12288, "
+            f"vocab 151936), batch {bsz}, prompt lengths U{{16..4096}}, sampler T 0.8 top_k 50 "
+            "top_p 0.95 min_p 0.05 repeat penalty 1.1 over 64")
+
+
 def gemm_bytes(m, n, k, out_bytes=2):
     return (m * k + n * k) * 2 + m * n * out_bytes
+
+
+def run_prefill(dec, shape, chunk, prompt_len, stream, tc_peak):
+    """Chunked prefill of one prompt of `prompt_len` synthetic tokens through
+    every layer (sequence slot 0), chunks of `chunk` rows.  Returns tokens/s
+    and the tensor-core roofline of the GEMMs (fp32-accumulated bf16 flops
+    over the GEMM kernels' own time, from an instrumented pass) and of the
+    whole pass (GEMM + attention flops over the wall time)."""
+    import torch
+    from invariant_deterministic_gb300 import kinv, synth
+    ids = torch.randint(0, shape.vocab, (prompt_len,), generator=synth.gen(synth.SEED_LEN + 99))
+    ids = ids.to(torch.int32).to(dec.dev)
+
+    def one_pass():
+        for p0 in range(0, prompt_len, chunk):
+            n = min(chunk, prompt_len - p0)
+            kinv.embed(dec.w["embed"], ids[p0: p0 + n], out=dec.x[:n])
+            dec.prefill_chunk(0, p0, n)
+            dec.close_residual(n)
+
+    with torch.cuda.stream(stream):
+        one_pass()                      # warm-up
+        stream.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        one_pass()
+        t1.record(stream)
+        stream.synchronize()
+        ms = t0.elapsed_time(t1)
+        timer = {}
+        dec.timer = timer
+        one_pass()
+        dec.timer = None
+        stream.synchronize()
+    d, f, hq, hk, dh = shape.d_model, shape.ffn, shape.n_q, shape.n_kv, shape.head_dim
+    lin_per_tok = 2 * (shape.qkv_dim * d + d * hq * dh + 2 * f * d + d * f) * shape.n_layers
+    attn_flops = 4 * hq * dh * sum(p + 1 for p in range(prompt_len)) * shape.n_layers
+    gemm_ms = sum(a.elapsed_time(b) for k, v in timer.items() if k.startswith("gemm") for a, b in v)
+    gemm_tflops = lin_per_tok * prompt_len / (gemm_ms / 1e3) / 1e12
+    all_tflops = (lin_per_tok * prompt_len + attn_flops) / (ms / 1e3) / 1e12
+    return {"chunk": chunk, "prompt_len": prompt_len, "ms": round(ms, 3),
+            "tokens_per_s": round(prompt_len / (ms / 1e3), 1),
+            "gemm": {"bound": "tensor", "achieved": round(gemm_tflops, 1), "peak": tc_peak,
+                     "unit": "TFLOP/s", "frac": round(gemm_tflops / tc_peak, 4),
+                     "ms": round(gemm_ms, 3)},
+            "whole_pass": {"achieved": round(all_tflops, 1), "unit": "TFLOP/s",
+                           "frac": round(all_tflops / tc_peak, 4)}}
 
 
 def run_kinv(args):
@@ -179,7 +233,8 @@ def run_kinv(args):
     sweep = sorted(set([args.batch] + [int(x) for x in args.sweep.split(",") if x]))
     bmax = max(sweep)
     per_b = args.warmup + args.steps + 3
-    shape, w, dec, lens0 = build_workload(bmax, per_b * len(sweep) + 8, args.layers, rank, dev)
+    shape, w, dec, lens0 = build_workload(bmax, per_b * len(sweep) + 8, args.layers, rank, dev,
+                                          max_chunk=max(args.prefill_chunks) if args.prefill else 0)
     hbm_peak, tc_peak, peak_kind = _peaks()
     launches_per_step = 9 * shape.n_layers + 5
 
@@ -308,6 +363,12 @@ def run_kinv(args):
     e2e = {"value": round(bsz * ws * args.steps / e2e_s, 2), "unit": UNIT,
            "h2d_bytes_per_step": bsz * 4, "d2h_bytes_per_step": bsz * 4}
 
+    # ---- chunked prefill (tensor-core bound) after the decode measurements
+    prefill = None
+    if args.prefill:
+        prefill = [run_prefill(dec, shape, c, args.prefill_len, stream, tc_peak)
+                   for c in args.prefill_chunks]
+
     cpu = None
     if rank == 0 and not args.no_cpu:
         cpu = oracle_sample(min(args.cpu_rows, bsz), w, dec, shape)
@@ -318,10 +379,7 @@ def run_kinv(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(head["ms_per_step"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: random-init weights ~N(0,0.02) bf16, prompt KV cache ~N(0,1) bf16",
-        "config": {"workload": f"Qwen3-8B-shaped decode step ({shape.n_layers} layers, d 4096, "
-                               f"32/8 heads of 128, FFN 12288, vocab 151936), batch {bsz}, prompt "
-                               "lengths U{16..4096}, sampler T 0.8 top_k 50 top_p 0.95 min_p 0.05 "
-                               "repeat penalty 1.1 over 64",
+        "config": {"workload": workload_name(shape.n_layers, bsz),
                    "batch": bsz, "layers": shape.n_layers, "split_len": 256,
                    "mean_kv_len": round(head["mean_kv_len"], 1), "graph": "CUDA graph per step",
                    "l2": "inputs larger than L2 (15 GB of weights streamed per step)",
@@ -329,6 +387,7 @@ def run_kinv(args):
         "step_roofline": {"bytes": step_bytes(shape, bsz, lens_now), "gbs": round(head["step_gbs"], 1),
                           "frac": round(head["step_hbm_frac"], 4)},
         "roofline": roofline,
+        "prefill": prefill,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -391,13 +450,14 @@ def oracle_sample(rows, w, dec, shape, budget_s=12.0):
 
 
 def run_reference(args):
-    """The CPU oracle as the reference arm: each step is a bounded sample
-    (one request through one decoder layer, the LM head and the sampler,
-    scaled to the 36-layer step)."""
+    """The CPU oracle as the reference arm, on the same workload as the GPU
+    arm: each step is a bounded sample -- the first min(batch, 16) requests
+    of the batch (same prompt lengths) through one decoder layer, the final
+    norm, the LM head and the sampler -- with the layer time scaled to the
+    36-layer step."""
     ws, rank, _ = _dist()
     if rank != 0:
         return
-    import numpy as np
     import torch
     from invariant_deterministic_gb300 import synth
     from oracle.gemm import gemm as ogemm
@@ -412,39 +472,40 @@ def run_reference(args):
           synth.layer_weights(4096, 32, 8, 128, 12288, 0, True, "cpu").items()}
     head = synth.bits(synth.normal_bf16((151936, 4096), 0.02, 998))
     fnorm = synth.bits(torch.ones(4096, dtype=torch.bfloat16))
-    rows = 1
-    plen = int(synth.uniform_int(1, 16, 4096, synth.SEED_LEN)[0])
-    kc = synth.bits(synth.normal_bf16((rows, plen + args.steps + args.warmup + 1, 8, 128), 1.0, 1))
-    vc = synth.bits(synth.normal_bf16((rows, plen + args.steps + args.warmup + 1, 8, 128), 1.0, 2))
+    bsz = args.batch
+    rows = min(bsz, 16)
+    lens = replica_lengths(bsz, 0)[:rows]
+    lmax = max(lens) + args.steps + args.warmup + 1
+    kc = synth.bits(synth.normal_bf16((rows, lmax, 8, 128), 1.0, 1))
+    vc = synth.bits(synth.normal_bf16((rows, lmax, 8, 128), 1.0, 2))
     x = synth.bits(synth.normal_bf16((rows, 4096), 1.0, 3))
+    params = [OP(temperature=0.8, top_k=50, top_p=0.95, min_p=0.05, repeat_penalty=1.1,
+                 repeat_last_n=64, seed=synth.SEED_REQ_BASE + b) for b in range(rows)]
+    hist = [[] for _ in range(rows)]
 
-    def one(p):
+    def one(step):
         t0 = time.perf_counter()
-        y = layer_step(x, lw, kc, vc, [(0, p)], oshape)
+        y = layer_step(x, lw, kc, vc, [(b, lens[b] + step) for b in range(rows)], oshape)
         t1 = time.perf_counter()
         logits = ogemm(ormsnorm(y, fnorm, 1e-6), head, out="f32")
-        osample(logits, [[]], [0], [OP()])
+        osample(logits, hist, [step] * rows, params)
         t2 = time.perf_counter()
         return (t1 - t0) * 36 + (t2 - t1)
 
-    p = plen
-    for _ in range(args.warmup):
-        one(p)
-        p += 1
-    times = []
-    for _ in range(args.steps):
-        times.append(one(p))
-        p += 1
+    for i in range(args.warmup):
+        one(i)
+    times = [one(args.warmup + i) for i in range(args.steps)]
     per_step = sum(times) / len(times)
     value = rows / per_step
-    sample = (f"1 request (prompt {plen}) x 1 Qwen3-8B-shaped decoder layer + final norm + LM head + "
-              "sampler per step, fp64 NumPy oracle; layer time scaled x36")
+    sample = (f"first {rows} of the batch's {bsz} requests x 1 Qwen3-8B-shaped decoder layer + "
+              "final norm + LM head + sampler per step, fp64 NumPy oracle; layer time scaled x36")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": "Qwen3-8B-shaped decode step, batch 1 (oracle sample)",
-                                        "batch": 1, "layers": 36},
+        "data": "synthetic: random-init weights ~N(0,0.02) bf16, prompt KV cache ~N(0,1) bf16",
+        "config": {"workload": workload_name(36, bsz), "batch": bsz, "layers": 36, "split_len": 256,
+                   "parallelism": f"replicas x{ws}"},
         "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -463,9 +524,13 @@ def main():
     ap.add_argument("--prof-steps", type=int, default=3)
     ap.add_argument("--cpu-rows", type=int, default=16)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false")
+    ap.add_argument("--prefill-len", type=int, default=4096)
+    ap.add_argument("--prefill-chunks", default="512,4096")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    args.prefill_chunks = [int(c) for c in str(args.prefill_chunks).split(",") if c]
     if args.impl == "reference":
         run_reference(args)
     else:
