@@ -2,7 +2,12 @@
 // the receipt records temperature, top_k, top_p, min_p, repeat_penalty,
 // repeat_last_n and the seed, so the same settings must give the same token).
 //
-// One thread block per row; nothing is shared between rows.
+// Eight thread blocks (one cluster) per row, each owning a contiguous eighth
+// of the vocabulary; they exchange the row maximum, threshold counts, radix
+// histograms and their candidates through distributed shared memory, and
+// rank 0 of the cluster finishes the row.  Nothing is shared between rows,
+// and every quantity exchanged is an exact maximum, an integer count or a set
+// of candidates, so the result does not depend on how the row is divided.
 //  1. Repeat penalty: a shared-memory bitmap marks the distinct ids among the
 //     row's last repeat_last_n history tokens; a marked logit z becomes z / r
 //     (z > 0) or z * r, both correctly rounded fp32 operations.
@@ -15,21 +20,26 @@
 //     total order, so the candidate list does not depend on the parking order.
 //     If more than kCap ids tie exactly at the threshold, the ties are taken
 //     lowest id first by an ordered block-wide scan.
-//  3. s_i = z_i / T; e_i = exp(s_i - s_0); one thread forms the running sums in
-//     candidate order and applies top-p, min-p and the draw.
+//  3. s_i = z_i / T; e_i = exp(s_i - s_0); the running sums in candidate
+//     order (a fixed-order warp scan) give top-p, min-p and the draw.
 //  4. The draw: u = (Philox4x32-10(counter = (step lo, step hi, 0, 0),
 //     key = (seed lo, seed hi)).word0 >> 8) * 2^-24 (Salmon et al., SC'11,
 //     restated here from the published round function and constants).
 #include <math.h>
+
+#include <mutex>
 
 #include "common.cuh"
 
 namespace kinv {
 namespace {
 
-constexpr int kThreadsS = 1024;
+constexpr int kThreadsS = 512;
+constexpr int kMaxCluster = 8;  // blocks sharing one row, at most
 constexpr int kMaxTopK = 1024;
 constexpr int kCap = 4096;  // candidates gathered before sorting
+constexpr int kRounds = 10;  // 16-byte vectors of the row each thread keeps in registers
+constexpr int kRegSpan = kThreadsS * 4 * kRounds;  // ids a block holds in registers
 
 __device__ __forceinline__ uint32_t ordered_key(float z) {
   if (isnan(z)) z = -INFINITY;
@@ -62,21 +72,29 @@ __device__ __forceinline__ Philox4 philox4x32_10(Philox4 c, uint32_t k0, uint32_
 }
 
 struct Smem {
-  uint32_t hist[2048];
-  unsigned long long cand[kCap];
+  unsigned long long cand[kCap];  // this block's candidates (rank 0: all of them)
+  uint32_t hist[2048];            // this block's radix histogram (read by the peers)
+  uint32_t comb[2048];            // the cluster's histogram
   float e[kMaxTopK];
   uint32_t warp_cnt[32];
-  uint32_t n_cand;
-  uint32_t eq_taken;
-  uint32_t thresh;      // gather ids whose key >= thresh
-  int k_rem;
-  int ok;
-  int result;
   float wmax[32];
   int wcnt[32][8];
+  unsigned long long wbest[32];
   int cnt[8];
-  float thresh_f;       // fast path: gather ids whose value >= thresh_f
+  uint32_t offs[kMaxCluster + 1];
+  // read by the peers
+  float x_max;
+  int x_cnt[8];
+  unsigned long long x_best;
+  uint32_t n_cand;
+  // this block's copy of the cluster-wide decisions
+  float m_all;
+  uint32_t eq_taken;
+  uint32_t thresh;
+  int k_rem;
+  int ok;
   int fast;
+  float thresh_f;
 };
 
 __device__ __forceinline__ float penalised(const float* __restrict__ row, int i,
@@ -86,33 +104,35 @@ __device__ __forceinline__ float penalised(const float* __restrict__ row, int i,
   return z;
 }
 
-// Visits every id of the row once, in rounds in which each thread loads
+// Visits every id in [v0, v1) once, in rounds in which each thread loads
 // four 16-byte vectors (16 logits) before using any of them, so a pass keeps
-// many loads in flight.  f(valid, id, key) sees the key of the penalised
-// logit; every lane runs the same number of rounds (f may use warp votes).
+// many loads in flight.  f(valid, id, value) sees the penalised logit (NaN as
+// -inf); every lane runs the same number of rounds (f may use warp votes).
 template <typename F>
-__device__ __forceinline__ void for_each_value(const float* __restrict__ row, int V,
+__device__ __forceinline__ void for_each_value(const float* __restrict__ row, int v0, int v1,
                                                const uint32_t* bitmap, float r, F&& f) {
   constexpr int U = 4;
   const int t = threadIdx.x;
-  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
-  const int V4 = vec ? (V >> 2) : 0;
-  const float4* row4 = reinterpret_cast<const float4*>(row);
-  for (int base = 0; base < V4; base += kThreadsS * U) {
+  const int n = v1 > v0 ? v1 - v0 : 0;
+  const float* seg = row + v0;
+  const bool vec = (reinterpret_cast<uintptr_t>(seg) & 15u) == 0;
+  const int n4 = vec ? (n >> 2) : 0;
+  const float4* seg4 = reinterpret_cast<const float4*>(seg);
+  for (int base = 0; base < n4; base += kThreadsS * U) {
     float4 x[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int i4 = base + u * kThreadsS + t;
-      x[u] = i4 < V4 ? row4[i4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      x[u] = i4 < n4 ? seg4[i4] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int i4 = base + u * kThreadsS + t;
-      const bool valid = i4 < V4;
+      const bool valid = i4 < n4;
       const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int i = 4 * i4 + e;
+        const int i = v0 + 4 * i4 + e;
         float z = xv[e];
         if (valid && ((bitmap[i >> 5] >> (i & 31)) & 1u)) z = z > 0.f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
         f(valid, i, isnan(z) ? -INFINITY : z);
@@ -120,19 +140,12 @@ __device__ __forceinline__ void for_each_value(const float* __restrict__ row, in
     }
   }
   // the ids not covered by whole vectors, one per thread and round
-  for (int base = 4 * V4; base < V; base += kThreadsS) {
-    const int i = base + t;
-    const bool valid = i < V;
+  for (int base = 4 * n4; base < n; base += kThreadsS) {
+    const int i = v0 + base + t;
+    const bool valid = base + t < n;
     const float z = valid ? penalised(row, i, bitmap, r) : 0.f;
     f(valid, i, isnan(z) ? -INFINITY : z);
   }
-}
-
-template <typename F>
-__device__ __forceinline__ void for_each_key(const float* __restrict__ row, int V,
-                                             const uint32_t* bitmap, float r, F&& f) {
-  for_each_value(row, V, bitmap, r,
-                 [&](bool valid, int i, float z) { f(valid, i, valid ? ordered_key(z) : 0u); });
 }
 
 __device__ __forceinline__ unsigned long long composite(uint32_t key, int id) {
@@ -159,6 +172,7 @@ __device__ void bitonic_desc(unsigned long long* a, int n) {
   }
 }
 
+template <bool kRegs>
 __global__ void __launch_bounds__(kThreadsS) sample_kernel(
     const float* __restrict__ logits, int64_t ld, int V, const kinv_sampling_params* __restrict__ params,
     const int32_t* __restrict__ history, int hist_ld, const int32_t* __restrict__ hist_len,
@@ -168,14 +182,21 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + sizeof(Smem));
   pdl_launch_dependents();
   pdl_wait();
-  const int b = blockIdx.x;
+  const int b = blockIdx.y;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int C = static_cast<int>(gridDim.x);  // the cluster: all blocks of this row
   const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
+  constexpr int kWarps = kThreadsS / 32;
   const float* row = logits + b * ld;
   const kinv_sampling_params prm = params[b];
   const int words = (V + 31) >> 5;
+  // this block's ids: a multiple of 128 per rank (whole vectors, whole bitmap words)
+  const int chunk = ((V + C - 1) / C + 127) / 128 * 128;
+  const int v0 = min(V, rank * chunk), v1 = min(V, v0 + chunk);
+  auto peer = [](const void* p, int q) { return map_to_rank(smem_addr(p), static_cast<uint32_t>(q)); };
 
-  // 1. penalty bitmap
+  // 1. penalty bitmap (the whole row, in every block)
   for (int i = t; i < words; i += kThreadsS) bitmap[i] = 0u;
   __syncthreads();
   const float r = prm.repeat_penalty;
@@ -188,31 +209,89 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
   }
   __syncthreads();
 
+  // This block's penalised logits (NaN as -inf), read once into registers
+  // when its share of the row fits (thread t holds ids v0 + 2048 q + 4 t ..
+  // + 3 for round q); otherwise every pass streams them from memory.
+  const bool in_regs = kRegs && v1 - v0 <= kRegSpan;
+  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
+  float4 vr[kRegs ? kRounds : 1];
+  if (in_regs) {
+#pragma unroll
+    for (int q = 0; q < (kRegs ? kRounds : 1); ++q) {
+      const int i = v0 + q * kThreadsS * 4 + 4 * t;
+      float x[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (vec && i + 3 < v1) {
+        const float4 f = *reinterpret_cast<const float4*>(row + i);
+        x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (i + e < v1) x[e] = row[i + e];
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int id = i + e;
+        float z = x[e];
+        if (id < v1 && ((bitmap[id >> 5] >> (id & 31)) & 1u)) z = z > 0.f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
+        x[e] = isnan(z) ? -INFINITY : z;
+      }
+      vr[q] = make_float4(x[0], x[1], x[2], x[3]);
+    }
+  }
+  // f(valid, id, value) over this block's ids; every lane makes the same calls
+  auto visit = [&](auto&& f) {
+    if (in_regs) {
+#pragma unroll
+      for (int q = 0; q < (kRegs ? kRounds : 1); ++q) {
+        const int i = v0 + q * kThreadsS * 4 + 4 * t;
+        f(i < v1, i, vr[q].x);
+        f(i + 1 < v1, i + 1, vr[q].y);
+        f(i + 2 < v1, i + 2, vr[q].z);
+        f(i + 3 < v1, i + 3, vr[q].w);
+      }
+    } else {
+      for_each_value(row, v0, v1, bitmap, r, f);
+    }
+  };
+  auto visit_key = [&](auto&& f) {
+    visit([&](bool valid, int i, float z) { f(valid, i, valid ? ordered_key(z) : 0u); });
+  };
+
   const float temp = prm.temperature;
   if (!(temp > 0.f)) {
     // greedy: maximum of the strict total order
     unsigned long long best = 0ull;
-    for (int i = t; i < V; i += kThreadsS) {
-      const unsigned long long c = composite(ordered_key(penalised(row, i, bitmap, r)), i);
+    visit([&](bool valid, int i, float z) {
+      const unsigned long long c = valid ? composite(ordered_key(z), i) : 0ull;
       best = c > best ? c : best;
-    }
+    });
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long x = __shfl_xor_sync(0xffffffffu, best, o);
       best = x > best ? x : best;
     }
-    if (lane == 0) sm.cand[warp] = best;
+    if (lane == 0) sm.wbest[warp] = best;
     __syncthreads();
     if (t == 0) {
-      unsigned long long m = sm.cand[0];
-      for (int w = 1; w < kThreadsS / 32; ++w) m = sm.cand[w] > m ? sm.cand[w] : m;
+      unsigned long long m = sm.wbest[0];
+      for (int w = 1; w < kWarps; ++w) m = sm.wbest[w] > m ? sm.wbest[w] : m;
+      sm.x_best = m;
+    }
+    cluster_sync();
+    if (rank == 0 && t == 0) {
+      unsigned long long m = 0ull;
+      for (int q = 0; q < C; ++q) {
+        const unsigned long long x = ld_dsmem_u64(peer(&sm.x_best, q));
+        m = x > m ? x : m;
+      }
       out[b] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(m & 0xFFFFFFFFull));
     }
+    cluster_sync();  // the peers stay until rank 0 has read them
     return;
   }
   const int k = (prm.top_k <= 0 || prm.top_k >= V) ? V : prm.top_k;
   if (k > kMaxTopK) {
-    if (t == 0) {
+    if (rank == 0 && t == 0) {
       out[b] = -1;
       if (status) atomicExch(status, DEV_SAMPLER_UNSUPPORTED);
     }
@@ -227,20 +306,32 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
   constexpr float kDeltas[8] = {0.5f, 1.f, 2.f, 4.f, 8.f, 16.f, 32.f, 64.f};
   {
     float mx = -INFINITY;
-    for_each_value(row, V, bitmap, r, [&](bool valid, int, float z) {
+    visit([&](bool valid, int, float z) {
       if (valid) mx = fmaxf(mx, z);
     });
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) sm.wmax[warp] = mx;
     __syncthreads();
-    float m = sm.wmax[0];
-    for (int w = 1; w < kThreadsS / 32; ++w) m = fmaxf(m, sm.wmax[w]);
+    if (t == 0) {
+      float m = sm.wmax[0];
+      for (int w = 1; w < kWarps; ++w) m = fmaxf(m, sm.wmax[w]);
+      sm.x_max = m;
+    }
+    cluster_sync();
+    if (warp == 0) {
+      float m = lane < C ? ld_dsmem_f32(peer(&sm.x_max, lane)) : -INFINITY;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) sm.m_all = m;
+    }
+    __syncthreads();
+    const float m = sm.m_all;
     float th[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) th[j] = __fsub_rn(m, kDeltas[j]);
     int c[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for_each_value(row, V, bitmap, r, [&](bool valid, int, float z) {
+    visit([&](bool valid, int, float z) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) c[j] += (valid && z >= th[j]) ? 1 : 0;
     });
@@ -253,7 +344,13 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
     __syncthreads();
     if (t < 8) {
       int tot = 0;
-      for (int w = 0; w < kThreadsS / 32; ++w) tot += sm.wcnt[w][t];
+      for (int w = 0; w < kWarps; ++w) tot += sm.wcnt[w][t];
+      sm.x_cnt[t] = tot;
+    }
+    cluster_sync();
+    if (t < 8) {
+      int tot = 0;
+      for (int q = 0; q < C; ++q) tot += static_cast<int>(ld_dsmem_u32(peer(&sm.x_cnt[t], q)));
       sm.cnt[t] = tot;
     }
     __syncthreads();
@@ -268,13 +365,13 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
           break;
         }
       }
-      sm.n_cand = 0;
     }
     __syncthreads();
   }
   const bool fast = sm.fast != 0;
 
-  // 2b. Otherwise, radix narrowing of the threshold
+  // 2b. Otherwise, radix narrowing of the threshold over the cluster's
+  // summed histograms (every block takes the same decision)
   uint32_t prefix = 0;  // fixed high bits of the threshold
   int fixed = 0;        // how many high bits are fixed
   int k_rem = k;        // how many ids are still needed at or below the prefix
@@ -287,13 +384,19 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
     const int nb = 1 << w;
     for (int i = t; i < nb; i += kThreadsS) sm.hist[i] = 0u;
     __syncthreads();
-    for_each_key(row, V, bitmap, r, [&](bool valid, int, uint32_t key) {
+    visit_key([&](bool valid, int, uint32_t key) {
       const bool in = valid && (fixed == 0 || (key >> (32 - fixed)) == prefix);
       const uint32_t digit = in ? (key >> shift) & (nb - 1) : 0xFFFFFFFFu;
       const unsigned peers = __match_any_sync(0xffffffffu, digit);
       if (in && lane == __ffs(peers) - 1) atomicAdd(&sm.hist[digit], __popc(peers));
     });
-    __syncthreads();
+    cluster_sync();  // every block's histogram is complete
+    for (int i = t; i < nb; i += kThreadsS) {
+      uint32_t tot = 0;
+      for (int q = 0; q < C; ++q) tot += ld_dsmem_u32(peer(&sm.hist[i], q));
+      sm.comb[i] = tot;
+    }
+    cluster_sync();  // every block has read the histograms (the next pass reuses them)
     if (warp == 0) {
       // lane l sums bins [nb - (l + 1) * nb / 32, nb - l * nb / 32) (lane 0 the
       // top block); an exclusive scan from the top finds the block holding
@@ -301,7 +404,7 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
       const int per = nb / 32;
       const int hi = nb - lane * per;
       int bsum = 0;
-      for (int d = hi - 1; d >= hi - per; --d) bsum += static_cast<int>(sm.hist[d]);
+      for (int d = hi - 1; d >= hi - per; --d) bsum += static_cast<int>(sm.comb[d]);
       int incl = bsum;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -314,11 +417,11 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
       if (lane == owner) {
         int cum = excl, d = hi - 1;
         for (; d > hi - per; --d) {
-          if (cum + static_cast<int>(sm.hist[d]) >= k_rem) break;
-          cum += sm.hist[d];
+          if (cum + static_cast<int>(sm.comb[d]) >= k_rem) break;
+          cum += sm.comb[d];
         }
         // ids with digit > d are all in; ids with digit == d hold the k_rem-th
-        const int at_or_above = above + cum + static_cast<int>(sm.hist[d]);
+        const int at_or_above = above + cum + static_cast<int>(sm.comb[d]);
         sm.thresh = ((prefix << w) | static_cast<uint32_t>(d)) << shift;
         sm.k_rem = k_rem - cum;
         sm.ok = at_or_above <= kCap ? 1 : 0;
@@ -343,21 +446,23 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
   __syncthreads();
   if (fast) {
     const float tf = sm.thresh_f;
-    for_each_value(row, V, bitmap, r, [&](bool valid, int i, float z) {
+    visit([&](bool valid, int i, float z) {
       if (valid && z >= tf) {
         const uint32_t slot = atomicAdd(&sm.n_cand, 1u);  // parking slot only
         sm.cand[slot] = composite(ordered_key(z), i);
       }
     });
   } else if (!exact_ties) {
-    for_each_key(row, V, bitmap, r, [&](bool valid, int i, uint32_t key) {
+    visit_key([&](bool valid, int i, uint32_t key) {
       if (valid && key >= thresh) {
         const uint32_t slot = atomicAdd(&sm.n_cand, 1u);  // parking slot only
         sm.cand[slot] = composite(key, i);
       }
     });
-  } else {
-    // every id above the threshold, plus the lowest-id ties, in id order
+  } else if (rank == 0) {
+    // More than kCap ids tie exactly at the threshold (rare): rank 0 takes
+    // every id above it plus the lowest-id ties, scanning the whole row in id
+    // order.
     const int need_eq = k_rem;
     for (int base = 0; base < V; base += kThreadsS) {
       const int i = base + t;
@@ -383,68 +488,113 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
       __syncthreads();
       if (t == 0) {
         uint32_t tot = 0;
-        for (int w2 = 0; w2 < kThreadsS / 32; ++w2) tot += sm.warp_cnt[w2];
+        for (int w2 = 0; w2 < kWarps; ++w2) tot += sm.warp_cnt[w2];
         sm.eq_taken += tot;
       }
       __syncthreads();
     }
   }
-  __syncthreads();
-  const int n_cand = static_cast<int>(sm.n_cand);
-  int n2 = 1;
-  while (n2 < n_cand) n2 <<= 1;
-  for (int i = n_cand + t; i < n2; i += kThreadsS) sm.cand[i] = 0ull;
-  __syncthreads();
-  bitonic_desc(sm.cand, n2);
+  cluster_sync();  // every block's candidates are parked
+  if (rank == 0) {
+    // rank 0 appends the peers' candidates after its own
+    if (t == 0) {
+      uint32_t off = sm.n_cand;
+      sm.offs[0] = 0;
+      for (int q = 1; q < C; ++q) {
+        sm.offs[q] = off;
+        off += ld_dsmem_u32(peer(&sm.n_cand, q));
+      }
+      sm.offs[C] = off;
+    }
+    __syncthreads();
+    for (int q = 1; q < C; ++q) {
+      const int n_q = static_cast<int>(sm.offs[q + 1] - sm.offs[q]);
+      const uint32_t src = peer(&sm.cand[0], q);
+      for (int i = t; i < n_q; i += kThreadsS) sm.cand[sm.offs[q] + i] = ld_dsmem_u64(src + 8u * i);
+    }
+  }
+  cluster_sync();  // the peers stay until rank 0 has read them
+  if (rank != 0) return;
+  const int n_cand = static_cast<int>(sm.offs[C]);
   const int kk = min(k, n_cand);
+  // The first kk candidates in the strict total order (composites are
+  // distinct).  Up to 1024 candidates: each one's position is the number of
+  // candidates above it; more: a bitonic sort.
+  unsigned long long* top = reinterpret_cast<unsigned long long*>(sm.hist);  // room for kMaxTopK
+  if (n_cand <= kMaxTopK) {
+    for (int i = t; i < n_cand; i += kThreadsS) {
+      const unsigned long long x = sm.cand[i];
+      int pos = 0;
+      for (int j = 0; j < n_cand; ++j) pos += sm.cand[j] > x ? 1 : 0;
+      if (pos < kk) top[pos] = x;
+    }
+  } else {
+    int n2 = 1;
+    while (n2 < n_cand) n2 <<= 1;
+    for (int i = n_cand + t; i < n2; i += kThreadsS) sm.cand[i] = 0ull;
+    __syncthreads();
+    bitonic_desc(sm.cand, n2);
+    for (int i = t; i < kk; i += kThreadsS) top[i] = sm.cand[i];
+  }
+  __syncthreads();
 
-  // 3. exponentials in candidate order
-  const float s0 = __fdiv_rn(key_value(static_cast<uint32_t>(sm.cand[0] >> 32)), temp);
+  // 3. exponentials in candidate order, then warp 0 forms the prefix sums
+  // P[i] = e_0 + ... + e_i (32 at a time: a warp scan with a fixed shuffle
+  // pattern plus the total of the chunks before) and applies top-p, min-p
+  // and the draw on them.
+  const float s0 = __fdiv_rn(key_value(static_cast<uint32_t>(top[0] >> 32)), temp);
   for (int i = t; i < kk; i += kThreadsS) {
-    const float si = __fdiv_rn(key_value(static_cast<uint32_t>(sm.cand[i] >> 32)), temp);
+    const float si = __fdiv_rn(key_value(static_cast<uint32_t>(top[i] >> 32)), temp);
     sm.e[i] = expf(__fsub_rn(si, s0));
   }
   __syncthreads();
-  if (t == 0) {
-    float total = 0.f;
-    for (int i = 0; i < kk; ++i) total = __fadd_rn(total, sm.e[i]);
-    int keep = kk;
-    if (prm.top_p < 1.0f) {
-      const float target = __fmul_rn(prm.top_p, total);
-      float cum = 0.f;
-      keep = kk;
-      for (int i = 0; i < kk; ++i) {
-        cum = __fadd_rn(cum, sm.e[i]);
-        if (cum >= target) {
-          keep = i + 1;
-          break;
-        }
-      }
+  if (warp != 0) return;
+  float* P = reinterpret_cast<float*>(sm.comb);  // room for kMaxTopK
+  float carry = 0.f;
+  for (int c0 = 0; c0 < kk; c0 += 32) {
+    const int i = c0 + lane;
+    float v = i < kk ? sm.e[i] : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v = __fadd_rn(v, y);
     }
-    if (prm.min_p > 0.0f) {
-      int n = 0;
-      while (n < keep && sm.e[n] >= prm.min_p) ++n;
-      keep = n > 0 ? n : 1;
-    }
-    float kept = 0.f;
-    for (int i = 0; i < keep; ++i) kept = __fadd_rn(kept, sm.e[i]);
-    const uint64_t st = static_cast<uint64_t>(step[b]);
-    const Philox4 w = philox4x32_10(
-        Philox4{static_cast<uint32_t>(st), static_cast<uint32_t>(st >> 32), 0u, 0u},
-        static_cast<uint32_t>(prm.seed), static_cast<uint32_t>(prm.seed >> 32));
-    const float u = static_cast<float>(w.x >> 8) * (1.0f / 16777216.0f);
-    const float target = __fmul_rn(u, kept);
-    int pick = keep - 1;
-    float cum = 0.f;
-    for (int i = 0; i < keep; ++i) {
-      cum = __fadd_rn(cum, sm.e[i]);
-      if (cum > target) {
-        pick = i;
-        break;
-      }
-    }
-    out[b] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(sm.cand[pick] & 0xFFFFFFFFull));
+    v = __fadd_rn(v, carry);
+    if (i < kk) P[i] = v;
+    carry = __shfl_sync(0xffffffffu, v, 31);
   }
+  __syncwarp();
+  // first i < n with pred(i), else n (warp-uniform)
+  auto first = [&](int n, auto&& pred) {
+    for (int c0 = 0; c0 < n; c0 += 32) {
+      const int i = c0 + lane;
+      const unsigned hit = __ballot_sync(0xffffffffu, i < n && pred(i));
+      if (hit) return c0 + __ffs(hit) - 1;
+    }
+    return n;
+  };
+  const float total = P[kk - 1];
+  int keep = kk;
+  if (prm.top_p < 1.0f) {
+    const float target = __fmul_rn(prm.top_p, total);
+    const int i = first(kk, [&](int j) { return P[j] >= target; });
+    keep = i < kk ? i + 1 : kk;
+  }
+  if (prm.min_p > 0.0f) {
+    const int n = first(keep, [&](int j) { return !(sm.e[j] >= prm.min_p); });
+    keep = n > 0 ? n : 1;
+  }
+  const float kept = P[keep - 1];
+  const uint64_t st = static_cast<uint64_t>(step[b]);
+  const Philox4 w = philox4x32_10(
+      Philox4{static_cast<uint32_t>(st), static_cast<uint32_t>(st >> 32), 0u, 0u},
+      static_cast<uint32_t>(prm.seed), static_cast<uint32_t>(prm.seed >> 32));
+  const float u = static_cast<float>(w.x >> 8) * (1.0f / 16777216.0f);
+  const float target = __fmul_rn(u, kept);
+  int pick = first(keep, [&](int j) { return P[j] > target; });
+  if (pick >= keep) pick = keep - 1;
+  if (lane == 0)
+    out[b] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(top[pick] & 0xFFFFFFFFull));
 }
 
 }  // namespace
@@ -471,15 +621,32 @@ extern "C" kinv_status kinv_sample(const float* logits, int64_t ld, int B, int V
   if (hist_len && (!history || hist_ld <= 0)) return KINV_ERR_INVALID_ARG;
   const size_t smem = sizeof(Smem) + static_cast<size_t>((V + 31) / 32) * 4;
   if (smem > static_cast<size_t>(max_smem_optin())) return KINV_ERR_UNSUPPORTED;
-  static bool configured[64] = {};
+  if (B > 65535) return KINV_ERR_UNSUPPORTED;
+  // Blocks per row: up to eight while the grid stays within one block per
+  // SM.  The token does not depend on this choice (every exchanged quantity
+  // is exact and the candidate set is the same), only the speed does.
+  int C = kMaxCluster;
+  while (C > 1 && static_cast<long long>(B) * C > sm_count()) C >>= 1;
+  const int chunk = ((V + C - 1) / C + 127) / 128 * 128;
+  const bool regs = chunk <= kRegSpan;
+  static bool configured[64][2] = {};
+  static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return KINV_ERR_CUDA;
-  if (dev < 64 && !configured[dev]) {
-    if (cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             max_smem_optin()) != cudaSuccess)
-      return KINV_ERR_CUDA;
-    configured[dev] = true;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return KINV_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!configured[dev][regs]) {
+      if (cudaFuncSetAttribute(regs ? sample_kernel<true> : sample_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin()) != cudaSuccess)
+        return KINV_ERR_CUDA;
+      configured[dev][regs] = true;
+    }
   }
-  return launch_kernel(sample_kernel, dim3(B), dim3(kThreadsS), smem, stream, 1, logits, ld, V, params,
-                       history, hist_ld, hist_len, step, out_tokens, device_status_word());
+  if (regs)
+    return launch_kernel(sample_kernel<true>, dim3(C, B), dim3(kThreadsS), smem, stream,
+                         static_cast<unsigned>(C), logits, ld, V, params, history, hist_ld, hist_len,
+                         step, out_tokens, device_status_word());
+  return launch_kernel(sample_kernel<false>, dim3(C, B), dim3(kThreadsS), smem, stream,
+                       static_cast<unsigned>(C), logits, ld, V, params, history, hist_ld, hist_len, step,
+                       out_tokens, device_status_word());
 }
