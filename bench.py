@@ -236,7 +236,10 @@ def run_kinv(args):
     shape, w, dec, lens0 = build_workload(bmax, per_b * len(sweep) + 8, args.layers, rank, dev,
                                           max_chunk=max(args.prefill_chunks) if args.prefill else 0)
     hbm_peak, tc_peak, peak_kind = _peaks()
-    launches_per_step = 9 * shape.n_layers + 5
+    # the RoPE/append kernel is fused into the QKV projection for batches of
+    # M.FUSED_ROPE_MIN_ROWS .. M.FUSED_ROPE_MAX_ROWS rows
+    fused_rope = M.FUSED_ROPE_MIN_ROWS <= args.batch <= M.FUSED_ROPE_MAX_ROWS
+    launches_per_step = (8 if fused_rope else 9) * shape.n_layers + 5
 
     def barrier():
         if ws > 1:
@@ -326,7 +329,7 @@ def run_kinv(args):
         # (over the step's GEMM launches), while the GEMM sources are unchanged
         traffic = None
         n_launch = sum(kernel_n.get(k, 0) for k in gemm_b)
-        if build.source_hash(["gemm.cu"]) == NCU_GEMM_TRAFFIC["src"] and bsz == NCU_GEMM_TRAFFIC["batch"]:
+        if build.source_hash(["gemm.cu", "rope.cuh"]) == NCU_GEMM_TRAFFIC["src"] and bsz == NCU_GEMM_TRAFFIC["batch"]:
             tb = NCU_GEMM_TRAFFIC["bytes"]
             traffic = round(sum(tb[k] * kernel_n.get(k, 0) for k in tb) / n_launch)
         alg_per_launch = round(gemm_bytes_step / n_launch)

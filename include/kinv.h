@@ -87,6 +87,24 @@ kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int64_t ldw,
                       void* C, int64_t ldc, kinv_dtype c_dtype,
                       int M, int N, int K, kinv_stream stream);
 
+/* QKV projection with kinv_rope_append in the epilogue: the product
+ * qkv = A . W_qkv^T is formed with the same tile, K order and split as
+ * kinv_gemm (N = (Hq + 2 Hkv) D), rounded to bf16 as kinv_gemm would store it,
+ * and then, without going through memory, handled exactly as kinv_rope_append
+ * handles its qkv rows (the same per-head arithmetic): q heads -> q_out, k heads
+ * (RoPE, optional QK-norm) and v heads -> the caches at (seq[m], pos[m]).  The
+ * result is bit-identical to kinv_gemm followed by kinv_rope_append
+ * ("Deterministic and bit-exact inference", *technical*: the matmul is one of
+ * the batch-invariant kernels; RoPE and the append reduce nothing across rows).
+ * A bf16 [M][K] (lda), W_qkv bf16 [N][K] (ldw); q_out bf16 [M][Hq][D]; caches,
+ * strides, seq, pos, norms, eps and rope_base as in kinv_rope_append.
+ * Requirements: D in {64, 128}, N % 128 == 0, K % 64 == 0, 16-byte alignment. */
+kinv_status kinv_gemm_qkv_rope(const void* A, int64_t lda, const void* W_qkv, int64_t ldw,
+                               void* q_out, void* k_cache, void* v_cache, int64_t seq_stride,
+                               int64_t tok_stride, const int32_t* seq, const int32_t* pos,
+                               const void* q_norm, const void* k_norm, float eps, int M, int Hq,
+                               int Hkv, int D, int K, float rope_base, kinv_stream stream);
+
 /* Gate/up projection with the SwiGLU applied in the epilogue:
  *   act[m][f] = bf16(silu(g) * u),  silu(g) = g / (1 + e^-g),
  *   g = A[m] . Wgate[f],  u = A[m] . Wup[f]  (fp32 accumulators, never rounded)

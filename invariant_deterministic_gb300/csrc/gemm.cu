@@ -31,9 +31,11 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "common.cuh"
+#include "rope.cuh"
 
 namespace kinv {
 namespace {
@@ -42,6 +44,7 @@ constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle row of bf16
 constexpr int kGemmThreads = 128;
 constexpr int A_STAGE = BM * BK * 2;
+constexpr int kRopeTabRows = 4;  // owned rows up to which the RoPE angles are formed ahead
 
 // tcgen05 instruction descriptor, kind::f16: fp32 accumulate (bits 4-5 = 1),
 // A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major, N >> 3 at bits
@@ -63,6 +66,24 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
 
 __device__ __forceinline__ float silu_times(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
+// The QKV projection's epilogue: the bf16 result rows (as a plain store would
+// round them) go through RoPE with the optional QK-norm (the same per-head
+// arithmetic as kinv_rope_append) straight into q and the KV cache.
+struct RopeEpilogue {
+  int on;
+  int D, Hq, Hkv;
+  __nv_bfloat16* q_out;  // [M][Hq][D]
+  __nv_bfloat16* k_cache;
+  __nv_bfloat16* v_cache;
+  int64_t seq_stride, tok_stride;
+  const int32_t* seq;
+  const int32_t* pos;
+  const __nv_bfloat16* q_norm;
+  const __nv_bfloat16* k_norm;
+  float eps;
+  RopeFreqs freqs;
+};
+
 struct GemmArgs {
   void* C;
   int64_t ldc;
@@ -76,8 +97,80 @@ struct GemmArgs {
   int stages;
   int splits;
   int own_rows;  // split-K: rows a rank owns at most (ceil(a_rows / splits))
+  int ring_bytes;  // the stage ring, or more when the epilogue's receive slots need it
   int* status;
+  RopeEpilogue rope;
 };
+
+// Rows [0, n) of a staged tile (bf16, row stride BN) are rows row_of(r) of the
+// QKV projection; each warp takes (row, head) items of the tile.
+// What the RoPE epilogue needs besides the staged rows, gathered ahead of the
+// epilogue into shared memory (decode: few owned rows): each row's position
+// and sequence, the cos and sin of its angles, and the norm gains of the
+// tile's heads.
+struct RopePre {
+  int* pos;             // [n]
+  int* seq;             // [n]
+  float* cs;            // [n][D/2][2]
+  __nv_bfloat16* nw;    // [BN / D][D]: the gains of the tile's q/k heads
+};
+
+// `pre` (nullable): RopePre for the staged rows; otherwise everything is read
+// or formed here.
+template <int D, int BN, typename RowOf>
+__device__ __forceinline__ void rope_rows(const __nv_bfloat16* stage, const RopePre* pre, int n,
+                                          int n0, int M, const RopeEpilogue& e, RowOf row_of) {
+  constexpr int HALF = D / 2;
+  constexpr int P = D / 64;
+  constexpr int HPT = BN / D;  // heads per tile
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int idx = warp; idx < n * HPT; idx += kGemmThreads / 32) {
+    const int r = idx / HPT, j = idx % HPT;
+    const int m = row_of(r);
+    if (m >= M) continue;
+    const int h = n0 / D + j;
+    const int p = pre ? pre->pos[r] : e.pos[m];
+    const int sq = pre ? pre->seq[r] : e.seq[m];
+    const int64_t tok = static_cast<int64_t>(sq) * e.seq_stride + static_cast<int64_t>(p) * e.tok_stride;
+    const __nv_bfloat16* src = stage + r * BN + j * D;
+    if (h >= e.Hq + e.Hkv) {  // value head: the bits as stored
+      __nv_bfloat16* dst = e.v_cache + tok + (h - e.Hq - e.Hkv) * D;
+      for (int c = lane; c < D / 8; c += 32)
+        reinterpret_cast<uint4*>(dst)[c] = reinterpret_cast<const uint4*>(src)[c];
+      continue;
+    }
+    float a[P], b[P], c[P], sn[P];
+#pragma unroll
+    for (int q = 0; q < P; ++q) {
+      a[q] = __bfloat162float(src[lane * P + q]);
+      b[q] = __bfloat162float(src[HALF + lane * P + q]);
+      if (pre) {
+        c[q] = pre->cs[(r * HALF + lane * P + q) * 2];
+        sn[q] = pre->cs[(r * HALF + lane * P + q) * 2 + 1];
+      } else {
+        rope_angle(p, e.freqs.inv_freq[lane * P + q], c[q], sn[q]);
+      }
+    }
+    const __nv_bfloat16* g = h < e.Hq ? e.q_norm : e.k_norm;
+    if (g && pre) g = pre->nw + j * D;
+    __nv_bfloat16* dst = h < e.Hq ? e.q_out + (static_cast<int64_t>(m) * e.Hq + h) * D
+                                  : e.k_cache + tok + (h - e.Hq) * D;
+    rope_norm_rotate<D>(a, b, c, sn, g, e.eps, lane, dst);
+  }
+}
+
+// Head size dispatch (a tile holds whole heads: the plan's tiles are 128 wide).
+template <int BN, typename RowOf>
+__device__ __forceinline__ void rope_dispatch(const __nv_bfloat16* stage, const RopePre* pre, int n,
+                                              int n0, int M, const RopeEpilogue& e, RowOf row_of) {
+  if constexpr (BN % 128 == 0) {
+    if (e.D == 128) {
+      rope_rows<128, BN>(stage, pre, n, n0, M, e, row_of);
+      return;
+    }
+  }
+  if constexpr (BN % 64 == 0) rope_rows<64, BN>(stage, pre, n, n0, M, e, row_of);
+}
 
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -103,9 +196,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // split-K partials received from every rank, [splits][own_rows][BN] fp32,
   // over the stage ring (idle by then in every rank of the cluster)
   float* recv = reinterpret_cast<float*>(base);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(w_st + stages * W_STAGE);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + args.ring_bytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // split-K RoPE epilogue with few owned rows (decode): what it needs is
+  // gathered by the otherwise idle warps 2 and 3 while the weights stream
+  const bool use_pre = args.rope.on && args.splits > 1 && args.own_rows <= kRopeTabRows;
+  RopePre pre{};
+  if (use_pre) {
+    pre.pos = reinterpret_cast<int*>(tmem_slot + 4);
+    pre.seq = pre.pos + args.own_rows;
+    pre.cs = reinterpret_cast<float*>(pre.seq + args.own_rows);
+    pre.nw = reinterpret_cast<__nv_bfloat16*>(pre.cs + args.own_rows * args.rope.D);
+  }
   auto full_bar = [&](int s) { return smem_addr(bars + s); };
   auto empty_bar = [&](int s) { return smem_addr(bars + stages + s); };
   const uint32_t done_bar = smem_addr(bars + 2 * stages);
@@ -207,6 +310,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   }
 
+  if (use_pre && warp >= 2) {
+    const RopeEpilogue& e = args.rope;
+    const int t2 = threadIdx.x - 64;
+    // the gains of the tile's q and k heads (weights: no dependency wait)
+    for (int idx = t2; idx < BN; idx += 64) {
+      const int h = n0 / e.D + idx / e.D;
+      const __nv_bfloat16* g = h < e.Hq ? e.q_norm : (h < e.Hq + e.Hkv ? e.k_norm : nullptr);
+      pre.nw[idx] = g ? g[idx % e.D] : __float2bfloat16_rn(0.f);
+    }
+    pdl_wait();  // positions are written by earlier kernels
+    const int half = e.D / 2;
+    const int owned = rank < rows_here ? (rows_here - rank + splits - 1) / splits : 0;
+    for (int i = t2; i < owned; i += 64) {
+      pre.pos[i] = e.pos[m0 + i * splits + rank];
+      pre.seq[i] = e.seq[m0 + i * splits + rank];
+    }
+    for (int idx = t2; idx < owned * half; idx += 64) {
+      const int i = idx / half, jj = idx % half;
+      rope_angle(e.pos[m0 + i * splits + rank], e.freqs.inv_freq[jj], pre.cs[idx * 2], pre.cs[idx * 2 + 1]);
+    }
+  }
+
   // ---- epilogue
   const bool ok = mbar_wait_bounded(done_bar, 0, args.status, DEV_TIMEOUT_GEMM_EPILOGUE);
   __syncwarp();
@@ -243,12 +368,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (splits == 1) {
+    __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(base);  // rope: the ring is idle now
     if (good) {
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(lane_base + c0, r);
-        if (m < args.M) {
+        if (args.rope.on) {
+          if (m < args.M) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              uint4 o;
+              o.x = pack_bf16(__uint_as_float(r[j + 0]), __uint_as_float(r[j + 1]));
+              o.y = pack_bf16(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+              o.z = pack_bf16(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5]));
+              o.w = pack_bf16(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7]));
+              *reinterpret_cast<uint4*>(stage + row_local * BN + c0 + j) = o;
+            }
+          }
+        } else if (m < args.M) {
           if (args.c_f32) {
             float* crow = static_cast<float*>(args.C) + m * args.ldc + n0 + c0;
 #pragma unroll
@@ -271,6 +409,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
+      }
+    }
+    if (args.rope.on) {
+      __syncthreads();
+      if (good) {
+        auto row_of = [&](int r) { return m0 + r; };
+        rope_dispatch<BN>(stage, nullptr, rows_here, n0, args.M, args.rope, row_of);
       }
     }
   } else {
@@ -304,7 +449,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     __syncthreads();  // this rank's own rows are in place
     const int owned = rank < rows_here ? (rows_here - rank + splits - 1) / splits : 0;
-    const bool got = mbar_wait_bounded(recv_bar, 0, args.status, DEV_TIMEOUT_GEMM_EPILOGUE);
+    const bool got =
+        __syncthreads_and(mbar_wait_bounded(recv_bar, 0, args.status, DEV_TIMEOUT_GEMM_EPILOGUE));
     if (good && got) {
       const int slot = own_rows * BN;
       if (args.swiglu) {
@@ -322,6 +468,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               __float2bfloat16_rn(silu_times(g, u));
         }
       } else {
+        // rope: the owned rows are staged after the receive slots
+        __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(recv + splits * slot);
         for (int idx = threadIdx.x; idx < owned * BN; idx += kGemmThreads) {
           const int i = idx / BN, col = idx % BN;
           const int nn = n0 + col;
@@ -330,10 +478,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           float acc = src[0];
           for (int q = 1; q < splits; ++q) acc = __fadd_rn(acc, src[q * slot]);
           const int mm = m0 + i * splits + rank;
-          if (args.c_f32)
+          if (args.rope.on)
+            stage[i * BN + col] = __float2bfloat16_rn(acc);
+          else if (args.c_f32)
             static_cast<float*>(args.C)[mm * args.ldc + nn] = acc;
           else
             static_cast<__nv_bfloat16*>(args.C)[mm * args.ldc + nn] = __float2bfloat16_rn(acc);
+        }
+        if (args.rope.on) {
+          __syncthreads();
+          auto row_of = [&](int r) { return m0 + r * splits + rank; };
+          rope_dispatch<BN>(stage, use_pre ? &pre : nullptr, owned, n0, args.M, args.rope, row_of);
         }
       }
     }
@@ -419,8 +574,8 @@ int ring_cap(long long ctas) {
   return static_cast<int>(smem_per_sm() / per_sm) - smem_reserved_per_block() - 1024 - 256;
 }
 
-size_t smem_bytes(int stages, int stage_bytes) {
-  return 1024 + static_cast<size_t>(stages) * stage_bytes + (2 * stages + 2) * 8 + 16;
+size_t smem_bytes(int stages, int ring_bytes, int tab_bytes) {
+  return 1024 + static_cast<size_t>(ring_bytes) + (2 * stages + 2) * 8 + 16 + tab_bytes;
 }
 
 template <int BN>
@@ -433,17 +588,23 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a
   // it), and the 128 rows one MMA reads from the start of the last A block
   // must stay inside the block's shared memory.
   a.own_rows = (a.a_rows + a.splits - 1) / a.splits;
-  const int recv_bytes = a.splits > 1 ? a.splits * a.own_rows * BN * 4 : 0;
+  // split-K receive slots, plus the staged bf16 rows of the RoPE epilogue
+  const int recv_bytes = a.splits > 1 ? a.splits * a.own_rows * BN * 4 +
+                                            (a.rope.on ? a.own_rows * BN * 2 : 0)
+                                      : (a.rope.on ? a.a_rows * BN * 2 : 0);
   const int cap = ring_cap(static_cast<long long>(a.splits) * grid_y * grid_z);
   const int limit = budget < cap ? budget : cap;
   const int stage = a.a_blk * a.j + BN * BK * 2 * a.j;
   int stages = limit / stage;
   stages = stages < 2 ? 2 : (stages > 8 ? 8 : stages);
-  while (static_cast<long long>(stages) * stage < recv_bytes ||
-         (stages - 1) * a.a_blk * a.j + (a.j - 1) * a.a_blk + A_STAGE > stages * stage)
-    ++stages;
+  while ((stages - 1) * a.a_blk * a.j + (a.j - 1) * a.a_blk + A_STAGE > stages * stage) ++stages;
   a.stages = stages;
-  const size_t smem = smem_bytes(stages, stage);
+  // the epilogue's receive slots reuse the ring and may run past it
+  a.ring_bytes = stages * stage > recv_bytes ? stages * stage : (recv_bytes + 15) / 16 * 16;
+  const int tab_bytes = a.rope.on && a.splits > 1 && a.own_rows <= kRopeTabRows
+                              ? a.own_rows * (8 + (a.rope.D / 2) * 8) + BN * 2
+                              : 0;
+  const size_t smem = smem_bytes(stages, a.ring_bytes, tab_bytes);
   if (smem > static_cast<size_t>(max_smem_optin())) return KINV_ERR_UNSUPPORTED;
   // the opt-in limit is raised once per device to the largest request seen
   static size_t configured[64] = {};
@@ -471,15 +632,17 @@ using namespace kinv;
 namespace kinv {
 namespace {
 kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, void* C, int64_t ldc,
-                      kinv_dtype c_dtype, int M, int N, int K, bool swiglu, cudaStream_t stream) {
+                      kinv_dtype c_dtype, int M, int N, int K, bool swiglu, const RopeEpilogue* rope,
+                      cudaStream_t stream) {
   if (M < 0 || N <= 0 || K <= 0) return KINV_ERR_INVALID_ARG;
   if (c_dtype != KINV_BF16 && c_dtype != KINV_F32) return KINV_ERR_INVALID_ARG;
   if (M == 0) return KINV_OK;
-  if (!A || !W || !C) return KINV_ERR_INVALID_ARG;
-  if (K % BK || N % 16 || (swiglu && (N % 128 || c_dtype != KINV_BF16))) return KINV_ERR_UNSUPPORTED;
-  if (lda < K || ldw < K || ldc < (swiglu ? N / 2 : N)) return KINV_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(W) || !aligned16(C) || lda % 8 || ldw % 8 ||
-      (c_dtype == KINV_BF16 ? ldc % 8 : ldc % 4))
+  if (!A || !W || (!C && !rope)) return KINV_ERR_INVALID_ARG;
+  if (K % BK || N % 16 || ((swiglu || rope) && (N % 128 || c_dtype != KINV_BF16)))
+    return KINV_ERR_UNSUPPORTED;
+  if (lda < K || ldw < K || (!rope && ldc < (swiglu ? N / 2 : N))) return KINV_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W) || (!rope && !aligned16(C)) || lda % 8 || ldw % 8 ||
+      (!rope && (c_dtype == KINV_BF16 ? ldc % 8 : ldc % 4)))
     return KINV_ERR_ALIGNMENT;
   const Plan p = plan_for(N, K);  // 128-wide tiles: 64 gate and the matching 64 up columns
   const int grid_y = (M + BM - 1) / BM;
@@ -511,7 +674,10 @@ kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, vo
   a.stages = 0;
   a.splits = p.splits;
   a.own_rows = 0;
+  a.ring_bytes = 0;
   a.status = device_status_word();
+  a.rope = rope ? *rope : RopeEpilogue{};
+  a.rope.on = rope ? 1 : 0;
   switch (p.bn) {
     case 64: return launch_gemm<64>(ta, tw, a, p.smem_budget, grid_y, grid_z, stream);
     case 128: return launch_gemm<128>(ta, tw, a, p.smem_budget, grid_y, grid_z, stream);
@@ -524,12 +690,47 @@ kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, vo
 extern "C" kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int64_t ldw, void* C,
                                  int64_t ldc, kinv_dtype c_dtype, int M, int N, int K,
                                  kinv_stream stream) {
-  return kinv::gemm_impl(A, lda, W, ldw, C, ldc, c_dtype, M, N, K, false, stream);
+  return kinv::gemm_impl(A, lda, W, ldw, C, ldc, c_dtype, M, N, K, false, nullptr, stream);
 }
 
 extern "C" kinv_status kinv_gemm_swiglu(const void* A, int64_t lda, const void* W_gu, int64_t ldw,
                                         void* act, int64_t ld_act, int M, int F, int K,
                                         kinv_stream stream) {
   if (F <= 0 || F % 64) return F <= 0 ? KINV_ERR_INVALID_ARG : KINV_ERR_UNSUPPORTED;
-  return kinv::gemm_impl(A, lda, W_gu, ldw, act, ld_act, KINV_BF16, M, 2 * F, K, true, stream);
+  return kinv::gemm_impl(A, lda, W_gu, ldw, act, ld_act, KINV_BF16, M, 2 * F, K, true, nullptr, stream);
+}
+
+extern "C" kinv_status kinv_gemm_qkv_rope(const void* A, int64_t lda, const void* W_qkv, int64_t ldw,
+                                          void* q_out, void* k_cache, void* v_cache,
+                                          int64_t seq_stride, int64_t tok_stride, const int32_t* seq,
+                                          const int32_t* pos, const void* q_norm, const void* k_norm,
+                                          float eps, int M, int Hq, int Hkv, int D, int K,
+                                          float rope_base, kinv_stream stream) {
+  if (M < 0 || Hq <= 0 || Hkv <= 0 || K <= 0 || !(rope_base > 0.f) || !(eps >= 0.f))
+    return KINV_ERR_INVALID_ARG;
+  if (M == 0) return KINV_OK;
+  if (!q_out || !k_cache || !v_cache || !seq || !pos) return KINV_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return KINV_ERR_UNSUPPORTED;
+  if (tok_stride < static_cast<int64_t>(Hkv) * D || seq_stride < 0) return KINV_ERR_INVALID_ARG;
+  if (!aligned16(q_out) || !aligned16(k_cache) || !aligned16(v_cache) || seq_stride % 8 ||
+      tok_stride % 8)
+    return KINV_ERR_ALIGNMENT;
+  kinv::RopeEpilogue e{};
+  e.D = D;
+  e.Hq = Hq;
+  e.Hkv = Hkv;
+  e.q_out = static_cast<__nv_bfloat16*>(q_out);
+  e.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+  e.v_cache = static_cast<__nv_bfloat16*>(v_cache);
+  e.seq_stride = seq_stride;
+  e.tok_stride = tok_stride;
+  e.seq = seq;
+  e.pos = pos;
+  e.q_norm = static_cast<const __nv_bfloat16*>(q_norm);
+  e.k_norm = static_cast<const __nv_bfloat16*>(k_norm);
+  e.eps = eps;
+  for (int i = 0; i < D / 2; ++i)
+    e.freqs.inv_freq[i] = std::pow(static_cast<double>(rope_base), -2.0 * i / D);
+  const int N = (Hq + 2 * Hkv) * D;
+  return kinv::gemm_impl(A, lda, W_qkv, ldw, nullptr, N, KINV_BF16, M, N, K, false, &e, stream);
 }

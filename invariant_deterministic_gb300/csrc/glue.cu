@@ -8,6 +8,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "rope.cuh"
 
 namespace kinv {
 namespace {
@@ -62,10 +63,6 @@ __global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ gu, int64_t ld_g
 }
 
 // Inverse frequencies base^(-2i/D), formed once per call on the host in fp64.
-struct RopeFreqs {
-  double inv_freq[64];
-};
-
 // One block per row.  The first D/2 threads compute this row's rotation
 // angles in fp64 (theta_i = p * inv_freq_i, then sin and cos) into shared
 // memory; then each warp takes one head (grid.y picks eight of the row's
@@ -89,18 +86,7 @@ __global__ void rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int64_
   const int r = blockIdx.x;
   const int p = pos[r];
   const int s = seq[r];
-  for (int i = threadIdx.x; i < HALF; i += blockDim.x) {
-    // theta in fp64, reduced to [-pi, pi] in fp64 (2 pi split into a head
-    // and a tail), then sin and cos of the reduced angle in fp32
-    const double theta = static_cast<double>(p) * freqs.inv_freq[i];
-    const double k = rint(theta * 0.15915494309189535);  // 1 / (2 pi)
-    double red = fma(-k, 6.283185307179586, theta);
-    red = fma(-k, 2.4492935982947064e-16, red);
-    float sv, cv;
-    sincosf(static_cast<float>(red), &sv, &cv);
-    cs[i] = cv;
-    sn[i] = sv;
-  }
+  for (int i = threadIdx.x; i < HALF; i += blockDim.x) rope_angle(p, freqs.inv_freq[i], cs[i], sn[i]);
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -118,38 +104,17 @@ __global__ void rope_append_kernel(const __nv_bfloat16* __restrict__ qkv, int64_
         reinterpret_cast<uint4*>(vdst_row + g * D)[c] = reinterpret_cast<const uint4*>(src)[c];
       continue;
     }
-    float a[P], b[P];
+    float a[P], b[P], c[P], sv[P];
 #pragma unroll
     for (int j = 0; j < P; ++j) {
       a[j] = __bfloat162float(src[lane * P + j]);
       b[j] = __bfloat162float(src[HALF + lane * P + j]);
-    }
-    const __nv_bfloat16* nw = h < Hq ? q_norm : k_norm;
-    if (nw) {
-      float acc = 0.f;
-#pragma unroll
-      for (int j = 0; j < P; ++j) acc = fmaf(a[j], a[j], acc);
-#pragma unroll
-      for (int j = 0; j < P; ++j) acc = fmaf(b[j], b[j], acc);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      acc = __shfl_sync(0xffffffffu, acc, 0);
-      const float inv = 1.0f / sqrtf(acc / static_cast<float>(D) + eps);
-#pragma unroll
-      for (int j = 0; j < P; ++j) {
-        a[j] = a[j] * inv * __bfloat162float(nw[lane * P + j]);
-        b[j] = b[j] * inv * __bfloat162float(nw[HALF + lane * P + j]);
-      }
+      c[j] = cs[lane * P + j];
+      sv[j] = sn[lane * P + j];
     }
     __nv_bfloat16* dst = h < Hq ? q_out + (static_cast<int64_t>(r) * Hq + h) * D
                                 : kdst_row + (h - Hq) * D;
-#pragma unroll
-    for (int j = 0; j < P; ++j) {
-      const int i = lane * P + j;
-      const float c = cs[i], sv = sn[i];
-      dst[i] = __float2bfloat16_rn(a[j] * c - b[j] * sv);
-      dst[HALF + i] = __float2bfloat16_rn(b[j] * c + a[j] * sv);
-    }
+    rope_norm_rotate<D>(a, b, c, sv, h < Hq ? q_norm : k_norm, eps, lane, dst);
   }
 }
 

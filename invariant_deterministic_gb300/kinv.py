@@ -40,6 +40,8 @@ SIGNATURES = {
     "kinv_last_device_status": (_i32, [_c_p]),
     "kinv_gemm": (_i32, [_c_p, _i64, _c_p, _i64, _c_p, _i64, _i32, _i32, _i32, _i32, _c_p]),
     "kinv_gemm_swiglu": (_i32, [_c_p, _i64, _c_p, _i64, _c_p, _i64, _i32, _i32, _i32, _c_p]),
+    "kinv_gemm_qkv_rope": (_i32, [_c_p, _i64, _c_p, _i64, _c_p, _c_p, _c_p, _i64, _i64, _c_p, _c_p,
+                                  _c_p, _c_p, _f32, _i32, _i32, _i32, _i32, _i32, _f32, _c_p]),
     "kinv_rmsnorm": (_i32, [_c_p, _i64, _c_p, _c_p, _c_p, _i64, _i32, _i32, _f32, _c_p]),
     "kinv_attn_decode_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "kinv_attn_decode": (_i32, [_c_p, _c_p, _c_p, _i64, _i64, _c_p, _c_p, _i32, _i32, _i32, _i32,
@@ -161,6 +163,22 @@ def gemm_swiglu(a: torch.Tensor, w_gu_il: torch.Tensor, out: torch.Tensor | None
     _check(lib().kinv_gemm_swiglu(_ptr(a), a.stride(0), _ptr(w_gu_il), w_gu_il.stride(0), _ptr(out),
                                   out.stride(0), m, f, k, _stream(stream)), "kinv_gemm_swiglu")
     return out
+
+
+def gemm_qkv_rope(a, w_qkv, q_out, k_cache, v_cache, seq, pos, n_q, n_kv, head_dim, rope_base,
+                  q_norm=None, k_norm=None, eps=1e-6, stream=None):
+    """kinv_gemm followed by kinv_rope_append in one kernel: q heads of
+    a . w_qkv^T -> q_out [M][Hq][D]; k and v heads into the caches
+    [B][Lmax][Hkv][D] at [seq][pos]."""
+    _need(a, torch.bfloat16, "a")
+    _need(w_qkv, torch.bfloat16, "w_qkv")
+    m, k = a.shape
+    _check(lib().kinv_gemm_qkv_rope(_ptr(a), a.stride(0), _ptr(w_qkv), w_qkv.stride(0), _ptr(q_out),
+                                    _ptr(k_cache), _ptr(v_cache), k_cache.stride(0), k_cache.stride(1),
+                                    _ptr(seq), _ptr(pos), _ptr(q_norm), _ptr(k_norm),
+                                    float(eps), m, n_q, n_kv, head_dim, k, float(rope_base), _stream(stream)),
+           "kinv_gemm_qkv_rope")
+    return q_out
 
 
 # ------------------------------------------------------------------ RMSNorm

@@ -65,6 +65,14 @@ def random_weights(shape: ModelShape, seed: int = synth.SEED_WEIGHTS, device="cu
     return w
 
 
+# From 2 to this many rows the QKV projection runs with RoPE and the KV append
+# in its epilogue (kinv_gemm_qkv_rope); otherwise kinv_gemm then
+# kinv_rope_append (measured faster at one row and at many).  Both give the
+# same bits, so the choice never changes a result.
+FUSED_ROPE_MIN_ROWS = 2
+FUSED_ROPE_MAX_ROWS = 32
+
+
 class Decoder:
     """Owns weights, the KV cache and every activation buffer for up to
     ``max_batch`` sequences of up to ``max_len`` tokens (and prefill chunks of
@@ -138,18 +146,31 @@ class Decoder:
             self.hist_len[b] = len(tail)
 
     # --------------------------------------------------------------- a layer
-    def layer(self, li: int, rows: int, first: bool, attention) -> None:
-        """One decoder layer on rows [0, rows) of the activation buffers.
-        ``x`` holds the residual stream and ``delta`` the previous layer's
-        FFN output (not yet added unless ``first``)."""
+    def layer(self, li: int, rows: int, first: bool, seq, pos, attention) -> None:
+        """One decoder layer on rows [0, rows) of the activation buffers; row
+        r is sequence seq[r] at position pos[r].  ``x`` holds the residual
+        stream and ``delta`` the previous layer's FFN output (not yet added
+        unless ``first``)."""
         s, lw = self.s, self.w["layers"][li]
         x, h = self.x[:rows], self.h[:rows]
         with self._t("rmsnorm"):
             kinv.rmsnorm(x, lw["attn_norm"], s.eps, residual=None if first else self.delta[:rows],
                          out=h)
-        with self._t("gemm_qkv"):
-            kinv.gemm(h, lw["w_qkv"], out=self.qkv[:rows])
         kc, vc = self.kv[li, 0], self.kv[li, 1]
+        qn = lw.get("q_norm") if s.qk_norm else None
+        kn = lw.get("k_norm") if s.qk_norm else None
+        if FUSED_ROPE_MIN_ROWS <= rows <= FUSED_ROPE_MAX_ROWS:
+            # the QKV projection with RoPE and the KV append in its epilogue
+            with self._t("gemm_qkv"):
+                kinv.gemm_qkv_rope(h, lw["w_qkv"], self.q[:rows], kc, vc, seq, pos, s.n_q, s.n_kv,
+                                   s.head_dim, s.rope_base, qn, kn, s.eps)
+        else:
+            # the same bits in two kernels (faster when many rows share a tile)
+            with self._t("gemm_qkv"):
+                kinv.gemm(h, lw["w_qkv"], out=self.qkv[:rows])
+            with self._t("rope_append"):
+                kinv.rope_append(self.qkv[:rows], self.q[:rows], kc, vc, seq, pos, s.n_q, s.n_kv,
+                                 s.head_dim, s.rope_base, qn, kn, s.eps)
         attention(li, rows, kc, vc)
         with self._t("gemm_o"):
             kinv.gemm(self.attn[:rows].view(rows, -1), lw["w_o"], out=self.o[:rows])
@@ -160,25 +181,17 @@ class Decoder:
         with self._t("gemm_down"):
             kinv.gemm(self.act[:rows], lw["w_down"], out=self.delta[:rows])
 
-    def _rope(self, li, rows, kc, vc, seq, pos):
-        s, lw = self.s, self.w["layers"][li]
-        kinv.rope_append(self.qkv[:rows], self.q[:rows], kc, vc, seq, pos, s.n_q, s.n_kv,
-                         s.head_dim, s.rope_base, lw.get("q_norm") if s.qk_norm else None,
-                         lw.get("k_norm") if s.qk_norm else None, s.eps)
-
     # ---------------------------------------------------------------- decode
     def decode_layers(self, bsz: int) -> None:
         """All layers for one new token of sequences 0..bsz-1 (rows = bsz);
         the token's hidden state must be in x; leaves the final residual
         pieces in x and delta."""
         def attention(li, rows, kc, vc):
-            with self._t("rope_append"):
-                self._rope(li, rows, kc, vc, self.seq[:rows], self.pos[:rows])
             with self._t("attn_decode"):
                 kinv.attn_decode(self.q[:rows], kc[:rows], vc[:rows], self.kv_len[:rows],
                                  out=self.attn[:rows], workspace=self.ws)
         for li in range(self.s.n_layers):
-            self.layer(li, bsz, li == 0, attention)
+            self.layer(li, bsz, li == 0, self.seq[:bsz], self.pos[:bsz], attention)
 
     def decode_step(self, bsz: int, sample: bool = True) -> None:
         """Embed tokens[:bsz], run every layer, the final norm, the LM head
@@ -213,12 +226,11 @@ class Decoder:
         q_off = torch.zeros(1, **i32)
 
         def attention(li, n, kc, vc):
-            self._rope(li, n, kc, vc, seq_t, pos_t)
             # a one-sequence view of the cache keeps the sequence index at 0
             kinv.attn_prefill(self.q[:n], kc[seq: seq + 1], vc[seq: seq + 1], q_start, q_len,
                               q_off, n, p0 + n, out=self.attn[:n], workspace=self.ws)
         for li in range(self.s.n_layers):
-            self.layer(li, rows, li == 0, attention)
+            self.layer(li, rows, li == 0, seq_t, pos_t, attention)
 
     def close_residual(self, rows: int) -> torch.Tensor:
         """x <- bf16(x + delta) for rows [0, rows): the last layer's output."""

@@ -105,3 +105,33 @@ def test_decode_advance(kinv):
     assert hist.cpu().tolist() == [[9, 0, 0, 0], [2, 3, 4, 8]]
     assert hl.cpu().tolist() == [1, 4] and step.cpu().tolist() == [1, 11]
     assert pos.cpu().tolist() == [6, 7] and kvl.cpu().tolist() == [7, 8]
+
+
+@pytest.mark.parametrize("d,hq,hkv,base,qk,k,m", [(64, 4, 2, 1e4, False, 256, 5), (128, 32, 8, 1e6, True, 4096, 1),
+                                                  (128, 32, 8, 1e6, True, 4096, 16),
+                                                  (128, 32, 8, 1e6, True, 4096, 200)])
+def test_gemm_qkv_rope_equals_gemm_then_rope_append(kinv, d, hq, hkv, base, qk, k, m):
+    """The fused projection writes the same bits as kinv_gemm followed by
+    kinv_rope_append: q, the new K/V cache slots, and nothing else."""
+    n = (hq + 2 * hkv) * d
+    a = synth.normal_bf16((m, k), 1.0, 30).cuda()
+    w = synth.normal_bf16((n, k), 0.02, 31).cuda()
+    bsz, lmax = 4, 300
+    seq = torch.arange(m, dtype=torch.int32) % bsz  # distinct (seq, pos) slots per row
+    pos = torch.arange(m, dtype=torch.int32) // bsz + 7
+    qn = (synth.normal_bf16((d,), 0.3, 32) + 1).cuda() if qk else None
+    kn = (synth.normal_bf16((d,), 0.3, 33) + 1).cuda() if qk else None
+    outs = []
+    for fused in (False, True):
+        kc = torch.zeros(bsz, lmax, hkv, d, dtype=torch.bfloat16, device="cuda")
+        vc = torch.zeros_like(kc)
+        q = torch.zeros(m, hq, d, dtype=torch.bfloat16, device="cuda")
+        if fused:
+            kinv.gemm_qkv_rope(a, w, q, kc, vc, seq.cuda(), pos.cuda(), hq, hkv, d, base, qn, kn, 1e-6)
+        else:
+            qkv = kinv.gemm(a, w)
+            kinv.rope_append(qkv, q, kc, vc, seq.cuda(), pos.cuda(), hq, hkv, d, base, qn, kn, 1e-6)
+        outs.append((q, kc, vc))
+    for x, y, name in zip(outs[0], outs[1], ("q", "k cache", "v cache")):
+        assert_same_bits(y, x, f"fused {name}")
+    assert kinv.last_device_status() == 0
