@@ -236,10 +236,11 @@ def run_kinv(args):
     shape, w, dec, lens0 = build_workload(bmax, per_b * len(sweep) + 8, args.layers, rank, dev,
                                           max_chunk=max(args.prefill_chunks) if args.prefill else 0)
     hbm_peak, tc_peak, peak_kind = _peaks()
-    # the RoPE/append kernel is fused into the QKV projection for batches of
-    # M.FUSED_ROPE_MIN_ROWS .. M.FUSED_ROPE_MAX_ROWS rows
+    # per layer: QKV (+ RoPE/append for M.FUSED_ROPE_MIN_ROWS .. MAX rows, else
+    # a separate RoPE/append kernel), attention split + merge, O, gate/up, down;
+    # per step: embed, row sums of squares, LM head, sampler, position update
     fused_rope = M.FUSED_ROPE_MIN_ROWS <= args.batch <= M.FUSED_ROPE_MAX_ROWS
-    launches_per_step = (8 if fused_rope else 9) * shape.n_layers + 5
+    launches_per_step = (6 if fused_rope else 7) * shape.n_layers + 5
 
     def barrier():
         if ws > 1:
@@ -309,9 +310,14 @@ def run_kinv(args):
     gemm_shapes = {"gemm_qkv": (shape.qkv_dim, d), "gemm_o": (d, shape.n_q * shape.head_dim),
                    "gemm_gate_up": (2 * f, d), "gemm_down": (d, f)}
     gemm_b = {k: gemm_bytes(bsz, n, kk) for k, (n, kk) in gemm_shapes.items()}
+    ss_b = bsz * (d // 128) * 4  # per-row partial sums of squares (folded RMSNorm)
     # the gate/up GEMM writes silu(g) * u: F columns, not 2F
-    gemm_b["gemm_gate_up"] = (bsz * d + 2 * f * d) * 2 + bsz * f * 2
-    gemm_b["gemm_lm_head"] = gemm_bytes(bsz, shape.vocab, d, 4)
+    gemm_b["gemm_gate_up"] = (bsz * d + 2 * f * d) * 2 + bsz * f * 2 + ss_b
+    gemm_b["gemm_qkv"] += ss_b
+    # O and down add into the residual stream: read and write it, write the sums
+    for k in ("gemm_o", "gemm_down"):
+        gemm_b[k] += bsz * d * 2 + ss_b
+    gemm_b["gemm_lm_head"] = gemm_bytes(bsz, shape.vocab, d, 4) + ss_b
     lens_now = dec.pos[:bsz].cpu().tolist()
     attn_b = sum(l * shape.n_kv * shape.head_dim * 4 for l in lens_now) + 2 * bsz * shape.n_q * shape.head_dim * 2
     # the GEMM kernel is one kernel (gemm_kernel) across the five projections

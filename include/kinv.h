@@ -87,6 +87,45 @@ kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int64_t ldw,
                       void* C, int64_t ldc, kinv_dtype c_dtype,
                       int M, int N, int K, kinv_stream stream);
 
+/* RMSNorm folded into the projections around it ("Deterministic and
+ * bit-exact inference", *technical*: batch-invariant RMSNorm and matmul).
+ * The RMSNorm of a residual-stream row x, h = x / rms(x) * g, feeds only a
+ * projection h . W^T, which equals (x . (W * g)^T) / rms(x) with the gain g
+ * folded into W's columns once.  So:
+ *  - a producing projection (`resid`) adds its bf16 output to the residual
+ *    stream in its epilogue, resid[m][n] = bf16(resid[m][n] + bf16(out)),
+ *    and leaves the new row's sum of squares over each 128-column tile in
+ *    ss_out[m][n / 128] (no other output; C may be NULL);
+ *  - a consuming projection (`row_ss`) multiplies its fp32 result row m by
+ *    1 / sqrt((row_ss[m][0] + row_ss[m][1] + ...) / norm_dim + eps), the
+ *    tiles added in ascending order, before its rounding or epilogue;
+ * so h is never rounded or stored.  Each partial and each row's total is
+ * formed in a fixed order, so the bits do not depend on the batch.
+ * row_ss: device fp32 [M][row_ss_tiles]; resid: device bf16 [M][N] (ld_resid,
+ * a multiple of 8, N % 128 == 0); ss_out: device fp32 [M][N / 128]. */
+typedef struct {
+  const float* row_ss;
+  int row_ss_tiles;
+  int norm_dim;
+  float eps;
+  void* resid;
+  int64_t ld_resid;
+  float* ss_out;
+} kinv_gemm_fusion;
+
+/* kinv_gemm with the folded-RMSNorm options above (fusion nullable: plain
+ * kinv_gemm).  Same tile, K order and split as kinv_gemm. */
+kinv_status kinv_gemm_fused(const void* A, int64_t lda, const void* W, int64_t ldw,
+                            void* C, int64_t ldc, kinv_dtype c_dtype, int M, int N, int K,
+                            const kinv_gemm_fusion* fusion, kinv_stream stream);
+
+/* Partial sums of squares of bf16 rows for a consuming projection's folded
+ * RMSNorm (the first layer, whose input comes from the embedding):
+ * ss_out[r][t] = sum over the 128 columns c of tile t of x[r][c]^2, in column
+ * order.  x: device bf16 [rows][dim] (ldx); dim % 128 == 0. */
+kinv_status kinv_row_sumsq(const void* x, int64_t ldx, int rows, int dim, float* ss_out,
+                           kinv_stream stream);
+
 /* QKV projection with kinv_rope_append in the epilogue: the product
  * qkv = A . W_qkv^T is formed with the same tile, K order and split as
  * kinv_gemm (N = (Hq + 2 Hkv) D), rounded to bf16 as kinv_gemm would store it,
@@ -98,12 +137,15 @@ kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int64_t ldw,
  * the batch-invariant kernels; RoPE and the append reduce nothing across rows).
  * A bf16 [M][K] (lda), W_qkv bf16 [N][K] (ldw); q_out bf16 [M][Hq][D]; caches,
  * strides, seq, pos, norms, eps and rope_base as in kinv_rope_append.
+ * fusion (nullable): the folded input RMSNorm (row_ss) of kinv_gemm_fused;
+ * `resid` is not allowed here.
  * Requirements: D in {64, 128}, N % 128 == 0, K % 64 == 0, 16-byte alignment. */
 kinv_status kinv_gemm_qkv_rope(const void* A, int64_t lda, const void* W_qkv, int64_t ldw,
                                void* q_out, void* k_cache, void* v_cache, int64_t seq_stride,
                                int64_t tok_stride, const int32_t* seq, const int32_t* pos,
                                const void* q_norm, const void* k_norm, float eps, int M, int Hq,
-                               int Hkv, int D, int K, float rope_base, kinv_stream stream);
+                               int Hkv, int D, int K, float rope_base,
+                               const kinv_gemm_fusion* fusion, kinv_stream stream);
 
 /* Gate/up projection with the SwiGLU applied in the epilogue:
  *   act[m][f] = bf16(silu(g) * u),  silu(g) = g / (1 + e^-g),
@@ -112,11 +154,13 @@ kinv_status kinv_gemm_qkv_rope(const void* A, int64_t lda, const void* W_qkv, in
  * bits do not depend on M).  W_gu holds the 2F weight rows interleaved in
  * blocks of 64: rows 128j .. 128j+63 are gate rows 64j .. 64j+63 and rows
  * 128j+64 .. 128j+127 are up rows 64j .. 64j+63.  act: bf16 [M][F], leading
- * dimension ld_act (a multiple of 8).  Requirements: F % 64 == 0, K % 64 == 0,
- * alignment as for kinv_gemm. */
+ * dimension ld_act (a multiple of 8).  fusion (nullable): the folded input
+ * RMSNorm (row_ss) of kinv_gemm_fused, applied to g and u; `resid` is not
+ * allowed here.  Requirements: F % 64 == 0, K % 64 == 0, alignment as for
+ * kinv_gemm. */
 kinv_status kinv_gemm_swiglu(const void* A, int64_t lda, const void* W_gu, int64_t ldw,
                              void* act, int64_t ld_act, int M, int F, int K,
-                             kinv_stream stream);
+                             const kinv_gemm_fusion* fusion, kinv_stream stream);
 
 /* --------------------------------------------------------------- RMSNorm
  * y[r][i] = x[r][i] / sqrt(mean_j x[r][j]^2 + eps) * w[i]

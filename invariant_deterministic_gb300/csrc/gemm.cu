@@ -66,6 +66,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
 
 __device__ __forceinline__ float silu_times(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
+// bf16(x + bf16(v)) for a bf16 x given by its bits: the residual stream plus
+// the projection's output as it would be stored
+__device__ __forceinline__ float residual_add(uint32_t x_bits, float v) {
+  const float x = __uint_as_float((x_bits & 0xFFFFu) << 16);
+  const float o = __bfloat162float(__float2bfloat16_rn(v));
+  return __bfloat162float(__float2bfloat16_rn(__fadd_rn(x, o)));
+}
+
+__host__ __device__ constexpr int rope_pre_bytes(int own_rows, int D, int BN) {
+  return own_rows * (8 + (D / 2) * 8) + BN * 2;
+}
+
 // The QKV projection's epilogue: the bf16 result rows (as a plain store would
 // round them) go through RoPE with the optional QK-norm (the same per-head
 // arithmetic as kinv_rope_append) straight into q and the KV cache.
@@ -100,6 +112,17 @@ struct GemmArgs {
   int ring_bytes;  // the stage ring, or more when the epilogue's receive slots need it
   int* status;
   RopeEpilogue rope;
+  // RMSNorm folded in (kinv_gemm_fusion): scale row m by 1/rms from the
+  // partial sums of squares row_ss[m][0 .. row_ss_tiles)
+  const float* row_ss;
+  int row_ss_tiles;
+  int norm_dim;
+  float eps;
+  // residual: resid[m][n] = bf16(resid[m][n] + bf16(product)), and the new
+  // row's sum of squares over this tile's 128 columns -> ss_out[m][n0 / 128]
+  __nv_bfloat16* resid;
+  int64_t ld_resid;
+  float* ss_out;
 };
 
 // Rows [0, n) of a staged tile (bf16, row stride BN) are rows row_of(r) of the
@@ -203,12 +226,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // gathered by the otherwise idle warps 2 and 3 while the weights stream
   const bool use_pre = args.rope.on && args.splits > 1 && args.own_rows <= kRopeTabRows;
   RopePre pre{};
+  unsigned char* tail = reinterpret_cast<unsigned char*>(tmem_slot + 4);
   if (use_pre) {
-    pre.pos = reinterpret_cast<int*>(tmem_slot + 4);
+    pre.pos = reinterpret_cast<int*>(tail);
     pre.seq = pre.pos + args.own_rows;
     pre.cs = reinterpret_cast<float*>(pre.seq + args.own_rows);
     pre.nw = reinterpret_cast<__nv_bfloat16*>(pre.cs + args.own_rows * args.rope.D);
+    tail += rope_pre_bytes(args.own_rows, args.rope.D, BN);
   }
+  float* row_inv = reinterpret_cast<float*>(tail);  // [BM] when row_ss is given
+  if (args.row_ss) tail += BM * 4;
+  float* red4 = reinterpret_cast<float*>(tail);     // [own_rows][4] for the split residual
   auto full_bar = [&](int s) { return smem_addr(bars + s); };
   auto empty_bar = [&](int s) { return smem_addr(bars + stages + s); };
   const uint32_t done_bar = smem_addr(bars + 2 * stages);
@@ -332,6 +360,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
 
+  if (args.row_ss && warp >= 2) {
+    // 1 / rms of this tile's rows from the partial sums of squares (written by
+    // the kernel that produced A), tiles added in ascending order
+    pdl_wait();
+    for (int r = threadIdx.x - 64; r < rows_here; r += 64) {
+      const float* ss = args.row_ss + static_cast<int64_t>(m0 + r) * args.row_ss_tiles;
+      float acc = ss[0];
+      for (int q = 1; q < args.row_ss_tiles; ++q) acc = __fadd_rn(acc, ss[q]);
+      row_inv[r] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(acc, static_cast<float>(args.norm_dim)),
+                                                       args.eps)));
+    }
+  }
+
   // ---- epilogue
   const bool ok = mbar_wait_bounded(done_bar, 0, args.status, DEV_TIMEOUT_GEMM_EPILOGUE);
   __syncwarp();
@@ -341,6 +382,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
   const bool good = ok && !*abort_flag && k_stages > 0;
   constexpr int HALF = BN / 2;
+  if (args.row_ss) __syncthreads();  // row_inv is complete
+  const float inv_here = args.row_ss && row_local < rows_here ? row_inv[row_local] : 1.0f;
+  auto scale32 = [&](uint32_t (&v)[32]) {
+    if (args.row_ss) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__fmul_rn(__uint_as_float(v[j]), inv_here));
+    }
+  };
 
   if (splits == 1 && args.swiglu) {
     // columns [0, BN/2) of the tile are gate features n0/2 .. n0/2 + BN/2 - 1,
@@ -350,6 +399,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t gv[32], uv[32];
       tmem_ld32(lane_base + c0, gv);
       tmem_ld32(lane_base + HALF + c0, uv);
+      scale32(gv);
+      scale32(uv);
       if (m < args.M) {
         __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(args.C) + m * args.ldc + n0 / 2 + c0;
 #pragma unroll
@@ -369,12 +420,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (splits == 1) {
     __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(base);  // rope: the ring is idle now
+    float ss_row = 0.f;  // residual: the new row's sum of squares over the tile, in column order
     if (good) {
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         uint32_t r[32];
         tmem_ld32(lane_base + c0, r);
-        if (args.rope.on) {
+        scale32(r);
+        if (args.resid) {
+          if (m < args.M) {
+            __nv_bfloat16* xrow = args.resid + m * args.ld_resid + n0 + c0;
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              const uint4 xv = *reinterpret_cast<const uint4*>(xrow + j);
+              const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+              uint32_t ow[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float s0 = residual_add(xw[q] & 0xFFFFu, __uint_as_float(r[j + 2 * q]));
+                const float s1 = residual_add(xw[q] >> 16, __uint_as_float(r[j + 2 * q + 1]));
+                ss_row = fmaf(s0, s0, ss_row);
+                ss_row = fmaf(s1, s1, ss_row);
+                ow[q] = pack_bf16(s0, s1);
+              }
+              *reinterpret_cast<uint4*>(xrow + j) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            }
+          }
+        } else if (args.rope.on) {
           if (m < args.M) {
 #pragma unroll
             for (int j = 0; j < 32; j += 8) {
@@ -411,6 +483,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
+    if (args.resid && good && m < args.M)
+      args.ss_out[static_cast<int64_t>(m) * (args.N / BN) + n0 / BN] = ss_row;
     if (args.rope.on) {
       __syncthreads();
       if (good) {
@@ -463,9 +537,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             g = __fadd_rn(g, src[q * slot]);
             u = __fadd_rn(u, src[q * slot + HALF]);
           }
+          if (args.row_ss) {
+            const float inv = row_inv[i * splits + rank];
+            g = __fmul_rn(g, inv);
+            u = __fmul_rn(u, inv);
+          }
           const int mm = m0 + i * splits + rank;
           static_cast<__nv_bfloat16*>(args.C)[mm * args.ldc + n0 / 2 + f] =
               __float2bfloat16_rn(silu_times(g, u));
+        }
+      } else if (args.resid) {
+        if constexpr (BN == kGemmThreads) {
+          // thread t takes column t of each owned row in turn; the row's sum of
+          // squares: a fixed butterfly in each warp, then the four warps in order
+          for (int i = 0; i < owned; ++i) {
+            const int col = threadIdx.x;
+            const float* src = recv + i * BN + col;
+            float acc = src[0];
+            for (int q = 1; q < splits; ++q) acc = __fadd_rn(acc, src[q * slot]);
+            const int mm = m0 + i * splits + rank;
+            __nv_bfloat16* xp = args.resid + mm * args.ld_resid + n0 + col;
+            const float sv = residual_add(*reinterpret_cast<const uint16_t*>(xp), acc);
+            *xp = __float2bfloat16_rn(sv);
+            float sq = __fmul_rn(sv, sv);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, o));
+            if (lane == 0) red4[i * 4 + warp] = sq;
+          }
+          __syncthreads();
+          for (int i = threadIdx.x; i < owned; i += kGemmThreads) {
+            const float sq = __fadd_rn(__fadd_rn(__fadd_rn(red4[i * 4], red4[i * 4 + 1]), red4[i * 4 + 2]),
+                                       red4[i * 4 + 3]);
+            args.ss_out[static_cast<int64_t>(m0 + i * splits + rank) * (args.N / BN) + n0 / BN] = sq;
+          }
         }
       } else {
         // rope: the owned rows are staged after the receive slots
@@ -477,6 +581,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const float* src = recv + i * BN + col;
           float acc = src[0];
           for (int q = 1; q < splits; ++q) acc = __fadd_rn(acc, src[q * slot]);
+          if (args.row_ss) acc = __fmul_rn(acc, row_inv[i * splits + rank]);
           const int mm = m0 + i * splits + rank;
           if (args.rope.on)
             stage[i * BN + col] = __float2bfloat16_rn(acc);
@@ -601,9 +706,10 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a
   a.stages = stages;
   // the epilogue's receive slots reuse the ring and may run past it
   a.ring_bytes = stages * stage > recv_bytes ? stages * stage : (recv_bytes + 15) / 16 * 16;
-  const int tab_bytes = a.rope.on && a.splits > 1 && a.own_rows <= kRopeTabRows
-                              ? a.own_rows * (8 + (a.rope.D / 2) * 8) + BN * 2
-                              : 0;
+  const int tab_bytes = (a.rope.on && a.splits > 1 && a.own_rows <= kRopeTabRows
+                             ? rope_pre_bytes(a.own_rows, a.rope.D, BN)
+                             : 0) +
+                        (a.row_ss ? BM * 4 : 0) + (a.resid && a.splits > 1 ? a.own_rows * 16 : 0);
   const size_t smem = smem_bytes(stages, a.ring_bytes, tab_bytes);
   if (smem > static_cast<size_t>(max_smem_optin())) return KINV_ERR_UNSUPPORTED;
   // the opt-in limit is raised once per device to the largest request seen
@@ -633,16 +739,27 @@ namespace kinv {
 namespace {
 kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, void* C, int64_t ldc,
                       kinv_dtype c_dtype, int M, int N, int K, bool swiglu, const RopeEpilogue* rope,
-                      cudaStream_t stream) {
+                      const kinv_gemm_fusion* fu, cudaStream_t stream) {
   if (M < 0 || N <= 0 || K <= 0) return KINV_ERR_INVALID_ARG;
   if (c_dtype != KINV_BF16 && c_dtype != KINV_F32) return KINV_ERR_INVALID_ARG;
   if (M == 0) return KINV_OK;
-  if (!A || !W || (!C && !rope)) return KINV_ERR_INVALID_ARG;
+  const bool resid = fu && fu->resid;
+  if (fu && fu->row_ss && (fu->row_ss_tiles <= 0 || fu->norm_dim <= 0 || !(fu->eps >= 0.f)))
+    return KINV_ERR_INVALID_ARG;
+  if (resid) {
+    // the residual stream is the only output
+    if (!fu->ss_out || swiglu || rope || fu->ld_resid < N) return KINV_ERR_INVALID_ARG;
+    if (N % 128) return KINV_ERR_UNSUPPORTED;
+    if (!aligned16(fu->resid) || fu->ld_resid % 8) return KINV_ERR_ALIGNMENT;
+    rope = nullptr;
+  }
+  const bool no_c = rope || resid;
+  if (!A || !W || (!C && !no_c)) return KINV_ERR_INVALID_ARG;
   if (K % BK || N % 16 || ((swiglu || rope) && (N % 128 || c_dtype != KINV_BF16)))
     return KINV_ERR_UNSUPPORTED;
-  if (lda < K || ldw < K || (!rope && ldc < (swiglu ? N / 2 : N))) return KINV_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(W) || (!rope && !aligned16(C)) || lda % 8 || ldw % 8 ||
-      (!rope && (c_dtype == KINV_BF16 ? ldc % 8 : ldc % 4)))
+  if (lda < K || ldw < K || (!no_c && ldc < (swiglu ? N / 2 : N))) return KINV_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W) || (!no_c && !aligned16(C)) || lda % 8 || ldw % 8 ||
+      (!no_c && (c_dtype == KINV_BF16 ? ldc % 8 : ldc % 4)))
     return KINV_ERR_ALIGNMENT;
   const Plan p = plan_for(N, K);  // 128-wide tiles: 64 gate and the matching 64 up columns
   const int grid_y = (M + BM - 1) / BM;
@@ -678,6 +795,13 @@ kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, vo
   a.status = device_status_word();
   a.rope = rope ? *rope : RopeEpilogue{};
   a.rope.on = rope ? 1 : 0;
+  a.row_ss = fu ? fu->row_ss : nullptr;
+  a.row_ss_tiles = fu ? fu->row_ss_tiles : 0;
+  a.norm_dim = fu ? fu->norm_dim : 0;
+  a.eps = fu ? fu->eps : 0.f;
+  a.resid = resid ? static_cast<__nv_bfloat16*>(fu->resid) : nullptr;
+  a.ld_resid = resid ? fu->ld_resid : 0;
+  a.ss_out = resid ? fu->ss_out : nullptr;
   switch (p.bn) {
     case 64: return launch_gemm<64>(ta, tw, a, p.smem_budget, grid_y, grid_z, stream);
     case 128: return launch_gemm<128>(ta, tw, a, p.smem_budget, grid_y, grid_z, stream);
@@ -690,14 +814,22 @@ kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, vo
 extern "C" kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int64_t ldw, void* C,
                                  int64_t ldc, kinv_dtype c_dtype, int M, int N, int K,
                                  kinv_stream stream) {
-  return kinv::gemm_impl(A, lda, W, ldw, C, ldc, c_dtype, M, N, K, false, nullptr, stream);
+  return kinv::gemm_impl(A, lda, W, ldw, C, ldc, c_dtype, M, N, K, false, nullptr, nullptr, stream);
+}
+
+extern "C" kinv_status kinv_gemm_fused(const void* A, int64_t lda, const void* W, int64_t ldw, void* C,
+                                       int64_t ldc, kinv_dtype c_dtype, int M, int N, int K,
+                                       const kinv_gemm_fusion* fusion, kinv_stream stream) {
+  return kinv::gemm_impl(A, lda, W, ldw, C, ldc, c_dtype, M, N, K, false, nullptr, fusion, stream);
 }
 
 extern "C" kinv_status kinv_gemm_swiglu(const void* A, int64_t lda, const void* W_gu, int64_t ldw,
                                         void* act, int64_t ld_act, int M, int F, int K,
-                                        kinv_stream stream) {
+                                        const kinv_gemm_fusion* fusion, kinv_stream stream) {
   if (F <= 0 || F % 64) return F <= 0 ? KINV_ERR_INVALID_ARG : KINV_ERR_UNSUPPORTED;
-  return kinv::gemm_impl(A, lda, W_gu, ldw, act, ld_act, KINV_BF16, M, 2 * F, K, true, nullptr, stream);
+  if (fusion && fusion->resid) return KINV_ERR_INVALID_ARG;
+  return kinv::gemm_impl(A, lda, W_gu, ldw, act, ld_act, KINV_BF16, M, 2 * F, K, true, nullptr, fusion,
+                         stream);
 }
 
 extern "C" kinv_status kinv_gemm_qkv_rope(const void* A, int64_t lda, const void* W_qkv, int64_t ldw,
@@ -705,7 +837,8 @@ extern "C" kinv_status kinv_gemm_qkv_rope(const void* A, int64_t lda, const void
                                           int64_t seq_stride, int64_t tok_stride, const int32_t* seq,
                                           const int32_t* pos, const void* q_norm, const void* k_norm,
                                           float eps, int M, int Hq, int Hkv, int D, int K,
-                                          float rope_base, kinv_stream stream) {
+                                          float rope_base, const kinv_gemm_fusion* fusion,
+                                          kinv_stream stream) {
   if (M < 0 || Hq <= 0 || Hkv <= 0 || K <= 0 || !(rope_base > 0.f) || !(eps >= 0.f))
     return KINV_ERR_INVALID_ARG;
   if (M == 0) return KINV_OK;
@@ -732,5 +865,6 @@ extern "C" kinv_status kinv_gemm_qkv_rope(const void* A, int64_t lda, const void
   for (int i = 0; i < D / 2; ++i)
     e.freqs.inv_freq[i] = std::pow(static_cast<double>(rope_base), -2.0 * i / D);
   const int N = (Hq + 2 * Hkv) * D;
-  return kinv::gemm_impl(A, lda, W_qkv, ldw, nullptr, N, KINV_BF16, M, N, K, false, &e, stream);
+  if (fusion && fusion->resid) return KINV_ERR_INVALID_ARG;
+  return kinv::gemm_impl(A, lda, W_qkv, ldw, nullptr, N, KINV_BF16, M, N, K, false, &e, fusion, stream);
 }

@@ -119,3 +119,49 @@ extern "C" kinv_status kinv_rmsnorm(void* x, int64_t ldx, const void* residual, 
                        static_cast<const __nv_bfloat16*>(w), static_cast<__nv_bfloat16*>(y), ldy, dim,
                        eps);
 }
+
+// ------------------------------------------------------------ row_sumsq
+namespace kinv {
+namespace {
+
+// One warp per (row, 128-column tile): lane l squares columns 4l .. 4l + 3 in
+// order (FMA), then a fixed butterfly adds the lanes.
+__global__ void row_sumsq_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, int rows, int tiles,
+                                 float* __restrict__ ss) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (item >= rows * tiles) return;
+  const int r = item / tiles, t = item % tiles;
+  const uint2 v = *reinterpret_cast<const uint2*>(x + r * ldx + t * 128 + lane * 4);
+  const float a0 = __uint_as_float(v.x << 16), a1 = __uint_as_float(v.x & 0xFFFF0000u);
+  const float a2 = __uint_as_float(v.y << 16), a3 = __uint_as_float(v.y & 0xFFFF0000u);
+  float acc = 0.f;
+  acc = fmaf(a0, a0, acc);
+  acc = fmaf(a1, a1, acc);
+  acc = fmaf(a2, a2, acc);
+  acc = fmaf(a3, a3, acc);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+  if (lane == 0) ss[static_cast<int64_t>(r) * tiles + t] = acc;
+}
+
+}  // namespace
+}  // namespace kinv
+
+extern "C" kinv_status kinv_row_sumsq(const void* x, int64_t ldx, int rows, int dim, float* ss_out,
+                                      kinv_stream stream) {
+  if (rows < 0 || dim <= 0 || ldx < dim) return KINV_ERR_INVALID_ARG;
+  if (rows == 0) return KINV_OK;
+  if (!x || !ss_out) return KINV_ERR_INVALID_ARG;
+  if (dim % 128) return KINV_ERR_UNSUPPORTED;
+  if (!kinv::aligned16(x) || ldx % 8) return KINV_ERR_ALIGNMENT;
+  const int tiles = dim / 128;
+  const int64_t items = static_cast<int64_t>(rows) * tiles;
+  if (items > (int64_t(1) << 30)) return KINV_ERR_UNSUPPORTED;
+  const int warps = 8;
+  return kinv::launch_kernel(kinv::row_sumsq_kernel, dim3(static_cast<unsigned>((items + warps - 1) / warps)),
+                             dim3(32 * warps), 0, stream, 1, static_cast<const __nv_bfloat16*>(x), ldx,
+                             rows, tiles, ss_out);
+}

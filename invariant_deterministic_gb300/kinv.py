@@ -39,9 +39,11 @@ SIGNATURES = {
     "kinv_build_id": (ctypes.c_char_p, []),
     "kinv_last_device_status": (_i32, [_c_p]),
     "kinv_gemm": (_i32, [_c_p, _i64, _c_p, _i64, _c_p, _i64, _i32, _i32, _i32, _i32, _c_p]),
-    "kinv_gemm_swiglu": (_i32, [_c_p, _i64, _c_p, _i64, _c_p, _i64, _i32, _i32, _i32, _c_p]),
+    "kinv_gemm_fused": (_i32, [_c_p, _i64, _c_p, _i64, _c_p, _i64, _i32, _i32, _i32, _i32, _c_p, _c_p]),
+    "kinv_row_sumsq": (_i32, [_c_p, _i64, _i32, _i32, _c_p, _c_p]),
+    "kinv_gemm_swiglu": (_i32, [_c_p, _i64, _c_p, _i64, _c_p, _i64, _i32, _i32, _i32, _c_p, _c_p]),
     "kinv_gemm_qkv_rope": (_i32, [_c_p, _i64, _c_p, _i64, _c_p, _c_p, _c_p, _i64, _i64, _c_p, _c_p,
-                                  _c_p, _c_p, _f32, _i32, _i32, _i32, _i32, _i32, _f32, _c_p]),
+                                  _c_p, _c_p, _f32, _i32, _i32, _i32, _i32, _i32, _f32, _c_p, _c_p]),
     "kinv_rmsnorm": (_i32, [_c_p, _i64, _c_p, _c_p, _c_p, _i64, _i32, _i32, _f32, _c_p]),
     "kinv_attn_decode_workspace": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "kinv_attn_decode": (_i32, [_c_p, _c_p, _c_p, _i64, _i64, _c_p, _c_p, _i32, _i32, _i32, _i32,
@@ -142,6 +144,53 @@ def gemm(a: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
     return out
 
 
+class GemmFusion(ctypes.Structure):
+    """kinv_gemm_fusion: the RMSNorm folded into the projections around it."""
+    _fields_ = [("row_ss", _c_p), ("row_ss_tiles", _i32), ("norm_dim", _i32), ("eps", _f32),
+                ("resid", _c_p), ("ld_resid", _i64), ("ss_out", _c_p)]
+
+
+def norm_in(row_ss: torch.Tensor, norm_dim: int, eps: float) -> GemmFusion:
+    """Consuming side: scale output row m by 1/rms from row_ss [M][tiles]."""
+    _need(row_ss, torch.float32, "row_ss")
+    return GemmFusion(row_ss=_ptr(row_ss), row_ss_tiles=row_ss.shape[1], norm_dim=norm_dim, eps=float(eps))
+
+
+def residual_out(resid: torch.Tensor, ss_out: torch.Tensor) -> GemmFusion:
+    """Producing side: resid <- bf16(resid + bf16(out)); ss_out [M][N/128]."""
+    _need(resid, torch.bfloat16, "resid")
+    _need(ss_out, torch.float32, "ss_out")
+    return GemmFusion(resid=_ptr(resid), ld_resid=resid.stride(0), ss_out=_ptr(ss_out))
+
+
+def _fusion_ptr(f):
+    return ctypes.byref(f) if f is not None else None
+
+
+def gemm_fused(a, w, fusion: GemmFusion, out=None, n=None, stream=None):
+    """kinv_gemm_fused.  With a residual fusion there is no other output
+    (out may be None); otherwise out is written as by gemm()."""
+    _need(a, torch.bfloat16, "a")
+    _need(w, torch.bfloat16, "w")
+    m, k = a.shape
+    n = w.shape[0] if n is None else n
+    dt = F32 if (out is not None and out.dtype == torch.float32) else BF16
+    _check(lib().kinv_gemm_fused(_ptr(a), a.stride(0), _ptr(w), w.stride(0), _ptr(out),
+                                 out.stride(0) if out is not None else n, dt, m, n, k,
+                                 _fusion_ptr(fusion), _stream(stream)), "kinv_gemm_fused")
+    return out
+
+
+def row_sumsq(x, ss_out, stream=None):
+    """ss_out[r][t] = sum of x[r][128t .. 128t+127]^2 (fp32)."""
+    _need(x, torch.bfloat16, "x")
+    _need(ss_out, torch.float32, "ss_out")
+    rows, dim = x.shape
+    _check(lib().kinv_row_sumsq(_ptr(x), x.stride(0), rows, dim, _ptr(ss_out), _stream(stream)),
+           "kinv_row_sumsq")
+    return ss_out
+
+
 def interleave_gate_up(w_gu: torch.Tensor) -> torch.Tensor:
     """[gate rows; up rows] ([2F][K]) -> the block-of-64 interleaved layout
     kinv_gemm_swiglu reads (a one-time weight layout change, a copy)."""
@@ -151,7 +200,7 @@ def interleave_gate_up(w_gu: torch.Tensor) -> torch.Tensor:
 
 
 def gemm_swiglu(a: torch.Tensor, w_gu_il: torch.Tensor, out: torch.Tensor | None = None,
-                stream=None) -> torch.Tensor:
+                fusion: GemmFusion | None = None, stream=None) -> torch.Tensor:
     """act[M][F] = bf16(silu(a . Wgate^T) * (a . Wup^T)), W in the interleaved
     layout of ``interleave_gate_up``."""
     _need(a, torch.bfloat16, "a")
@@ -161,12 +210,13 @@ def gemm_swiglu(a: torch.Tensor, w_gu_il: torch.Tensor, out: torch.Tensor | None
     if out is None:
         out = torch.empty(m, f, dtype=torch.bfloat16, device=a.device)
     _check(lib().kinv_gemm_swiglu(_ptr(a), a.stride(0), _ptr(w_gu_il), w_gu_il.stride(0), _ptr(out),
-                                  out.stride(0), m, f, k, _stream(stream)), "kinv_gemm_swiglu")
+                                  out.stride(0), m, f, k, _fusion_ptr(fusion), _stream(stream)),
+           "kinv_gemm_swiglu")
     return out
 
 
 def gemm_qkv_rope(a, w_qkv, q_out, k_cache, v_cache, seq, pos, n_q, n_kv, head_dim, rope_base,
-                  q_norm=None, k_norm=None, eps=1e-6, stream=None):
+                  q_norm=None, k_norm=None, eps=1e-6, fusion=None, stream=None):
     """kinv_gemm followed by kinv_rope_append in one kernel: q heads of
     a . w_qkv^T -> q_out [M][Hq][D]; k and v heads into the caches
     [B][Lmax][Hkv][D] at [seq][pos]."""
@@ -176,7 +226,8 @@ def gemm_qkv_rope(a, w_qkv, q_out, k_cache, v_cache, seq, pos, n_q, n_kv, head_d
     _check(lib().kinv_gemm_qkv_rope(_ptr(a), a.stride(0), _ptr(w_qkv), w_qkv.stride(0), _ptr(q_out),
                                     _ptr(k_cache), _ptr(v_cache), k_cache.stride(0), k_cache.stride(1),
                                     _ptr(seq), _ptr(pos), _ptr(q_norm), _ptr(k_norm),
-                                    float(eps), m, n_q, n_kv, head_dim, k, float(rope_base), _stream(stream)),
+                                    float(eps), m, n_q, n_kv, head_dim, k, float(rope_base),
+                                    _fusion_ptr(fusion), _stream(stream)),
            "kinv_gemm_qkv_rope")
     return q_out
 

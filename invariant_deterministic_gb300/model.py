@@ -4,13 +4,19 @@ SwiGLU, down GEMM), an untied LM head and the seeded sampler.
 
 Every arithmetic step is a kinv kernel; this module only owns buffers and
 issues the calls in order on the current CUDA stream, so a whole decode step
-can be captured into a CUDA graph.  The residual add that closes one layer is
-fused into the RMSNorm that opens the next (and into the final norm).
+can be captured into a CUDA graph.  Kernels per layer: the QKV projection
+(with RoPE and the KV append for 2..32 rows), split-KV attention (split and
+merge), the O projection, the gate/up projection with SwiGLU, the down
+projection.  The RMSNorms are folded into the projections (kinv_gemm_fusion):
+the O and down projections add their output to the residual stream x and
+leave per-tile sums of squares of the new rows; the QKV and gate/up
+projections and the LM head scale their rows by 1/rms, with the norm gains
+folded into their weight columns once.
 
 Layouts (all bf16 unless noted):
   embed, lm_head [V][d]; per layer w_qkv [(Hq + 2 Hkv) D][d], w_o [d][Hq D],
   w_gu [2F][d] (gate rows then up rows; the decoder keeps a copy interleaved
-  in blocks of 32 for the fused gate/up + SwiGLU GEMM), w_down [d][F], norm
+  in blocks of 64 for the fused gate/up + SwiGLU GEMM), w_down [d][F], norm
   gains [d] / [D];
   KV cache [layers][2][B][Lmax][Hkv][D] (k then v), token-major per sequence.
 """
@@ -65,6 +71,14 @@ def random_weights(shape: ModelShape, seed: int = synth.SEED_WEIGHTS, device="cu
     return w
 
 
+def fold_gain(w: torch.Tensor, g: torch.Tensor) -> torch.Tensor:
+    """W * g over the input columns (bf16), the RMSNorm gain moved into the
+    projection it feeds; W itself when every gain is 1."""
+    if bool(torch.all(g == 1)):
+        return w
+    return (w.float() * g.float()[None, :]).to(torch.bfloat16)
+
+
 # From 2 to this many rows the QKV projection runs with RoPE and the KV append
 # in its epilogue (kinv_gemm_qkv_rope); otherwise kinv_gemm then
 # kinv_rope_append (measured faster at one row and at many).  Both give the
@@ -91,15 +105,19 @@ class Decoder:
         bf = dict(dtype=torch.bfloat16, device=self.dev)
         self.kv = torch.zeros(s.n_layers, 2, max_batch, max_len, s.n_kv, s.head_dim, **bf)
         self.x = torch.zeros(rows, s.d_model, **bf)
-        self.h = torch.zeros(rows, s.d_model, **bf)
         self.qkv = torch.zeros(rows, s.qkv_dim, **bf)
         self.q = torch.zeros(rows, s.n_q, s.head_dim, **bf)
         self.attn = torch.zeros(rows, s.n_q, s.head_dim, **bf)
-        self.o = torch.zeros(rows, s.d_model, **bf)
-        # gate/up weights in the interleaved layout of kinv_gemm_swiglu
-        self.w_gu_il = [kinv.interleave_gate_up(lw["w_gu"]) for lw in weights["layers"]]
+        # norm gains folded into the projections they feed; gate/up weights in
+        # the interleaved layout of kinv_gemm_swiglu
+        self.w_qkv_f = [fold_gain(lw["w_qkv"], lw["attn_norm"]) for lw in weights["layers"]]
+        self.w_gu_il = [kinv.interleave_gate_up(fold_gain(lw["w_gu"], lw["ffn_norm"]))
+                        for lw in weights["layers"]]
+        if "lm_head" in weights:
+            self.lm_head_f = fold_gain(weights["lm_head"], weights["final_norm"])
         self.act = torch.zeros(rows, s.ffn, **bf)
-        self.delta = torch.zeros(rows, s.d_model, **bf)
+        # per-row sums of squares of the residual stream over 128-column tiles
+        self.ss = torch.zeros(rows, s.d_model // 128, dtype=torch.float32, device=self.dev)
         ws = kinv.attn_decode_workspace(max_batch, s.n_q, s.head_dim, max_len)
         if max_chunk:
             ws = max(ws, kinv.attn_prefill_workspace(max_chunk, s.n_q, s.head_dim, max_len))
@@ -146,40 +164,36 @@ class Decoder:
             self.hist_len[b] = len(tail)
 
     # --------------------------------------------------------------- a layer
-    def layer(self, li: int, rows: int, first: bool, seq, pos, attention) -> None:
-        """One decoder layer on rows [0, rows) of the activation buffers; row
-        r is sequence seq[r] at position pos[r].  ``x`` holds the residual
-        stream and ``delta`` the previous layer's FFN output (not yet added
-        unless ``first``)."""
+    def layer(self, li: int, rows: int, seq, pos, attention) -> None:
+        """One decoder layer on rows [0, rows): ``x`` holds the residual stream
+        and ``ss`` its per-tile sums of squares; row r is sequence seq[r] at
+        position pos[r].  Leaves the updated stream and sums in place."""
         s, lw = self.s, self.w["layers"][li]
-        x, h = self.x[:rows], self.h[:rows]
-        with self._t("rmsnorm"):
-            kinv.rmsnorm(x, lw["attn_norm"], s.eps, residual=None if first else self.delta[:rows],
-                         out=h)
+        x = self.x[:rows]
+        norm_in = kinv.norm_in(self.ss[:rows], s.d_model, s.eps)
         kc, vc = self.kv[li, 0], self.kv[li, 1]
         qn = lw.get("q_norm") if s.qk_norm else None
         kn = lw.get("k_norm") if s.qk_norm else None
         if FUSED_ROPE_MIN_ROWS <= rows <= FUSED_ROPE_MAX_ROWS:
             # the QKV projection with RoPE and the KV append in its epilogue
             with self._t("gemm_qkv"):
-                kinv.gemm_qkv_rope(h, lw["w_qkv"], self.q[:rows], kc, vc, seq, pos, s.n_q, s.n_kv,
-                                   s.head_dim, s.rope_base, qn, kn, s.eps)
+                kinv.gemm_qkv_rope(x, self.w_qkv_f[li], self.q[:rows], kc, vc, seq, pos, s.n_q, s.n_kv,
+                                   s.head_dim, s.rope_base, qn, kn, s.eps, fusion=norm_in)
         else:
             # the same bits in two kernels (faster when many rows share a tile)
             with self._t("gemm_qkv"):
-                kinv.gemm(h, lw["w_qkv"], out=self.qkv[:rows])
+                kinv.gemm_fused(x, self.w_qkv_f[li], norm_in, out=self.qkv[:rows])
             with self._t("rope_append"):
                 kinv.rope_append(self.qkv[:rows], self.q[:rows], kc, vc, seq, pos, s.n_q, s.n_kv,
                                  s.head_dim, s.rope_base, qn, kn, s.eps)
         attention(li, rows, kc, vc)
         with self._t("gemm_o"):
-            kinv.gemm(self.attn[:rows].view(rows, -1), lw["w_o"], out=self.o[:rows])
-        with self._t("rmsnorm"):
-            kinv.rmsnorm(x, lw["ffn_norm"], s.eps, residual=self.o[:rows], out=h)
+            kinv.gemm_fused(self.attn[:rows].view(rows, -1), lw["w_o"],
+                            kinv.residual_out(x, self.ss[:rows]))
         with self._t("gemm_gate_up"):
-            kinv.gemm_swiglu(h, self.w_gu_il[li], out=self.act[:rows])
+            kinv.gemm_swiglu(x, self.w_gu_il[li], out=self.act[:rows], fusion=norm_in)
         with self._t("gemm_down"):
-            kinv.gemm(self.act[:rows], lw["w_down"], out=self.delta[:rows])
+            kinv.gemm_fused(self.act[:rows], lw["w_down"], kinv.residual_out(x, self.ss[:rows]))
 
     # ---------------------------------------------------------------- decode
     def decode_layers(self, bsz: int) -> None:
@@ -190,8 +204,10 @@ class Decoder:
             with self._t("attn_decode"):
                 kinv.attn_decode(self.q[:rows], kc[:rows], vc[:rows], self.kv_len[:rows],
                                  out=self.attn[:rows], workspace=self.ws)
+        with self._t("row_sumsq"):
+            kinv.row_sumsq(self.x[:bsz], self.ss[:bsz])
         for li in range(self.s.n_layers):
-            self.layer(li, bsz, li == 0, self.seq[:bsz], self.pos[:bsz], attention)
+            self.layer(li, bsz, self.seq[:bsz], self.pos[:bsz], attention)
 
     def decode_step(self, bsz: int, sample: bool = True) -> None:
         """Embed tokens[:bsz], run every layer, the final norm, the LM head
@@ -201,11 +217,9 @@ class Decoder:
         with self._t("embed"):
             kinv.embed(self.w["embed"], self.tokens[:bsz], out=self.x[:bsz])
         self.decode_layers(bsz)
-        with self._t("rmsnorm"):
-            kinv.rmsnorm(self.x[:bsz], self.w["final_norm"], s.eps, residual=self.delta[:bsz],
-                         out=self.h[:bsz])
-        with self._t("gemm_lm_head"):
-            kinv.gemm(self.h[:bsz], self.w["lm_head"], out=self.logits[:bsz])
+        with self._t("gemm_lm_head"):  # with the final RMSNorm folded in
+            kinv.gemm_fused(self.x[:bsz], self.lm_head_f, kinv.norm_in(self.ss[:bsz], s.d_model, s.eps),
+                            out=self.logits[:bsz])
         if sample:
             with self._t("sample"):
                 kinv.sample(self.logits[:bsz], self.params, self.history[:bsz],
@@ -229,12 +243,13 @@ class Decoder:
             # a one-sequence view of the cache keeps the sequence index at 0
             kinv.attn_prefill(self.q[:n], kc[seq: seq + 1], vc[seq: seq + 1], q_start, q_len,
                               q_off, n, p0 + n, out=self.attn[:n], workspace=self.ws)
+        kinv.row_sumsq(self.x[:rows], self.ss[:rows])
         for li in range(self.s.n_layers):
-            self.layer(li, rows, li == 0, seq_t, pos_t, attention)
+            self.layer(li, rows, seq_t, pos_t, attention)
 
     def close_residual(self, rows: int) -> torch.Tensor:
-        """x <- bf16(x + delta) for rows [0, rows): the last layer's output."""
-        kinv.add(self.x[:rows], self.delta[:rows], out=self.x[:rows])
+        """The last layer's output for rows [0, rows) (the residual stream;
+        every layer already added its projections to it)."""
         return self.x[:rows]
 
 

@@ -36,3 +36,19 @@ def gemm_f64_rows(a_bits: np.ndarray, w_bits: np.ndarray, rows, cols=None) -> np
     a = bf16.to_f64(a_bits[rows])
     w = bf16.to_f64(w_bits if cols is None else w_bits[cols])
     return a @ w.T
+
+
+def matmul(a: np.ndarray, w_bits: np.ndarray, out: str = "bf16") -> np.ndarray:
+    """The same product for an fp64 left operand that was never rounded to bf16
+    (a normalised row that the GPU path keeps inside its projection)."""
+    w = bf16.to_f64(w_bits)
+    if a.shape[1] != w.shape[1]:
+        raise ValueError("inner dimensions differ")
+    c = np.asarray(a, dtype=np.float64) @ w.T
+    if out == "bf16":
+        return bf16.from_f64(c)
+    if out == "f32":
+        return c.astype(np.float32)
+    if out == "f64":
+        return c
+    raise ValueError(out)

@@ -15,8 +15,11 @@ FFN, grouped-query attention):
     [g u] = h2 . Wgu^T ; x3 = x2 + (silu(g) * u) . Wdown^T
 
 bf16 rounding happens at each stored tensor, the same boundaries as the GPU
-path (g and u are not stored: the gate/up product and SwiGLU are one GPU
-step).  Weights are bf16 bit arrays; the dictionaries below name them.
+path.  The GPU path stores neither g and u (the gate/up product and SwiGLU are
+one step) nor the normalised rows h, h2 and the final one: each RMSNorm is
+folded into the projection it feeds, (x / rms(x) * w) . W^T computed as
+(x . (W * w)^T) / rms(x), so here those rows stay unrounded fp64.  Weights are
+bf16 bit arrays; the dictionaries below name them.
 """
 from __future__ import annotations
 
@@ -25,8 +28,8 @@ from dataclasses import dataclass
 import numpy as np
 
 from . import attention, bf16, glue
-from .gemm import gemm
-from .rmsnorm import rmsnorm
+from .gemm import gemm, matmul
+from .rmsnorm import rmsnorm, rmsnorm_f64
 from .rope import rope
 from .sampler import sample
 
@@ -54,8 +57,8 @@ def layer_step(x_bits, lw: dict, k_cache, v_cache, pos, shape: Shape):
     """
     hq, hk, dh = shape.n_q, shape.n_kv, shape.head_dim
     m = x_bits.shape[0]
-    h = rmsnorm(x_bits, lw["attn_norm"], shape.eps)
-    qkv = gemm(h, lw["w_qkv"]).reshape(m, hq + 2 * hk, dh)
+    h = rmsnorm_f64(bf16.to_f64(x_bits), bf16.to_f64(lw["attn_norm"]), shape.eps)
+    qkv = matmul(h, lw["w_qkv"]).reshape(m, hq + 2 * hk, dh)
     positions = np.array([p for _, p in pos], dtype=np.int64)
     qn = lw.get("q_norm") if shape.qk_norm else None
     kn = lw.get("k_norm") if shape.qk_norm else None
@@ -69,9 +72,10 @@ def layer_step(x_bits, lw: dict, k_cache, v_cache, pos, shape: Shape):
     for i, (b, p) in enumerate(pos):
         a[i] = attention.decode(q[i: i + 1], k_cache[b: b + 1], v_cache[b: b + 1], [p + 1])[0]
     o = gemm(a.reshape(m, hq * dh), lw["w_o"])
-    h2, x2 = rmsnorm(o, lw["ffn_norm"], shape.eps, residual_bits=x_bits)
+    x2 = glue.add(x_bits, o)
+    h2 = rmsnorm_f64(bf16.to_f64(x2), bf16.to_f64(lw["ffn_norm"]), shape.eps)
     # gate/up and SwiGLU form one GPU kernel: g and u are not rounded to bf16
-    act = glue.swiglu_f64(gemm(h2, lw["w_gu"], out="f64"))
+    act = glue.swiglu_f64(matmul(h2, lw["w_gu"], out="f64"))
     return glue.add(x2, gemm(act, lw["w_down"]))
 
 
@@ -83,8 +87,8 @@ def decode_step(tokens, model: dict, k_caches, v_caches, lengths, shape: Shape,
     pos = [(b, int(lengths[b])) for b in range(len(tokens))]
     for li, lw in enumerate(model["layers"]):
         x = layer_step(x, lw, k_caches[li], v_caches[li], pos, shape)
-    h = rmsnorm(x, model["final_norm"], shape.eps)
-    logits = gemm(h, model["lm_head"], out="f32")
+    h = rmsnorm_f64(bf16.to_f64(x), bf16.to_f64(model["final_norm"]), shape.eps)
+    logits = matmul(h, model["lm_head"], out="f32")
     if not sample_tokens:
         return logits, None, None
     toks, ties = sample(logits, histories, steps, params)

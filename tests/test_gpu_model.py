@@ -123,10 +123,14 @@ def test_full_depth_alone_vs_cobatched(M):
 
 def test_every_stage_of_the_step_matches_the_oracle(M):
     """Each kernel of a 2-layer 8B-shaped decode step, fed the GPU's own
-    inputs for that stage, matches the oracle within the tolerance."""
+    inputs for that stage, matches the oracle within the tolerance.  The
+    RMSNorms are folded into the projections: the O and down projections add
+    their output to the residual stream and leave per-tile sums of squares;
+    the QKV and gate/up projections and the LM head scale their rows by
+    1/rms (the oracle: the unrounded fp64 normalised row times W)."""
     from oracle import attention as oattn, glue as oglue
-    from oracle.gemm import gemm as og
-    from oracle.rmsnorm import rmsnorm as orms
+    from oracle.gemm import gemm as og, matmul as omm
+    from oracle.rmsnorm import rmsnorm_f64
     from oracle.rope import rope as orope
     kinv = M.kinv
     shape = _shape(M, 2)
@@ -138,21 +142,26 @@ def test_every_stage_of_the_step_matches_the_oracle(M):
     dec.set_positions(L)
     dec.tokens[:B] = torch.tensor([5, 77, 151935], dtype=torch.int32, device="cuda")
     b = synth.bits
-    kinv.embed(w["embed"], dec.tokens[:B], out=dec.x[:B])
-    assert np.array_equal(b(dec.x[:B]), oglue.embed(b(w["embed"]), [5, 77, 151935]))
+
+    def normed(x_bits, g):
+        return rmsnorm_f64(obf.to_f64(x_bits), obf.to_f64(b(g)), 1e-6)
+
+    def check_ss(x_bits, name):
+        x = obf.to_f64(x_bits)
+        ref = (x * x).reshape(B, -1, 128).sum(-1)
+        assert np.allclose(dec.ss[:B].cpu().numpy(), ref, rtol=1e-5, atol=0), name
+
+    x, ss = dec.x[:B], dec.ss[:B]
+    kinv.embed(w["embed"], dec.tokens[:B], out=x)
+    assert np.array_equal(b(x), oglue.embed(b(w["embed"]), [5, 77, 151935]))
+    kinv.row_sumsq(x, ss)
+    check_ss(b(x), "sums of squares of the embedding rows")
     for li in range(2):
         lw = w["layers"][li]
-        x0, d0 = b(dec.x[:B]), b(dec.delta[:B])
-        kinv.rmsnorm(dec.x[:B], lw["attn_norm"], 1e-6, residual=None if li == 0 else dec.delta[:B],
-                     out=dec.h[:B])
-        if li == 0:
-            assert_close(f64(dec.h[:B]), obf.to_f64(orms(x0, b(lw["attn_norm"]), 1e-6)), "attn norm")
-        else:
-            y, s = orms(x0, b(lw["attn_norm"]), 1e-6, residual_bits=d0)
-            assert_close(f64(dec.x[:B]), obf.to_f64(s), "residual")
-            assert_close(f64(dec.h[:B]), obf.to_f64(y), "attn norm")
-        kinv.gemm(dec.h[:B], lw["w_qkv"], out=dec.qkv[:B])
-        assert_close(f64(dec.qkv[:B]), obf.to_f64(og(b(dec.h[:B]), b(lw["w_qkv"]))), "qkv")
+        x0 = b(x)
+        kinv.gemm_fused(x, dec.w_qkv_f[li], kinv.norm_in(ss, 4096, 1e-6), out=dec.qkv[:B])
+        assert_close(f64(dec.qkv[:B]), obf.to_f64(omm(normed(x0, lw["attn_norm"]), b(lw["w_qkv"]))),
+                     "qkv with the attention norm folded in")
         qkv = b(dec.qkv[:B]).reshape(B, 48, 128)
         kc, vc = dec.kv[li, 0], dec.kv[li, 1]
         kinv.rope_append(dec.qkv[:B], dec.q[:B], kc, vc, dec.seq[:B], dec.pos[:B], 32, 8, 128, 1e6,
@@ -166,25 +175,23 @@ def test_every_stage_of_the_step_matches_the_oracle(M):
         kinv.attn_decode(dec.q[:B], kc[:B], vc[:B], dec.kv_len[:B], out=dec.attn[:B], workspace=dec.ws)
         ref = oattn.decode(b(dec.q[:B]), b(kc[:B]), b(vc[:B]), [n + 1 for n in L])
         assert_close(f64(dec.attn[:B]), obf.to_f64(ref), "attention")
-        kinv.gemm(dec.attn[:B].view(B, -1), lw["w_o"], out=dec.o[:B])
-        assert_close(f64(dec.o[:B]), obf.to_f64(og(b(dec.attn[:B]).reshape(B, -1), b(lw["w_o"]))), "o")
-        x1, o1 = b(dec.x[:B]), b(dec.o[:B])
-        kinv.rmsnorm(dec.x[:B], lw["ffn_norm"], 1e-6, residual=dec.o[:B], out=dec.h[:B])
-        y, s = orms(x1, b(lw["ffn_norm"]), 1e-6, residual_bits=o1)
-        assert_close(f64(dec.x[:B]), obf.to_f64(s), "x2")
-        assert_close(f64(dec.h[:B]), obf.to_f64(y), "ffn norm")
-        kinv.gemm_swiglu(dec.h[:B], dec.w_gu_il[li], out=dec.act[:B])
-        gu = og(b(dec.h[:B]), b(lw["w_gu"]), out="f64")
-        assert_close(f64(dec.act[:B]), obf.to_f64(oglue.swiglu_f64(gu)), "gate/up + swiglu")
-        kinv.gemm(dec.act[:B], lw["w_down"], out=dec.delta[:B])
-        assert_close(f64(dec.delta[:B]), obf.to_f64(og(b(dec.act[:B]), b(lw["w_down"]))), "down")
-    x1, d1 = b(dec.x[:B]), b(dec.delta[:B])
-    kinv.rmsnorm(dec.x[:B], w["final_norm"], 1e-6, residual=dec.delta[:B], out=dec.h[:B])
-    y, s = orms(x1, b(w["final_norm"]), 1e-6, residual_bits=d1)
-    assert_close(f64(dec.h[:B]), obf.to_f64(y), "final norm")
-    kinv.gemm(dec.h[:B], w["lm_head"], out=dec.logits[:B])
-    assert_close(f64(dec.logits[:B]), og(b(dec.h[:B]), b(w["lm_head"]), out="f64"), "logits",
-                 atol=1e-4, rtol=1e-4)
+        x1 = b(x)
+        kinv.gemm_fused(dec.attn[:B].view(B, -1), lw["w_o"], kinv.residual_out(x, ss))
+        o_ref = og(b(dec.attn[:B]).reshape(B, -1), b(lw["w_o"]))
+        assert_close(f64(x), obf.to_f64(oglue.add(x1, o_ref)), "x + o")
+        check_ss(b(x), "sums of squares after the O projection")
+        x2 = b(x)
+        kinv.gemm_swiglu(x, dec.w_gu_il[li], out=dec.act[:B], fusion=kinv.norm_in(ss, 4096, 1e-6))
+        gu = omm(normed(x2, lw["ffn_norm"]), b(lw["w_gu"]), out="f64")
+        assert_close(f64(dec.act[:B]), obf.to_f64(oglue.swiglu_f64(gu)), "gate/up + swiglu, norm folded in")
+        kinv.gemm_fused(dec.act[:B], lw["w_down"], kinv.residual_out(x, ss))
+        d_ref = og(b(dec.act[:B]), b(lw["w_down"]))
+        assert_close(f64(x), obf.to_f64(oglue.add(x2, d_ref)), "x + down")
+        check_ss(b(x), "sums of squares after the down projection")
+    xf = b(x)
+    kinv.gemm_fused(x, dec.lm_head_f, kinv.norm_in(ss, 4096, 1e-6), out=dec.logits[:B])
+    assert_close(f64(dec.logits[:B]), omm(normed(xf, w["final_norm"]), b(w["lm_head"]), out="f64"),
+                 "logits with the final norm folded in", atol=1e-4, rtol=1e-4)
     assert kinv.last_device_status() == 0
 
 

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 from oracle import bf16, glue
-from oracle.gemm import gemm
+from oracle.gemm import gemm, matmul
 from oracle.rmsnorm import rmsnorm
 from oracle.rope import rope
 
@@ -71,6 +71,21 @@ def test_gemm_matches_numpy_matmul_float32_library():
     w = _bits_from_f32(rng.standard_normal((33, 128)) * 0.02)
     ref = torch.from_numpy(bf16.to_f64(a)) @ torch.from_numpy(bf16.to_f64(w)).T
     assert np.allclose(gemm(a, w, out="f64"), ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_matmul_of_unrounded_rows():
+    """An fp64 left operand is used as is: times W = I it comes back rounded
+    once to bf16 (1/3 is not a bf16 value), and integer rows multiply exactly."""
+    a = np.array([[1.0 / 3.0, -2.5, 1e-3, 7.0]])
+    eye = _bits_from_f32(np.eye(4))
+    assert np.array_equal(matmul(a, eye, out="f64"), a)
+    assert np.array_equal(matmul(a, eye), bf16.from_f64(a))
+    assert matmul(a, eye, out="f64")[0, 0] != bf16.to_f64(bf16.from_f64(a))[0, 0]
+    rng = np.random.default_rng(4)
+    ai = rng.integers(-8, 9, (3, 32)).astype(np.float64)
+    w = rng.integers(-8, 9, (5, 32))
+    exact = [[sum(int(ai[i, t]) * int(w[j, t]) for t in range(32)) for j in range(5)] for i in range(3)]
+    assert np.array_equal(matmul(ai, _bits_from_f32(w), out="f64"), np.array(exact, dtype=np.float64))
 
 
 # ---------------------------------------------------------------- RMSNorm
