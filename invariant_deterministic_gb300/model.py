@@ -247,6 +247,25 @@ class Decoder:
         for li in range(self.s.n_layers):
             self.layer(li, rows, seq_t, pos_t, attention)
 
+    def prefill(self, seq: int, tokens: torch.Tensor, p0: int = 0, chunk: int = 0) -> torch.Tensor:
+        """Prefill ``tokens`` (int32, device) as positions p0.. of sequence
+        ``seq`` in chunks of ``chunk`` rows (0: as large as the buffers allow);
+        returns the last row's final residual stream (a copy).  Any chunking
+        gives the same bits (the kernels' per-row arithmetic does not depend
+        on the rows beside it)."""
+        n = int(tokens.shape[0])
+        chunk = chunk or self.max_rows
+        for c0 in range(0, n, chunk):
+            rows = min(chunk, n - c0)
+            kinv.embed(self.w["embed"], tokens[c0: c0 + rows], out=self.x[:rows])
+            self.prefill_chunk(seq, p0 + c0, rows)
+        return self.x[rows - 1].clone()
+
+    def copy_prefix(self, src: int, dst: int, n: int) -> None:
+        """Sequence dst takes sequence src's cached keys and values for
+        positions 0..n-1 (every layer): a cached prompt prefix, reused."""
+        self.kv[:, :, dst, :n].copy_(self.kv[:, :, src, :n])
+
     def close_residual(self, rows: int) -> torch.Tensor:
         """The last layer's output for rows [0, rows) (the residual stream;
         every layer already added its projections to it)."""
@@ -267,3 +286,38 @@ class _EventPair:
         self.b.record()
         self.timer.setdefault(self.name, []).append((self.a, self.b))
         return False
+
+
+class PrefixCache:
+    """Host-side index of prompt prefixes whose keys and values sit in a
+    Decoder's cache.  The cached rows of a prefix are a function of its tokens
+    alone (batch- and chunk-invariant kernels, causal attention), so a new
+    request sharing the prefix can copy them instead of recomputing them and
+    gets the same bits."""
+
+    def __init__(self, dec: Decoder):
+        self.dec = dec
+        self.entries = {}  # tuple(tokens) -> slot
+
+    def insert(self, tokens, slot: int) -> None:
+        self.entries[tuple(int(t) for t in tokens)] = slot
+
+    def longest(self, tokens):
+        """(slot, n): the longest registered prefix of ``tokens``, or (None, 0)."""
+        toks = tuple(int(t) for t in tokens)
+        best = (None, 0)
+        for key, slot in self.entries.items():
+            n = len(key)
+            if best[1] < n <= len(toks) and toks[:n] == key:
+                best = (slot, n)
+        return best
+
+    def prefill(self, slot: int, tokens: torch.Tensor, chunk: int = 0) -> tuple[int, torch.Tensor]:
+        """Prefill ``tokens`` into ``slot``, starting from the longest cached
+        prefix; returns (reused positions, last row's final residual)."""
+        src, n = self.longest(tokens.tolist())
+        if src is not None and n == tokens.shape[0]:
+            n -= 1  # recompute the last token: its hidden state is the output
+        if src is not None and n > 0 and src != slot:
+            self.dec.copy_prefix(src, slot, n)
+        return n, self.dec.prefill(slot, tokens[n:], p0=n, chunk=chunk)

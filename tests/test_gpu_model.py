@@ -234,3 +234,23 @@ def test_first_step_logits_match_oracle(M):
             t, near = sample_row(logits[r, 0].cpu().numpy(), hist[r], 0, params[r])
             if not near:
                 assert t == int(toks[r, 0])
+
+
+def test_prefix_cache_reuse_gives_the_same_bits(M):
+    """A request whose prompt starts with a cached prefix copies that prefix's
+    keys and values and prefills only the rest: its KV cache and last hidden
+    row equal those of prefilling the whole prompt at once (so everything
+    decoded from them is the same too)."""
+    shape = _shape(M, 2)
+    w = M.random_weights(shape, device="cuda")
+    prompt = synth.uniform_int(1000, 0, shape.vocab - 1, 90).cuda()
+    n_pre = 700
+    dec = M.Decoder(shape, w, max_batch=3, max_len=1100, max_chunk=1000)
+    whole = dec.prefill(0, prompt)                       # slot 0: the whole prompt at once
+    cache = M.PrefixCache(dec)
+    dec.prefill(1, prompt[:n_pre], chunk=256)           # slot 1: the shared prefix, in chunks
+    cache.insert(prompt[:n_pre].tolist(), 1)
+    reused, last = cache.prefill(2, prompt, chunk=128)  # slot 2: prefix from the cache
+    assert reused == n_pre
+    assert_same_bits(last, whole, "last hidden row")
+    assert_same_bits(dec.kv[:, :, 2, :1000], dec.kv[:, :, 0, :1000], "KV cache")
