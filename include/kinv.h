@@ -273,15 +273,22 @@ kinv_status kinv_attn_prefill(const void* q, const void* k_cache, const void* v_
  * key = (seed lo, seed hi)).word0 >> 8) * 2^-24 picks the first kept candidate
  * whose running sum of e exceeds u * (sum of kept e).  The counter is the
  * request's own step, never its batch slot: the drawn token depends only on
- * the row's logits, history, settings and step.  One thread block per row;
- * ranking and thresholds are compare-only on fp32 values; sums in fixed order.
+ * the row's logits, history, settings and step.  A cluster of up to eight
+ * thread blocks shares a row (the count follows the batch size; the token
+ * does not depend on it); ranking and thresholds are compare-only on fp32
+ * values; sums in fixed order.
+ * top_k <= 0 (or >= V) means the whole vocabulary: e is then summed over all
+ * V ids (per 128-id block, blocks in order) and the top-p / min-p cut must
+ * fall within the 1024 most likely ids.
  *
  * logits: device fp32 [B][ld]; params: device kinv_sampling_params [B];
  * history: device int32 [B][hist_ld], row b holding hist_len[b] ids, oldest
  * first; step: device int64 [B]; out_tokens: device int32 [B].
- * Requirements: 1 <= V; ld >= V; top_k in [1, 1024] unless temperature <= 0;
- * hist_len[b] <= hist_ld.  Rows whose settings are outside this set get token
- * -1 and the device status word records KINV_ERR_UNSUPPORTED. */
+ * Requirements: 1 <= V; ld >= V; top_k in [1, 1024] or the whole vocabulary
+ * (V <= 262144, and top_p < 1 or min_p > 0 cutting within the 1024 most
+ * likely ids) unless temperature <= 0; hist_len[b] <= hist_ld.  Rows whose
+ * settings or logits fall outside this set get token -1 and the device status
+ * word records KINV_ERR_UNSUPPORTED. */
 typedef struct {
   float temperature;
   float top_p;

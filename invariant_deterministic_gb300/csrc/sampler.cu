@@ -38,6 +38,7 @@ constexpr int kThreadsS = 512;
 constexpr int kMaxCluster = 8;  // blocks sharing one row, at most
 constexpr int kMaxTopK = 1024;
 constexpr int kCap = 4096;  // candidates gathered before sorting
+constexpr int kMaxBlocks = 2048;  // full-vocabulary mode: 128-id blocks of the row (V <= 262144)
 constexpr int kRounds = 10;  // 16-byte vectors of the row each thread keeps in registers
 constexpr int kRegSpan = kThreadsS * 4 * kRounds;  // ids a block holds in registers
 
@@ -89,6 +90,8 @@ struct Smem {
   uint32_t n_cand;
   // this block's copy of the cluster-wide decisions
   float m_all;
+  float blk[kMaxBlocks];  // full vocabulary: sums of e over 128-id blocks (rank 0: every block)
+  float total_all;
   uint32_t eq_taken;
   uint32_t thresh;
   int k_rem;
@@ -289,8 +292,12 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
     cluster_sync();  // the peers stay until rank 0 has read them
     return;
   }
-  const int k = (prm.top_k <= 0 || prm.top_k >= V) ? V : prm.top_k;
-  if (k > kMaxTopK) {
+  // Full vocabulary (no top-k) over more than kMaxTopK ids: the top kMaxTopK
+  // are gathered as candidates and the softmax total runs over the whole row;
+  // the top-p / min-p cut must fall inside those candidates.
+  const bool full = (prm.top_k <= 0 || prm.top_k >= V) && V > kMaxTopK;
+  const int k = full ? kMaxTopK : ((prm.top_k <= 0 || prm.top_k >= V) ? V : prm.top_k);
+  if (k > kMaxTopK || (full && (V + 127) / 128 > kMaxBlocks)) {
     if (rank == 0 && t == 0) {
       out[b] = -1;
       if (status) atomicExch(status, DEV_SAMPLER_UNSUPPORTED);
@@ -494,7 +501,28 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
       __syncthreads();
     }
   }
-  cluster_sync();  // every block's candidates are parked
+  if (full) {
+    // e = exp(z / T - z_max / T) summed over each 128-id block of this block's
+    // share: lane l takes ids 4l .. 4l + 3 of the block in order, then a fixed
+    // butterfly -- the same for any number of blocks per row
+    const float s0 = __fdiv_rn(sm.m_all, temp);
+    for (int blk = v0 / 128 + warp; blk * 128 < v1; blk += kWarps) {
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = blk * 128 + 4 * lane + e;
+        if (i < V) {
+          float z = penalised(row, i, bitmap, r);
+          if (isnan(z)) z = -INFINITY;
+          acc = __fadd_rn(acc, expf(__fsub_rn(__fdiv_rn(z, temp), s0)));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+      if (lane == 0) sm.blk[blk - v0 / 128] = acc;
+    }
+  }
+  cluster_sync();  // every block's candidates (and block sums) are parked
   if (rank == 0) {
     // rank 0 appends the peers' candidates after its own
     if (t == 0) {
@@ -505,6 +533,26 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
         off += ld_dsmem_u32(peer(&sm.n_cand, q));
       }
       sm.offs[C] = off;
+    }
+    if (full) {
+      // every block sum of the row, in block order (own blocks are in place)
+      const int nblk = (V + 127) / 128;
+      for (int q = 1; q < C && q * chunk < V; ++q) {
+        const int b0 = q * chunk / 128, b1 = min(nblk, (min(V, q * chunk + chunk) + 127) / 128);
+        const uint32_t src = peer(&sm.blk[0], q);
+        for (int i = b0 + t; i < b1; i += kThreadsS) sm.blk[i] = ld_dsmem_f32(src + 4u * (i - b0));
+      }
+    }
+    __syncthreads();
+    if (full && warp == 0) {
+      // the row's total: lane l adds blocks l, l + 32, ... in order, then a
+      // fixed butterfly (the shape depends on V only)
+      const int nblk = (V + 127) / 128;
+      float acc = 0.f;
+      for (int i = lane; i < nblk; i += 32) acc = __fadd_rn(acc, sm.blk[i]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+      if (lane == 0) sm.total_all = acc;
     }
     __syncthreads();
     for (int q = 1; q < C; ++q) {
@@ -573,16 +621,27 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
     }
     return n;
   };
-  const float total = P[kk - 1];
+  const float total = full ? sm.total_all : P[kk - 1];
   int keep = kk;
+  bool cut = false;  // full vocabulary: did a filter end inside the candidates?
   if (prm.top_p < 1.0f) {
     const float target = __fmul_rn(prm.top_p, total);
     const int i = first(kk, [&](int j) { return P[j] >= target; });
     keep = i < kk ? i + 1 : kk;
+    cut = i < kk;
   }
   if (prm.min_p > 0.0f) {
     const int n = first(keep, [&](int j) { return !(sm.e[j] >= prm.min_p); });
+    cut = cut || n < keep;
     keep = n > 0 ? n : 1;
+  }
+  if (full && !cut) {
+    // the kept set may reach past the candidates: not supported
+    if (lane == 0) {
+      out[b] = -1;
+      if (status) atomicExch(status, DEV_SAMPLER_UNSUPPORTED);
+    }
+    return;
   }
   const float kept = P[keep - 1];
   const uint64_t st = static_cast<uint64_t>(step[b]);

@@ -33,7 +33,11 @@ within a margin of a boundary is reported as a near tie, and token parity is
 not asserted for such a row.  The margin (relative to the sum) bounds the
 kernel's fp32 error: a sequential sum of k terms below 1 is off by at most
 k * 2^-24 relative, and each exponential by a few units in the last place, so
-``tie_tol(k) = 1e-5 + k * 6e-8``.
+``tie_tol(k) = 1e-5 + k * 6e-8``.  Over the whole vocabulary (no top-k) the
+kernel still forms its running sums over at most 1024 ranked candidates, and
+the whole-row total per 128-id block and then in 32 strided runs of blocks,
+so k is the candidate count (at most 1024) and the total adds
+``whole_sum_tol(V)`` more.
 """
 from __future__ import annotations
 
@@ -46,6 +50,16 @@ from .philox import sampler_uniform
 
 def tie_tol(k: int) -> float:
     return 1e-5 + k * 6e-8
+
+
+def whole_sum_tol(v: int) -> float:
+    """Relative error bound of an fp32 sum of v terms taken as 128-term blocks
+    (4 in order per lane, then a 32-lane butterfly) and then 32 strided runs of
+    blocks added in order and by a butterfly: one rounding per addition along
+    the longest chain."""
+    blocks = (v + 127) // 128
+    chain = 4 + 5 + (blocks + 31) // 32 + 5
+    return chain * 2.0 ** -24
 
 
 @dataclass
@@ -86,7 +100,8 @@ def sample_row(logits_f32: np.ndarray, history, step: int, p: SamplingParams):
         order = order[:k]
     s = (z[order] / t).astype(np.float64)          # fp32 division, widened exactly
     e = np.exp(s - s[0])
-    tol = tie_tol(len(order))
+    whole = len(order) > 1024
+    tol = tie_tol(min(len(order), 1024)) + (whole_sum_tol(v) if whole else 0.0)
     near = False
     keep = len(order)
     if p.top_p < 1.0:

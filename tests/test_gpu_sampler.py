@@ -142,3 +142,50 @@ def test_unsupported_top_k_reports_status(kinv):
     assert got[0] == -1 and got[1] >= 0
     assert kinv.last_device_status() == kinv.ERR_UNSUPPORTED
     assert kinv.last_device_status() == 0
+
+
+def _peaked(rows, vocab, seed, boost=12.0, n_top=20):
+    """N(0, 1.3) logits with n_top ids per row raised by `boost`: the top-p /
+    min-p cut falls among those ids even over the whole vocabulary."""
+    g = synth.gen(seed)
+    logits = torch.randn(rows, vocab, generator=g) * 1.3
+    for b in range(rows):
+        ids = torch.randint(0, vocab, (n_top,), generator=g)
+        logits[b, ids] += boost + torch.rand(n_top, generator=g) * 2.0
+    return logits.cuda()
+
+
+@pytest.mark.parametrize("top_k,top_p,min_p", [(0, 0.9, 0.0), (-1, 1.0, 0.05), (0, 0.95, 0.02)])
+def test_whole_vocabulary_top_p_min_p(kinv, top_k, top_p, min_p):
+    """top_k <= 0 samples over all 151936 ids (softmax total over the whole
+    row); tokens match the oracle away from near ties, and a row's token does
+    not depend on the batch (the number of blocks sharing a row follows it)."""
+    vocab, bsz = 151936, 32
+    logits = _peaked(bsz, vocab, 80)
+    plist = [kinv.SamplingParams(temperature=0.8, top_k=top_k, top_p=top_p, min_p=min_p,
+                                 repeat_penalty=1.1, repeat_last_n=64, seed=900 + b) for b in range(bsz)]
+    hists = [list(range(10 * b, 10 * b + 30)) for b in range(bsz)]
+    steps = list(range(bsz))
+    got = _run(kinv, logits, plist, hists, steps)
+    ref, ties = _oracle(logits, plist, hists, steps)
+    assert (got >= 0).all()
+    assert ties.sum() <= bsz // 4, f"{ties.sum()} near ties"
+    assert np.array_equal(got[~ties], ref[~ties]), np.nonzero(got != ref)
+    for b in (0, 17):
+        one = _run(kinv, logits[b: b + 1].contiguous(), plist[b: b + 1], hists[b: b + 1], steps[b: b + 1])
+        assert one[0] == got[b]
+    assert kinv.last_device_status() == 0
+
+
+def test_whole_vocabulary_cut_beyond_the_candidates_is_unsupported(kinv):
+    """Flat logits: top-p 0.95 over the whole vocabulary would keep most of it,
+    past the 1024 ranked candidates -- token -1 and the unsupported status; the
+    peaked row beside it is sampled."""
+    vocab = 151936
+    logits = torch.cat([torch.zeros(1, vocab), _peaked(1, vocab, 81).cpu()]).cuda()
+    p = [kinv.SamplingParams(top_k=0, top_p=0.95, min_p=0.0, seed=1),
+         kinv.SamplingParams(top_k=0, top_p=0.95, min_p=0.0, seed=2)]
+    got = _run(kinv, logits, p, [[], []], [0, 0])
+    assert got[0] == -1 and got[1] >= 0
+    assert kinv.last_device_status() == kinv.ERR_UNSUPPORTED
+    assert kinv.last_device_status() == 0
