@@ -803,7 +803,6 @@ kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, vo
   a.ld_resid = resid ? fu->ld_resid : 0;
   a.ss_out = resid ? fu->ss_out : nullptr;
   switch (p.bn) {
-    case 64: return launch_gemm<64>(ta, tw, a, p.smem_budget, grid_y, grid_z, stream);
     case 128: return launch_gemm<128>(ta, tw, a, p.smem_budget, grid_y, grid_z, stream);
     default: return KINV_ERR_UNSUPPORTED;
   }

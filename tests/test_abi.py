@@ -57,6 +57,24 @@ def test_host_validation_without_gpu(lib):
     assert L.kinv_gemm(fake + 2, 64, fake, 64, fake, 64, 0, 4, 64, 64, None) == lib.ERR_ALIGNMENT
     assert L.kinv_gemm(None, 64, fake, 64, fake, 64, 0, 4, 64, 64, None) == lib.ERR_INVALID_ARG
     assert L.kinv_gemm(fake, 64, fake, 64, fake, 64, 0, 0, 64, 64, None) == lib.OK  # M = 0
+    # folded RMSNorm options: residual output needs N % 128 and sums; row scale needs its shape
+    import ctypes
+    resid = lib.GemmFusion(resid=fake, ld_resid=192, ss_out=fake)
+    assert L.kinv_gemm_fused(fake, 64, fake, 64, None, 0, 0, 4, 192, 64, ctypes.byref(resid),
+                             None) == lib.ERR_UNSUPPORTED
+    no_ss = lib.GemmFusion(resid=fake, ld_resid=256, ss_out=None)
+    assert L.kinv_gemm_fused(fake, 64, fake, 64, None, 0, 0, 4, 256, 64, ctypes.byref(no_ss),
+                             None) == lib.ERR_INVALID_ARG
+    bad_norm = lib.GemmFusion(row_ss=fake, row_ss_tiles=0, norm_dim=256, eps=1e-6)
+    assert L.kinv_gemm_fused(fake, 64, fake, 64, fake, 256, 0, 4, 256, 64, ctypes.byref(bad_norm),
+                             None) == lib.ERR_INVALID_ARG
+    assert L.kinv_gemm_swiglu(fake, 64, fake, 64, fake, 64, 4, 96, 64, None, None) == lib.ERR_UNSUPPORTED
+    assert L.kinv_gemm_swiglu(fake, 64, fake, 64, fake, 64, 4, 128, 64, ctypes.byref(resid),
+                              None) == lib.ERR_INVALID_ARG
+    assert L.kinv_gemm_qkv_rope(fake, 64, fake, 64, fake, fake, fake, 0, 96, fake, fake, None, None,
+                                1e-6, 4, 2, 1, 96, 64, 1e4, None, None) == lib.ERR_UNSUPPORTED
+    assert L.kinv_row_sumsq(fake, 100, 4, 100, fake, None) == lib.ERR_UNSUPPORTED
+    assert L.kinv_row_sumsq(fake, 64, 4, 128, fake, None) == lib.ERR_INVALID_ARG  # ldx < dim
     # RMSNorm
     assert L.kinv_rmsnorm(fake, 100, None, fake, fake, 100, 2, 100, 1e-6, None) == lib.ERR_UNSUPPORTED
     assert L.kinv_rmsnorm(fake, 64, None, fake, fake, 64, 2, 64, -1.0, None) == lib.ERR_INVALID_ARG
