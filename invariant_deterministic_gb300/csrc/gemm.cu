@@ -45,6 +45,7 @@ constexpr int BK = 64;  // one 128-byte swizzle row of bf16
 constexpr int kGemmThreads = 128;
 constexpr int A_STAGE = BM * BK * 2;
 constexpr int kRopeTabRows = 4;  // owned rows up to which the RoPE angles are formed ahead
+constexpr int kPushMaxRows = 32;  // split-K tiles of more rows have the owners pull the partials
 
 // tcgen05 instruction descriptor, kind::f16: fp32 accumulate (bits 4-5 = 1),
 // A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major, N >> 3 at bits
@@ -109,6 +110,7 @@ struct GemmArgs {
   int stages;
   int splits;
   int own_rows;  // split-K: rows a rank owns at most (ceil(a_rows / splits))
+  int pull;      // split-K with many rows: owners read the partials (coalesced) instead of receiving them
   int ring_bytes;  // the stage ring, or more when the epilogue's receive slots need it
   int* status;
   RopeEpilogue rope;
@@ -224,7 +226,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // split-K RoPE epilogue with few owned rows (decode): what it needs is
   // gathered by the otherwise idle warps 2 and 3 while the weights stream
-  const bool use_pre = args.rope.on && args.splits > 1 && args.own_rows <= kRopeTabRows;
+  const bool use_pre = args.rope.on && args.splits > 1 && !args.pull && args.own_rows <= kRopeTabRows;
   RopePre pre{};
   unsigned char* tail = reinterpret_cast<unsigned char*>(tmem_slot + 4);
   if (use_pre) {
@@ -492,6 +494,112 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         rope_dispatch<BN>(stage, nullptr, rows_here, n0, args.M, args.rope, row_of);
       }
     }
+  } else if (args.pull) {
+    // Constant split-K, many rows: every rank stages its fp32 partial rows in
+    // its own (idle) ring; after a cluster barrier the owner of row m (rank
+    // m % splits) reads that row from every rank -- a warp per row, lane l
+    // taking columns 4l .. 4l + 3 -- and adds them in rank order.  The
+    // arithmetic of every output is the push path's below, so a row's bits do
+    // not depend on which path its M took.
+    if constexpr (BN == kGemmThreads) {
+      constexpr int LDP = BN + 4;  // padded row of the staged partials (floats)
+      float* part = reinterpret_cast<float*>(base);  // this rank's MMAs are done: its ring is idle
+      if (warp * 32 < rows_here) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + c0, r);
+          if (row_local < rows_here) {
+#pragma unroll
+            for (int q = 0; q < 32; q += 4)
+              *reinterpret_cast<uint4*>(part + row_local * LDP + c0 + q) = make_uint4(r[q], r[q + 1], r[q + 2], r[q + 3]);
+          }
+        }
+      }
+      cluster_sync();  // every rank's partials are staged
+      const int owned = rank < rows_here ? (rows_here - rank + splits - 1) / splits : 0;
+      __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(part + args.a_rows * LDP);  // rope rows
+      for (int i = warp; i < owned && good; i += kGemmThreads / 32) {
+        const int ml = i * splits + rank;
+        const int mm = m0 + ml;
+        const uint32_t off = smem_addr(part + ml * LDP + 4 * lane);
+        float4 acc = ld_dsmem_v4(map_to_rank(off, 0));
+        for (int q = 1; q < splits; ++q) {
+          const float4 v = ld_dsmem_v4(map_to_rank(off, q));
+          acc.x = __fadd_rn(acc.x, v.x);
+          acc.y = __fadd_rn(acc.y, v.y);
+          acc.z = __fadd_rn(acc.z, v.z);
+          acc.w = __fadd_rn(acc.w, v.w);
+        }
+        float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+        if (args.row_ss) {
+          const float inv = row_inv[ml];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) a4[e] = __fmul_rn(a4[e], inv);
+        }
+        if (args.swiglu) {
+          // lanes 0..15 hold gate columns 4l.., lanes 16..31 the matching up columns
+          float u4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) u4[e] = __shfl_down_sync(0xffffffffu, a4[e], 16);
+          if (lane < 16) {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.C) + mm * args.ldc + n0 / 2 + 4 * lane;
+            *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(silu_times(a4[0], u4[0]), silu_times(a4[1], u4[1])),
+                                                        pack_bf16(silu_times(a4[2], u4[2]), silu_times(a4[3], u4[3])));
+          }
+        } else if (args.resid) {
+          __nv_bfloat16* xp = args.resid + mm * args.ld_resid + n0 + 4 * lane;
+          const uint2 xv = *reinterpret_cast<const uint2*>(xp);
+          float sv[4];
+          sv[0] = residual_add(xv.x & 0xFFFFu, a4[0]);
+          sv[1] = residual_add(xv.x >> 16, a4[1]);
+          sv[2] = residual_add(xv.y & 0xFFFFu, a4[2]);
+          sv[3] = residual_add(xv.y >> 16, a4[3]);
+          *reinterpret_cast<uint2*>(xp) = make_uint2(pack_bf16(sv[0], sv[1]), pack_bf16(sv[2], sv[3]));
+          // the push path's per-warp butterfly over columns 32w .. 32w + 31
+          // (xor 16, 8, 4, 2, 1 on the column index) in this layout: column
+          // 4l + e -> lane bits 2..0 and element bits 1..0
+          float q4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) q4[e] = __fmul_rn(sv[e], sv[e]);
+#pragma unroll
+          for (int o = 4; o > 0; o >>= 1) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) q4[e] = __fadd_rn(q4[e], __shfl_xor_sync(0xffffffffu, q4[e], o));
+          }
+          {
+            const float t0 = __fadd_rn(q4[0], q4[2]), t1 = __fadd_rn(q4[1], q4[3]);
+            q4[0] = __fadd_rn(t0, t1);
+          }
+          // group totals at lanes 0, 8, 16, 24; then the four groups in order
+          const float g1 = __shfl_sync(0xffffffffu, q4[0], 8);
+          const float g2 = __shfl_sync(0xffffffffu, q4[0], 16);
+          const float g3 = __shfl_sync(0xffffffffu, q4[0], 24);
+          if (lane == 0)
+            args.ss_out[static_cast<int64_t>(mm) * (args.N / BN) + n0 / BN] =
+                __fadd_rn(__fadd_rn(__fadd_rn(q4[0], g1), g2), g3);
+        } else if (args.rope.on) {
+          *reinterpret_cast<uint2*>(stage + i * BN + 4 * lane) =
+              make_uint2(pack_bf16(a4[0], a4[1]), pack_bf16(a4[2], a4[3]));
+        } else if (args.c_f32) {
+          if (n0 + 4 * lane < args.N)
+            *reinterpret_cast<float4*>(static_cast<float*>(args.C) + mm * args.ldc + n0 + 4 * lane) =
+                make_float4(a4[0], a4[1], a4[2], a4[3]);
+        } else {
+          if (n0 + 4 * lane < args.N)
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(args.C) + mm * args.ldc + n0 + 4 * lane) =
+                make_uint2(pack_bf16(a4[0], a4[1]), pack_bf16(a4[2], a4[3]));
+        }
+      }
+      if (args.rope.on) {
+        __syncthreads();
+        if (good) {
+          auto row_of = [&](int r) { return m0 + r * splits + rank; };
+          rope_dispatch<BN>(stage, nullptr, owned, n0, args.M, args.rope, row_of);
+        }
+      }
+      cluster_sync();  // every owner has read its rows: the peers may leave
+    }
   } else {
     // Constant split-K.  Rank r pushes row m of its partial tile into slot r of
     // the owner rank m % splits (row index m / splits there; the owner's own
@@ -693,10 +801,15 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a
   // it), and the 128 rows one MMA reads from the start of the last A block
   // must stay inside the block's shared memory.
   a.own_rows = (a.a_rows + a.splits - 1) / a.splits;
-  // split-K receive slots, plus the staged bf16 rows of the RoPE epilogue
-  const int recv_bytes = a.splits > 1 ? a.splits * a.own_rows * BN * 4 +
+  // split-K with many rows: owners pull the partials (coalesced reads) from
+  // rows staged in each rank's ring; otherwise ranks push into receive slots
+  a.pull = a.splits > 1 && a.a_rows > kPushMaxRows && BN == kGemmThreads ? 1 : 0;
+  // split-K receive slots (or the staged partial rows), plus the staged bf16
+  // rows of the RoPE epilogue
+  const int recv_bytes = a.pull ? a.a_rows * (BN + 4) * 4 + (a.rope.on ? a.own_rows * BN * 2 : 0)
+                         : a.splits > 1 ? a.splits * a.own_rows * BN * 4 +
                                             (a.rope.on ? a.own_rows * BN * 2 : 0)
-                                      : (a.rope.on ? a.a_rows * BN * 2 : 0);
+                                        : (a.rope.on ? a.a_rows * BN * 2 : 0);
   const int cap = ring_cap(static_cast<long long>(a.splits) * grid_y * grid_z);
   const int limit = budget < cap ? budget : cap;
   const int stage = a.a_blk * a.j + BN * BK * 2 * a.j;
@@ -706,10 +819,10 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a
   a.stages = stages;
   // the epilogue's receive slots reuse the ring and may run past it
   a.ring_bytes = stages * stage > recv_bytes ? stages * stage : (recv_bytes + 15) / 16 * 16;
-  const int tab_bytes = (a.rope.on && a.splits > 1 && a.own_rows <= kRopeTabRows
+  const int tab_bytes = (a.rope.on && a.splits > 1 && !a.pull && a.own_rows <= kRopeTabRows
                              ? rope_pre_bytes(a.own_rows, a.rope.D, BN)
                              : 0) +
-                        (a.row_ss ? BM * 4 : 0) + (a.resid && a.splits > 1 ? a.own_rows * 16 : 0);
+                        (a.row_ss ? BM * 4 : 0) + (a.resid && a.splits > 1 && !a.pull ? a.own_rows * 16 : 0);
   const size_t smem = smem_bytes(stages, a.ring_bytes, tab_bytes);
   if (smem > static_cast<size_t>(max_smem_optin())) return KINV_ERR_UNSUPPORTED;
   // the opt-in limit is raised once per device to the largest request seen
@@ -791,6 +904,7 @@ kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, vo
   a.stages = 0;
   a.splits = p.splits;
   a.own_rows = 0;
+  a.pull = 0;
   a.ring_bytes = 0;
   a.status = device_status_word();
   a.rope = rope ? *rope : RopeEpilogue{};
