@@ -46,6 +46,10 @@ constexpr int kGemmThreads = 128;
 constexpr int A_STAGE = BM * BK * 2;
 constexpr int kRopeTabRows = 4;  // owned rows up to which the RoPE angles are formed ahead
 constexpr int kPushMaxRows = 32;  // split-K tiles of more rows have the owners pull the partials
+constexpr int kMaxSplits = 8;     // K splits (cluster size) at most
+// mbarriers after the ring: full and empty per stage, done, recv, and one
+// "ready" per K-split rank (push path)
+__host__ __device__ constexpr int bar_count(int stages) { return 2 * stages + 2 + kMaxSplits; }
 
 // tcgen05 instruction descriptor, kind::f16: fp32 accumulate (bits 4-5 = 1),
 // A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major, N >> 3 at bits
@@ -222,7 +226,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // over the stage ring (idle by then in every rank of the cluster)
   float* recv = reinterpret_cast<float*>(base);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + args.ring_bytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + bar_count(stages));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // split-K RoPE epilogue with few owned rows (decode): what it needs is
   // gathered by the otherwise idle warps 2 and 3 while the weights stream
@@ -239,10 +243,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   float* row_inv = reinterpret_cast<float*>(tail);  // [BM] when row_ss is given
   if (args.row_ss) tail += BM * 4;
   float* red4 = reinterpret_cast<float*>(tail);     // [own_rows][4] for the split residual
+  const bool push = args.splits > 1 && !args.pull;
+  // the residual rows a rank owns in the push path ([own_rows][BN] bf16),
+  // read while the weights stream
+  const bool use_resid_pre = push && args.resid != nullptr;
+  uint16_t* resid_pre = reinterpret_cast<uint16_t*>(red4 + (use_resid_pre ? args.own_rows * 4 : 0));
   auto full_bar = [&](int s) { return smem_addr(bars + s); };
   auto empty_bar = [&](int s) { return smem_addr(bars + stages + s); };
   const uint32_t done_bar = smem_addr(bars + 2 * stages);
   const uint32_t recv_bar = smem_addr(bars + 2 * stages + 1);
+  // ready_bar(q) completes when rank q's MMAs are done (its ring may take partials)
+  auto ready_bar = [&](int q) { return smem_addr(bars + 2 * stages + 2 + q); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int splits = args.splits;
@@ -262,6 +273,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(done_bar, 1);
     mbar_init(recv_bar, 1);
+    if (push)
+      for (int q = 0; q < splits; ++q) mbar_init(ready_bar(q), 1);
     *abort_flag = 0;
     fence_mbar_init();
     if (splits > 1) {
@@ -275,6 +288,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // push path: the peers' barriers are initialised before any remote arrive
+  // or store reaches them (the matching wait comes at the epilogue)
+  if (push) cluster_arrive_relaxed();
 
   int issued = 0;
   if (warp == 0) {
@@ -373,6 +389,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       row_inv[r] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(acc, static_cast<float>(args.norm_dim)),
                                                        args.eps)));
     }
+  }
+
+  if (use_resid_pre && warp >= 2) {
+    // the residual rows this rank owns (written by earlier kernels)
+    pdl_wait();
+    constexpr int CH = BN / 8;  // 16-byte chunks per row
+    const int owned = rank < rows_here ? (rows_here - rank + splits - 1) / splits : 0;
+    for (int idx = threadIdx.x - 64; idx < owned * CH; idx += 64) {
+      const int i = idx / CH, c = idx % CH;
+      const __nv_bfloat16* src = args.resid + static_cast<int64_t>(m0 + i * splits + rank) * args.ld_resid + n0 + c * 8;
+      *reinterpret_cast<uint4*>(resid_pre + i * BN + c * 8) = *reinterpret_cast<const uint4*>(src);
+    }
+  }
+
+  // push path: the peers' barriers are initialised (every rank arrived at its
+  // start), waited for here, before the MMAs finish
+  if (push) {
+    __syncwarp();
+    cluster_wait();
   }
 
   // ---- epilogue
@@ -604,9 +639,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // Constant split-K.  Rank r pushes row m of its partial tile into slot r of
     // the owner rank m % splits (row index m / splits there; the owner's own
     // rows are plain local stores); once all slots of its rows are in, the
-    // owner adds them in rank order and stores.
-    // every rank's MMAs have drained its ring (and its receive barrier is set)
-    cluster_sync();
+    // owner adds them in rank order and stores.  The slots overlay the
+    // owner's ring: a row goes out once the owner has announced (ready_bar)
+    // that its MMAs are done.
+    if (warp == 0 && lane < splits) mbar_arrive_cluster_relaxed(map_to_rank(ready_bar(rank), lane));
     const int own_rows = args.own_rows;
     if (warp * 32 < rows_here) {
       const bool row_ok = row_local < rows_here;
@@ -614,17 +650,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       float* dst_local = recv + (rank * own_rows + (row_ok ? row_local / splits : 0)) * BN;
       const uint32_t dst_base = map_to_rank(smem_addr(dst_local), owner);
       const uint32_t dst_bar = map_to_rank(recv_bar, owner);
+      bool can = true;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(lane_base + c0, r);
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        uint32_t r[64];
+        tmem_ld64(lane_base + c0, r);
+        if (c0 == 0 && row_ok && owner != rank)
+          can = mbar_wait_cluster_relaxed_bounded(ready_bar(owner), 0, args.status, DEV_TIMEOUT_GEMM_EPILOGUE);
+        if (!can) continue;
         if (row_ok && owner == rank) {
 #pragma unroll
-          for (int q = 0; q < 32; q += 4)
+          for (int q = 0; q < 64; q += 4)
             *reinterpret_cast<uint4*>(dst_local + c0 + q) = make_uint4(r[q], r[q + 1], r[q + 2], r[q + 3]);
         } else if (row_ok) {
 #pragma unroll
-          for (int q = 0; q < 32; q += 4)
+          for (int q = 0; q < 64; q += 4)
             st_async_v4(dst_base + (c0 + q) * 4, r[q], r[q + 1], r[q + 2], r[q + 3], dst_bar);
         }
       }
@@ -665,7 +705,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int q = 1; q < splits; ++q) acc = __fadd_rn(acc, src[q * slot]);
             const int mm = m0 + i * splits + rank;
             __nv_bfloat16* xp = args.resid + mm * args.ld_resid + n0 + col;
-            const float sv = residual_add(*reinterpret_cast<const uint16_t*>(xp), acc);
+            const float sv = residual_add(resid_pre[i * BN + col], acc);
             *xp = __float2bfloat16_rn(sv);
             float sq = __fmul_rn(sv, sv);
 #pragma unroll
@@ -708,6 +748,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   // ---- teardown
+  if (push && warp == 0 && lane < splits) {
+    // no peer may still be about to arrive on this block's barriers
+    mbar_wait_cluster_relaxed_bounded(ready_bar(lane), 0, args.status, DEV_TIMEOUT_GEMM_EPILOGUE);
+  }
   if (*abort_flag && warp == 0 && lane == 0) {
     // give loads still in flight a bounded chance to land before the block exits
     for (int kt = issued - stages > 0 ? issued - stages : 0; kt < issued; ++kt)
@@ -788,7 +832,7 @@ int ring_cap(long long ctas) {
 }
 
 size_t smem_bytes(int stages, int ring_bytes, int tab_bytes) {
-  return 1024 + static_cast<size_t>(ring_bytes) + (2 * stages + 2) * 8 + 16 + tab_bytes;
+  return 1024 + static_cast<size_t>(ring_bytes) + bar_count(stages) * 8 + 16 + tab_bytes;
 }
 
 template <int BN>
@@ -810,7 +854,15 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a
                          : a.splits > 1 ? a.splits * a.own_rows * BN * 4 +
                                             (a.rope.on ? a.own_rows * BN * 2 : 0)
                                         : (a.rope.on ? a.a_rows * BN * 2 : 0);
-  const int cap = ring_cap(static_cast<long long>(a.splits) * grid_y * grid_z);
+  // what the block keeps after the ring and its barriers: the RoPE inputs,
+  // 1/rms per row, the split residual's partial sums and its residual rows
+  const bool push = a.splits > 1 && !a.pull;
+  const int tab_bytes = (a.rope.on && push && a.own_rows <= kRopeTabRows
+                             ? rope_pre_bytes(a.own_rows, a.rope.D, BN)
+                             : 0) +
+                        (a.row_ss ? BM * 4 : 0) +
+                        (a.resid && push ? a.own_rows * 16 + a.own_rows * BN * 2 : 0);
+  const int cap = ring_cap(static_cast<long long>(a.splits) * grid_y * grid_z) - tab_bytes;
   const int limit = budget < cap ? budget : cap;
   const int stage = a.a_blk * a.j + BN * BK * 2 * a.j;
   int stages = limit / stage;
@@ -819,10 +871,6 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a
   a.stages = stages;
   // the epilogue's receive slots reuse the ring and may run past it
   a.ring_bytes = stages * stage > recv_bytes ? stages * stage : (recv_bytes + 15) / 16 * 16;
-  const int tab_bytes = (a.rope.on && a.splits > 1 && !a.pull && a.own_rows <= kRopeTabRows
-                             ? rope_pre_bytes(a.own_rows, a.rope.D, BN)
-                             : 0) +
-                        (a.row_ss ? BM * 4 : 0) + (a.resid && a.splits > 1 && !a.pull ? a.own_rows * 16 : 0);
   const size_t smem = smem_bytes(stages, a.ring_bytes, tab_bytes);
   if (smem > static_cast<size_t>(max_smem_optin())) return KINV_ERR_UNSUPPORTED;
   // the opt-in limit is raised once per device to the largest request seen
