@@ -47,9 +47,10 @@ constexpr int A_STAGE = BM * BK * 2;
 constexpr int kRopeTabRows = 4;  // owned rows up to which the RoPE angles are formed ahead
 constexpr int kPushMaxRows = 32;  // split-K tiles of more rows have the owners pull the partials
 constexpr int kMaxSplits = 8;     // K splits (cluster size) at most
-// mbarriers after the ring: full and empty per stage, done, recv, and one
-// "ready" per K-split rank (push path)
-__host__ __device__ constexpr int bar_count(int stages) { return 2 * stages + 2 + kMaxSplits; }
+// mbarriers after the ring: full and empty per stage, done, recv, one
+// "ready" per K-split rank (push path), "read" (pull path) and a spare that
+// keeps the count even (what follows them must stay 16-byte aligned)
+__host__ __device__ constexpr int bar_count(int stages) { return 2 * stages + 4 + kMaxSplits; }
 
 // tcgen05 instruction descriptor, kind::f16: fp32 accumulate (bits 4-5 = 1),
 // A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major, N >> 3 at bits
@@ -232,7 +233,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // gathered by the otherwise idle warps 2 and 3 while the weights stream
   const bool use_pre = args.rope.on && args.splits > 1 && !args.pull && args.own_rows <= kRopeTabRows;
   RopePre pre{};
-  unsigned char* tail = reinterpret_cast<unsigned char*>(tmem_slot + 4);
+  // the tables after the barriers take 16-byte vector accesses
+  unsigned char* tail = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(tmem_slot + 4) + 15) & ~static_cast<uintptr_t>(15));
   if (use_pre) {
     pre.pos = reinterpret_cast<int*>(tail);
     pre.seq = pre.pos + args.own_rows;
@@ -254,6 +257,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t recv_bar = smem_addr(bars + 2 * stages + 1);
   // ready_bar(q) completes when rank q's MMAs are done (its ring may take partials)
   auto ready_bar = [&](int q) { return smem_addr(bars + 2 * stages + 2 + q); };
+  // read_bar completes when every rank has read this rank's staged rows (pull path)
+  const uint32_t read_bar = smem_addr(bars + 2 * stages + 2 + kMaxSplits);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int splits = args.splits;
@@ -275,6 +280,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(recv_bar, 1);
     if (push)
       for (int q = 0; q < splits; ++q) mbar_init(ready_bar(q), 1);
+    if (splits > 1 && args.pull) mbar_init(read_bar, splits);
     *abort_flag = 0;
     fence_mbar_init();
     if (splits > 1) {
@@ -626,14 +632,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 make_uint2(pack_bf16(a4[0], a4[1]), pack_bf16(a4[2], a4[3]));
         }
       }
-      if (args.rope.on) {
-        __syncthreads();
-        if (good) {
-          auto row_of = [&](int r) { return m0 + r * splits + rank; };
-          rope_dispatch<BN>(stage, nullptr, owned, n0, args.M, args.rope, row_of);
-        }
+      __syncthreads();  // this rank's reads of the peers' rows are done
+      if (warp == 0 && lane < splits) mbar_arrive_cluster_relaxed(map_to_rank(read_bar, lane));
+      if (args.rope.on && good) {
+        auto row_of = [&](int r) { return m0 + r * splits + rank; };
+        rope_dispatch<BN>(stage, nullptr, owned, n0, args.M, args.rope, row_of);
       }
-      cluster_sync();  // every owner has read its rows: the peers may leave
     }
   } else {
     // Constant split-K.  Rank r pushes row m of its partial tile into slot r of
@@ -752,6 +756,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // no peer may still be about to arrive on this block's barriers
     mbar_wait_cluster_relaxed_bounded(ready_bar(lane), 0, args.status, DEV_TIMEOUT_GEMM_EPILOGUE);
   }
+  if (splits > 1 && args.pull && threadIdx.x == 0) {
+    // every rank has read this block's staged rows (and will not touch it again)
+    mbar_wait_cluster_relaxed_bounded(read_bar, 0, args.status, DEV_TIMEOUT_GEMM_EPILOGUE);
+  }
   if (*abort_flag && warp == 0 && lane == 0) {
     // give loads still in flight a bounded chance to land before the block exits
     for (int kt = issued - stages > 0 ? issued - stages : 0; kt < issued; ++kt)
@@ -832,7 +840,7 @@ int ring_cap(long long ctas) {
 }
 
 size_t smem_bytes(int stages, int ring_bytes, int tab_bytes) {
-  return 1024 + static_cast<size_t>(ring_bytes) + bar_count(stages) * 8 + 16 + tab_bytes;
+  return 1024 + static_cast<size_t>(ring_bytes) + bar_count(stages) * 8 + 16 + 16 + tab_bytes;
 }
 
 template <int BN>
