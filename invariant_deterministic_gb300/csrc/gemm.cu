@@ -51,6 +51,7 @@ constexpr int kMaxSplits = 8;     // K splits (cluster size) at most
 // "ready" per K-split rank (push path), "read" (pull path) and a spare that
 // keeps the count even (what follows them must stay 16-byte aligned)
 __host__ __device__ constexpr int bar_count(int stages) { return 2 * stages + 4 + kMaxSplits; }
+static_assert(bar_count(1) % 2 == 0 && bar_count(2) % 2 == 0, "an even barrier count keeps the tables 16-byte aligned");
 
 // tcgen05 instruction descriptor, kind::f16: fp32 accumulate (bits 4-5 = 1),
 // A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major, N >> 3 at bits
