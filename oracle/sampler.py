@@ -1,17 +1,21 @@
 """The seeded sampler (test infrastructure only).
 
 Follows Kinetic "Receipts", *Making a receipt*: a receipt records every sampler
-setting -- temperature, top_k, top_p, min_p, repeat_penalty, repeat_last_n --
-and the seed; a request without a seed gets a fresh one that is recorded.  The
+setting -- temperature, top_k, top_p, min_p, the repeat, presence and
+frequency penalties, repeat_last_n -- and the seed; a request without a seed gets a fresh one that is recorded.  The
 receipt's example uses temperature 0.8, top_k 50, top_p 0.95, min_p 0.05,
-repeat_penalty 1.1, repeat_last_n 64, seed 42.
+repeat_penalty 1.1, presence_penalty 0, frequency_penalty 0, repeat_last_n 64,
+seed 42.
 
 The pages list the settings but not the order in which they act, nor their
 exact forms.  The reading taken here (the usual one for these knobs):
 
-1. Repeat penalty, once per distinct id among the last ``repeat_last_n`` tokens
-   of the request (n < 0: all of them, n = 0: none): z <- z / r if z > 0 else
-   z * r.
+1. Penalties, once per distinct id among the last ``repeat_last_n`` tokens
+   of the request (n < 0: all of them, n = 0: none), c its count there:
+   first the repeat penalty, z <- z / r if z > 0 else z * r; then the presence
+   and frequency penalties, z <- z - (c * f + p) (f the frequency penalty, p
+   the presence penalty; each operation rounded to fp32, skipped when both
+   are 0).
 2. Temperature <= 0 is greedy: the largest z, lowest id on ties.
 3. Candidates: the top_k largest z ordered by (z descending, id ascending);
    top_k <= 0 or >= V keeps every id in that order.
@@ -71,19 +75,27 @@ class SamplingParams:
     repeat_penalty: float = 1.1
     repeat_last_n: int = 64
     seed: int = 42
+    presence_penalty: float = 0.0
+    frequency_penalty: float = 0.0
 
 
 def penalize(logits_f32: np.ndarray, history, p: SamplingParams) -> np.ndarray:
     z = np.array(logits_f32, dtype=np.float32, copy=True)
     r = np.float32(p.repeat_penalty)
+    fq = np.float32(p.frequency_penalty)
+    pr = np.float32(p.presence_penalty)
+    additive = fq != 0 or pr != 0
     n = int(p.repeat_last_n)
     hist = list(history)
-    if r == np.float32(1.0) or n == 0 or not hist:
+    if (r == np.float32(1.0) and not additive) or n == 0 or not hist:
         return z
-    window = hist if n < 0 else hist[-n:]
-    for t in sorted(set(int(t) for t in window)):
+    window = [int(t) for t in (hist if n < 0 else hist[-n:])]
+    for t in sorted(set(window)):
         if 0 <= t < z.shape[0]:
             z[t] = z[t] / r if z[t] > 0 else z[t] * r
+            if additive:
+                c = np.float32(window.count(t))
+                z[t] = z[t] - (c * fq + pr)
     return z
 
 

@@ -91,6 +91,35 @@ def test_repeat_penalty_closed_form():
     assert np.array_equal(penalize(z, [0, 1], _greedy_params(repeat_penalty=2.0, repeat_last_n=0)), z)
 
 
+def test_presence_and_frequency_penalties_closed_form():
+    # window (last 4) = [1, 0, 1, 1]: id 1 three times, id 0 once; id 4 outside
+    z = np.array([2.0, -2.0, 1.0, 0.0, 3.0], np.float32)
+    p = _greedy_params(repeat_penalty=1.0, repeat_last_n=4, frequency_penalty=0.5, presence_penalty=0.25)
+    got = penalize(z, [4, 1, 0, 1, 1], p)
+    # id 0: 2 - (1 * 0.5 + 0.25) = 1.25; id 1: -2 - (3 * 0.5 + 0.25) = -3.75
+    assert np.array_equal(got, np.array([1.25, -3.75, 1.0, 0.0, 3.0], np.float32))
+    # after the repeat penalty: id 0: 2 / 2 - 0.75 = 0.25; id 1: -2 * 2 - 1.75 = -5.75
+    p2 = _greedy_params(repeat_penalty=2.0, repeat_last_n=4, frequency_penalty=0.5, presence_penalty=0.25)
+    assert np.array_equal(penalize(z, [4, 1, 0, 1, 1], p2),
+                          np.array([0.25, -5.75, 1.0, 0.0, 3.0], np.float32))
+    # presence alone subtracts once per distinct id, frequency alone scales with the count
+    pp = _greedy_params(repeat_penalty=1.0, repeat_last_n=-1, presence_penalty=1.0)
+    assert np.array_equal(penalize(z, [0, 0, 0, 2], pp), np.array([1.0, -2.0, 0.0, 0.0, 3.0], np.float32))
+    fp = _greedy_params(repeat_penalty=1.0, repeat_last_n=-1, frequency_penalty=1.0)
+    assert np.array_equal(penalize(z, [0, 0, 0, 2], fp), np.array([-1.0, -2.0, 0.0, 0.0, 3.0], np.float32))
+    # both zero: the repeat penalty alone (the receipt's example settings)
+    assert np.array_equal(penalize(z, [0, 1], _greedy_params(repeat_penalty=2.0, repeat_last_n=-1)),
+                          penalize(z, [0, 1], _greedy_params(repeat_penalty=2.0, repeat_last_n=-1,
+                                                              presence_penalty=0.0, frequency_penalty=0.0)))
+    # a penalty can move the greedy pick: id 4 (3.0) outranks id 0 (2.0) until id 4 is
+    # penalised by more than 1
+    z2 = np.array([2.0, 0.0, 0.0, 0.0, 3.0], np.float32)
+    assert sample_row(z2, [4, 4], 0, _greedy_params(temperature=0.0, repeat_penalty=1.0,
+                                                      frequency_penalty=0.75, repeat_last_n=-1))[0] == 0
+    assert sample_row(z2, [4, 4], 0, _greedy_params(temperature=0.0, repeat_penalty=1.0,
+                                                      frequency_penalty=0.25, repeat_last_n=-1))[0] == 4
+
+
 def _freq(z, p, n, hist=()):
     toks = [sample_row(z, list(hist), s, p)[0] for s in range(n)]
     return np.bincount(toks, minlength=len(z))
