@@ -263,8 +263,11 @@ kinv_status kinv_attn_prefill(const void* q, const void* k_cache, const void* v_
 /* --------------------------------------------------------------- sampler
  * Seeded sampler with the settings a Kinetic receipt records (Kinetic
  * "Receipts", *Making a receipt*, the `sampling` object).  Per row b, in this
- * order: repeat penalty over the distinct ids among the last repeat_last_n
- * history tokens (z/r if z > 0 else z*r; n < 0: all, n == 0: none);
+ * order: penalties over the distinct ids among the last repeat_last_n
+ * history tokens (n < 0: all, n == 0: none), first the repeat penalty
+ * (z/r if z > 0 else z*r), then, when presence_penalty or frequency_penalty is
+ * not 0, z - (c * frequency_penalty + presence_penalty) with c the id's count
+ * in that window (each operation rounded to fp32);
  * temperature <= 0 -> greedy argmax (lowest id on ties); otherwise the top_k
  * candidates ordered by (z desc, id asc); s = z / temperature;
  * e_i = exp(s_i - s_0); top-p keeps the shortest prefix whose sum of e reaches
@@ -297,6 +300,8 @@ typedef struct {
   int32_t top_k;
   int32_t repeat_last_n;
   uint64_t seed;
+  float presence_penalty;   /* 0: off */
+  float frequency_penalty;  /* 0: off */
 } kinv_sampling_params;
 
 size_t kinv_sample_workspace(int B, int V);

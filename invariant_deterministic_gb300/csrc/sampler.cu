@@ -1,6 +1,7 @@
 // Seeded, batch-invariant sampler (Kinetic "Receipts", *Making a receipt*:
-// the receipt records temperature, top_k, top_p, min_p, repeat_penalty,
-// repeat_last_n and the seed, so the same settings must give the same token).
+// the receipt records temperature, top_k, top_p, min_p, the repeat, presence
+// and frequency penalties, repeat_last_n and the seed, so the same settings
+// must give the same token).
 //
 // Eight thread blocks (one cluster) per row, each owning a contiguous eighth
 // of the vocabulary; they exchange the row maximum, threshold counts, radix
@@ -8,9 +9,11 @@
 // rank 0 of the cluster finishes the row.  Nothing is shared between rows,
 // and every quantity exchanged is an exact maximum, an integer count or a set
 // of candidates, so the result does not depend on how the row is divided.
-//  1. Repeat penalty: a shared-memory bitmap marks the distinct ids among the
+//  1. Penalties: a shared-memory bitmap marks the distinct ids among the
 //     row's last repeat_last_n history tokens; a marked logit z becomes z / r
-//     (z > 0) or z * r, both correctly rounded fp32 operations.
+//     (z > 0) or z * r, and then, when a presence (p) or frequency (f)
+//     penalty is set, z - (c * f + p) with c the id's count in that window;
+//     every operation a correctly rounded fp32 one.
 //  2. Ranking uses the order-preserving 32-bit key of each penalised fp32
 //     value and, for equal keys, the lower id first: a strict total order.
 //     Greedy (temperature <= 0) takes its maximum.  Otherwise radix passes over
@@ -40,6 +43,7 @@ constexpr int kMaxTopK = 1024;
 constexpr int kCap = 4096;  // candidates gathered before sorting
 constexpr int kMaxBlocks = 2048;  // full-vocabulary mode: 128-id blocks of the row (V <= 262144)
 constexpr int kRounds = 10;  // 16-byte vectors of the row each thread keeps in registers
+constexpr int kWinMax = 256;  // penalty windows up to this long are counted from shared memory
 constexpr int kRegSpan = kThreadsS * 4 * kRounds;  // ids a block holds in registers
 
 __device__ __forceinline__ uint32_t ordered_key(float z) {
@@ -98,13 +102,32 @@ struct Smem {
   int ok;
   int fast;
   float thresh_f;
+  int32_t win[kWinMax];  // the penalty window, when a presence or frequency penalty is set
 };
 
-__device__ __forceinline__ float penalised(const float* __restrict__ row, int i,
-                                           const uint32_t* bitmap, float r) {
-  float z = row[i];
-  if ((bitmap[i >> 5] >> (i & 31)) & 1u) z = z > 0.f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
+// The penalties of one row (step 1 above).
+struct Penalty {
+  const uint32_t* bitmap;  // distinct ids of the window
+  const int32_t* win;      // the window itself (shared memory, or the history row)
+  int n;                   // its length
+  float r, f, p;           // repeat, frequency and presence penalties
+  bool additive;           // f or p is set
+};
+
+__device__ __forceinline__ float penalise(float z, int id, const Penalty& pe) {
+  if ((pe.bitmap[id >> 5] >> (id & 31)) & 1u) {
+    z = z > 0.f ? __fdiv_rn(z, pe.r) : __fmul_rn(z, pe.r);
+    if (pe.additive) {
+      int c = 0;
+      for (int j = 0; j < pe.n; ++j) c += pe.win[j] == id ? 1 : 0;
+      z = __fsub_rn(z, __fadd_rn(__fmul_rn(static_cast<float>(c), pe.f), pe.p));
+    }
+  }
   return z;
+}
+
+__device__ __forceinline__ float penalised(const float* __restrict__ row, int i, const Penalty& pe) {
+  return penalise(row[i], i, pe);
 }
 
 // Visits every id in [v0, v1) once, in rounds in which each thread loads
@@ -113,7 +136,7 @@ __device__ __forceinline__ float penalised(const float* __restrict__ row, int i,
 // -inf); every lane runs the same number of rounds (f may use warp votes).
 template <typename F>
 __device__ __forceinline__ void for_each_value(const float* __restrict__ row, int v0, int v1,
-                                               const uint32_t* bitmap, float r, F&& f) {
+                                               const Penalty& pe, F&& f) {
   constexpr int U = 4;
   const int t = threadIdx.x;
   const int n = v1 > v0 ? v1 - v0 : 0;
@@ -137,7 +160,7 @@ __device__ __forceinline__ void for_each_value(const float* __restrict__ row, in
       for (int e = 0; e < 4; ++e) {
         const int i = v0 + 4 * i4 + e;
         float z = xv[e];
-        if (valid && ((bitmap[i >> 5] >> (i & 31)) & 1u)) z = z > 0.f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
+        if (valid) z = penalise(z, i, pe);
         f(valid, i, isnan(z) ? -INFINITY : z);
       }
     }
@@ -146,7 +169,7 @@ __device__ __forceinline__ void for_each_value(const float* __restrict__ row, in
   for (int base = 4 * n4; base < n; base += kThreadsS) {
     const int i = v0 + base + t;
     const bool valid = base + t < n;
-    const float z = valid ? penalised(row, i, bitmap, r) : 0.f;
+    const float z = valid ? penalised(row, i, pe) : 0.f;
     f(valid, i, isnan(z) ? -INFINITY : z);
   }
 }
@@ -203,14 +226,20 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
   for (int i = t; i < words; i += kThreadsS) bitmap[i] = 0u;
   __syncthreads();
   const float r = prm.repeat_penalty;
+  const bool additive = prm.frequency_penalty != 0.f || prm.presence_penalty != 0.f;
   const int hl = hist_len ? min(max(hist_len[b], 0), hist_ld) : 0;
   int n_pen = prm.repeat_last_n < 0 ? hl : min(prm.repeat_last_n, hl);
-  if (r == 1.0f) n_pen = 0;
+  if (r == 1.0f && !additive) n_pen = 0;
+  const int32_t* win_g = n_pen > 0 ? history + static_cast<int64_t>(b) * hist_ld + hl - n_pen : nullptr;
+  const bool win_in_smem = additive && n_pen <= kWinMax;
   for (int i = t; i < n_pen; i += kThreadsS) {
-    const int id = history[static_cast<int64_t>(b) * hist_ld + hl - n_pen + i];
+    const int id = win_g[i];
     if (id >= 0 && id < V) atomicOr(&bitmap[id >> 5], 1u << (id & 31));  // idempotent bit set
+    if (win_in_smem) sm.win[i] = id;
   }
   __syncthreads();
+  const Penalty pe{bitmap, win_in_smem ? sm.win : win_g, additive ? n_pen : 0, r, prm.frequency_penalty,
+                   prm.presence_penalty, additive};
 
   // This block's penalised logits (NaN as -inf), read once into registers
   // when its share of the row fits (thread t holds ids v0 + 2048 q + 4 t ..
@@ -235,7 +264,7 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
       for (int e = 0; e < 4; ++e) {
         const int id = i + e;
         float z = x[e];
-        if (id < v1 && ((bitmap[id >> 5] >> (id & 31)) & 1u)) z = z > 0.f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
+        if (id < v1) z = penalise(z, id, pe);
         x[e] = isnan(z) ? -INFINITY : z;
       }
       vr[q] = make_float4(x[0], x[1], x[2], x[3]);
@@ -253,7 +282,7 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
         f(i + 3 < v1, i + 3, vr[q].w);
       }
     } else {
-      for_each_value(row, v0, v1, bitmap, r, f);
+      for_each_value(row, v0, v1, pe, f);
     }
   };
   auto visit_key = [&](auto&& f) {
@@ -474,7 +503,7 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
     for (int base = 0; base < V; base += kThreadsS) {
       const int i = base + t;
       uint32_t key = 0;
-      if (i < V) key = ordered_key(penalised(row, i, bitmap, r));
+      if (i < V) key = ordered_key(penalised(row, i, pe));
       const bool gt = i < V && key > thresh;
       const bool eq = i < V && key == thresh;
       if (gt) {
@@ -512,7 +541,7 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
       for (int e = 0; e < 4; ++e) {
         const int i = blk * 128 + 4 * lane + e;
         if (i < V) {
-          float z = penalised(row, i, bitmap, r);
+          float z = penalised(row, i, pe);
           if (isnan(z)) z = -INFINITY;
           acc = __fadd_rn(acc, expf(__fsub_rn(__fdiv_rn(z, temp), s0)));
         }

@@ -329,6 +329,8 @@ class SamplingParams:
     repeat_penalty: float = 1.1
     repeat_last_n: int = 64
     seed: int = 42
+    presence_penalty: float = 0.0
+    frequency_penalty: float = 0.0
 
 
 def sample(logits, params_dev, history, hist_len, step, out=None, stream=None):

@@ -134,7 +134,8 @@ class Decoder:
         self.history = torch.zeros(max_batch, self.hist_ld, **i32)
         self.hist_len = torch.zeros(max_batch, **i32)
         self.step = torch.zeros(max_batch, dtype=torch.int64, device=self.dev)
-        self.params = torch.zeros(max_batch * 32, dtype=torch.uint8, device=self.dev)
+        self.params = torch.zeros(max_batch * synth.SAMPLING_DTYPE.itemsize, dtype=torch.uint8,
+                                  device=self.dev)
         # optional per-call timing: name -> list of (start, end) CUDA events
         self.timer = None
 

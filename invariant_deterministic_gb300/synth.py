@@ -76,14 +76,19 @@ def layer_weights(d: int, n_q: int, n_kv: int, head_dim: int, ffn: int, seed: in
     return w
 
 
+# kinv_sampling_params, field by field
+SAMPLING_DTYPE = np.dtype([("temperature", "<f4"), ("top_p", "<f4"), ("min_p", "<f4"),
+                           ("repeat_penalty", "<f4"), ("top_k", "<i4"), ("repeat_last_n", "<i4"),
+                           ("seed", "<u8"), ("presence_penalty", "<f4"), ("frequency_penalty", "<f4")])
+
+
 def sampling_struct(params_list) -> np.ndarray:
     """Pack per-request sampler settings into the C struct layout
     {float temperature, top_p, min_p, repeat_penalty; int32 top_k,
-    repeat_last_n; uint64 seed} (32 bytes)."""
-    dt = np.dtype([("temperature", "<f4"), ("top_p", "<f4"), ("min_p", "<f4"),
-                   ("repeat_penalty", "<f4"), ("top_k", "<i4"), ("repeat_last_n", "<i4"),
-                   ("seed", "<u8")])
-    a = np.zeros(len(params_list), dtype=dt)
+    repeat_last_n; uint64 seed; float presence_penalty, frequency_penalty}
+    (40 bytes)."""
+    a = np.zeros(len(params_list), dtype=SAMPLING_DTYPE)
     for i, p in enumerate(params_list):
-        a[i] = (p.temperature, p.top_p, p.min_p, p.repeat_penalty, p.top_k, p.repeat_last_n, p.seed)
+        a[i] = (p.temperature, p.top_p, p.min_p, p.repeat_penalty, p.top_k, p.repeat_last_n, p.seed,
+                getattr(p, "presence_penalty", 0.0), getattr(p, "frequency_penalty", 0.0))
     return a

@@ -103,6 +103,50 @@ def test_setting_variants(kinv):
     assert np.array_equal(got2[~ties2], ref2[~ties2])
 
 
+def test_presence_and_frequency_penalties(kinv):
+    """Presence and frequency penalties on top of the repeat penalty, with the
+    window counted from shared memory (<= 256 ids) and from the history row
+    (400 ids); zero penalties give the bits of the repeat penalty alone."""
+    vocab = 151936
+    g = synth.gen(74)
+    hist_ld = 512
+    variants = [
+        dict(temperature=0.0, top_k=50, top_p=1.0, min_p=0.0, repeat_penalty=1.1, repeat_last_n=64,
+             presence_penalty=0.5, frequency_penalty=0.4),
+        dict(temperature=0.8, top_k=50, top_p=0.95, min_p=0.05, repeat_penalty=1.0, repeat_last_n=64,
+             presence_penalty=0.0, frequency_penalty=0.7),
+        dict(temperature=1.0, top_k=200, top_p=1.0, min_p=0.0, repeat_penalty=1.2, repeat_last_n=-1,
+             presence_penalty=1.5, frequency_penalty=0.0),
+        dict(temperature=0.0, top_k=20, top_p=1.0, min_p=0.0, repeat_penalty=1.0, repeat_last_n=400,
+             presence_penalty=-0.5, frequency_penalty=0.3),
+    ]
+    plist, hists, steps = [], [], []
+    for i, v in enumerate(variants):
+        for j in range(6):
+            plist.append(kinv.SamplingParams(**v, seed=31 * i + j))
+            # few distinct ids, many repeats: counts up to dozens
+            hists.append(torch.randint(0, 40, (400,), generator=g).tolist())
+            steps.append(7 * i + j)
+    logits = (torch.randn(len(plist), vocab, generator=g) * 2).cuda()
+    logits[:, :40] += 4.0   # the history ids are the top candidates
+    got = _run(kinv, logits, plist, hists, steps, hist_ld=hist_ld)
+    z = logits.cpu().numpy()
+    for b, p in enumerate(plist):
+        op = OParams(**{k: getattr(p, k) for k in OParams.__dataclass_fields__})
+        t, tie = sample_row(z[b], hists[b][-hist_ld:], steps[b], op)
+        if not tie:
+            assert got[b] == t, (b, got[b], t)
+    # zero presence and frequency: the bits of the repeat penalty alone
+    zero = [kinv.SamplingParams(**{**variants[0], "presence_penalty": 0.0, "frequency_penalty": 0.0},
+                                seed=3) for _ in range(4)]
+    a = _run(kinv, logits[:4].contiguous(), zero, hists[:4], steps[:4], hist_ld=hist_ld)
+    ref = [sample_row(z[b], hists[b][-hist_ld:], steps[b],
+                      OParams(**{k: getattr(zero[b], k) for k in OParams.__dataclass_fields__}))[0]
+           for b in range(4)]
+    assert list(a) == ref
+    assert kinv.last_device_status() == 0
+
+
 def test_exact_ties_take_lowest_ids(kinv):
     vocab = 151936
     logits = torch.zeros(3, vocab, device="cuda")
