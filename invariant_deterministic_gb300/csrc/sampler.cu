@@ -119,6 +119,7 @@ __device__ __forceinline__ float penalise(float z, int id, const Penalty& pe) {
     z = z > 0.f ? __fdiv_rn(z, pe.r) : __fmul_rn(z, pe.r);
     if (pe.additive) {
       int c = 0;
+#pragma unroll 1  // a rolled loop: unrolled at every inlined visit it made the kernel spill
       for (int j = 0; j < pe.n; ++j) c += pe.win[j] == id ? 1 : 0;
       z = __fsub_rn(z, __fadd_rn(__fmul_rn(static_cast<float>(c), pe.f), pe.p));
     }
