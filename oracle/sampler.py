@@ -2,7 +2,7 @@
 
 Follows Kinetic "Receipts", *Making a receipt*: a receipt records every sampler
 setting -- temperature, top_k, top_p, min_p, the repeat, presence and
-frequency penalties, repeat_last_n -- and the seed; a request without a seed gets a fresh one that is recorded.  The
+frequency penalties, logit bias, repeat_last_n -- and the seed; a request without a seed gets a fresh one that is recorded.  The
 receipt's example uses temperature 0.8, top_k 50, top_p 0.95, min_p 0.05,
 repeat_penalty 1.1, presence_penalty 0, frequency_penalty 0, repeat_last_n 64,
 seed 42.
@@ -10,6 +10,8 @@ seed 42.
 The pages list the settings but not the order in which they act, nor their
 exact forms.  The reading taken here (the usual one for these knobs):
 
+0. Logit bias: each (id, b) of the request's list adds b to logit id (fp32,
+   in list order; ids outside the vocabulary are ignored).
 1. Penalties, once per distinct id among the last ``repeat_last_n`` tokens
    of the request (n < 0: all of them, n = 0: none), c its count there:
    first the repeat penalty, z <- z / r if z > 0 else z * r; then the presence
@@ -77,6 +79,16 @@ class SamplingParams:
     seed: int = 42
     presence_penalty: float = 0.0
     frequency_penalty: float = 0.0
+    logit_bias: dict = None   # {id: bias}; applied in insertion order
+
+
+def bias_logits(logits_f32: np.ndarray, p: SamplingParams) -> np.ndarray:
+    z = np.array(logits_f32, dtype=np.float32, copy=True)
+    for t, b in (p.logit_bias or {}).items():
+        t = int(t)
+        if 0 <= t < z.shape[0]:
+            z[t] = z[t] + np.float32(b)
+    return z
 
 
 def penalize(logits_f32: np.ndarray, history, p: SamplingParams) -> np.ndarray:
@@ -101,7 +113,7 @@ def penalize(logits_f32: np.ndarray, history, p: SamplingParams) -> np.ndarray:
 
 def sample_row(logits_f32: np.ndarray, history, step: int, p: SamplingParams):
     """Returns (token, near_tie)."""
-    z = penalize(logits_f32, history, p)
+    z = penalize(bias_logits(logits_f32, p), history, p)
     v = z.shape[0]
     t = np.float32(p.temperature)
     if not (t > 0):

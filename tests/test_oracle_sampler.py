@@ -8,7 +8,7 @@ import pytest
 from scipy import stats
 
 from oracle import philox
-from oracle.sampler import SamplingParams, penalize, sample_row
+from oracle.sampler import SamplingParams, bias_logits, penalize, sample_row
 
 
 def test_philox_two_restatements_agree():
@@ -118,6 +118,26 @@ def test_presence_and_frequency_penalties_closed_form():
                                                       frequency_penalty=0.75, repeat_last_n=-1))[0] == 0
     assert sample_row(z2, [4, 4], 0, _greedy_params(temperature=0.0, repeat_penalty=1.0,
                                                       frequency_penalty=0.25, repeat_last_n=-1))[0] == 4
+
+
+def test_logit_bias_closed_form():
+    z = np.array([2.0, -2.0, 1.0, 0.0, 3.0], np.float32)
+    p = _greedy_params(logit_bias={1: 1.5, 4: -np.inf, 9: 100.0})   # id 9 is outside V = 5
+    assert np.array_equal(bias_logits(z, p), np.array([2.0, -0.5, 1.0, 0.0, -np.inf], np.float32))
+    # a banned id is never drawn, greedy or sampled
+    assert sample_row(z, [], 0, _greedy_params(temperature=0.0, logit_bias={4: -np.inf}))[0] == 0
+    for step in range(50):
+        assert sample_row(z, [], step, _greedy_params(logit_bias={4: -np.inf}))[0] != 4
+    # a large bias forces an id
+    assert sample_row(z, [], 3, _greedy_params(logit_bias={3: 50.0}))[0] == 3
+    # the bias comes before the penalties: id 0 biased to 6, then halved by the repeat penalty
+    pb = _greedy_params(repeat_penalty=2.0, repeat_last_n=-1, logit_bias={0: 4.0})
+    assert np.array_equal(penalize(bias_logits(z, pb), [0], pb),
+                          np.array([3.0, -2.0, 1.0, 0.0, 3.0], np.float32))
+    # an empty or absent list changes nothing (bit for bit, -0.0 included)
+    zn = np.array([-0.0, 1.0], np.float32)
+    assert np.signbit(bias_logits(zn, _greedy_params(logit_bias={}))[0])
+    assert np.signbit(bias_logits(zn, _greedy_params())[0])
 
 
 def _freq(z, p, n, hist=()):
