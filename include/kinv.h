@@ -263,7 +263,9 @@ kinv_status kinv_attn_prefill(const void* q, const void* k_cache, const void* v_
 /* --------------------------------------------------------------- sampler
  * Seeded sampler with the settings a Kinetic receipt records (Kinetic
  * "Receipts", *Making a receipt*, the `sampling` object).  Per row b, in this
- * order: penalties over the distinct ids among the last repeat_last_n
+ * order: the logit bias (each entry (id, bias) of the row's list adds bias to
+ * logit id in fp32, in list order; ids outside [0, V) are ignored); the
+ * penalties over the distinct ids among the last repeat_last_n
  * history tokens (n < 0: all, n == 0: none), first the repeat penalty
  * (z/r if z > 0 else z*r), then, when presence_penalty or frequency_penalty is
  * not 0, z - (c * frequency_penalty + presence_penalty) with c the id's count
@@ -289,9 +291,16 @@ kinv_status kinv_attn_prefill(const void* q, const void* k_cache, const void* v_
  * first; step: device int64 [B]; out_tokens: device int32 [B].
  * Requirements: 1 <= V; ld >= V; top_k in [1, 1024] or the whole vocabulary
  * (V <= 262144, and top_p < 1 or min_p > 0 cutting within the 1024 most
- * likely ids) unless temperature <= 0; hist_len[b] <= hist_ld.  Rows whose
+ * likely ids) unless temperature <= 0; hist_len[b] <= hist_ld <= 1024
+ * (else KINV_ERR_UNSUPPORTED before launch); at most 1024 logit-bias entries
+ * per row (further entries are ignored).  Rows whose
  * settings or logits fall outside this set get token -1 and the device status
  * word records KINV_ERR_UNSUPPORTED. */
+typedef struct {
+  int32_t id;
+  float bias;
+} kinv_logit_bias;
+
 typedef struct {
   float temperature;
   float top_p;
@@ -302,6 +311,9 @@ typedef struct {
   uint64_t seed;
   float presence_penalty;   /* 0: off */
   float frequency_penalty;  /* 0: off */
+  const kinv_logit_bias* logit_bias;  /* device, n_logit_bias entries; NULL: none */
+  int32_t n_logit_bias;               /* at most 1024 */
+  int32_t reserved;                   /* 0 */
 } kinv_sampling_params;
 
 size_t kinv_sample_workspace(int B, int V);

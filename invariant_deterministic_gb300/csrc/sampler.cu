@@ -9,11 +9,16 @@
 // rank 0 of the cluster finishes the row.  Nothing is shared between rows,
 // and every quantity exchanged is an exact maximum, an integer count or a set
 // of candidates, so the result does not depend on how the row is divided.
-//  1. Penalties: a shared-memory bitmap marks the distinct ids among the
-//     row's last repeat_last_n history tokens; a marked logit z becomes z / r
-//     (z > 0) or z * r, and then, when a presence (p) or frequency (f)
-//     penalty is set, z - (c * f + p) with c the id's count in that window;
-//     every operation a correctly rounded fp32 one.
+//  1. Logit bias and penalties: a shared-memory bitmap marks the distinct
+//     ids among the row's last repeat_last_n history tokens and the ids of
+//     its logit-bias list.  A marked logit first gets its bias entries added
+//     (list order); then, if the id is in the window, z becomes z / r
+//     (z > 0) or z * r, and, when a presence (p) or frequency (f) penalty is
+//     set, z - (c * f + p) with c the id's count in the window; every
+//     operation a correctly rounded fp32 one.  Each block computes the final
+//     value of every marked id once, stored by the id's rank among the marked
+//     ids (a per-word prefix count of the bitmap), so a visit of a marked id
+//     is one table read.
 //  2. Ranking uses the order-preserving 32-bit key of each penalised fp32
 //     value and, for equal keys, the lower id first: a strict total order.
 //     Greedy (temperature <= 0) takes its maximum.  Otherwise radix passes over
@@ -43,7 +48,9 @@ constexpr int kMaxTopK = 1024;
 constexpr int kCap = 4096;  // candidates gathered before sorting
 constexpr int kMaxBlocks = 2048;  // full-vocabulary mode: 128-id blocks of the row (V <= 262144)
 constexpr int kRounds = 10;  // 16-byte vectors of the row each thread keeps in registers
-constexpr int kWinMax = 256;  // penalty windows up to this long are counted from shared memory
+constexpr int kMaxHist = 1024;  // history row length (the penalty window) at most
+constexpr int kMaxBias = 1024;  // logit-bias entries per row at most
+constexpr int kMaxMarked = kMaxHist + kMaxBias;  // ids a row's bias and penalties can touch
 constexpr int kRegSpan = kThreadsS * 4 * kRounds;  // ids a block holds in registers
 
 __device__ __forceinline__ uint32_t ordered_key(float z) {
@@ -102,27 +109,34 @@ struct Smem {
   int ok;
   int fast;
   float thresh_f;
-  int32_t win[kWinMax];  // the penalty window, when a presence or frequency penalty is set
+  float mk_val[kMaxMarked];  // the final logit of each marked id, by rank
+  int mk_cnt[kMaxMarked];    // its count in the penalty window
 };
 
 // The penalties of one row (step 1 above).
 struct Penalty {
-  const uint32_t* bitmap;  // distinct ids of the window
-  const int32_t* win;      // the window itself (shared memory, or the history row)
-  int n;                   // its length
-  float r, f, p;           // repeat, frequency and presence penalties
-  bool additive;           // f or p is set
+  const uint32_t* bitmap;   // marked ids: the window's and the bias list's
+  const uint16_t* mk_base;  // marked ids in the words before each word
+  const float* mk_val;      // the final logit of each marked id, by rank
 };
 
 __device__ __forceinline__ float penalise(float z, int id, const Penalty& pe) {
-  if ((pe.bitmap[id >> 5] >> (id & 31)) & 1u) {
-    z = z > 0.f ? __fdiv_rn(z, pe.r) : __fmul_rn(z, pe.r);
-    if (pe.additive) {
-      int c = 0;
-#pragma unroll 1  // a rolled loop: unrolled at every inlined visit it made the kernel spill
-      for (int j = 0; j < pe.n; ++j) c += pe.win[j] == id ? 1 : 0;
-      z = __fsub_rn(z, __fadd_rn(__fmul_rn(static_cast<float>(c), pe.f), pe.p));
-    }
+  const uint32_t word = pe.bitmap[id >> 5];
+  const uint32_t below = (1u << (id & 31)) - 1u;
+  if ((word >> (id & 31)) & 1u) z = pe.mk_val[pe.mk_base[id >> 5] + __popc(word & below)];
+  return z;
+}
+
+// The final logit of a marked id with window count c: its bias entries in
+// list order, then, if it is in the window (c > 0), the repeat penalty and the
+// presence and frequency penalties.
+__device__ float marked_value(float z, int id, const kinv_logit_bias* bias, int nb, int c, float r, float f,
+                              float p, bool additive) {
+  for (int j = 0; j < nb; ++j)
+    if (bias[j].id == id) z = __fadd_rn(z, bias[j].bias);
+  if (c > 0) {
+    z = z > 0.f ? __fdiv_rn(z, r) : __fmul_rn(z, r);
+    if (additive) z = __fsub_rn(z, __fadd_rn(__fmul_rn(static_cast<float>(c), f), p));
   }
   return z;
 }
@@ -207,6 +221,7 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem_raw + sizeof(Smem));
+  uint16_t* mk_base = reinterpret_cast<uint16_t*>(bitmap + ((V + 31) >> 5));
   pdl_launch_dependents();
   pdl_wait();
   const int b = blockIdx.y;
@@ -223,28 +238,10 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
   const int v0 = min(V, rank * chunk), v1 = min(V, v0 + chunk);
   auto peer = [](const void* p, int q) { return map_to_rank(smem_addr(p), static_cast<uint32_t>(q)); };
 
-  // 1. penalty bitmap (the whole row, in every block)
-  for (int i = t; i < words; i += kThreadsS) bitmap[i] = 0u;
-  __syncthreads();
-  const float r = prm.repeat_penalty;
-  const bool additive = prm.frequency_penalty != 0.f || prm.presence_penalty != 0.f;
-  const int hl = hist_len ? min(max(hist_len[b], 0), hist_ld) : 0;
-  int n_pen = prm.repeat_last_n < 0 ? hl : min(prm.repeat_last_n, hl);
-  if (r == 1.0f && !additive) n_pen = 0;
-  const int32_t* win_g = n_pen > 0 ? history + static_cast<int64_t>(b) * hist_ld + hl - n_pen : nullptr;
-  const bool win_in_smem = additive && n_pen <= kWinMax;
-  for (int i = t; i < n_pen; i += kThreadsS) {
-    const int id = win_g[i];
-    if (id >= 0 && id < V) atomicOr(&bitmap[id >> 5], 1u << (id & 31));  // idempotent bit set
-    if (win_in_smem) sm.win[i] = id;
-  }
-  __syncthreads();
-  const Penalty pe{bitmap, win_in_smem ? sm.win : win_g, additive ? n_pen : 0, r, prm.frequency_penalty,
-                   prm.presence_penalty, additive};
-
-  // This block's penalised logits (NaN as -inf), read once into registers
-  // when its share of the row fits (thread t holds ids v0 + 2048 q + 4 t ..
-  // + 3 for round q); otherwise every pass streams them from memory.
+  // This block's logits, read once into registers when its share of the row
+  // fits (thread t holds ids v0 + 2048 q + 4 t .. + 3 for round q); the loads
+  // are in flight while the penalty tables below are built, and the penalties
+  // are applied after.  Otherwise every pass streams the row from memory.
   const bool in_regs = kRegs && v1 - v0 <= kRegSpan;
   const bool vec = (reinterpret_cast<uintptr_t>(row) & 15u) == 0;
   float4 vr[kRegs ? kRounds : 1];
@@ -261,11 +258,90 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
         for (int e = 0; e < 4; ++e)
           if (i + e < v1) x[e] = row[i + e];
       }
+      vr[q] = make_float4(x[0], x[1], x[2], x[3]);
+    }
+  }
+
+  // 1. penalty bitmap (the whole row, in every block)
+  for (int i = t; i < words; i += kThreadsS) bitmap[i] = 0u;
+  __syncthreads();
+  const float r = prm.repeat_penalty;
+  const bool additive = prm.frequency_penalty != 0.f || prm.presence_penalty != 0.f;
+  const int nb = prm.logit_bias ? min(max(prm.n_logit_bias, 0), kMaxBias) : 0;
+  const int hl = hist_len ? min(max(hist_len[b], 0), hist_ld) : 0;
+  int n_pen = prm.repeat_last_n < 0 ? hl : min(prm.repeat_last_n, hl);
+  if (r == 1.0f && !additive) n_pen = 0;
+  const int32_t* win_g = n_pen > 0 ? history + static_cast<int64_t>(b) * hist_ld + hl - n_pen : nullptr;
+  for (int i = t; i < n_pen; i += kThreadsS) {
+    const int id = win_g[i];
+    if (id >= 0 && id < V) atomicOr(&bitmap[id >> 5], 1u << (id & 31));  // idempotent bit set
+  }
+  for (int i = t; i < nb; i += kThreadsS) {
+    const int id = prm.logit_bias[i].id;
+    if (id >= 0 && id < V) atomicOr(&bitmap[id >> 5], 1u << (id & 31));
+  }
+  __syncthreads();
+  for (int i = t; i < kMaxMarked; i += kThreadsS) sm.mk_cnt[i] = 0;
+  // rank of the marked ids: thread t takes words [t * per, (t + 1) * per),
+  // a block-wide exclusive scan of their bit counts gives its first rank
+  {
+    const int per = (words + kThreadsS - 1) / kThreadsS;
+    const int w0 = min(words, t * per), w1 = min(words, w0 + per);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(bitmap[w]);
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) sm.warp_cnt[warp] = static_cast<uint32_t>(x);
+    __syncthreads();
+    int run = x - cnt;
+    for (int w2 = 0; w2 < warp; ++w2) run += static_cast<int>(sm.warp_cnt[w2]);
+    for (int w = w0; w < w1; ++w) {
+      mk_base[w] = static_cast<uint16_t>(run);
+      run += __popc(bitmap[w]);
+    }
+  }
+  __syncthreads();
+  // window counts by rank, then each marked id's final logit
+  auto rank_of = [&](int id) {
+    return mk_base[id >> 5] + __popc(bitmap[id >> 5] & ((1u << (id & 31)) - 1u));
+  };
+  for (int i = t; i < n_pen; i += kThreadsS) {
+    const int id = win_g[i];
+    if (id >= 0 && id < V) atomicAdd(&sm.mk_cnt[rank_of(id)], 1);
+  }
+  __syncthreads();
+  {
+    const int per = (words + kThreadsS - 1) / kThreadsS;
+    const int w0 = min(words, t * per), w1 = min(words, w0 + per);
+    for (int w = w0; w < w1; ++w) {
+      uint32_t bits = bitmap[w];
+      int k = mk_base[w];
+      while (bits) {
+        const int id = w * 32 + __ffs(bits) - 1;
+        bits &= bits - 1u;
+        sm.mk_val[k] = marked_value(row[id], id, prm.logit_bias, nb, sm.mk_cnt[k], r, prm.frequency_penalty,
+                                    prm.presence_penalty, additive);
+        ++k;
+      }
+    }
+  }
+  __syncthreads();
+  const Penalty pe{bitmap, mk_base, sm.mk_val};
+
+  if (in_regs) {
+    // the penalties and NaN as -inf, on the values loaded at the start
+#pragma unroll
+    for (int q = 0; q < (kRegs ? kRounds : 1); ++q) {
+      const int i = v0 + q * kThreadsS * 4 + 4 * t;
+      float x[4] = {vr[q].x, vr[q].y, vr[q].z, vr[q].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int id = i + e;
         float z = x[e];
-        if (id < v1) z = penalise(z, id, pe);
+        if (i + e < v1) z = penalise(z, i + e, pe);
         x[e] = isnan(z) ? -INFINITY : z;
       }
       vr[q] = make_float4(x[0], x[1], x[2], x[3]);
@@ -697,6 +773,13 @@ extern "C" size_t kinv_sample_workspace(int B, int V) {
   return 0;
 }
 
+// Smem, the bitmap of marked ids ((V + 31) / 32 words) and the rank of each
+// word's first marked id (uint16 per word)
+static size_t sampler_smem_bytes(int V) {
+  const size_t words = (static_cast<size_t>(V) + 31) / 32;
+  return sizeof(Smem) + words * 4 + (words * 2 + 15) / 16 * 16;
+}
+
 extern "C" kinv_status kinv_sample(const float* logits, int64_t ld, int B, int V,
                                    const kinv_sampling_params* params, const int32_t* history,
                                    int hist_ld, const int32_t* hist_len, const int64_t* step,
@@ -708,7 +791,8 @@ extern "C" kinv_status kinv_sample(const float* logits, int64_t ld, int B, int V
   if (B == 0) return KINV_OK;
   if (!logits || !params || !step || !out_tokens) return KINV_ERR_INVALID_ARG;
   if (hist_len && (!history || hist_ld <= 0)) return KINV_ERR_INVALID_ARG;
-  const size_t smem = sizeof(Smem) + static_cast<size_t>((V + 31) / 32) * 4;
+  if (hist_ld > kMaxHist) return KINV_ERR_UNSUPPORTED;
+  const size_t smem = sampler_smem_bytes(V);
   if (smem > static_cast<size_t>(max_smem_optin())) return KINV_ERR_UNSUPPORTED;
   if (B > 65535) return KINV_ERR_UNSUPPORTED;
   // Blocks per row: up to eight while the grid stays within one block per

@@ -14,6 +14,7 @@ import math
 import os
 from dataclasses import dataclass
 
+import numpy as np
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -331,6 +332,18 @@ class SamplingParams:
     seed: int = 42
     presence_penalty: float = 0.0
     frequency_penalty: float = 0.0
+    logit_bias: dict = None   # {id: bias}, applied in insertion order
+
+
+def sampling_params_device(params_list, device="cuda"):
+    """kinv_sampling_params [B] packed on the device, and the device buffer
+    of logit-bias entries they point to (None without any); keep both alive
+    while sampling with them."""
+    from . import synth
+    entries, _ = synth.bias_entries(params_list)
+    bias = torch.from_numpy(entries.view(np.uint8).copy()).to(device) if len(entries) else None
+    packed = synth.sampling_struct(params_list, bias.data_ptr() if bias is not None else 0)
+    return torch.from_numpy(packed.view(np.uint8).copy()).to(device), bias
 
 
 def sample(logits, params_dev, history, hist_len, step, out=None, stream=None):

@@ -148,7 +148,11 @@ class Decoder:
 
     # ------------------------------------------------------------ state setup
     def set_sampling(self, params_list) -> None:
-        packed = synth.sampling_struct(params_list)
+        entries, _ = synth.bias_entries(params_list)
+        # the logit-bias entries the packed settings point to (kept while in use)
+        self.bias = (torch.from_numpy(entries.view(np.uint8).copy()).to(self.dev)
+                     if len(entries) else None)
+        packed = synth.sampling_struct(params_list, self.bias.data_ptr() if self.bias is not None else 0)
         self.params[: packed.nbytes].copy_(torch.from_numpy(packed.view(np.uint8)))
 
     def set_positions(self, pos) -> None:

@@ -76,19 +76,35 @@ def layer_weights(d: int, n_q: int, n_kv: int, head_dim: int, ffn: int, seed: in
     return w
 
 
-# kinv_sampling_params, field by field
+# kinv_sampling_params and kinv_logit_bias, field by field
 SAMPLING_DTYPE = np.dtype([("temperature", "<f4"), ("top_p", "<f4"), ("min_p", "<f4"),
                            ("repeat_penalty", "<f4"), ("top_k", "<i4"), ("repeat_last_n", "<i4"),
-                           ("seed", "<u8"), ("presence_penalty", "<f4"), ("frequency_penalty", "<f4")])
+                           ("seed", "<u8"), ("presence_penalty", "<f4"), ("frequency_penalty", "<f4"),
+                           ("logit_bias", "<u8"), ("n_logit_bias", "<i4"), ("reserved", "<i4")])
+BIAS_DTYPE = np.dtype([("id", "<i4"), ("bias", "<f4")])
 
 
-def sampling_struct(params_list) -> np.ndarray:
+def bias_entries(params_list):
+    """The rows' logit-bias lists back to back (kinv_logit_bias entries, in
+    each dict's insertion order) and the index of each row's first entry."""
+    rows, starts = [], []
+    for p in params_list:
+        starts.append(len(rows))
+        rows.extend((int(t), float(v)) for t, v in (getattr(p, "logit_bias", None) or {}).items())
+    return np.array(rows, dtype=BIAS_DTYPE), starts
+
+
+def sampling_struct(params_list, bias_base: int = 0) -> np.ndarray:
     """Pack per-request sampler settings into the C struct layout
-    {float temperature, top_p, min_p, repeat_penalty; int32 top_k,
-    repeat_last_n; uint64 seed; float presence_penalty, frequency_penalty}
-    (40 bytes)."""
+    (SAMPLING_DTYPE, 56 bytes).  bias_base: device address of the entries of
+    bias_entries(params_list), which row i's logit_bias points into."""
+    _, starts = bias_entries(params_list)
     a = np.zeros(len(params_list), dtype=SAMPLING_DTYPE)
     for i, p in enumerate(params_list):
+        nb = len(getattr(p, "logit_bias", None) or {})
+        if nb and not bias_base:
+            raise ValueError("a logit-bias list needs bias_base (the entries' device address)")
         a[i] = (p.temperature, p.top_p, p.min_p, p.repeat_penalty, p.top_k, p.repeat_last_n, p.seed,
-                getattr(p, "presence_penalty", 0.0), getattr(p, "frequency_penalty", 0.0))
+                getattr(p, "presence_penalty", 0.0), getattr(p, "frequency_penalty", 0.0),
+                bias_base + BIAS_DTYPE.itemsize * starts[i] if nb else 0, nb, 0)
     return a

@@ -91,6 +91,8 @@ def test_host_validation_without_gpu(lib):
     assert need >= 2 * 32 * 128 * 4
     # sampler / glue
     assert L.kinv_sample(fake, 10, 2, 20, fake, None, 0, None, fake, fake, None, 0, None) == lib.ERR_INVALID_ARG
+    # history rows longer than 1024 ids (the penalty window) are not supported
+    assert L.kinv_sample(fake, 20, 2, 20, fake, fake, 2000, fake, fake, fake, None, 0, None) == lib.ERR_UNSUPPORTED
     assert L.kinv_swiglu(fake, 20, fake, 10, 2, 10, None) == lib.ERR_UNSUPPORTED
     assert L.kinv_rope_append(fake, 512, fake, fake, fake, 0, 128, fake, fake, None, None, 1e-6,
                               1, 2, 1, 96, 1e4, None) == lib.ERR_UNSUPPORTED

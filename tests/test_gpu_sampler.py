@@ -29,8 +29,7 @@ def _receipt_params():
 
 def _run(kinv, logits, plist, hists, steps, hist_ld=64):
     bsz = logits.shape[0]
-    packed = synth.sampling_struct(plist)
-    pdev = torch.from_numpy(packed.view(np.uint8).copy()).cuda()
+    pdev, _bias = kinv.sampling_params_device(plist)
     hist = torch.zeros(bsz, hist_ld, dtype=torch.int32)
     hl = torch.zeros(bsz, dtype=torch.int32)
     for b, h in enumerate(hists):
@@ -144,6 +143,52 @@ def test_presence_and_frequency_penalties(kinv):
                       OParams(**{k: getattr(zero[b], k) for k in OParams.__dataclass_fields__}))[0]
            for b in range(4)]
     assert list(a) == ref
+    assert kinv.last_device_status() == 0
+
+
+def test_logit_bias(kinv):
+    """Logit-bias lists (bans with -inf, forced ids, small biases on ids the
+    penalties also touch) match the oracle token for token; a row's bias does
+    not change its batch-mates' tokens."""
+    vocab = 151936
+    g = synth.gen(75)
+    plist, hists, steps = [], [], []
+    logits = (torch.randn(24, vocab, generator=g) * 2)
+    logits[:, :40] += 4.0
+    for b in range(24):
+        kind = b % 4
+        if kind == 0:     # ban the row's ten most likely ids
+            top = torch.topk(logits[b], 10).indices.tolist()
+            bias = {t: float("-inf") for t in top}
+        elif kind == 1:   # force one id
+            bias = {int(torch.randint(1000, vocab, (1,), generator=g)): 50.0}
+        elif kind == 2:   # small biases on history ids, with penalties on
+            bias = {t: float(torch.randn(1, generator=g)) for t in range(0, 40, 3)}
+        else:             # no bias at all
+            bias = None
+        plist.append(kinv.SamplingParams(temperature=0.0 if b % 8 == 0 else 0.9, top_k=100, top_p=0.95,
+                                         min_p=0.0, repeat_penalty=1.2, repeat_last_n=32,
+                                         presence_penalty=0.3 if kind == 2 else 0.0,
+                                         frequency_penalty=0.2 if kind == 2 else 0.0,
+                                         logit_bias=bias, seed=900 + b))
+        hists.append(torch.randint(0, 40, (50,), generator=g).tolist())
+        steps.append(11 * b)
+    logits = logits.cuda()
+    got = _run(kinv, logits, plist, hists, steps)
+    z = logits.cpu().numpy()
+    for b, p in enumerate(plist):
+        op = OParams(**{k: getattr(p, k) for k in OParams.__dataclass_fields__})
+        t, tie = sample_row(z[b], hists[b][-64:], steps[b], op)
+        if not tie:
+            assert got[b] == t, (b, got[b], t)
+        if b % 4 == 0:
+            assert got[b] not in set(p.logit_bias), (b, got[b])
+        if b % 4 == 1:
+            assert got[b] == next(iter(p.logit_bias)), (b, got[b])
+    # the rows without a bias draw the same tokens with biased rows beside them or alone
+    for b in (3, 7):
+        one = _run(kinv, logits[b: b + 1].contiguous(), plist[b: b + 1], hists[b: b + 1], steps[b: b + 1])
+        assert one[0] == got[b]
     assert kinv.last_device_status() == 0
 
 
