@@ -1,8 +1,8 @@
 """The seeded sampler (test infrastructure only).
 
 Follows Kinetic "Receipts", *Making a receipt*: a receipt records every sampler
-setting -- temperature, top_k, top_p, min_p, the repeat, presence and
-frequency penalties, logit bias, repeat_last_n -- and the seed; a request without a seed gets a fresh one that is recorded.  The
+setting -- temperature, top_k, top_p, min_p, typical-p, the repeat, presence
+and frequency penalties, logit bias, repeat_last_n -- and the seed; a request without a seed gets a fresh one that is recorded.  The
 receipt's example uses temperature 0.8, top_k 50, top_p 0.95, min_p 0.05,
 repeat_penalty 1.1, presence_penalty 0, frequency_penalty 0, repeat_last_n 64,
 seed 42.
@@ -22,10 +22,18 @@ exact forms.  The reading taken here (the usual one for these knobs):
 3. Candidates: the top_k largest z ordered by (z descending, id ascending);
    top_k <= 0 or >= V keeps every id in that order.
 4. s = z / T; e_i = exp(s_i - s_0) (s_0 is the largest, so e_0 = 1).
-5. Top-p (only if top_p < 1): keep the shortest prefix whose sum of e reaches
-   top_p * sum(e) (at least one candidate).
+4a. Typical-p (only if typical_p < 1; locally typical sampling, Meister et
+   al. 2022): with p_i = e_i / sum(e) over the candidates and
+   H = -sum p_i log p_i, order the candidates by |-log p_i - H| (then by
+   candidate order) and keep the shortest such prefix whose p reaches
+   typical_p (at least one).  The kept set keeps its candidate order and may
+   leave out the most likely id.
+5. Top-p (only if top_p < 1): over the kept candidates in candidate order,
+   keep the shortest prefix whose sum of e reaches top_p * (their sum of e)
+   (at least one candidate).
 6. Min-p (only if min_p > 0): keep the candidates with p_i >= min_p * p_max,
-   i.e. e_i >= min_p, since e_0 = 1 is the largest.
+   p_max the largest kept p, i.e. e_i >= min_p * e_first (e_first the first
+   kept e; = 1 unless typical-p left out the first candidate).
 7. Draw u = Philox4x32-10 word 0 >> 8, times 2^-24, keyed by the request seed,
    counter = the request-local token index; return the first kept candidate
    whose running sum of e exceeds u * (sum of kept e).
@@ -80,6 +88,7 @@ class SamplingParams:
     presence_penalty: float = 0.0
     frequency_penalty: float = 0.0
     logit_bias: dict = None   # {id: bias}; applied in insertion order
+    typical_p: float = 1.0
 
 
 def bias_logits(logits_f32: np.ndarray, p: SamplingParams) -> np.ndarray:
@@ -127,29 +136,55 @@ def sample_row(logits_f32: np.ndarray, history, step: int, p: SamplingParams):
     whole = len(order) > 1024
     tol = tie_tol(min(len(order), 1024)) + (whole_sum_tol(v) if whole else 0.0)
     near = False
-    keep = len(order)
+    n = len(order)
+    kept = np.ones(n, dtype=bool)               # the set, in candidate order
+    tp = float(np.float32(p.typical_p))
+    if tp < 1.0:
+        pr = e / e.sum()
+        pos = pr > 0
+        lp = np.log(np.where(pos, pr, 1.0))
+        h = -float(np.sum(np.where(pos, pr * lp, 0.0)))
+        eps = np.where(pos, np.abs(-lp - h), np.inf)
+        torder = np.lexsort((np.arange(n), eps))  # typicality ascending, then candidate order
+        cum_t = np.cumsum(pr[torder])
+        m = max(1, min(int(np.searchsorted(cum_t, tp, side="left")) + 1, n))
+        # the cut moves if the kept mass sits at typical_p, or if the last kept
+        # and the first dropped candidate are equally typical within the error
+        if np.any(np.abs(cum_t[max(0, m - 2): m] - tp) <= tol):
+            near = True
+        if m < n and abs(eps[torder[m]] - eps[torder[m - 1]]) <= 4 * tol * (1.0 + abs(h)):
+            near = True
+        kept[:] = False
+        kept[torder[:m]] = True
+    em = np.where(kept, e, 0.0)
+    keep = n
     if p.top_p < 1.0:
-        cum = np.cumsum(e)
+        cum = np.cumsum(em)
         target = float(np.float32(p.top_p)) * cum[-1]
         keep = int(np.searchsorted(cum, target, side="left")) + 1
-        keep = max(1, min(keep, len(order)))
+        keep = max(1, min(keep, n))
         # the cut moves if cum[keep-1] or cum[keep-2] sits at the target
         if np.any(np.abs(cum[max(0, keep - 2): keep] - target) <= tol * cum[-1]):
             near = True
+    first = int(np.argmax(kept))                # the first kept candidate
     if p.min_p > 0.0:
-        mp = float(np.float32(p.min_p))
-        ok = e[:keep] >= mp
-        n_ok = int(np.count_nonzero(ok))
-        # the cut moves if the last kept or the first dropped e sits at min_p
-        if np.any(np.abs(e[max(0, n_ok - 1): min(n_ok + 1, keep)] - mp) <= tol):
+        thr = float(np.float32(p.min_p)) * e[first]
+        idx_k = [j for j in range(keep) if kept[j]]
+        ok = [j for j in idx_k if e[j] >= thr]
+        drop = [j for j in idx_k if not e[j] >= thr]
+        # the cut moves if the last kept or the first dropped e sits at the threshold
+        edge = ([ok[-1]] if ok else []) + ([drop[0]] if drop else [])
+        if any(abs(e[j] - thr) <= tol for j in edge):
             near = True
-        keep = max(1, n_ok)
-    e = e[:keep]
-    cum = np.cumsum(e)
+        keep = drop[0] if drop else keep
+        keep = max(keep, first + 1)
+    em = em[:keep]
+    cum = np.cumsum(em)
     u = sampler_uniform(p.seed, step)
     target = u * cum[-1]
     idx = int(np.searchsorted(cum, target, side="right"))
-    idx = min(idx, keep - 1)
+    if idx >= keep:                               # (u < 1 never gets here) the last kept one
+        idx = max(j for j in range(keep) if kept[j])
     # the pick moves if cum[idx] or cum[idx-1] sits at the target
     if np.any(np.abs(cum[max(0, idx - 1): idx + 1] - target) <= tol * cum[-1]):
         near = True

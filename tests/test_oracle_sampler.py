@@ -140,6 +140,34 @@ def test_logit_bias_closed_form():
     assert np.signbit(bias_logits(zn, _greedy_params())[0])
 
 
+def test_typical_p_closed_form():
+    # p = (0.4, 0.3, 0.3): H = -(0.4 ln 0.4 + 0.6 ln 0.3) = 1.0889; |-ln p - H| =
+    # (0.1726, 0.1151, 0.1151): the two 0.3 ids are the most typical, so
+    # typical_p 0.5 keeps ids 1 and 2 (mass 0.6) and leaves out the most likely id
+    z = np.log(np.array([0.4, 0.3, 0.3])).astype(np.float32)
+    tp = _greedy_params(typical_p=0.5)
+    toks = [sample_row(z, [], s, tp)[0] for s in range(400)]
+    assert set(toks) == {1, 2}
+    assert 140 < toks.count(1) < 260          # ids 1 and 2 equally likely
+    # typical_p 0.25: the single most typical id (id 1: ties go by candidate order)
+    assert {sample_row(z, [], s, _greedy_params(typical_p=0.25))[0] for s in range(50)} == {1}
+    # typical_p 1: no filter (the same draws as without it)
+    for s in range(50):
+        assert sample_row(z, [], s, _greedy_params(typical_p=1.0))[0] == sample_row(z, [], s, _greedy_params())[0]
+    # min-p is relative to the largest kept probability: with ids 1 and 2 kept
+    # (e = 0.75 each), min_p 0.9 keeps both (it would keep neither, so only
+    # one, against the dropped id 0)
+    both = {sample_row(z, [], s, _greedy_params(typical_p=0.5, min_p=0.9))[0] for s in range(100)}
+    assert both == {1, 2}
+    # top-p over the kept set: p = (0.5, 0.3, 0.2), typical_p 0.5 keeps ids 0 and 1
+    # (|-ln p - H| = 0.337, 0.174, 0.580); top_p 0.6 of their mass (e 1 + 0.6)
+    # keeps id 0 alone, where 0.6 of all three (e 2.0) would keep ids 0 and 1
+    z2 = np.log(np.array([0.5, 0.3, 0.2])).astype(np.float32)
+    assert {sample_row(z2, [], s, _greedy_params(typical_p=0.5))[0] for s in range(200)} == {0, 1}
+    assert {sample_row(z2, [], s, _greedy_params(typical_p=0.5, top_p=0.6))[0] for s in range(50)} == {0}
+    assert {sample_row(z2, [], s, _greedy_params(top_p=0.6))[0] for s in range(200)} == {0, 1}
+
+
 def _freq(z, p, n, hist=()):
     toks = [sample_row(z, list(hist), s, p)[0] for s in range(n)]
     return np.bincount(toks, minlength=len(z))
