@@ -272,9 +272,13 @@ kinv_status kinv_attn_prefill(const void* q, const void* k_cache, const void* v_
  * in that window (each operation rounded to fp32);
  * temperature <= 0 -> greedy argmax (lowest id on ties); otherwise the top_k
  * candidates ordered by (z desc, id asc); s = z / temperature;
- * e_i = exp(s_i - s_0); top-p keeps the shortest prefix whose sum of e reaches
- * top_p * sum(e) (skipped when top_p >= 1); min-p keeps e_i >= min_p (skipped
- * when min_p <= 0); then u = (Philox4x32-10(counter = (step lo, step hi, 0, 0),
+ * e_i = exp(s_i - s_0); typical-p (when 0 < typical_p < 1) keeps, with
+ * p_i = e_i / sum(e) and H = -sum p_i log p_i, the shortest set of candidates
+ * taken by |-log p_i - H| ascending (then candidate order) whose p reaches
+ * typical_p, and the steps below see only that set, in candidate order;
+ * top-p keeps the shortest prefix whose sum of e reaches top_p * sum(e)
+ * (skipped when top_p >= 1); min-p keeps e_i >= min_p * e_first, e_first the
+ * first kept candidate's e (skipped when min_p <= 0); then u = (Philox4x32-10(counter = (step lo, step hi, 0, 0),
  * key = (seed lo, seed hi)).word0 >> 8) * 2^-24 picks the first kept candidate
  * whose running sum of e exceeds u * (sum of kept e).  The counter is the
  * request's own step, never its batch slot: the drawn token depends only on
@@ -291,7 +295,7 @@ kinv_status kinv_attn_prefill(const void* q, const void* k_cache, const void* v_
  * first; step: device int64 [B]; out_tokens: device int32 [B].
  * Requirements: 1 <= V; ld >= V; top_k in [1, 1024] or the whole vocabulary
  * (V <= 262144, and top_p < 1 or min_p > 0 cutting within the 1024 most
- * likely ids) unless temperature <= 0; hist_len[b] <= hist_ld <= 1024
+ * likely ids, typical-p off) unless temperature <= 0; hist_len[b] <= hist_ld <= 1024
  * (else KINV_ERR_UNSUPPORTED before launch); at most 1024 logit-bias entries
  * per row (further entries are ignored).  Rows whose
  * settings or logits fall outside this set get token -1 and the device status
@@ -313,7 +317,7 @@ typedef struct {
   float frequency_penalty;  /* 0: off */
   const kinv_logit_bias* logit_bias;  /* device, n_logit_bias entries; NULL: none */
   int32_t n_logit_bias;               /* at most 1024 */
-  int32_t reserved;                   /* 0 */
+  float typical_p;                    /* on when 0 < typical_p < 1 */
 } kinv_sampling_params;
 
 size_t kinv_sample_workspace(int B, int V);

@@ -109,6 +109,7 @@ struct Smem {
   int ok;
   int fast;
   float thresh_f;
+  float typ_h;               // typical-p: -(entropy) of the candidates
   float mk_val[kMaxMarked];  // the final logit of each marked id, by rank
   int mk_cnt[kMaxMarked];    // its count in the penalty window
 };
@@ -702,22 +703,100 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
     sm.e[i] = expf(__fsub_rn(si, s0));
   }
   __syncthreads();
-  if (warp != 0) return;
   float* P = reinterpret_cast<float*>(sm.comb);  // room for kMaxTopK
-  float carry = 0.f;
-  for (int c0 = 0; c0 < kk; c0 += 32) {
-    const int i = c0 + lane;
-    float v = i < kk ? sm.e[i] : 0.f;
+  // P[i] = v(0) + ... + v(i) over the candidates, by warp 0
+  auto prefix_sums = [&](auto&& v_of) {
+    float carry = 0.f;
+    for (int c0 = 0; c0 < kk; c0 += 32) {
+      const int i = c0 + lane;
+      float v = i < kk ? v_of(i) : 0.f;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v = __fadd_rn(v, y);
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v = __fadd_rn(v, y);
+      }
+      v = __fadd_rn(v, carry);
+      if (i < kk) P[i] = v;
+      carry = __shfl_sync(0xffffffffu, v, 31);
     }
-    v = __fadd_rn(v, carry);
-    if (i < kk) P[i] = v;
-    carry = __shfl_sync(0xffffffffu, v, 31);
+    __syncwarp();
+  };
+  if (warp == 0) prefix_sums([&](int i) { return sm.e[i]; });
+  // Typical-p (0 < typical_p < 1): p_i = e_i / P[kk-1], H = -sum p_i log p_i
+  // (lane l adds terms l, l + 32, ... in order, then a fixed butterfly); the
+  // candidates sorted by (|-log p_i - H|, i) ascending; the shortest such
+  // prefix whose p (a fixed-order warp scan) reaches typical_p is kept.
+  const bool typical = prm.typical_p > 0.f && prm.typical_p < 1.0f;
+  uint32_t* kmask = reinterpret_cast<uint32_t*>(sm.cand + 3072);  // kept candidates (typical-p)
+  if (typical) {
+    if (full) {  // typical-p over the whole vocabulary: not supported
+      if (t == 0) {
+        out[b] = -1;
+        if (status) atomicExch(status, DEV_SAMPLER_UNSUPPORTED);
+      }
+      return;
+    }
+    __syncthreads();  // P
+    const float total = P[kk - 1];
+    float* lp = reinterpret_cast<float*>(sm.cand + 2048);
+    for (int i = t; i < kk; i += kThreadsS) {
+      const float pi = __fdiv_rn(sm.e[i], total);
+      lp[i] = pi > 0.f ? logf(pi) : 0.f;
+    }
+    for (int i = t; i < 32; i += kThreadsS) kmask[i] = 0u;
+    __syncthreads();
+    if (warp == 0) {
+      float acc = 0.f;
+      for (int i = lane; i < kk; i += 32) acc = __fadd_rn(acc, __fmul_rn(__fdiv_rn(sm.e[i], total), lp[i]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+      if (lane == 0) sm.typ_h = acc;
+    }
+    __syncthreads();
+    const float h = -sm.typ_h;
+    int n2 = 1;
+    while (n2 < kk) n2 <<= 1;
+    for (int i = t; i < n2; i += kThreadsS) {
+      unsigned long long key = 0ull;  // padding sorts last
+      if (i < kk) {
+        const float pi = __fdiv_rn(sm.e[i], total);
+        const float eps = pi > 0.f ? fabsf(__fsub_rn(-lp[i], h)) : INFINITY;
+        key = composite(~ordered_key(eps), i);  // descending order = (eps, i) ascending
+      }
+      sm.cand[i] = key;
+    }
+    __syncthreads();
+    bitonic_desc(sm.cand, n2);
+    if (warp == 0) {
+      auto idx_at = [&](int i) { return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(sm.cand[i] & 0xFFFFFFFFull)); };
+      int m = kk;
+      float carry = 0.f;
+      for (int c0 = 0; c0 < kk; c0 += 32) {
+        const int i = c0 + lane;
+        float v = i < kk ? __fdiv_rn(sm.e[idx_at(i)], total) : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v = __fadd_rn(v, y);
+        }
+        v = __fadd_rn(v, carry);
+        const unsigned hit = __ballot_sync(0xffffffffu, i < kk && v >= prm.typical_p);
+        if (hit) {
+          m = c0 + __ffs(hit);
+          break;
+        }
+        carry = __shfl_sync(0xffffffffu, v, 31);
+      }
+      for (int i = lane; i < m; i += 32) {
+        const int j = idx_at(i);
+        atomicOr(&kmask[j >> 5], 1u << (j & 31));
+      }
+      __syncwarp();
+      prefix_sums([&](int i) { return (kmask[i >> 5] >> (i & 31)) & 1u ? sm.e[i] : 0.f; });
+    }
   }
-  __syncwarp();
+  if (warp != 0) return;
+  auto kept_at = [&](int j) { return !typical || ((kmask[j >> 5] >> (j & 31)) & 1u); };
   // first i < n with pred(i), else n (warp-uniform)
   auto first = [&](int n, auto&& pred) {
     for (int c0 = 0; c0 < n; c0 += 32) {
@@ -736,10 +815,12 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
     keep = i < kk ? i + 1 : kk;
     cut = i < kk;
   }
+  const int j0 = first(kk, kept_at);  // the first kept candidate (the largest kept e)
   if (prm.min_p > 0.0f) {
-    const int n = first(keep, [&](int j) { return !(sm.e[j] >= prm.min_p); });
+    const float thr = __fmul_rn(prm.min_p, sm.e[j0]);
+    const int n = first(keep, [&](int j) { return kept_at(j) && !(sm.e[j] >= thr); });
     cut = cut || n < keep;
-    keep = n > 0 ? n : 1;
+    keep = n > j0 ? n : j0 + 1;
   }
   if (full && !cut) {
     // the kept set may reach past the candidates: not supported
@@ -757,7 +838,10 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
   const float u = static_cast<float>(w.x >> 8) * (1.0f / 16777216.0f);
   const float target = __fmul_rn(u, kept);
   int pick = first(keep, [&](int j) { return P[j] > target; });
-  if (pick >= keep) pick = keep - 1;
+  if (pick >= keep) {  // (u < 1 never gets here) the last kept candidate
+    pick = keep - 1;
+    while (pick > 0 && !kept_at(pick)) --pick;
+  }
   if (lane == 0)
     out[b] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(top[pick] & 0xFFFFFFFFull));
 }

@@ -333,6 +333,7 @@ class SamplingParams:
     presence_penalty: float = 0.0
     frequency_penalty: float = 0.0
     logit_bias: dict = None   # {id: bias}, applied in insertion order
+    typical_p: float = 1.0    # on when 0 < typical_p < 1
 
 
 def sampling_params_device(params_list, device="cuda"):

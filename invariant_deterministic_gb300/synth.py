@@ -80,7 +80,7 @@ def layer_weights(d: int, n_q: int, n_kv: int, head_dim: int, ffn: int, seed: in
 SAMPLING_DTYPE = np.dtype([("temperature", "<f4"), ("top_p", "<f4"), ("min_p", "<f4"),
                            ("repeat_penalty", "<f4"), ("top_k", "<i4"), ("repeat_last_n", "<i4"),
                            ("seed", "<u8"), ("presence_penalty", "<f4"), ("frequency_penalty", "<f4"),
-                           ("logit_bias", "<u8"), ("n_logit_bias", "<i4"), ("reserved", "<i4")])
+                           ("logit_bias", "<u8"), ("n_logit_bias", "<i4"), ("typical_p", "<f4")])
 BIAS_DTYPE = np.dtype([("id", "<i4"), ("bias", "<f4")])
 
 
@@ -106,5 +106,6 @@ def sampling_struct(params_list, bias_base: int = 0) -> np.ndarray:
             raise ValueError("a logit-bias list needs bias_base (the entries' device address)")
         a[i] = (p.temperature, p.top_p, p.min_p, p.repeat_penalty, p.top_k, p.repeat_last_n, p.seed,
                 getattr(p, "presence_penalty", 0.0), getattr(p, "frequency_penalty", 0.0),
-                bias_base + BIAS_DTYPE.itemsize * starts[i] if nb else 0, nb, 0)
+                bias_base + BIAS_DTYPE.itemsize * starts[i] if nb else 0, nb,
+                getattr(p, "typical_p", 1.0))
     return a

@@ -22,7 +22,7 @@ exact forms.  The reading taken here (the usual one for these knobs):
 3. Candidates: the top_k largest z ordered by (z descending, id ascending);
    top_k <= 0 or >= V keeps every id in that order.
 4. s = z / T; e_i = exp(s_i - s_0) (s_0 is the largest, so e_0 = 1).
-4a. Typical-p (only if typical_p < 1; locally typical sampling, Meister et
+4a. Typical-p (only if 0 < typical_p < 1; locally typical sampling, Meister et
    al. 2022): with p_i = e_i / sum(e) over the candidates and
    H = -sum p_i log p_i, order the candidates by |-log p_i - H| (then by
    candidate order) and keep the shortest such prefix whose p reaches
@@ -139,7 +139,7 @@ def sample_row(logits_f32: np.ndarray, history, step: int, p: SamplingParams):
     n = len(order)
     kept = np.ones(n, dtype=bool)               # the set, in candidate order
     tp = float(np.float32(p.typical_p))
-    if tp < 1.0:
+    if 0.0 < tp < 1.0:
         pr = e / e.sum()
         pos = pr > 0
         lp = np.log(np.where(pos, pr, 1.0))

@@ -192,6 +192,41 @@ def test_logit_bias(kinv):
     assert kinv.last_device_status() == 0
 
 
+def test_typical_p(kinv):
+    """Typical-p with top-k, top-p, min-p and temperature against the oracle;
+    over the whole vocabulary it is not supported (token -1)."""
+    vocab = 151936
+    g = synth.gen(76)
+    variants = [
+        dict(temperature=1.0, top_k=50, top_p=1.0, min_p=0.0, typical_p=0.5),
+        dict(temperature=0.8, top_k=200, top_p=0.95, min_p=0.05, typical_p=0.9),
+        dict(temperature=1.3, top_k=1024, top_p=1.0, min_p=0.1, typical_p=0.2),
+        dict(temperature=0.7, top_k=20, top_p=0.8, min_p=0.0, typical_p=0.95),
+    ]
+    plist, steps = [], []
+    for i, v in enumerate(variants):
+        for j in range(8):
+            plist.append(kinv.SamplingParams(**v, repeat_penalty=1.1, repeat_last_n=16, seed=77 * i + j))
+            steps.append(5 * i + j)
+    hists = [torch.randint(0, 50, (20,), generator=g).tolist() for _ in plist]
+    logits = (torch.randn(len(plist), vocab, generator=g) * 2.5).cuda()
+    got = _run(kinv, logits, plist, hists, steps)
+    ref, ties = _oracle(logits, plist, hists, steps)
+    assert ties.sum() <= 8, f"{ties.sum()} near ties"
+    assert np.array_equal(got[~ties], ref[~ties]), np.nonzero(got != ref)
+    # a typical-p pick can leave out the most likely id: seen in these rows
+    z = logits.cpu().numpy()
+    top1 = z.argmax(axis=1)
+    assert np.any(got[:8] != top1[:8])
+    assert kinv.last_device_status() == 0
+    whole = [kinv.SamplingParams(temperature=1.0, top_k=0, top_p=0.9, min_p=0.0, typical_p=0.5,
+                                 repeat_penalty=1.0, repeat_last_n=0, seed=1)]
+    out = _run(kinv, logits[:1].contiguous(), whole, [[]], [0])
+    assert out[0] == -1
+    assert kinv.last_device_status() == kinv.ERR_UNSUPPORTED
+    assert kinv.last_device_status() == 0
+
+
 def test_exact_ties_take_lowest_ids(kinv):
     vocab = 151936
     logits = torch.zeros(3, vocab, device="cuda")
