@@ -217,7 +217,9 @@ def run_prefill(dec, shape, chunk, prompt_len, stream, tc_peak):
                      "unit": "TFLOP/s", "frac": round(gemm_tflops / tc_peak, 4),
                      "ms": round(gemm_ms, 3)},
             "whole_pass": {"achieved": round(all_tflops, 1), "unit": "TFLOP/s",
-                           "frac": round(all_tflops / tc_peak, 4)}}
+                           "frac": round(all_tflops / tc_peak, 4)},
+            # per stage, from the instrumented (serialised) pass
+            "stage_ms": {k: round(sum(a.elapsed_time(b) for a, b in v), 3) for k, v in sorted(timer.items())}}
 
 
 def run_kinv(args):

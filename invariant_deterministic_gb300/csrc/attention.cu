@@ -39,6 +39,7 @@ constexpr int kSplit = 256;      // keys per split (the fixed split size)
 constexpr int kThreads = 256;    // eight warps, 32 keys each for the scores
 constexpr int kRowsMma = 16;     // (row, head) pairs of one block: the MMA's 16 rows
 constexpr int kMaxG = 8;         // query heads per kv head
+constexpr int kPrefillTiles = 4; // prefill: 16-row MMA tiles of (row, head) pairs per block
 
 struct AttnParams {
   const __nv_bfloat16* q;
@@ -333,6 +334,260 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   }
 }
 
+// The split kernel for prefill: MT 16-row MMA tiles of (row, head) pairs per
+// block, sharing the block's K and V tiles (so each tile load serves MT times
+// the rows).  Every pair is one MMA row and meets exactly the arithmetic of
+// attn_split_kernel (the same MMAs in the same order, the same softmax, sums
+// and rounding), so a prefill row has the bits of the decode row.
+template <int D, int MT>
+__global__ void __launch_bounds__(kThreads, 2) attn_split_tiles_kernel(const AttnParams p) {
+  constexpr int C8 = D / 8;               // 16-byte chunks per key row
+  constexpr int SUB = 64;                 // keys per load stage
+  constexpr int NSUB = kSplit / SUB;      // the K stages are reused for V
+  constexpr int KS = D / 16;              // 16-wide k steps of q . k
+  constexpr int PR = kRowsMma * MT;       // (row, head) pairs of a block
+  // Tiles in shared memory, rows of 16-byte chunks; chunk c of row r is
+  // stored at chunk c ^ (r & 7), so the eight row addresses of every ldmatrix
+  // phase fall in eight different bank groups.
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(smem_raw);                 // [256][D]
+  __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(smem_raw + kSplit * D * 2);  // P [PR][256]
+  // the block's q rows [PR][D] (swizzled like K) live where P goes, until the scores are done
+  __nv_bfloat16* qs = pt;
+  static_assert(kRowsMma * MT * D <= kRowsMma * MT * kSplit, "q rows fit in the P tile");
+  __shared__ float wmax[kThreads / 32][PR];
+  __shared__ float wsum[kThreads / 32][PR];
+
+  pdl_launch_dependents();
+  pdl_wait();
+  RowSet rs;
+  if (!block_rows(p, rs)) return;
+  // kv heads are the fastest grid index: the blocks reading the 256-byte
+  // slices of the same token rows run side by side
+  const int g = blockIdx.x;
+  const int s = blockIdx.y;
+  const int k0 = s * kSplit;
+  const int lenmax = rs.len0 + rs.nrows - 1;           // the last row sees the most keys
+  const int nmax = min(kSplit, lenmax - k0);
+  if (nmax <= 0) return;
+  const int G = p.G;
+  const int RG = rs.nrows * G;                         // (row, head) pairs: MMA rows 0..RG-1
+  const int t = threadIdx.x;
+  const int lane = t & 31, warp = t >> 5;
+  const int gq = lane >> 2, tq = lane & 3;             // fragment row / column group
+  const int64_t seq_off = rs.seq * p.seq_stride + static_cast<int64_t>(k0) * p.tok_stride + g * D;
+  const uint32_t kv_base = smem_addr(kv);
+  const uint32_t pt_base = smem_addr(pt);
+  auto count = [&](int r) { return r < RG ? min(kSplit, rs.len0 + r / G - k0) : 0; };
+
+  auto load_sub = [&](const __nv_bfloat16* src, int j) {
+    const int rows = min(SUB, nmax - j * SUB);
+    for (int idx = t; idx < rows * C8; idx += kThreads) {
+      const int r = idx / C8, c = idx % C8;
+      const int key = j * SUB + r;
+      cp_async16(kv_base + static_cast<uint32_t>(key * D * 2 + ((c ^ (key & 7)) << 4)),
+                 src + seq_off + static_cast<int64_t>(key) * p.tok_stride + c * 8);
+    }
+  };
+#pragma unroll
+  for (int j = 0; j < NSUB; ++j) load_sub(p.k, j);
+  cp_async_commit();
+
+  // the q rows of the block's pairs, once (pair r: row r / G, head g * G + r % G);
+  // rows of pairs past RG, in a tile that has pairs, read as zero
+  const uint32_t qs_base = smem_addr(qs);
+  const int tiles = (RG + kRowsMma - 1) / kRowsMma;
+  for (int idx = t; idx < tiles * kRowsMma * C8; idx += kThreads) {
+    const int r = idx / C8, c = idx % C8;
+    if (r < RG)
+      cp_async16(qs_base + static_cast<uint32_t>(r * D * 2 + ((c ^ (r & 7)) << 4)),
+                 p.q + (static_cast<int64_t>(rs.row0 + r / G) * p.Hq + g * G + r % G) * D + c * 8);
+    else
+      *reinterpret_cast<uint4*>(qs + r * D + ((c ^ (r & 7)) << 3)) = make_uint4(0, 0, 0, 0);
+  }
+  cp_async_commit();
+  uint32_t qa[KS][4];
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // --- scores: warp w owns keys 32w .. 32w + 31 (four 8-key n blocks), for
+  // every tile of pairs
+  float sc[MT][4][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sc[mt][nb][i] = 0.f;
+    if (mt * kRowsMma >= RG) continue;  // (block-uniform)
+    // q fragments (A operand) of tile mt: lane l gives row mt * 16 + (l & 15),
+    // 8-column block 2 ks + (l >> 4) -- the MMA's a0..a3
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int qrow = mt * kRowsMma + (lane & 15);
+      const int c = 2 * ks + (lane >> 4);
+      ldsm_x4(qs_base + static_cast<uint32_t>(qrow * D * 2 + ((c ^ (qrow & 7)) << 4)), qa[ks][0], qa[ks][1],
+              qa[ks][2], qa[ks][3]);
+    }
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) {
+      const int key = warp * 32 + nb * 8 + (lane & 7);
+#pragma unroll
+      for (int kp = 0; kp < KS / 2; ++kp) {
+        const int c = kp * 4 + (lane >> 3);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kv_base + static_cast<uint32_t>(key * D * 2 + ((c ^ (key & 7)) << 4)), b0, b1, b2, b3);
+        mma_bf16_16816(sc[mt][nb], qa[2 * kp], b0, b1);
+        mma_bf16_16816(sc[mt][nb], qa[2 * kp + 1], b2, b3);
+      }
+    }
+  }
+  __syncthreads();  // every warp is done with K: the stages take V now
+#pragma unroll
+  for (int j = 0; j < NSUB; ++j) load_sub(p.v, j);
+  // keys the split does not hold read as zero (their weights are zero, and a
+  // stale NaN times zero would not be)
+  for (int idx = t; idx < (kSplit - nmax) * C8; idx += kThreads) {
+    const int key = nmax + idx / C8, c = idx % C8;
+    *reinterpret_cast<uint4*>(kv + key * D + ((c ^ (key & 7)) << 3)) = make_uint4(0, 0, 0, 0);
+  }
+  cp_async_commit();
+
+  // --- softmax statistics.  A lane holds rows gq and gq + 8 of each tile,
+  // keys 32w + 8nb + 2tq (+1).  Maxima: lane, then the four lanes of a row
+  // (exact), then the eight warps.  Weights are rounded to bf16 once; the sum
+  // adds the rounded weights: a lane's eight in (nb, pair) order, a fixed
+  // butterfly over the four lanes, the eight warps in ascending order.
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    if (mt * kRowsMma >= RG) continue;
+    const int r_lo = mt * kRowsMma + gq, r_hi = r_lo + 8;
+    const int cnt_lo = count(r_lo), cnt_hi = count(r_hi);
+    float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = warp * 32 + nb * 8 + 2 * tq + e;
+        sc[mt][nb][e] = key < cnt_lo ? __fmul_rn(sc[mt][nb][e], p.scale) : -INFINITY;
+        sc[mt][nb][2 + e] = key < cnt_hi ? __fmul_rn(sc[mt][nb][2 + e], p.scale) : -INFINITY;
+        mx_lo = fmaxf(mx_lo, sc[mt][nb][e]);
+        mx_hi = fmaxf(mx_hi, sc[mt][nb][2 + e]);
+      }
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, o));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, o));
+    }
+    if (tq == 0) {
+      wmax[warp][r_lo] = mx_lo;
+      wmax[warp][r_hi] = mx_hi;
+    }
+  }
+  __syncthreads();
+  float m_lo[MT], m_hi[MT];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    m_lo[mt] = m_hi[mt] = -INFINITY;
+    if (mt * kRowsMma >= RG) continue;
+    const int r_lo = mt * kRowsMma + gq, r_hi = r_lo + 8;
+    m_lo[mt] = wmax[0][r_lo];
+    m_hi[mt] = wmax[0][r_hi];
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) {
+      m_lo[mt] = fmaxf(m_lo[mt], wmax[w][r_lo]);
+      m_hi[mt] = fmaxf(m_hi[mt], wmax[w][r_hi]);
+    }
+    float sum_lo = 0.f, sum_hi = 0.f;
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) {
+      float e4[4];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float xl = sc[mt][nb][e] == -INFINITY ? 0.f : expf(__fsub_rn(sc[mt][nb][e], m_lo[mt]));
+        const float xh = sc[mt][nb][2 + e] == -INFINITY ? 0.f : expf(__fsub_rn(sc[mt][nb][2 + e], m_hi[mt]));
+        e4[e] = __bfloat162float(__float2bfloat16_rn(xl));
+        e4[2 + e] = __bfloat162float(__float2bfloat16_rn(xh));
+        sum_lo = __fadd_rn(sum_lo, e4[e]);
+        sum_hi = __fadd_rn(sum_hi, e4[2 + e]);
+      }
+      const int kc = warp * 4 + nb;                       // 8-key chunk of P
+      const uint32_t off_lo = static_cast<uint32_t>(r_lo * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
+      const uint32_t off_hi = static_cast<uint32_t>(r_hi * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_lo) = pack_bf16(e4[0], e4[1]);
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_hi) = pack_bf16(e4[2], e4[3]);
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      sum_lo = __fadd_rn(sum_lo, __shfl_xor_sync(0xffffffffu, sum_lo, o));
+      sum_hi = __fadd_rn(sum_hi, __shfl_xor_sync(0xffffffffu, sum_hi, o));
+    }
+    if (tq == 0) {
+      wsum[warp][r_lo] = sum_lo;
+      wsum[warp][r_hi] = sum_hi;
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // --- o = P . V: warp w owns columns 16w .. 16w + 15 (two 8-wide n
+  // blocks) over all 256 keys, sixteen k steps of 16 keys in ascending order;
+  // each V fragment serves every tile.
+  if (warp < D / 16) {
+    float oc[MT][2][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+      for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) oc[mt][nb][i] = 0.f;
+#pragma unroll 4
+    for (int kk = 0; kk < kSplit / 16; ++kk) {
+      uint32_t b0, b1, b2, b3;
+      {
+        const int key = kk * 16 + (lane & 15);
+        const int c = warp * 2 + (lane >> 4);
+        ldsm_x4_t(kv_base + static_cast<uint32_t>(key * D * 2 + ((c ^ (key & 7)) << 4)), b0, b1, b2, b3);
+      }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        if (mt >= tiles) continue;
+        uint32_t a[4];
+        const int prow = mt * kRowsMma + (lane & 15);
+        const int kc = 2 * kk + (lane >> 4);
+        ldsm_x4(pt_base + static_cast<uint32_t>(prow * kSplit * 2 + ((kc ^ (prow & 7)) << 4)), a[0], a[1],
+                a[2], a[3]);
+        mma_bf16_16816(oc[mt][0], a, b0, b1);
+        mma_bf16_16816(oc[mt][1], a, b2, b3);
+      }
+    }
+    // rows gq and gq + 8 of each tile, columns 16w + 8nb + 2tq (+1)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = mt * kRowsMma + gq + 8 * h;
+        if (r < RG && count(r) > 0) {
+          const int row = r / G, i = r % G;
+          const int64_t base = (static_cast<int64_t>(rs.row0 + row) * p.Hq + g * G + i) * p.S + s;
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb)
+            *reinterpret_cast<float2*>(p.ws_o + base * D + warp * 16 + nb * 8 + 2 * tq) =
+                make_float2(oc[mt][nb][2 * h], oc[mt][nb][2 * h + 1]);
+          if (warp == 0 && tq == 0) {
+            float l = wsum[0][r];
+#pragma unroll
+            for (int w = 1; w < kThreads / 32; ++w) l = __fadd_rn(l, wsum[w][r]);
+            p.ws_ml[base * 2 + 0] = h ? m_hi[mt] : m_lo[mt];
+            p.ws_ml[base * 2 + 1] = l;
+          }
+        }
+      }
+    }
+  }
+}
+
 // One block per (query head, row); thread d folds column d.
 template <int D>
 __global__ void attn_merge_kernel(const AttnParams p) {
@@ -386,24 +641,30 @@ __global__ void attn_merge_kernel(const AttnParams p) {
   *dst = __float2bfloat16_rn(__fdiv_rn(o_acc, l_acc));
 }
 
-template <int D>
+template <int D, int MT>
 size_t split_smem_bytes() {
-  return static_cast<size_t>(kSplit) * D * 2 + static_cast<size_t>(kRowsMma) * kSplit * 2;
+  return static_cast<size_t>(kSplit) * D * 2 + static_cast<size_t>(kRowsMma) * MT * kSplit * 2;
 }
 
-template <int D>
+// MT == 1: attn_split_kernel (decode); otherwise attn_split_tiles_kernel.
+template <int D, int MT>
 kinv_status launch(const AttnParams& p, dim3 split_grid, dim3 merge_grid, cudaStream_t stream) {
-  const size_t smem = split_smem_bytes<D>();
+  void (*kernel)(const AttnParams);
+  if constexpr (MT == 1)
+    kernel = attn_split_kernel<D>;
+  else
+    kernel = attn_split_tiles_kernel<D, MT>;
+  const size_t smem = split_smem_bytes<D, MT>();
   static bool configured[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KINV_ERR_CUDA;
   if (dev < 64 && !configured[dev]) {
-    if (cudaFuncSetAttribute(attn_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(split_smem_bytes<D>())) != cudaSuccess)
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
       return KINV_ERR_CUDA;
     configured[dev] = true;
   }
-  const kinv_status st = launch_kernel(attn_split_kernel<D>, split_grid, dim3(kThreads), smem, stream, 1, p);
+  const kinv_status st = launch_kernel(kernel, split_grid, dim3(kThreads), smem, stream, 1, p);
   if (st != KINV_OK) return st;
   return launch_kernel(attn_merge_kernel<D>, merge_grid, dim3(D), 0, stream, 1, p);
 }
@@ -475,8 +736,8 @@ extern "C" kinv_status kinv_attn_decode(const void* q, const void* k_cache, cons
   p.rg_cap = ((p.G + 3) / 4) * 4;
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   const dim3 split_grid(Hkv, S, B), merge_grid(Hq, B, 1);
-  return D == 128 ? launch<128>(p, split_grid, merge_grid, stream)
-                  : launch<64>(p, split_grid, merge_grid, stream);
+  return D == 128 ? launch<128, 1>(p, split_grid, merge_grid, stream)
+                  : launch<64, 1>(p, split_grid, merge_grid, stream);
 }
 
 extern "C" size_t kinv_attn_prefill_workspace(int total_rows, int Hq, int D, int max_kv,
@@ -517,16 +778,16 @@ extern "C" kinv_status kinv_attn_prefill(const void* q, const void* k_cache, con
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.G = Hq / Hkv;
-  p.R = kRowsMma / p.G;
+  p.R = kRowsMma * kPrefillTiles / p.G;
   p.S = S;
   p.groups_per_seq = (max_q_len + p.R - 1) / p.R;
-  p.rg_cap = ((p.R * p.G + 3) / 4) * 4;
+  p.rg_cap = p.R * p.G;
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   const int64_t groups = static_cast<int64_t>(B) * p.groups_per_seq;
   if (groups > 65535 || max_q_len > 65535 || B > 65535) return KINV_ERR_UNSUPPORTED;
   const dim3 split_grid(Hkv, S, static_cast<unsigned>(groups)), merge_grid(Hq, max_q_len, B);
-  return D == 128 ? launch<128>(p, split_grid, merge_grid, stream)
-                  : launch<64>(p, split_grid, merge_grid, stream);
+  return D == 128 ? launch<128, kPrefillTiles>(p, split_grid, merge_grid, stream)
+                  : launch<64, kPrefillTiles>(p, split_grid, merge_grid, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -604,6 +865,6 @@ extern "C" kinv_status kinv_attn_decode_noalloc(const void* q, const void* k_cac
   p.rg_cap = ((p.G + 3) / 4) * 4;
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
   const dim3 split_grid(Hkv, S, B), merge_grid(Hq, B, 1);
-  return D == 128 ? launch<128>(p, split_grid, merge_grid, stream)
-                  : launch<64>(p, split_grid, merge_grid, stream);
+  return D == 128 ? launch<128, 1>(p, split_grid, merge_grid, stream)
+                  : launch<64, 1>(p, split_grid, merge_grid, stream);
 }

@@ -246,8 +246,9 @@ class Decoder:
 
         def attention(li, n, kc, vc):
             # a one-sequence view of the cache keeps the sequence index at 0
-            kinv.attn_prefill(self.q[:n], kc[seq: seq + 1], vc[seq: seq + 1], q_start, q_len,
-                              q_off, n, p0 + n, out=self.attn[:n], workspace=self.ws)
+            with self._t("attn_prefill"):
+                kinv.attn_prefill(self.q[:n], kc[seq: seq + 1], vc[seq: seq + 1], q_start, q_len,
+                                  q_off, n, p0 + n, out=self.attn[:n], workspace=self.ws)
         kinv.row_sumsq(self.x[:rows], self.ss[:rows])
         for li in range(self.s.n_layers):
             self.layer(li, rows, seq_t, pos_t, attention)
