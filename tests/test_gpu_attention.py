@@ -69,7 +69,8 @@ def test_decode_config3_invariance_and_sampled_parity(kinv):
         assert_close(f64(out[b: b + 1]), obf.to_f64(ref), f"oracle seq {b} (L={n})")
 
 
-@pytest.mark.parametrize("hq,hkv,d", [(4, 2, 64), (32, 8, 128)])
+# 2, 4, 8 and 1 query heads per kv head: 32, 16, 8 and 64 rows per prefill block
+@pytest.mark.parametrize("hq,hkv,d", [(4, 2, 64), (32, 8, 128), (8, 1, 128), (2, 2, 64)])
 def test_prefill_parity_chunk_invariance_and_decode_equality(kinv, hq, hkv, d):
     lmax, p0, t_len = 1100, 200, 700
     k, v = _cache(1, lmax, hkv, d, 40)
