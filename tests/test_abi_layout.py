@@ -51,3 +51,23 @@ def test_struct_layouts_match_the_header(tmp_path):
     assert ctypes.sizeof(kinv.GemmFusion) == c[("kinv_gemm_fusion", "size")]
     for f, _ in kinv.GemmFusion._fields_:
         assert getattr(kinv.GemmFusion, f).offset == c[("kinv_gemm_fusion", f)], f
+
+
+def test_sampling_struct_packing():
+    """Row i's logit_bias points at its first entry of bias_entries(), its
+    count and every other setting land in their fields; a bias list needs a
+    device base address."""
+    P = kinv.SamplingParams
+    rows = [P(seed=1), P(seed=2, logit_bias={5: 1.5, 9: -2.0}, typical_p=0.5),
+            P(seed=3, presence_penalty=0.25, frequency_penalty=0.5), P(seed=4, logit_bias={7: 3.0})]
+    entries, starts = synth.bias_entries(rows)
+    assert starts == [0, 0, 2, 2]
+    assert entries.tolist() == [(5, 1.5), (9, -2.0), (7, 3.0)]
+    a = synth.sampling_struct(rows, bias_base=0x10000)
+    assert a["logit_bias"].tolist() == [0, 0x10000, 0, 0x10000 + 2 * synth.BIAS_DTYPE.itemsize]
+    assert a["n_logit_bias"].tolist() == [0, 2, 0, 1]
+    assert a["seed"].tolist() == [1, 2, 3, 4]
+    assert a["typical_p"].tolist() == [1.0, 0.5, 1.0, 1.0]
+    assert a["presence_penalty"].tolist()[2] == 0.25 and a["frequency_penalty"].tolist()[2] == 0.5
+    with pytest.raises(ValueError):
+        synth.sampling_struct(rows)
