@@ -27,7 +27,9 @@
  *    host before any launch.  Launch failures return KINV_ERR_CUDA.  A device
  *    wait that runs out of time (every spin in the kernels is bounded) records
  *    a code in a device status word that kinv_last_device_status() reports.
- *  - Calls are thread-safe; the only global state is per-device attributes.
+ *  - Calls are thread-safe; the only global state is a lock-guarded cache,
+ *    per CUDA context, of device attributes, of the device address of the
+ *    status word and of kernel shared-memory limits.
  */
 #ifndef KINV_H
 #define KINV_H
@@ -65,9 +67,22 @@ const char* kinv_device_class(void);
 const char* kinv_build_id(void);
 
 /* Synchronises `stream`, then returns and clears the device status word of the
- * current device: KINV_OK, or KINV_ERR_TIMEOUT if a bounded wait gave up since
- * the last call.  Returns KINV_ERR_CUDA if the synchronisation itself fails. */
+ * current device: KINV_OK, or the last code recorded since the previous call --
+ * KINV_ERR_TIMEOUT (a bounded wait gave up), KINV_ERR_INVALID_ARG (an
+ * attention call met a device-side length outside its stated bounds) or
+ * KINV_ERR_UNSUPPORTED (a sampler row outside the supported settings).
+ * Returns KINV_ERR_CUDA if the synchronisation itself fails. */
 int kinv_last_device_status(kinv_stream stream);
+
+/* Self-test of the bounded device waits (no counterpart on the pages; the
+ * failure-detection rule every kernel here follows): launches one thread
+ * block that waits on a shared-memory barrier nothing ever completes, for at
+ * most limit_ns nanoseconds (1000 <= limit_ns <= 100000000), with the same
+ * bounded-wait code the GEMM's pipeline waits use.  The wait gives up, records
+ * KINV_ERR_TIMEOUT in the status word and the block exits, so the next
+ * kinv_last_device_status() returns KINV_ERR_TIMEOUT and the context stays
+ * usable.  Errors: KINV_ERR_INVALID_ARG for a limit outside the range. */
+kinv_status kinv_test_bounded_wait(int64_t limit_ns, kinv_stream stream);
 
 /* ------------------------------------------------------------------ GEMM
  * C[M][N] = A[M][K] . W[N][K]^T   ("Deterministic and bit-exact inference",
@@ -93,7 +108,8 @@ kinv_status kinv_gemm(const void* A, int64_t lda, const void* W, int64_t ldw,
  * projection h . W^T, which equals (x . (W * g)^T) / rms(x) with the gain g
  * folded into W's columns once.  So:
  *  - a producing projection (`resid`) adds its bf16 output to the residual
- *    stream in its epilogue, resid[m][n] = bf16(resid[m][n] + bf16(out)),
+ *    stream in its epilogue, resid[m][n] = bf16(resid[m][n] + out) with out
+ *    the fp32 product (one rounding: the projection's output is not stored),
  *    and leaves the new row's sum of squares over each 128-column tile in
  *    ss_out[m][n / 128] (no other output; C may be NULL);
  *  - a consuming projection (`row_ss`) multiplies its fp32 result row m by
@@ -190,12 +206,17 @@ kinv_status kinv_rmsnorm(void* x, int64_t ldx, const void* residual,
  * (max, sum of exponentials, unnormalised output) and the partials are folded
  * in ascending split order.  The cut depends only on L_b, so a sequence's bits
  * do not depend on its batch-mates or their lengths.  L_b == 0 gives zeros.
+ * Within a split the softmax weights e = exp(s - max) are formed in fp32 and
+ * enter the tensor cores as the bf16 pair hi = bf16(e), lo = bf16(e - hi)
+ * (P.V = hi.V + lo.V, each in fp32), so they keep about 16 significant bits.
  *
  * q, out: device bf16 [B][Hq][D] (contiguous).  k_cache, v_cache: device bf16;
  *   element (b, j, g, d) is at b*seq_stride + j*tok_stride + g*D + d
  *   (elements); e.g. a contiguous [B][Lmax][Hkv][D] cache has
  *   seq_stride = Lmax*Hkv*D, tok_stride = Hkv*D.
- * kv_len: device int32 [B], each in [0, Lmax].
+ * kv_len: device int32 [B], each in [0, Lmax]; a sequence whose kv_len lies
+ *   outside gets zeros, and the status word records KINV_ERR_INVALID_ARG
+ *   (no key beyond Lmax is read).
  * workspace: device, at least kinv_attn_decode_workspace(B, Hq, D, Lmax,
  *   split_len) bytes, 16-byte aligned.
  * Requirements: D in {64, 128}; Hq % Hkv == 0; Hq / Hkv in {1, 2, 4, 8};
@@ -223,8 +244,10 @@ kinv_status kinv_attn_decode(const void* q, const void* k_cache, const void* v_c
  *  - A call whose partials need more than KINV_NOALLOC_SCRATCH_BYTES (that is,
  *    kinv_attn_decode_workspace(B, Hq, D, Lmax, split_len) is larger) returns
  *    KINV_ERR_WORKSPACE and launches nothing.
- *  - The first call on each device looks up the array's device address (with
- *    that device current); make that first call before any stream capture.
+ *  - The first call in each CUDA context (normally once per device) looks up
+ *    the array's device address with that device current, checks the lookup
+ *    and caches the address for that context; make that first call before any
+ *    stream capture.
  *  - Every call on a device shares the one array, which keeps whatever the
  *    last call left in it (each call writes every partial it later reads, so
  *    nothing needs clearing).  Calls that overlap on the GPU -- on two streams,
@@ -249,7 +272,10 @@ kinv_status kinv_attn_decode_noalloc(const void* q, const void* k_cache, const v
  * q, out: device bf16 [total_rows][Hq][D].  q_start, q_len, q_offset: device
  * int32 [B].  Caches and strides as for decode.  max_q_len bounds q_len[b],
  * max_kv bounds q_start[b] + q_len[b] (both used to size the grid and the
- * workspace).  Requirements as for decode. */
+ * workspace), and q_offset[b] + q_len[b] <= total_rows; a sequence whose
+ * device-side values break one of these bounds (or is negative) is left out
+ * -- its rows of `out` are not written -- and the status word records
+ * KINV_ERR_INVALID_ARG.  Requirements as for decode. */
 size_t kinv_attn_prefill_workspace(int total_rows, int Hq, int D, int max_kv, int split_len);
 kinv_status kinv_attn_prefill(const void* q, const void* k_cache, const void* v_cache,
                               int64_t seq_stride, int64_t tok_stride,

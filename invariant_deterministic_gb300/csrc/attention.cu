@@ -12,11 +12,16 @@
 //   s_t  = (q . k_t) * scale   warp w forms keys 32w..32w+31: eight 16-wide
 //                              k steps of d, ascending, accumulated in fp32
 //   m    = max_t s_t           (max is exact in any order)
-//   p_t  = bf16(exp(s_t - m))  the weights are rounded to bf16 once
-//   l    = sum_t p_t           a lane's eight keys in order, a fixed
+//   e_t  = exp(s_t - m)        in fp32, then carried as the bf16 pair
+//   hi_t = bf16(e_t), lo_t = bf16(e_t - hi_t)   (about 16 significant bits)
+//   l    = sum_t (hi_t + lo_t) a lane's eight keys in order, a fixed
 //                              butterfly over four lanes, warps in order
-//   o[d] = sum_t p_t v_t[d]    sixteen 16-key k steps, ascending, in fp32
-// and (m, l, o) is stored as the split's fp32 partial.  A key a pair cannot
+//   o[d] = sum_t hi_t v_t[d] + sum_t lo_t v_t[d]
+//                              each sum sixteen 16-key k steps, ascending,
+//                              in fp32; the two sums added once at the end
+// and (m, l, o) is stored as the split's fp32 partial.  The tensor cores take
+// P one bf16 half at a time: P's tile holds hi for the first pass and lo for
+// the second (the lo values wait in registers).  A key a pair cannot
 // see (beyond its count) gets p_t = 0; keys past the split's end read zero V.
 // An MMA row depends only on its own q row and weights, so a pair's bits are
 // the same whichever pairs share the block.
@@ -59,7 +64,31 @@ struct AttnParams {
   int groups_per_seq;       // prefill: ceil(max_q_len / R)
   int rg_cap;               // R * G: sizes the query and weight buffers
   float scale;
+  // bounds the device-side lengths must keep (the host cannot read them):
+  // decode 0 <= kv_len[b] <= max_len; prefill 0 <= q_len[b] <= max_q_len,
+  // 0 <= q_start[b] <= max_len - q_len[b], 0 <= q_offset[b] <= total_rows - q_len[b]
+  int max_len;              // decode: Lmax; prefill: max_kv
+  int max_q_len;
+  int total_rows;
+  int* status;              // device status word (a sequence outside the bounds)
 };
+
+// A sequence whose device-side lengths break the bounds above is left out
+// (decode writes zeros for it, prefill leaves its rows untouched) and the call
+// records DEV_ATTN_BAD_LENGTH, so no access leaves the caller's buffers.
+__device__ __forceinline__ bool seq_ok(const AttnParams& p, int b) {
+  if (!p.prefill) {
+    const int n = p.kv_len[b];
+    return n >= 0 && n <= p.max_len;
+  }
+  const int n = p.q_len[b], st = p.q_start[b], off = p.q_offset[b];
+  return n >= 0 && n <= p.max_q_len && st >= 0 && st <= p.max_len - n && off >= 0 &&
+         off <= p.total_rows - n;
+}
+
+__device__ __forceinline__ void report_bad_length(const AttnParams& p) {
+  if (threadIdx.x == 0 && p.status) atomicExch(p.status, DEV_ATTN_BAD_LENGTH);
+}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -81,6 +110,11 @@ struct RowSet {
 };
 
 __device__ __forceinline__ bool block_rows(const AttnParams& p, RowSet& rs) {
+  const int bq = p.prefill ? static_cast<int>(blockIdx.z) / p.groups_per_seq : static_cast<int>(blockIdx.z);
+  if (!seq_ok(p, bq)) {
+    report_bad_length(p);
+    return false;
+  }
   if (!p.prefill) {
     const int b = blockIdx.z;
     rs.nrows = 1;
@@ -121,6 +155,14 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       "{%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// A softmax weight as the pair hi + lo of bf16 values: hi = bf16(x) and
+// lo = bf16(x - hi) (x - hi is exact in fp32), so hi + lo carries x to about
+// 16 significant bits where bf16 alone keeps 8.
+__device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
+  hi = __bfloat162float(__float2bfloat16_rn(x));
+  lo = __bfloat162float(__float2bfloat16_rn(__fsub_rn(x, hi)));
 }
 
 template <int D>
@@ -255,24 +297,31 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
     m_hi = fmaxf(m_hi, wmax[w][gq + 8]);
   }
   float sum_lo = 0.f, sum_hi = 0.f;
+  // writes the weights held in w[nb][0..3] (rows gq and gq + 8) into P's tile
+  auto write_p = [&](const float (&w)[4][4]) {
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) {
+      const int kc = warp * 4 + nb;                       // 8-key chunk of P
+      const uint32_t off_lo = static_cast<uint32_t>(gq * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
+      const uint32_t off_hi = static_cast<uint32_t>((gq + 8) * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_lo) = pack_bf16(w[nb][0], w[nb][1]);
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_hi) = pack_bf16(w[nb][2], w[nb][3]);
+    }
+  };
+  float hi[4][4];  // the high halves; sc keeps the low halves for the second pass
 #pragma unroll
   for (int nb = 0; nb < 4; ++nb) {
-    float e4[4];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const float xl = sc[nb][e] == -INFINITY ? 0.f : expf(__fsub_rn(sc[nb][e], m_lo));
       const float xh = sc[nb][2 + e] == -INFINITY ? 0.f : expf(__fsub_rn(sc[nb][2 + e], m_hi));
-      e4[e] = __bfloat162float(__float2bfloat16_rn(xl));
-      e4[2 + e] = __bfloat162float(__float2bfloat16_rn(xh));
-      sum_lo = __fadd_rn(sum_lo, e4[e]);
-      sum_hi = __fadd_rn(sum_hi, e4[2 + e]);
+      split_bf16(xl, hi[nb][e], sc[nb][e]);
+      split_bf16(xh, hi[nb][2 + e], sc[nb][2 + e]);
+      sum_lo = __fadd_rn(sum_lo, __fadd_rn(hi[nb][e], sc[nb][e]));
+      sum_hi = __fadd_rn(sum_hi, __fadd_rn(hi[nb][2 + e], sc[nb][2 + e]));
     }
-    const int kc = warp * 4 + nb;                       // 8-key chunk of P
-    const uint32_t off_lo = static_cast<uint32_t>(gq * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
-    const uint32_t off_hi = static_cast<uint32_t>((gq + 8) * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
-    *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_lo) = pack_bf16(e4[0], e4[1]);
-    *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_hi) = pack_bf16(e4[2], e4[3]);
   }
+  write_p(hi);
 #pragma unroll
   for (int o = 1; o <= 2; o <<= 1) {
     sum_lo = __fadd_rn(sum_lo, __shfl_xor_sync(0xffffffffu, sum_lo, o));
@@ -286,13 +335,14 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   __syncthreads();
 
   // --- o = P . V: warp w owns columns 16w .. 16w + 15 (two 8-wide n
-  // blocks) over all 256 keys, sixteen k steps of 16 keys in ascending order.
-  if (warp < D / 16) {
-    float oc[2][4];
+  // blocks) over all 256 keys, sixteen k steps of 16 keys in ascending order;
+  // once over the high halves of P, once over the low halves.
+  auto pv = [&](float (&acc)[2][4]) {
 #pragma unroll
     for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) oc[nb][i] = 0.f;
+      for (int i = 0; i < 4; ++i) acc[nb][i] = 0.f;
+    if (warp >= D / 16) return;
 #pragma unroll 4
     for (int kk = 0; kk < kSplit / 16; ++kk) {
       uint32_t a[4];
@@ -308,9 +358,17 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
         const int c = warp * 2 + (lane >> 4);
         ldsm_x4_t(kv_base + static_cast<uint32_t>(key * D * 2 + ((c ^ (key & 7)) << 4)), b0, b1, b2, b3);
       }
-      mma_bf16_16816(oc[0], a, b0, b1);
-      mma_bf16_16816(oc[1], a, b2, b3);
+      mma_bf16_16816(acc[0], a, b0, b1);
+      mma_bf16_16816(acc[1], a, b2, b3);
     }
+  };
+  float oc[2][4], ol[2][4];
+  pv(oc);
+  __syncthreads();  // every warp is done with the high halves
+  write_p(sc);
+  __syncthreads();
+  pv(ol);
+  if (warp < D / 16) {
     // rows gq and gq + 8, columns 16w + 8nb + 2tq (+1)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -321,7 +379,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
 #pragma unroll
         for (int nb = 0; nb < 2; ++nb)
           *reinterpret_cast<float2*>(p.ws_o + base * D + warp * 16 + nb * 8 + 2 * tq) =
-              make_float2(oc[nb][2 * h], oc[nb][2 * h + 1]);
+              make_float2(__fadd_rn(oc[nb][2 * h], ol[nb][2 * h]), __fadd_rn(oc[nb][2 * h + 1], ol[nb][2 * h + 1]));
         if (warp == 0 && tq == 0) {
           float l = wsum[0][r];
 #pragma unroll
@@ -486,6 +544,19 @@ __global__ void __launch_bounds__(kThreads, 2) attn_split_tiles_kernel(const Att
     }
   }
   __syncthreads();
+  // writes the weights held in w[nb][0..3] (rows gq and gq + 8 of tile mt)
+  // into P's tile
+  auto write_p = [&](int mt, const float (&w)[4][4]) {
+    const int r_lo = mt * kRowsMma + gq, r_hi = r_lo + 8;
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) {
+      const int kc = warp * 4 + nb;                       // 8-key chunk of P
+      const uint32_t off_lo = static_cast<uint32_t>(r_lo * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
+      const uint32_t off_hi = static_cast<uint32_t>(r_hi * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_lo) = pack_bf16(w[nb][0], w[nb][1]);
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_hi) = pack_bf16(w[nb][2], w[nb][3]);
+    }
+  };
   float m_lo[MT], m_hi[MT];
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
@@ -500,24 +571,20 @@ __global__ void __launch_bounds__(kThreads, 2) attn_split_tiles_kernel(const Att
       m_hi[mt] = fmaxf(m_hi[mt], wmax[w][r_hi]);
     }
     float sum_lo = 0.f, sum_hi = 0.f;
+    float hi[4][4];  // the high halves; sc keeps the low halves for the second pass
 #pragma unroll
     for (int nb = 0; nb < 4; ++nb) {
-      float e4[4];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const float xl = sc[mt][nb][e] == -INFINITY ? 0.f : expf(__fsub_rn(sc[mt][nb][e], m_lo[mt]));
         const float xh = sc[mt][nb][2 + e] == -INFINITY ? 0.f : expf(__fsub_rn(sc[mt][nb][2 + e], m_hi[mt]));
-        e4[e] = __bfloat162float(__float2bfloat16_rn(xl));
-        e4[2 + e] = __bfloat162float(__float2bfloat16_rn(xh));
-        sum_lo = __fadd_rn(sum_lo, e4[e]);
-        sum_hi = __fadd_rn(sum_hi, e4[2 + e]);
+        split_bf16(xl, hi[nb][e], sc[mt][nb][e]);
+        split_bf16(xh, hi[nb][2 + e], sc[mt][nb][2 + e]);
+        sum_lo = __fadd_rn(sum_lo, __fadd_rn(hi[nb][e], sc[mt][nb][e]));
+        sum_hi = __fadd_rn(sum_hi, __fadd_rn(hi[nb][2 + e], sc[mt][nb][2 + e]));
       }
-      const int kc = warp * 4 + nb;                       // 8-key chunk of P
-      const uint32_t off_lo = static_cast<uint32_t>(r_lo * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
-      const uint32_t off_hi = static_cast<uint32_t>(r_hi * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
-      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_lo) = pack_bf16(e4[0], e4[1]);
-      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_hi) = pack_bf16(e4[2], e4[3]);
     }
+    write_p(mt, hi);
 #pragma unroll
     for (int o = 1; o <= 2; o <<= 1) {
       sum_lo = __fadd_rn(sum_lo, __shfl_xor_sync(0xffffffffu, sum_lo, o));
@@ -533,15 +600,16 @@ __global__ void __launch_bounds__(kThreads, 2) attn_split_tiles_kernel(const Att
 
   // --- o = P . V: warp w owns columns 16w .. 16w + 15 (two 8-wide n
   // blocks) over all 256 keys, sixteen k steps of 16 keys in ascending order;
-  // each V fragment serves every tile.
-  if (warp < D / 16) {
-    float oc[MT][2][4];
+  // each V fragment serves every tile.  Once over the high halves of P, once
+  // over the low halves, the two sums added at the end.
+  auto pv = [&](float (&acc)[MT][2][4]) {
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
       for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) oc[mt][nb][i] = 0.f;
+        for (int i = 0; i < 4; ++i) acc[mt][nb][i] = 0.f;
+    if (warp >= D / 16) return;
 #pragma unroll 4
     for (int kk = 0; kk < kSplit / 16; ++kk) {
       uint32_t b0, b1, b2, b3;
@@ -558,10 +626,20 @@ __global__ void __launch_bounds__(kThreads, 2) attn_split_tiles_kernel(const Att
         const int kc = 2 * kk + (lane >> 4);
         ldsm_x4(pt_base + static_cast<uint32_t>(prow * kSplit * 2 + ((kc ^ (prow & 7)) << 4)), a[0], a[1],
                 a[2], a[3]);
-        mma_bf16_16816(oc[mt][0], a, b0, b1);
-        mma_bf16_16816(oc[mt][1], a, b2, b3);
+        mma_bf16_16816(acc[mt][0], a, b0, b1);
+        mma_bf16_16816(acc[mt][1], a, b2, b3);
       }
     }
+  };
+  float oc[MT][2][4], ol[MT][2][4];
+  pv(oc);
+  __syncthreads();  // every warp is done with the high halves
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+    if (mt * kRowsMma < RG) write_p(mt, sc[mt]);
+  __syncthreads();
+  pv(ol);
+  if (warp < D / 16) {
     // rows gq and gq + 8 of each tile, columns 16w + 8nb + 2tq (+1)
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
@@ -574,7 +652,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_split_tiles_kernel(const Att
 #pragma unroll
           for (int nb = 0; nb < 2; ++nb)
             *reinterpret_cast<float2*>(p.ws_o + base * D + warp * 16 + nb * 8 + 2 * tq) =
-                make_float2(oc[mt][nb][2 * h], oc[mt][nb][2 * h + 1]);
+                make_float2(__fadd_rn(oc[mt][nb][2 * h], ol[mt][nb][2 * h]),
+                            __fadd_rn(oc[mt][nb][2 * h + 1], ol[mt][nb][2 * h + 1]));
           if (warp == 0 && tq == 0) {
             float l = wsum[0][r];
 #pragma unroll
@@ -596,10 +675,19 @@ __global__ void attn_merge_kernel(const AttnParams p) {
   int row, len;
   if (!p.prefill) {
     row = blockIdx.y;
-    len = p.kv_len[row];
+    if (!seq_ok(p, row)) {
+      report_bad_length(p);
+      len = 0;  // zeros
+    } else {
+      len = p.kv_len[row];
+    }
   } else {
     const int b = blockIdx.z;
     const int i = blockIdx.y;
+    if (!seq_ok(p, b)) {
+      if (i == 0) report_bad_length(p);
+      return;
+    }
     if (i >= p.q_len[b]) return;
     row = p.q_offset[b] + i;
     len = p.q_start[b] + i + 1;
@@ -611,7 +699,7 @@ __global__ void attn_merge_kernel(const AttnParams p) {
     *dst = __float2bfloat16_rn(0.f);
     return;
   }
-  const int ns = (len + kSplit - 1) / kSplit;
+  const int ns = min((len + kSplit - 1) / kSplit, p.S);
   const int64_t base = (static_cast<int64_t>(row) * p.Hq + h) * p.S;
   float m_acc = -INFINITY, l_acc = 0.f, o_acc = 0.f;
   constexpr int CH = 8;  // partials loaded ahead of the (sequential) fold
@@ -655,15 +743,8 @@ kinv_status launch(const AttnParams& p, dim3 split_grid, dim3 merge_grid, cudaSt
   else
     kernel = attn_split_tiles_kernel<D, MT>;
   const size_t smem = split_smem_bytes<D, MT>();
-  static bool configured[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return KINV_ERR_CUDA;
-  if (dev < 64 && !configured[dev]) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess)
-      return KINV_ERR_CUDA;
-    configured[dev] = true;
-  }
+  const kinv_status attr = ensure_smem(reinterpret_cast<const void*>(kernel), smem);
+  if (attr != KINV_OK) return attr;
   const kinv_status st = launch_kernel(kernel, split_grid, dim3(kThreads), smem, stream, 1, p);
   if (st != KINV_OK) return st;
   return launch_kernel(attn_merge_kernel<D>, merge_grid, dim3(D), 0, stream, 1, p);
@@ -701,20 +782,31 @@ extern "C" size_t kinv_attn_decode_workspace(int B, int Hq, int D, int Lmax, int
   return workspace_bytes(B, Hq, D, (Lmax + split_len - 1) / split_len);
 }
 
-extern "C" kinv_status kinv_attn_decode(const void* q, const void* k_cache, const void* v_cache,
-                                        int64_t seq_stride, int64_t tok_stride,
-                                        const int32_t* kv_len, void* out, int B, int Hq, int Hkv,
-                                        int D, int Lmax, int split_len, float scale,
-                                        void* workspace, size_t ws_bytes, kinv_stream stream) {
+namespace kinv {
+namespace {
+// Host-side checks of a decode call (no CUDA call is made): the same order for
+// kinv_attn_decode and kinv_attn_decode_noalloc.
+kinv_status decode_check(const void* q, const void* k_cache, const void* v_cache, int64_t seq_stride,
+                         int64_t tok_stride, const int32_t* kv_len, const void* out, int B, int Hq,
+                         int Hkv, int D, int Lmax, int split_len, const void* workspace,
+                         size_t ws_bytes) {
   if (B < 0 || Lmax < 0) return KINV_ERR_INVALID_ARG;
   if (B == 0) return KINV_OK;
   if (!kv_len) return KINV_ERR_INVALID_ARG;
-  kinv_status st = check_common(q, k_cache, v_cache, seq_stride, tok_stride, out, Hq, Hkv, D,
-                                split_len, workspace);
+  const kinv_status st = check_common(q, k_cache, v_cache, seq_stride, tok_stride, out, Hq, Hkv, D,
+                                      split_len, workspace);
   if (st != KINV_OK) return st;
   if (B > 65535) return KINV_ERR_UNSUPPORTED;
   const int S = Lmax > 0 ? (Lmax + kSplit - 1) / kSplit : 1;
   if (ws_bytes < workspace_bytes(B, Hq, D, S)) return KINV_ERR_WORKSPACE;
+  return KINV_OK;
+}
+
+// Enqueues a checked decode call with its partials in `workspace`.
+kinv_status decode_launch(const void* q, const void* k_cache, const void* v_cache, int64_t seq_stride,
+                          int64_t tok_stride, const int32_t* kv_len, void* out, int B, int Hq, int Hkv,
+                          int D, int Lmax, float scale, void* workspace, cudaStream_t stream) {
+  const int S = Lmax > 0 ? (Lmax + kSplit - 1) / kSplit : 1;
   AttnParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k_cache);
@@ -735,9 +827,27 @@ extern "C" kinv_status kinv_attn_decode(const void* q, const void* k_cache, cons
   p.groups_per_seq = 1;
   p.rg_cap = ((p.G + 3) / 4) * 4;
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
+  p.max_len = Lmax;
+  p.max_q_len = 0;
+  p.total_rows = B;
+  p.status = device_status_word();
   const dim3 split_grid(Hkv, S, B), merge_grid(Hq, B, 1);
   return D == 128 ? launch<128, 1>(p, split_grid, merge_grid, stream)
                   : launch<64, 1>(p, split_grid, merge_grid, stream);
+}
+}  // namespace
+}  // namespace kinv
+
+extern "C" kinv_status kinv_attn_decode(const void* q, const void* k_cache, const void* v_cache,
+                                        int64_t seq_stride, int64_t tok_stride,
+                                        const int32_t* kv_len, void* out, int B, int Hq, int Hkv,
+                                        int D, int Lmax, int split_len, float scale,
+                                        void* workspace, size_t ws_bytes, kinv_stream stream) {
+  const kinv_status st = decode_check(q, k_cache, v_cache, seq_stride, tok_stride, kv_len, out, B, Hq, Hkv,
+                                      D, Lmax, split_len, workspace, ws_bytes);
+  if (st != KINV_OK || B == 0) return st;
+  return decode_launch(q, k_cache, v_cache, seq_stride, tok_stride, kv_len, out, B, Hq, Hkv, D, Lmax, scale,
+                       workspace, stream);
 }
 
 extern "C" size_t kinv_attn_prefill_workspace(int total_rows, int Hq, int D, int max_kv,
@@ -783,6 +893,10 @@ extern "C" kinv_status kinv_attn_prefill(const void* q, const void* k_cache, con
   p.groups_per_seq = (max_q_len + p.R - 1) / p.R;
   p.rg_cap = p.R * p.G;
   p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
+  p.max_len = max_kv;
+  p.max_q_len = max_q_len;
+  p.total_rows = total_rows;
+  p.status = device_status_word();
   const int64_t groups = static_cast<int64_t>(B) * p.groups_per_seq;
   if (groups > 65535 || max_q_len > 65535 || B > 65535) return KINV_ERR_UNSUPPORTED;
   const dim3 split_grid(Hkv, S, static_cast<unsigned>(groups)), merge_grid(Hq, max_q_len, B);
@@ -795,6 +909,7 @@ extern "C" kinv_status kinv_attn_prefill(const void* q, const void* k_cache, con
 // device memory.  The split partials go to a scratch array compiled into the
 // library instead of a caller-provided workspace.
 
+#include <map>
 #include <mutex>
 
 // Scratch shared by every kinv_attn_decode_noalloc call on a device (held by
@@ -805,20 +920,23 @@ namespace kinv {
 namespace {
 
 // In host code the array's name is a host-side stand-in, not a device
-// address: the device address is looked up once per device, with that device
-// current, and cached.
+// address: the device address is looked up with the device current, checked,
+// and cached per CUDA context (a context created again after cudaDeviceReset
+// loads the module afresh and gets its own lookup).
 void* noalloc_scratch_address() {
   static std::mutex mu;
-  static void* addr[64] = {};
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  static std::map<unsigned long long, void*> addr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, kinv_noalloc_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = p;
+  unsigned long long ctx = context_id();
+  if (ctx != 0) {
+    auto it = addr.find(ctx);
+    if (it != addr.end()) return it->second;
   }
-  return addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, kinv_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+  ctx = context_id();  // the lookup makes the primary context current if none was
+  if (ctx != 0) addr[ctx] = p;
+  return p;
 }
 
 }  // namespace
@@ -829,42 +947,15 @@ extern "C" kinv_status kinv_attn_decode_noalloc(const void* q, const void* k_cac
                                                 int64_t tok_stride, const int32_t* kv_len,
                                                 void* out, int B, int Hq, int Hkv, int D, int Lmax,
                                                 int split_len, float scale, kinv_stream stream) {
-  if (B < 0 || Lmax < 0) return KINV_ERR_INVALID_ARG;
-  if (B == 0) return KINV_OK;
-  if (!kv_len || Hq <= 0 || D <= 0) return KINV_ERR_INVALID_ARG;
-  if (B > 65535) return KINV_ERR_UNSUPPORTED;
-  if (split_len != kSplit) return KINV_ERR_UNSUPPORTED;
-  const int S = Lmax > 0 ? (Lmax + kSplit - 1) / kSplit : 1;
-  const size_t need = workspace_bytes(B, Hq, D, S);
-  if (need > static_cast<size_t>(KINV_NOALLOC_SCRATCH_BYTES)) return KINV_ERR_WORKSPACE;
-  // shape and alignment checks first (no CUDA call), with a stand-in pointer
+  // the checks of kinv_attn_decode, in its order, with an aligned stand-in
+  // for the workspace and the scratch array's size as its size
   const void* aligned_placeholder = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
-  kinv_status st = check_common(q, k_cache, v_cache, seq_stride, tok_stride, out, Hq, Hkv, D,
-                                split_len, aligned_placeholder);
-  if (st != KINV_OK) return st;
+  const kinv_status st = decode_check(q, k_cache, v_cache, seq_stride, tok_stride, kv_len, out, B, Hq, Hkv,
+                                      D, Lmax, split_len, aligned_placeholder,
+                                      static_cast<size_t>(KINV_NOALLOC_SCRATCH_BYTES));
+  if (st != KINV_OK || B == 0) return st;
   void* scratch = noalloc_scratch_address();
   if (!scratch) return KINV_ERR_CUDA;
-  AttnParams p{};
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k = static_cast<const __nv_bfloat16*>(k_cache);
-  p.v = static_cast<const __nv_bfloat16*>(v_cache);
-  p.seq_stride = seq_stride;
-  p.tok_stride = tok_stride;
-  p.kv_len = kv_len;
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.ws_o = static_cast<float*>(scratch);
-  const size_t o_bytes = static_cast<size_t>(B) * Hq * S * D * 4;
-  p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + ((o_bytes + 255) / 256) * 256);
-  p.prefill = 0;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.G = Hq / Hkv;
-  p.R = 1;
-  p.S = S;
-  p.groups_per_seq = 1;
-  p.rg_cap = ((p.G + 3) / 4) * 4;
-  p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
-  const dim3 split_grid(Hkv, S, B), merge_grid(Hq, B, 1);
-  return D == 128 ? launch<128, 1>(p, split_grid, merge_grid, stream)
-                  : launch<64, 1>(p, split_grid, merge_grid, stream);
+  return decode_launch(q, k_cache, v_cache, seq_stride, tok_stride, kv_len, out, B, Hq, Hkv, D, Lmax, scale,
+                       scratch, stream);
 }

@@ -19,6 +19,12 @@ namespace kinv {
 // waits gave up (or that met a setting they cannot handle), read and cleared
 // by kinv_last_device_status().  Returns nullptr if CUDA is unusable.
 int* device_status_word();
+// An id of the calling thread's current CUDA context (0 if none): host-side
+// caches of device addresses and kernel attributes are kept per context.
+unsigned long long context_id();
+// Raises `kernel`'s dynamic shared memory limit to at least `bytes` in the
+// current context (once per context and kernel; thread-safe).
+kinv_status ensure_smem(const void* kernel, size_t bytes);
 int sm_count();
 // Maximum dynamic shared memory per block on the current device.
 int max_smem_optin();
@@ -38,6 +44,7 @@ enum : int {
   DEV_TIMEOUT_GEMM_EPILOGUE = dev_code(3, KINV_ERR_TIMEOUT),
   DEV_SAMPLER_UNSUPPORTED = dev_code(4, KINV_ERR_UNSUPPORTED),
   DEV_TIMEOUT_TEST = dev_code(5, KINV_ERR_TIMEOUT),
+  DEV_ATTN_BAD_LENGTH = dev_code(6, KINV_ERR_INVALID_ARG),
 };
 
 // ---------------------------------------------------------------- device side

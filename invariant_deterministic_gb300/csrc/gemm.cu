@@ -73,12 +73,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
 
 __device__ __forceinline__ float silu_times(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
-// bf16(x + bf16(v)) for a bf16 x given by its bits: the residual stream plus
-// the projection's output as it would be stored
+// bf16(x + v) for a bf16 x given by its bits and the projection's fp32
+// result v: the residual stream is the stored tensor, the projection's output
+// is never stored, so the sum is rounded once
 __device__ __forceinline__ float residual_add(uint32_t x_bits, float v) {
   const float x = __uint_as_float((x_bits & 0xFFFFu) << 16);
-  const float o = __bfloat162float(__float2bfloat16_rn(v));
-  return __bfloat162float(__float2bfloat16_rn(__fadd_rn(x, o)));
+  return __bfloat162float(__float2bfloat16_rn(__fadd_rn(x, v)));
 }
 
 __host__ __device__ constexpr int rope_pre_bytes(int own_rows, int D, int BN) {
@@ -126,7 +126,7 @@ struct GemmArgs {
   int row_ss_tiles;
   int norm_dim;
   float eps;
-  // residual: resid[m][n] = bf16(resid[m][n] + bf16(product)), and the new
+  // residual: resid[m][n] = bf16(resid[m][n] + product), and the new
   // row's sum of squares over this tile's 128 columns -> ss_out[m][n0 / 128]
   __nv_bfloat16* resid;
   int64_t ld_resid;
@@ -882,20 +882,9 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a
   a.ring_bytes = stages * stage > recv_bytes ? stages * stage : (recv_bytes + 15) / 16 * 16;
   const size_t smem = smem_bytes(stages, a.ring_bytes, tab_bytes);
   if (smem > static_cast<size_t>(max_smem_optin())) return KINV_ERR_UNSUPPORTED;
-  // the opt-in limit is raised once per device to the largest request seen
-  static size_t configured[64] = {};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return KINV_ERR_CUDA;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (configured[dev] < smem) {
-      if (cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(smem)) != cudaSuccess)
-        return KINV_ERR_CUDA;
-      configured[dev] = smem;
-    }
-  }
+  // the opt-in limit is raised (once per context) to the largest request seen
+  const kinv_status attr = ensure_smem(reinterpret_cast<const void*>(gemm_kernel<BN>), smem);
+  if (attr != KINV_OK) return attr;
   return launch_kernel(gemm_kernel<BN>, dim3(a.splits, grid_y, grid_z), dim3(kGemmThreads), smem,
                        stream, static_cast<unsigned>(a.splits), ta, tw, a);
 }

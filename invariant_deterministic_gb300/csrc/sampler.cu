@@ -886,19 +886,9 @@ extern "C" kinv_status kinv_sample(const float* logits, int64_t ld, int B, int V
   while (C > 1 && static_cast<long long>(B) * C > sm_count()) C >>= 1;
   const int chunk = ((V + C - 1) / C + 127) / 128 * 128;
   const bool regs = chunk <= kRegSpan;
-  static bool configured[64][2] = {};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return KINV_ERR_CUDA;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!configured[dev][regs]) {
-      if (cudaFuncSetAttribute(regs ? sample_kernel<true> : sample_kernel<false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin()) != cudaSuccess)
-        return KINV_ERR_CUDA;
-      configured[dev][regs] = true;
-    }
-  }
+  const kinv_status attr = ensure_smem(reinterpret_cast<const void*>(regs ? sample_kernel<true> : sample_kernel<false>),
+                                       static_cast<size_t>(max_smem_optin()));
+  if (attr != KINV_OK) return attr;
   if (regs)
     return launch_kernel(sample_kernel<true>, dim3(C, B), dim3(kThreadsS), smem, stream,
                          static_cast<unsigned>(C), logits, ld, V, params, history, hist_ld, hist_len,

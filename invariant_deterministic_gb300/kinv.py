@@ -39,6 +39,7 @@ SIGNATURES = {
     "kinv_device_class": (ctypes.c_char_p, []),
     "kinv_build_id": (ctypes.c_char_p, []),
     "kinv_last_device_status": (_i32, [_c_p]),
+    "kinv_test_bounded_wait": (_i32, [_i64, _c_p]),
     "kinv_gemm": (_i32, [_c_p, _i64, _c_p, _i64, _c_p, _i64, _i32, _i32, _i32, _i32, _c_p]),
     "kinv_gemm_fused": (_i32, [_c_p, _i64, _c_p, _i64, _c_p, _i64, _i32, _i32, _i32, _i32, _c_p, _c_p]),
     "kinv_row_sumsq": (_i32, [_c_p, _i64, _i32, _i32, _c_p, _c_p]),
@@ -125,6 +126,12 @@ def last_device_status(stream=None) -> int:
     return lib().kinv_last_device_status(_stream(stream))
 
 
+def test_bounded_wait(limit_ns: int, stream=None) -> None:
+    """kinv_test_bounded_wait: one block waits on a barrier nothing
+    completes, gives up after limit_ns and records KINV_ERR_TIMEOUT."""
+    _check(lib().kinv_test_bounded_wait(int(limit_ns), _stream(stream)), "kinv_test_bounded_wait")
+
+
 # --------------------------------------------------------------------- GEMM
 def gemm(a: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
          out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
@@ -158,7 +165,8 @@ def norm_in(row_ss: torch.Tensor, norm_dim: int, eps: float) -> GemmFusion:
 
 
 def residual_out(resid: torch.Tensor, ss_out: torch.Tensor) -> GemmFusion:
-    """Producing side: resid <- bf16(resid + bf16(out)); ss_out [M][N/128]."""
+    """Producing side: resid <- bf16(resid + out), out the fp32 product
+    (rounded once); ss_out [M][N/128]."""
     _need(resid, torch.bfloat16, "resid")
     _need(ss_out, torch.float32, "ss_out")
     return GemmFusion(resid=_ptr(resid), ld_resid=resid.stride(0), ss_out=_ptr(ss_out))
@@ -284,7 +292,14 @@ def attn_decode_noalloc(q, k_cache, v_cache, kv_len, out, split_len=SPLIT_LEN, s
     NOALLOC_SCRATCH_BYTES; calls sharing a device must not overlap on the GPU).
     ``out`` must be given, since this path allocates nothing."""
     _need(q, torch.bfloat16, "q")
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
     _need(kv_len, torch.int32, "kv_len")
+    _need(out, torch.bfloat16, "out")
+    if tuple(out.shape) != tuple(q.shape) or not out.is_contiguous() or not q.is_contiguous():
+        raise ValueError("attn_decode_noalloc: q and out must be contiguous [B][Hq][D] of one shape")
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or v_cache.stride() != k_cache.stride():
+        raise ValueError("attn_decode_noalloc: the caches must share shape and strides")
     bsz, hq, d = q.shape
     lmax, hkv = k_cache.shape[1], k_cache.shape[2]
     _check(lib().kinv_attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), k_cache.stride(0),

@@ -1,5 +1,6 @@
 """Layer glue without reductions (test infrastructure only): embedding gather,
-residual add, SwiGLU.  None of these sums across elements, so each is
+residual add (of two bf16 tensors, or of a bf16 tensor and an unrounded
+product), SwiGLU.  None of these sums across elements, so each is
 batch-invariant by construction; they are here because the decoder step needs
 them.  SwiGLU: a = silu(g) * u with silu(g) = g / (1 + e^-g)."""
 from __future__ import annotations
@@ -15,6 +16,12 @@ def embed(table_bits: np.ndarray, ids) -> np.ndarray:
 
 def add(x_bits, y_bits) -> np.ndarray:
     return bf16.from_f64(bf16.to_f64(x_bits) + bf16.to_f64(y_bits))
+
+
+def add_f64(x_bits, y: np.ndarray) -> np.ndarray:
+    """bf16(x + y) for a bf16 x and an unrounded fp64 y: the residual stream
+    plus a projection output that is never stored on its own, rounded once."""
+    return bf16.from_f64(bf16.to_f64(x_bits) + np.asarray(y, dtype=np.float64))
 
 
 def silu(g: np.ndarray) -> np.ndarray:

@@ -16,7 +16,9 @@ FFN, grouped-query attention):
 
 bf16 rounding happens at each stored tensor, the same boundaries as the GPU
 path.  The GPU path stores neither g and u (the gate/up product and SwiGLU are
-one step) nor the normalised rows h, h2 and the final one: each RMSNorm is
+one step), nor the O and down products (each is added into the residual
+stream x in the projection that forms it, so x2 = bf16(x + o) is rounded
+once), nor the normalised rows h, h2 and the final one: each RMSNorm is
 folded into the projection it feeds, (x / rms(x) * w) . W^T computed as
 (x . (W * w)^T) / rms(x), so here those rows stay unrounded fp64.  Weights are
 bf16 bit arrays; the dictionaries below name them.
@@ -71,12 +73,13 @@ def layer_step(x_bits, lw: dict, k_cache, v_cache, pos, shape: Shape):
     a = np.zeros_like(q)
     for i, (b, p) in enumerate(pos):
         a[i] = attention.decode(q[i: i + 1], k_cache[b: b + 1], v_cache[b: b + 1], [p + 1])[0]
-    o = gemm(a.reshape(m, hq * dh), lw["w_o"])
-    x2 = glue.add(x_bits, o)
+    # the O and down projections add into the residual stream: their outputs
+    # are not stored, so each sum is rounded once
+    x2 = glue.add_f64(x_bits, gemm(a.reshape(m, hq * dh), lw["w_o"], out="f64"))
     h2 = rmsnorm_f64(bf16.to_f64(x2), bf16.to_f64(lw["ffn_norm"]), shape.eps)
     # gate/up and SwiGLU form one GPU kernel: g and u are not rounded to bf16
     act = glue.swiglu_f64(matmul(h2, lw["w_gu"], out="f64"))
-    return glue.add(x2, gemm(act, lw["w_down"]))
+    return glue.add_f64(x2, gemm(act, lw["w_down"], out="f64"))
 
 
 def decode_step(tokens, model: dict, k_caches, v_caches, lengths, shape: Shape,

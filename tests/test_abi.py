@@ -97,3 +97,6 @@ def test_host_validation_without_gpu(lib):
     assert L.kinv_rope_append(fake, 512, fake, fake, fake, 0, 128, fake, fake, None, None, 1e-6,
                               1, 2, 1, 96, 1e4, None) == lib.ERR_UNSUPPORTED
     assert L.kinv_add(fake, fake, fake, 12, None) == lib.ERR_UNSUPPORTED
+    # the bounded-wait self-test checks its limit before any CUDA call
+    assert L.kinv_test_bounded_wait(10, None) == lib.ERR_INVALID_ARG
+    assert L.kinv_test_bounded_wait(10**9, None) == lib.ERR_INVALID_ARG

@@ -127,3 +127,46 @@ def test_workspace_too_small_is_rejected(kinv):
     with pytest.raises(kinv.KinvError) as e:
         kinv.attn_decode(q, k, v, torch.tensor([3, 4], dtype=torch.int32, device="cuda"), workspace=ws)
     assert e.value.status == kinv.ERR_WORKSPACE
+
+
+def test_device_lengths_outside_bounds_are_left_out_and_reported(kinv):
+    """kv_len is device data the host cannot check: a sequence whose length
+    lies outside [0, Lmax] (decode) or whose rows or keys fall outside the
+    stated bounds (prefill) is left out and the status word says so.  The
+    workspace past what the call needs is filled with NaN bit patterns and the
+    cache past Lmax with NaN too, so a read beyond either would show in the
+    other sequences' outputs."""
+    hq, hkv, d, lmax = 4, 2, 64, 512
+    pad = 300
+    i32 = dict(dtype=torch.int32, device="cuda")
+    kfull, vfull = _cache(3, lmax + pad, hkv, d, 70)
+    kfull[:, lmax:] = float("nan")
+    vfull[:, lmax:] = float("nan")
+    k, v = kfull[:, :lmax], vfull[:, :lmax]          # strides of the padded buffer
+    q = synth.normal_bf16((3, hq, d), 1.0, 71).cuda()
+    need = kinv.attn_decode_workspace(3, hq, d, lmax)
+    ws = torch.full((need + (1 << 20),), 0xFF, dtype=torch.uint8, device="cuda")
+    good = kinv.attn_decode(q, k, v, torch.tensor([100, 5, 7], **i32))
+    assert kinv.last_device_status() == 0
+    for bad_slot, bad_len in ((1, lmax + pad), (2, lmax + 1), (0, -3)):
+        lens = [100, 5, 7]
+        lens[bad_slot] = bad_len
+        out = kinv.attn_decode(q, k, v, torch.tensor(lens, **i32), workspace=ws)
+        assert kinv.last_device_status() == kinv.ERR_INVALID_ARG
+        assert torch.all(out[bad_slot] == 0)
+        for b in range(3):
+            if b != bad_slot:
+                assert_same_bits(out[b], good[b], f"sequence {b} beside a bad length at {bad_slot}")
+    # prefill: sequence 1 claims keys past max_kv; sequence 0 is untouched by it
+    rows = [5, 6]
+    qp = synth.normal_bf16((11, hq, d), 1.0, 72).cuda()
+    out = torch.full_like(qp, 7.0)
+    starts, offs = [20, lmax - 3], [0, 5]
+    kinv.attn_prefill(qp, k[:2], v[:2], torch.tensor(starts, **i32), torch.tensor(rows, **i32),
+                      torch.tensor(offs, **i32), 6, lmax, out=out)
+    assert kinv.last_device_status() == kinv.ERR_INVALID_ARG
+    assert torch.all(out[5:] == 7.0)
+    alone = kinv.attn_prefill(qp[:5].contiguous(), k[:1], v[:1], torch.tensor([20], **i32),
+                              torch.tensor([5], **i32), torch.zeros(1, **i32), 5, 25)
+    assert_same_bits(out[:5], alone, "valid sequence beside an out-of-bounds one")
+    assert kinv.last_device_status() == 0

@@ -75,11 +75,9 @@ def test_8b_shapes_row_bits_independent_of_m(kinv, n, k):
     mixed[perm[:64]] = a[:64]
     got = kinv.gemm(mixed, w)
     assert_same_bits(got[perm[:64]], full[:64], "rows among other batch-mates")
-    # oracle on sampled rows and columns
-    rows = [0, 1, 6, 15, 63, 127, 128, 255]
-    cols = torch.randint(0, n, (64,), generator=synth.gen(10)).numpy()
-    ref = gemm_f64_rows(synth.bits(a), synth.bits(w), rows, cols)
-    assert_close(f64(full)[rows][:, cols], obf.round_f64(ref), f"oracle N={n} K={k}")
+    # the oracle on every row and column of the M = 256 product
+    ref = ogemm(synth.bits(a), synth.bits(w), out="f64")
+    assert_close(f64(full), obf.round_f64(ref), f"oracle N={n} K={k}, all of M = 256")
     assert kinv.last_device_status() == 0
 
 
@@ -178,3 +176,59 @@ def test_gemm_swiglu_rejects_bad_f(kinv):
     w = torch.zeros(2 * 96, 64, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(kinv.KinvError):
         kinv.gemm_swiglu(a, w)
+
+
+# ---------------------------------------------------------------- folded RMSNorm epilogues
+@pytest.mark.parametrize("m", [64, 256])
+def test_fused_epilogues_match_the_oracle_on_whole_rows(kinv, m):
+    """The epilogues of kinv_gemm_fused / kinv_gemm_swiglu at 64 and 256 rows
+    (the owners of split-K rows pull the partials), against the oracle on every
+    element: the row scale 1/rms from per-tile sums of squares (QKV, gate/up),
+    the residual add with the new rows' sums of squares (O, down).  The same
+    rows computed in a 4-row call (partials pushed to their owners) have the
+    same bits."""
+    from oracle.gemm import matmul
+    from oracle.rmsnorm import rmsnorm_f64
+    d, f = 4096, 12288
+    b = synth.bits
+    w_qkv = synth.normal_bf16((6144, d), 0.02, 81).cuda()
+    w_o = synth.normal_bf16((d, d), 0.02, 82).cuda()
+    w_gu = synth.normal_bf16((2 * f, d), 0.02, 83).cuda()
+    w_down = synth.normal_bf16((d, f), 0.02, 84).cuda()
+    w_il = kinv.interleave_gate_up(w_gu)
+    x = synth.normal_bf16((m, d), 1.0, 85).cuda()
+    attn = synth.normal_bf16((m, d), 1.0, 86).cuda()
+    ss = torch.empty(m, d // 128, dtype=torch.float32, device="cuda")
+    kinv.row_sumsq(x, ss)
+
+    def check_ss(xb, ss_t, what):
+        v = obf.to_f64(xb)
+        assert np.allclose(ss_t.cpu().numpy(), (v * v).reshape(m, -1, 128).sum(-1), rtol=1e-5, atol=0), what
+
+    check_ss(b(x), ss, "sums of squares of x")
+    normed = lambda xb: rmsnorm_f64(obf.to_f64(xb), np.ones(d), 1e-6)
+    qkv = kinv.gemm_fused(x, w_qkv, kinv.norm_in(ss, d, 1e-6), out=torch.empty(m, 6144, dtype=torch.bfloat16, device="cuda"))
+    assert_close(f64(qkv), obf.to_f64(matmul(normed(b(x)), b(w_qkv))), f"QKV with the row scale, M={m}")
+    x1 = x.clone()
+    ss1 = torch.empty_like(ss)
+    kinv.gemm_fused(attn, w_o, kinv.residual_out(x1, ss1))
+    ref_x1 = oglue.add_f64(b(x), ogemm(b(attn), b(w_o), out="f64"))
+    assert_close(f64(x1), obf.to_f64(ref_x1), f"x + O, M={m}")
+    check_ss(b(x1), ss1, "sums of squares after O")
+    act = kinv.gemm_swiglu(x1, w_il, fusion=kinv.norm_in(ss1, d, 1e-6))
+    ref_act = oglue.swiglu_f64(matmul(normed(b(x1)), b(w_gu), out="f64"))
+    assert_close(f64(act), obf.to_f64(ref_act), f"gate/up + SwiGLU with the row scale, M={m}")
+    x2 = x1.clone()
+    ss2 = torch.empty_like(ss)
+    kinv.gemm_fused(act, w_down, kinv.residual_out(x2, ss2))
+    ref_x2 = oglue.add_f64(b(x1), ogemm(b(act), b(w_down), out="f64"))
+    assert_close(f64(x2), obf.to_f64(ref_x2), f"x + down, M={m}")
+    check_ss(b(x2), ss2, "sums of squares after down")
+    # rows 0..3 alone (the push path) give the same bits
+    x1s, ss1s = x[:4].clone(), torch.empty_like(ss[:4])
+    kinv.gemm_fused(attn[:4].contiguous(), w_o, kinv.residual_out(x1s, ss1s))
+    assert_same_bits(x1s, x1[:4], "x + O: 4 rows vs in the larger call")
+    assert_same_bits(ss1s, ss1[:4], "sums of squares: 4 rows vs in the larger call")
+    acts = kinv.gemm_swiglu(x1[:4].contiguous(), w_il, fusion=kinv.norm_in(ss1[:4].contiguous(), d, 1e-6))
+    assert_same_bits(acts, act[:4], "gate/up: 4 rows vs in the larger call")
+    assert kinv.last_device_status() == 0

@@ -14,7 +14,7 @@ import torch
 
 from helpers import assert_close, assert_same_bits, ensure_lib, f64, gpu, synth
 from oracle import bf16 as obf
-from oracle.model import Shape, decode_step as odecode
+from oracle.model import Shape
 from oracle.sampler import SamplingParams as OParams
 
 pytestmark = gpu
@@ -110,6 +110,55 @@ def test_tagged_request_alone_vs_cobatched(M):
         assert_same_bits(l[slot], alone_l[0], f"logits, batch of {len(reqs)}")
 
 
+def _decode_tagged(M, shape, w, reqs, lengths, steps, lmax, tag=0):
+    """Decode `steps` tokens for requests `reqs` (slot i holds request
+    reqs[i]); returns every slot's tokens [bsz][steps] and the tagged
+    request's logits at the first and last step."""
+    bsz = len(reqs)
+    dec = M.Decoder(shape, w, max_batch=bsz, max_len=lmax)
+    for i, r in enumerate(reqs):
+        _fill_prompt_cache(dec, i, r, lengths[r], shape)
+    dec.set_sampling([M.kinv.SamplingParams(seed=1000 + r) for r in reqs])
+    hist = [synth.uniform_int(64, 0, shape.vocab - 1, 6000 + r).tolist() for r in reqs]
+    dec.set_history(hist)
+    dec.set_positions([lengths[r] for r in reqs])
+    dec.tokens[:bsz] = torch.tensor([h[-1] for h in hist], dtype=torch.int32, device="cuda")
+    slot = reqs.index(tag)
+    toks = torch.empty(bsz, steps, dtype=torch.int32, device="cuda")
+    logits = []
+    for s_ in range(steps):
+        dec.decode_step(bsz)
+        toks[:, s_] = dec.tokens[:bsz]
+        if s_ in (0, steps - 1):
+            logits.append(dec.logits[slot].clone())
+    assert M.kinv.last_device_status() == 0
+    out = toks.cpu(), torch.stack(logits)
+    del dec
+    torch.cuda.empty_cache()
+    return out
+
+
+def test_tagged_request_alone_vs_batches_of_128_and_256_over_256_tokens(M):
+    """The busy-server check at the full batch range: request 0 decodes 256
+    tokens alone, then among 127 and 255 other requests (prompt lengths
+    U{16..4096}, each with its own seed) at a middle and at the last slot; its
+    tokens and its logits bits are the same every time.  Two layers, full
+    widths and vocabulary."""
+    shape = _shape(M, 2)
+    w = M.random_weights(shape, device="cuda")
+    n_req = 256
+    lengths = synth.uniform_int(n_req, 16, 4096, synth.SEED_LEN).tolist()
+    steps = 256
+    lmax = max(lengths) + steps + 8
+    alone_t, alone_l = _decode_tagged(M, shape, w, [0], lengths, steps, lmax)
+    perm = torch.randperm(n_req - 1, generator=synth.gen(44)).add(1).tolist()
+    for reqs in (perm[:64] + [0] + perm[64:127], perm[:255] + [0]):
+        t, l = _decode_tagged(M, shape, w, reqs, lengths, steps, lmax)
+        slot = reqs.index(0)
+        assert torch.equal(t[slot], alone_t[0]), f"tokens differ in a batch of {len(reqs)}"
+        assert_same_bits(l, alone_l, f"logits, batch of {len(reqs)}")
+
+
 def test_full_depth_alone_vs_cobatched(M):
     shape = M.QWEN3_8B
     w = M.random_weights(shape, device="cuda")
@@ -177,16 +226,16 @@ def test_every_stage_of_the_step_matches_the_oracle(M):
         assert_close(f64(dec.attn[:B]), obf.to_f64(ref), "attention")
         x1 = b(x)
         kinv.gemm_fused(dec.attn[:B].view(B, -1), lw["w_o"], kinv.residual_out(x, ss))
-        o_ref = og(b(dec.attn[:B]).reshape(B, -1), b(lw["w_o"]))
-        assert_close(f64(x), obf.to_f64(oglue.add(x1, o_ref)), "x + o")
+        o_ref = og(b(dec.attn[:B]).reshape(B, -1), b(lw["w_o"]), out="f64")
+        assert_close(f64(x), obf.to_f64(oglue.add_f64(x1, o_ref)), "x + o")
         check_ss(b(x), "sums of squares after the O projection")
         x2 = b(x)
         kinv.gemm_swiglu(x, dec.w_gu_il[li], out=dec.act[:B], fusion=kinv.norm_in(ss, 4096, 1e-6))
         gu = omm(normed(x2, lw["ffn_norm"]), b(lw["w_gu"]), out="f64")
         assert_close(f64(dec.act[:B]), obf.to_f64(oglue.swiglu_f64(gu)), "gate/up + swiglu, norm folded in")
         kinv.gemm_fused(dec.act[:B], lw["w_down"], kinv.residual_out(x, ss))
-        d_ref = og(b(dec.act[:B]), b(lw["w_down"]))
-        assert_close(f64(x), obf.to_f64(oglue.add(x2, d_ref)), "x + down")
+        d_ref = og(b(dec.act[:B]), b(lw["w_down"]), out="f64")
+        assert_close(f64(x), obf.to_f64(oglue.add_f64(x2, d_ref)), "x + down")
         check_ss(b(x), "sums of squares after the down projection")
     xf = b(x)
     kinv.gemm_fused(x, dec.lm_head_f, kinv.norm_in(ss, 4096, 1e-6), out=dec.logits[:B])
@@ -195,45 +244,81 @@ def test_every_stage_of_the_step_matches_the_oracle(M):
     assert kinv.last_device_status() == 0
 
 
-def test_first_step_logits_match_oracle(M):
-    """End to end over two layers: bf16 roundings that differ by one unit in a
-    few elements (and attention's bf16 weights) compound through the layers,
-    so this end-to-end check uses the norm-relative criterion (<= 1e-2) and a
-    95% per-element share; the per-stage test above holds every kernel to the
-    per-element tolerance."""
-    shape = _shape(M, 2)
+def _first_step(M, layers, lengths):
+    """One decode step of an 8B-shaped stack (full widths and vocabulary) for
+    requests with synthetic prompt caches; returns the GPU's logits and final
+    residual rows, the oracle's (its own end-to-end computation from the same
+    weights, caches, tokens and settings), the GPU's sampled tokens, the
+    histories, the settings and the oracle's near-tie flags."""
+    from oracle import glue as oglue
+    from oracle.gemm import matmul
+    from oracle.model import layer_step
+    from oracle.rmsnorm import rmsnorm_f64
+    from oracle.sampler import sample as osample
+    shape = _shape(M, layers)
     w = M.random_weights(shape, device="cuda")
-    lengths = [16, 16]
-    toks, logits = _decode_tokens(M, shape, w, [0, 1], lengths, 1, 64)
-    # the oracle sees the same bits: weights, caches, history, settings
+    bsz = len(lengths)
+    lmax = max(lengths) + 16
+    dec = M.Decoder(shape, w, max_batch=bsz, max_len=lmax)
+    for r in range(bsz):
+        dec.kv[:, :, r, : lengths[r]].copy_(
+            synth.normal_bf16((layers, 2, lengths[r], 8, 128), 1.0, 5000 + r, "cuda"))
+    hist = [synth.uniform_int(64, 0, shape.vocab - 1, 6000 + r).tolist() for r in range(bsz)]
+    dec.set_sampling([M.kinv.SamplingParams(seed=1000 + r) for r in range(bsz)])
+    dec.set_history(hist)
+    dec.set_positions(lengths)
+    dec.tokens[:bsz] = torch.tensor([h[-1] for h in hist], dtype=torch.int32, device="cuda")
+    kv = synth.bits(dec.kv[:, :, :bsz])
+    dec.decode_step(bsz)
+    g_logits = f64(dec.logits[:bsz])
+    g_hidden = f64(dec.x[:bsz])
+    toks = dec.tokens[:bsz].cpu().tolist()
+    assert M.kinv.last_device_status() == 0
     oshape = Shape(d_model=4096, n_q=32, n_kv=8, head_dim=128, ffn=12288, vocab=shape.vocab,
-                   n_layers=2, eps=1e-6, rope_base=1e6, qk_norm=True)
-    om = {"embed": synth.bits(w["embed"]), "lm_head": synth.bits(w["lm_head"]),
-          "final_norm": synth.bits(w["final_norm"]),
-          "layers": [{k: synth.bits(v) for k, v in lw.items()} for lw in w["layers"]]}
-    kc = [np.zeros((2, 64, 8, 128), np.uint16) for _ in range(2)]
-    vc = [np.zeros((2, 64, 8, 128), np.uint16) for _ in range(2)]
+                   n_layers=layers, eps=1e-6, rope_base=1e6, qk_norm=True)
+    x = oglue.embed(synth.bits(w["embed"]), [h[-1] for h in hist])
+    for li in range(layers):
+        lw = {k: synth.bits(v) for k, v in w["layers"][li].items()}
+        x = layer_step(x, lw, kv[li, 0].copy(), kv[li, 1].copy(), [(b, lengths[b]) for b in range(bsz)], oshape)
+    h = rmsnorm_f64(obf.to_f64(x), obf.to_f64(synth.bits(w["final_norm"])), 1e-6)
+    o_logits = matmul(h, synth.bits(w["lm_head"]), out="f32").astype(np.float64)
+    params = [OParams(seed=1000 + r) for r in range(bsz)]
+    _, ties = osample(o_logits.astype(np.float32), hist, [0] * bsz, params)
+    return g_logits, g_hidden, o_logits, obf.to_f64(x), toks, hist, params, ties
+
+
+def test_first_step_one_layer_end_to_end_matches_oracle(M):
+    """Embedding, one 8B-shaped layer, final norm, LM head and sampler, end to
+    end against the oracle's own computation: every element of the final
+    residual rows (bf16) and of all 2 x 151936 logits within the per-element
+    tolerance, and the sampled token equal to the oracle sampler's on the
+    GPU's logits."""
+    from oracle.sampler import sample_row
+    g_l, g_h, o_l, o_h, toks, hist, params, ties = _first_step(M, 1, [16, 300])
+    assert_close(g_h, o_h, "final residual rows, one layer")
+    assert_close(g_l, o_l, "logits, one layer")
     for r in range(2):
-        kv = synth.bits(synth.normal_bf16((2, 2, 16, 8, 128), 1.0, 5000 + r, "cuda"))
-        for li in range(2):
-            kc[li][r, :16] = kv[li, 0]
-            vc[li][r, :16] = kv[li, 1]
-    hist = [synth.uniform_int(64, 0, shape.vocab - 1, 6000 + r).tolist() for r in range(2)]
-    tokens = [h[-1] for h in hist]
-    params = [OParams(seed=1000 + r) for r in range(2)]
-    ologits, otoks, ties = odecode(tokens, om, kc, vc, lengths, oshape, histories=hist,
-                                   steps=[0, 0], params=params)
-    g, r = f64(logits[:, 0]), ologits.astype(np.float64)
-    assert np.linalg.norm(g - r) / np.linalg.norm(r) <= 1e-2
-    assert np.mean(np.abs(g - r) <= 2e-2 + 1e-2 * np.abs(r)) >= 0.95
-    for r in range(2):
-        if not ties[r]:
-            # the kernel's logits differ from the oracle's in low bits, so
-            # compare the sampler on the GPU's own logits: same token
-            from oracle.sampler import sample_row
-            t, near = sample_row(logits[r, 0].cpu().numpy(), hist[r], 0, params[r])
-            if not near:
-                assert t == int(toks[r, 0])
+        t, near = sample_row(g_l[r].astype(np.float32), hist[r], 0, params[r])
+        if not near:
+            assert t == toks[r]
+
+
+def test_first_step_two_layers_within_the_rounding_noise(M):
+    """Over two layers the GPU and the oracle round to bf16 at the same
+    tensors, but a value that lies within fp32 accumulation error of a bf16
+    rounding boundary rounds one way on each side; the one-unit differences
+    feed the next layer and compound (an fp32-accumulating restatement of the
+    oracle on the CPU, tests/test_oracle_noise_floor.py, shows the same spread).
+    Each kernel is held to the per-element tolerance on its own inputs in
+    test_every_stage_of_the_step_matches_the_oracle; end to end over two layers
+    the check is the norm-relative error (<= 1e-2 per tensor) and the share of
+    elements within the per-element bound: >= 99.9 % of the logits, >= 97 % of
+    the final residual rows."""
+    g_l, g_h, o_l, o_h, toks, hist, params, ties = _first_step(M, 2, [16, 300])
+    for name, g, r, share in (("logits", g_l, o_l, 0.999), ("final residual rows", g_h, o_h, 0.97)):
+        assert np.linalg.norm(g - r) / np.linalg.norm(r) <= 1e-2, name
+        within = np.mean(np.abs(g - r) <= 2e-2 + 1e-2 * np.abs(r))
+        assert within >= share, f"{name}: {within:.5f} of elements within the per-element bound"
 
 
 def test_prefix_cache_reuse_gives_the_same_bits(M):

@@ -147,6 +147,28 @@ def test_rope_closed_form_small():
     assert np.array_equal(got, bf16.round_f64(np.array([-math.sin(3), 0, math.cos(3), 0])))
 
 
+def test_rope_qk_norm_closed_form_norm_before_rotation():
+    # QK-norm then RoPE, D = 4, base 1e4, position 3, gains g = (2, 3, 0.5, 5):
+    # a one-hot head a.e0 has mean square a^2 / 4, so the normalised head is
+    # 2 sign(a) e0 (up to eps), times g0; the pair (0, 2) then rotates by 3.
+    # Rotating first would give g2 (not g0) on element 2.
+    g = _bits_from_f32(np.array([2.0, 3.0, 0.5, 5.0]))
+    eps = 1e-6
+    for a in (1.5, -0.75):
+        x = _bits_from_f32(np.array([[[a, 0.0, 0.0, 0.0]]]))
+        got = bf16.to_f64(rope(x, [3], 1e4, norm_w_bits=g, eps=eps))[0, 0]
+        n = a / math.sqrt(a * a / 4 + eps) * 2.0
+        assert np.array_equal(got, bf16.round_f64(np.array([n * math.cos(3), 0.0, n * math.sin(3), 0.0])))
+    # a constant head c.(1, 1, 1, 1) normalises to sign(c) (up to eps) before the gains
+    x = _bits_from_f32(np.array([[[4.0, 4.0, 4.0, 4.0]]]))
+    got = bf16.to_f64(rope(x, [3], 1e4, norm_w_bits=g, eps=eps))[0, 0]
+    u = 4.0 / math.sqrt(16.0 + eps)
+    t0, t1 = 3.0, 3.0 / 100.0
+    ref = [u * 2.0 * math.cos(t0) - u * 0.5 * math.sin(t0), u * 3.0 * math.cos(t1) - u * 5.0 * math.sin(t1),
+           u * 0.5 * math.cos(t0) + u * 2.0 * math.sin(t0), u * 5.0 * math.cos(t1) + u * 3.0 * math.sin(t1)]
+    assert np.array_equal(got, bf16.round_f64(np.array(ref)))
+
+
 def test_rope_identity_norm_and_relative_position():
     from oracle.rope import rope_f64
     rng = np.random.default_rng(6)
@@ -173,5 +195,10 @@ def test_swiglu_and_add_closed_forms():
     a, b = _bits_from_f32([[1.0, 256.0]]), _bits_from_f32([[2.0 ** -8, 1.0]])
     # 1 + 2^-8 ties to 1 (even); 256 + 1 = 257 rounds to 256 (8 significant bits, tie to even)
     assert np.array_equal(bf16.to_f64(glue.add(a, b)), [[1.0, 256.0]])
+    # an unrounded addend is rounded once with the sum: 1 + (2^-8 + 2^-20) lies
+    # above the tie and rounds up, where rounding the addend first (to 2^-8)
+    # would tie back to 1
+    got = bf16.to_f64(glue.add_f64(_bits_from_f32([[1.0, 1.0]]), np.array([[2.0 ** -8 + 2.0 ** -20, -0.5]])))
+    assert np.array_equal(got, [[1.0 + 2.0 ** -7, 0.5]])
     tab = _bits_from_f32(np.arange(12.0).reshape(4, 3))
     assert np.array_equal(glue.embed(tab, [2, 0]), tab[[2, 0]])

@@ -47,7 +47,13 @@ def test_noalloc_matches_workspace_path_twice(kinv):
         torch.cuda.synchronize()
         assert_close(f64(got), f64(ref), f"no-alloc call {call + 1}")
         assert_same_bits(got, ref, f"no-alloc call {call + 1}")
+        # the Python wrapper reaches the same entry point with the same bits
+        wrapped = torch.full_like(q, float("nan"))
+        kinv.attn_decode_noalloc(q, k, v, kv_len, wrapped)
+        assert_same_bits(wrapped, got, f"wrapper, call {call + 1}")
     assert kinv.last_device_status() == 0
+    with pytest.raises(TypeError):
+        kinv.attn_decode_noalloc(q, k, v, kv_len, torch.empty(q.shape, dtype=torch.float32, device="cuda"))
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(kinv):
@@ -55,7 +61,14 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(kinv):
     need = kinv.attn_decode_workspace(bsz, hq, d, lmax)
     assert need > kinv.NOALLOC_SCRATCH_BYTES
     q = torch.zeros(bsz, hq, d, dtype=torch.bfloat16, device="cuda")
-    kv = torch.zeros(bsz, 1, hkv, d, dtype=torch.bfloat16, device="cuda").expand(bsz, lmax, hkv, d)
+    # one sequence's worth of cache seen by every sequence (sequence stride 0):
+    # valid strides, and every access would stay inside the buffer
+    one = torch.zeros(lmax * hkv * d, dtype=torch.bfloat16, device="cuda")
+    kv = one.as_strided((bsz, lmax, hkv, d), (0, hkv * d, d, 1))
     kv_len = torch.ones(bsz, dtype=torch.int32, device="cuda")
     out = torch.empty_like(q)
     assert _call_noalloc(kinv, q, kv, kv, kv_len, out) == kinv.ERR_WORKSPACE
+    # argument errors come first, in kinv_attn_decode's order: a misaligned
+    # output is reported as such even when the size is also too large
+    bad_out = torch.empty(q.numel() + 8, dtype=torch.bfloat16, device="cuda")[1:1 + q.numel()].view(q.shape)
+    assert _call_noalloc(kinv, q, kv, kv, kv_len, bad_out) == kinv.ERR_ALIGNMENT
