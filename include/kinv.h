@@ -362,6 +362,15 @@ kinv_status kinv_sample(const float* logits, int64_t ld, int B, int V,
 kinv_status kinv_embed(const void* table, int vocab, int dim, const int32_t* ids,
                        void* out, int rows, kinv_stream stream);
 
+/* out[n][k] = bf16(w[n][k] * g[k]) (fp32 product): an RMSNorm gain g moved
+ * into the input columns of the projection it feeds, once, when the weights are
+ * loaded ("Deterministic and bit-exact inference", *technical*: RMSNorm and
+ * matmul; see kinv_gemm_fusion).  w, out: device bf16 [N][K] (ldw, ldo
+ * multiples of 8; out may equal w); g: device bf16 [K]; K % 8 == 0,
+ * N <= 262140, 16-byte aligned bases. */
+kinv_status kinv_scale_columns(const void* w, int64_t ldw, const void* g, void* out, int64_t ldo,
+                               int N, int K, kinv_stream stream);
+
 /* out = bf16(x + y), n elements, bf16, n % 8 == 0, 16-byte aligned. */
 kinv_status kinv_add(const void* x, const void* y, void* out, int64_t n, kinv_stream stream);
 

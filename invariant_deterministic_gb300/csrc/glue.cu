@@ -43,6 +43,26 @@ __global__ void add_kernel(const uint4* x, const uint4* y, uint4* out, int64_t n
   }
 }
 
+// out[n][k] = bf16(w[n][k] * g[k]), fp32 product: an RMSNorm gain moved into
+// the columns of the projection it feeds.  One thread per 8 columns.
+__global__ void scale_columns_kernel(const __nv_bfloat16* __restrict__ w, int64_t ldw,
+                                     const uint4* __restrict__ g, __nv_bfloat16* __restrict__ out,
+                                     int64_t ldo, int K8) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int n = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= K8) return;
+  const uint4 a = *reinterpret_cast<const uint4*>(w + n * ldw + c * 8);
+  const uint4 b = g[c];
+  uint4 o;
+  o.x = pack_bf16(__fmul_rn(bf16_lo(a.x), bf16_lo(b.x)), __fmul_rn(bf16_hi(a.x), bf16_hi(b.x)));
+  o.y = pack_bf16(__fmul_rn(bf16_lo(a.y), bf16_lo(b.y)), __fmul_rn(bf16_hi(a.y), bf16_hi(b.y)));
+  o.z = pack_bf16(__fmul_rn(bf16_lo(a.z), bf16_lo(b.z)), __fmul_rn(bf16_hi(a.z), bf16_hi(b.z)));
+  o.w = pack_bf16(__fmul_rn(bf16_lo(a.w), bf16_lo(b.w)), __fmul_rn(bf16_hi(a.w), bf16_hi(b.w)));
+  *reinterpret_cast<uint4*>(out + n * ldo + c * 8) = o;
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 __global__ void swiglu_kernel(const __nv_bfloat16* __restrict__ gu, int64_t ld_gu,
@@ -178,6 +198,28 @@ extern "C" kinv_status kinv_add(const void* x, const void* y, void* out, int64_t
   const int grid = static_cast<int>(blocks < 4096 ? blocks : 4096);
   return launch_kernel(add_kernel, dim3(grid), dim3(256), 0, stream, 1, static_cast<const uint4*>(x),
                        static_cast<const uint4*>(y), static_cast<uint4*>(out), n8);
+}
+
+extern "C" kinv_status kinv_scale_columns(const void* w, int64_t ldw, const void* g, void* out,
+                                          int64_t ldo, int N, int K, kinv_stream stream) {
+  if (N < 0 || K <= 0) return KINV_ERR_INVALID_ARG;
+  if (N == 0) return KINV_OK;
+  if (!w || !g || !out || ldw < K || ldo < K) return KINV_ERR_INVALID_ARG;
+  if (K % 8) return KINV_ERR_UNSUPPORTED;
+  if (!aligned16(w) || !aligned16(g) || !aligned16(out) || ldw % 8 || ldo % 8) return KINV_ERR_ALIGNMENT;
+  if (N > 65535 * 4) return KINV_ERR_UNSUPPORTED;
+  const int K8 = K / 8;
+  // rows in chunks of at most 65535 grid rows
+  for (int n0 = 0; n0 < N; n0 += 65535) {
+    const int rows = N - n0 < 65535 ? N - n0 : 65535;
+    const kinv_status st = launch_kernel(
+        scale_columns_kernel, dim3((K8 + 127) / 128, rows), dim3(128), 0, stream, 1,
+        static_cast<const __nv_bfloat16*>(w) + static_cast<int64_t>(n0) * ldw, ldw,
+        static_cast<const uint4*>(g), static_cast<__nv_bfloat16*>(out) + static_cast<int64_t>(n0) * ldo, ldo,
+        K8);
+    if (st != KINV_OK) return st;
+  }
+  return KINV_OK;
 }
 
 extern "C" kinv_status kinv_swiglu(const void* gu, int64_t ld_gu, void* out, int64_t ld_out,

@@ -60,6 +60,7 @@ SIGNATURES = {
                            _c_p]),
     "kinv_embed": (_i32, [_c_p, _i32, _i32, _c_p, _c_p, _i32, _c_p]),
     "kinv_add": (_i32, [_c_p, _c_p, _c_p, _i64, _c_p]),
+    "kinv_scale_columns": (_i32, [_c_p, _i64, _c_p, _c_p, _i64, _i32, _i32, _c_p]),
     "kinv_swiglu": (_i32, [_c_p, _i64, _c_p, _i64, _i32, _i32, _c_p]),
     "kinv_rope_append": (_i32, [_c_p, _i64, _c_p, _c_p, _c_p, _i64, _i64, _c_p, _c_p, _c_p, _c_p,
                                 _f32, _i32, _i32, _i32, _i32, _f32, _c_p]),
@@ -392,6 +393,18 @@ def add(x, y, out=None, stream=None):
     if out is None:
         out = torch.empty_like(x)
     _check(lib().kinv_add(_ptr(x), _ptr(y), _ptr(out), x.numel(), _stream(stream)), "kinv_add")
+    return out
+
+
+def scale_columns(w, g, out=None, stream=None):
+    """out[n][k] = bf16(w[n][k] * g[k]): a norm gain folded into a weight."""
+    _need(w, torch.bfloat16, "w")
+    _need(g, torch.bfloat16, "g")
+    n, k = w.shape
+    if out is None:
+        out = torch.empty_like(w)
+    _check(lib().kinv_scale_columns(_ptr(w), w.stride(0), _ptr(g), _ptr(out), out.stride(0), n, k,
+                                    _stream(stream)), "kinv_scale_columns")
     return out
 
 

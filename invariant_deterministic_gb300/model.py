@@ -72,11 +72,12 @@ def random_weights(shape: ModelShape, seed: int = synth.SEED_WEIGHTS, device="cu
 
 
 def fold_gain(w: torch.Tensor, g: torch.Tensor) -> torch.Tensor:
-    """W * g over the input columns (bf16), the RMSNorm gain moved into the
-    projection it feeds; W itself when every gain is 1."""
+    """bf16(W * g) over the input columns (kinv_scale_columns), the RMSNorm
+    gain moved into the projection it feeds; W itself when every gain is 1
+    (the product would return W's bits)."""
     if bool(torch.all(g == 1)):
         return w
-    return (w.float() * g.float()[None, :]).to(torch.bfloat16)
+    return kinv.scale_columns(w, g)
 
 
 # From 2 to this many rows the QKV projection runs with RoPE and the KV append

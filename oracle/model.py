@@ -20,7 +20,9 @@ one step), nor the O and down products (each is added into the residual
 stream x in the projection that forms it, so x2 = bf16(x + o) is rounded
 once), nor the normalised rows h, h2 and the final one: each RMSNorm is
 folded into the projection it feeds, (x / rms(x) * w) . W^T computed as
-(x . (W * w)^T) / rms(x), so here those rows stay unrounded fp64.  Weights are
+(x . (W * w)^T) / rms(x), so here those rows stay unrounded fp64 and the gain
+sits in the stored weight bf16(W * w) (``fold``), rounded like every stored
+tensor.  Weights are
 bf16 bit arrays; the dictionaries below name them.
 """
 from __future__ import annotations
@@ -50,6 +52,19 @@ class Shape:
     qk_norm: bool = False
 
 
+def fold(w_bits, g_bits):
+    """bf16(W[n][k] * g[k]): an RMSNorm gain moved into the input columns of
+    the projection it feeds.  The folded weight is what the step stores and
+    reads, so it is rounded to bf16 like every stored tensor."""
+    if np.all(np.asarray(g_bits) == 0x3F80):  # every gain 1.0: W itself, exactly
+        return w_bits
+    return bf16.from_f64(bf16.to_f64(w_bits) * bf16.to_f64(g_bits)[None, :])
+
+
+def _unit(d):
+    return np.ones(d, dtype=np.float64)
+
+
 def layer_step(x_bits, lw: dict, k_cache, v_cache, pos, shape: Shape):
     """One decoder layer for rows x [M][d].  Row m belongs to sequence seq[m]
     at absolute position pos[m]; ``k_cache``/``v_cache`` are
@@ -59,8 +74,9 @@ def layer_step(x_bits, lw: dict, k_cache, v_cache, pos, shape: Shape):
     """
     hq, hk, dh = shape.n_q, shape.n_kv, shape.head_dim
     m = x_bits.shape[0]
-    h = rmsnorm_f64(bf16.to_f64(x_bits), bf16.to_f64(lw["attn_norm"]), shape.eps)
-    qkv = matmul(h, lw["w_qkv"]).reshape(m, hq + 2 * hk, dh)
+    d = x_bits.shape[1]
+    h = rmsnorm_f64(bf16.to_f64(x_bits), _unit(d), shape.eps)
+    qkv = matmul(h, fold(lw["w_qkv"], lw["attn_norm"])).reshape(m, hq + 2 * hk, dh)
     positions = np.array([p for _, p in pos], dtype=np.int64)
     qn = lw.get("q_norm") if shape.qk_norm else None
     kn = lw.get("k_norm") if shape.qk_norm else None
@@ -76,10 +92,17 @@ def layer_step(x_bits, lw: dict, k_cache, v_cache, pos, shape: Shape):
     # the O and down projections add into the residual stream: their outputs
     # are not stored, so each sum is rounded once
     x2 = glue.add_f64(x_bits, gemm(a.reshape(m, hq * dh), lw["w_o"], out="f64"))
-    h2 = rmsnorm_f64(bf16.to_f64(x2), bf16.to_f64(lw["ffn_norm"]), shape.eps)
+    h2 = rmsnorm_f64(bf16.to_f64(x2), _unit(d), shape.eps)
     # gate/up and SwiGLU form one GPU kernel: g and u are not rounded to bf16
-    act = glue.swiglu_f64(matmul(h2, lw["w_gu"], out="f64"))
+    act = glue.swiglu_f64(matmul(h2, fold(lw["w_gu"], lw["ffn_norm"]), out="f64"))
     return glue.add_f64(x2, gemm(act, lw["w_down"], out="f64"))
+
+
+def final_logits(x_bits, model: dict, shape: Shape):
+    """The final RMSNorm (its gain folded into the LM head) and the LM head:
+    fp32 logits [M][V] of the residual rows x."""
+    h = rmsnorm_f64(bf16.to_f64(x_bits), _unit(x_bits.shape[1]), shape.eps)
+    return matmul(h, fold(model["lm_head"], model["final_norm"]), out="f32")
 
 
 def decode_step(tokens, model: dict, k_caches, v_caches, lengths, shape: Shape,
@@ -90,8 +113,7 @@ def decode_step(tokens, model: dict, k_caches, v_caches, lengths, shape: Shape,
     pos = [(b, int(lengths[b])) for b in range(len(tokens))]
     for li, lw in enumerate(model["layers"]):
         x = layer_step(x, lw, k_caches[li], v_caches[li], pos, shape)
-    h = rmsnorm_f64(bf16.to_f64(x), bf16.to_f64(model["final_norm"]), shape.eps)
-    logits = matmul(h, model["lm_head"], out="f32")
+    logits = final_logits(x, model, shape)
     if not sample_tokens:
         return logits, None, None
     toks, ties = sample(logits, histories, steps, params)

@@ -170,7 +170,8 @@ def test_full_depth_alone_vs_cobatched(M):
     assert_same_bits(l[2], alone_l[0], "logits at full depth")
 
 
-def test_every_stage_of_the_step_matches_the_oracle(M):
+@pytest.mark.parametrize("gains", [False, True], ids=["unit_gains", "random_gains"])
+def test_every_stage_of_the_step_matches_the_oracle(M, gains):
     """Each kernel of a 2-layer 8B-shaped decode step, fed the GPU's own
     inputs for that stage, matches the oracle within the tolerance.  The
     RMSNorms are folded into the projections: the O and down projections add
@@ -184,6 +185,8 @@ def test_every_stage_of_the_step_matches_the_oracle(M):
     kinv = M.kinv
     shape = _shape(M, 2)
     w = M.random_weights(shape, device="cuda")
+    if gains:
+        _random_gains(w)
     B, L = 3, [16, 300, 1]
     dec = M.Decoder(shape, w, max_batch=B, max_len=512)
     for r in range(B):
@@ -192,8 +195,10 @@ def test_every_stage_of_the_step_matches_the_oracle(M):
     dec.tokens[:B] = torch.tensor([5, 77, 151935], dtype=torch.int32, device="cuda")
     b = synth.bits
 
-    def normed(x_bits, g):
-        return rmsnorm_f64(obf.to_f64(x_bits), obf.to_f64(b(g)), 1e-6)
+    from oracle.model import fold
+
+    def normed(x_bits):
+        return rmsnorm_f64(obf.to_f64(x_bits), np.ones(x_bits.shape[1]), 1e-6)
 
     def check_ss(x_bits, name):
         x = obf.to_f64(x_bits)
@@ -209,7 +214,7 @@ def test_every_stage_of_the_step_matches_the_oracle(M):
         lw = w["layers"][li]
         x0 = b(x)
         kinv.gemm_fused(x, dec.w_qkv_f[li], kinv.norm_in(ss, 4096, 1e-6), out=dec.qkv[:B])
-        assert_close(f64(dec.qkv[:B]), obf.to_f64(omm(normed(x0, lw["attn_norm"]), b(lw["w_qkv"]))),
+        assert_close(f64(dec.qkv[:B]), obf.to_f64(omm(normed(x0), fold(b(lw["w_qkv"]), b(lw["attn_norm"])))),
                      "qkv with the attention norm folded in")
         qkv = b(dec.qkv[:B]).reshape(B, 48, 128)
         kc, vc = dec.kv[li, 0], dec.kv[li, 1]
@@ -231,7 +236,7 @@ def test_every_stage_of_the_step_matches_the_oracle(M):
         check_ss(b(x), "sums of squares after the O projection")
         x2 = b(x)
         kinv.gemm_swiglu(x, dec.w_gu_il[li], out=dec.act[:B], fusion=kinv.norm_in(ss, 4096, 1e-6))
-        gu = omm(normed(x2, lw["ffn_norm"]), b(lw["w_gu"]), out="f64")
+        gu = omm(normed(x2), fold(b(lw["w_gu"]), b(lw["ffn_norm"])), out="f64")
         assert_close(f64(dec.act[:B]), obf.to_f64(oglue.swiglu_f64(gu)), "gate/up + swiglu, norm folded in")
         kinv.gemm_fused(dec.act[:B], lw["w_down"], kinv.residual_out(x, ss))
         d_ref = og(b(dec.act[:B]), b(lw["w_down"]), out="f64")
@@ -239,12 +244,23 @@ def test_every_stage_of_the_step_matches_the_oracle(M):
         check_ss(b(x), "sums of squares after the down projection")
     xf = b(x)
     kinv.gemm_fused(x, dec.lm_head_f, kinv.norm_in(ss, 4096, 1e-6), out=dec.logits[:B])
-    assert_close(f64(dec.logits[:B]), omm(normed(xf, w["final_norm"]), b(w["lm_head"]), out="f64"),
+    assert_close(f64(dec.logits[:B]), omm(normed(xf), fold(b(w["lm_head"]), b(w["final_norm"])), out="f64"),
                  "logits with the final norm folded in", atol=1e-4, rtol=1e-4)
     assert kinv.last_device_status() == 0
 
 
-def _first_step(M, layers, lengths):
+def _random_gains(w, seed=4242):
+    """Replace every norm gain with bf16 values drawn from U(0.5, 1.5)."""
+    g = synth.gen(seed)
+    draw = lambda t: (0.5 + torch.rand(t.shape, generator=g)).to(torch.bfloat16).to(t.device)
+    for lw in w["layers"]:
+        for key in ("attn_norm", "ffn_norm", "q_norm", "k_norm"):
+            if key in lw:
+                lw[key] = draw(lw[key])
+    w["final_norm"] = draw(w["final_norm"])
+
+
+def _first_step(M, layers, lengths, gains=False):
     """One decode step of an 8B-shaped stack (full widths and vocabulary) for
     requests with synthetic prompt caches; returns the GPU's logits and final
     residual rows, the oracle's (its own end-to-end computation from the same
@@ -252,11 +268,13 @@ def _first_step(M, layers, lengths):
     histories, the settings and the oracle's near-tie flags."""
     from oracle import glue as oglue
     from oracle.gemm import matmul
-    from oracle.model import layer_step
+    from oracle.model import fold, layer_step
     from oracle.rmsnorm import rmsnorm_f64
     from oracle.sampler import sample as osample
     shape = _shape(M, layers)
     w = M.random_weights(shape, device="cuda")
+    if gains:
+        _random_gains(w)
     bsz = len(lengths)
     lmax = max(lengths) + 16
     dec = M.Decoder(shape, w, max_batch=bsz, max_len=lmax)
@@ -280,8 +298,8 @@ def _first_step(M, layers, lengths):
     for li in range(layers):
         lw = {k: synth.bits(v) for k, v in w["layers"][li].items()}
         x = layer_step(x, lw, kv[li, 0].copy(), kv[li, 1].copy(), [(b, lengths[b]) for b in range(bsz)], oshape)
-    h = rmsnorm_f64(obf.to_f64(x), obf.to_f64(synth.bits(w["final_norm"])), 1e-6)
-    o_logits = matmul(h, synth.bits(w["lm_head"]), out="f32").astype(np.float64)
+    h = rmsnorm_f64(obf.to_f64(x), np.ones(x.shape[1]), 1e-6)
+    o_logits = matmul(h, fold(synth.bits(w["lm_head"]), synth.bits(w["final_norm"])), out="f32").astype(np.float64)
     params = [OParams(seed=1000 + r) for r in range(bsz)]
     _, ties = osample(o_logits.astype(np.float32), hist, [0] * bsz, params)
     return g_logits, g_hidden, o_logits, obf.to_f64(x), toks, hist, params, ties
@@ -301,6 +319,17 @@ def test_first_step_one_layer_end_to_end_matches_oracle(M):
         t, near = sample_row(g_l[r].astype(np.float32), hist[r], 0, params[r])
         if not near:
             assert t == toks[r]
+
+
+def test_first_step_one_layer_with_non_unit_gains(M):
+    """The same end-to-end check with every norm gain drawn from U(0.5, 1.5):
+    the attention, FFN and final gains are folded into the weights they feed
+    (kinv_scale_columns, one bf16 rounding of W * g), the QK-norm gains are
+    applied per head; the oracle applies every gain to the unrounded
+    normalised rows."""
+    g_l, g_h, o_l, o_h, toks, hist, params, ties = _first_step(M, 1, [16, 300], gains=True)
+    assert_close(g_h, o_h, "final residual rows, non-unit gains")
+    assert_close(g_l, o_l, "logits, non-unit gains")
 
 
 def test_first_step_two_layers_within_the_rounding_noise(M):

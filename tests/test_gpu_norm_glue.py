@@ -135,3 +135,20 @@ def test_gemm_qkv_rope_equals_gemm_then_rope_append(kinv, d, hq, hkv, base, qk, 
     for x, y, name in zip(outs[0], outs[1], ("q", "k cache", "v cache")):
         assert_same_bits(y, x, f"fused {name}")
     assert kinv.last_device_status() == 0
+
+
+def test_scale_columns_matches_the_oracle_product(kinv):
+    """kinv_scale_columns: bf16(w * g) per element (the fp32 product of two
+    bf16 values is exact, so one rounding), for a gain vector with values
+    that are and are not powers of two."""
+    n, k = 300, 512
+    w = synth.normal_bf16((n, k), 0.02, 91).cuda()
+    g = (0.5 + torch.rand(k, generator=synth.gen(92))).to(torch.bfloat16)
+    g[:8] = torch.tensor([1, 2, 0.5, 4, 0.25, -1, 0, 3], dtype=torch.bfloat16)
+    got = kinv.scale_columns(w, g.cuda())
+    ref = obf.from_f64(obf.to_f64(synth.bits(w)) * obf.to_f64(synth.bits(g))[None, :])
+    assert np.array_equal(synth.bits(got), ref)
+    # in place
+    w2 = w.clone()
+    kinv.scale_columns(w2, g.cuda(), out=w2)
+    assert_same_bits(w2, got, "in place")

@@ -122,3 +122,14 @@ def test_layer_ffn_side_closed_form():
     ref = np.full((2, 256), 0x3F80, np.uint16)
     ref[:, 11] = _b(1.0 + act)
     assert np.array_equal(out, ref)
+
+
+def test_fold_rounds_the_gained_weight_once_per_column():
+    """fold(W, g) = bf16(W[n][k] * g[k]): a column gain, rounded to bf16.
+    (1 + 2^-7)^2 = 1 + 2^-6 + 2^-14 lies below the midpoint to the next bf16
+    value, so it rounds to 1 + 2^-6; powers of two scale exactly."""
+    from oracle.model import fold
+    w = np.array([[_b(1.0 + 2.0 ** -7), _b(3.0)], [_b(-0.5), _b(1.0)]], np.uint16)
+    g = np.array([_b(1.0 + 2.0 ** -7), _b(0.25)], np.uint16)
+    got = bf16.to_f64(fold(w, g))
+    assert np.array_equal(got, [[1.0 + 2.0 ** -6, 0.75], [-0.5 * (1.0 + 2.0 ** -7), 0.25]])
