@@ -131,6 +131,9 @@ struct GemmArgs {
   __nv_bfloat16* resid;
   int64_t ld_resid;
   float* ss_out;
+  // the large-M tile kernel's schedule
+  int kb_per_split;  // 64-wide K blocks of one K range
+  int tiles_m, tiles_n;
 };
 
 // Rows [0, n) of a staged tile (bf16, row stride BN) are rows row_of(r) of the
@@ -271,7 +274,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int k_stages = args.k_stages;
   const int kb0 = rank * k_stages * jb;  // first K block of this split
 
-  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full_bar(s), 1);
@@ -295,6 +297,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // dependents are released once this block holds its tensor memory (a
+  // dependent block that allocated first would wait on this grid)
+  pdl_launch_dependents();
   // push path: the peers' barriers are initialised before any remote arrive
   // or store reaches them (the matching wait comes at the epilogue)
   if (push) cluster_arrive_relaxed();
@@ -774,6 +779,297 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// The large-M schedule: gemm_kernel's per-element arithmetic, laid out for the
+// tensor cores instead of the weight stream.
+//
+// For an output element gemm_kernel forms, for each of the plan's `splits`
+// contiguous K ranges r, a partial p_r accumulated from zero over the range's
+// 64-wide K blocks in ascending order (16-deep bf16 MMA steps, fp32 in TMEM),
+// then ((p_0 + p_1) + p_2) + ... in fp32 in rank order, then the epilogue.
+// With many rows the K split only costs: every 128-row tile goes through a
+// cluster reduction whose epilogue does not overlap the MMAs.  Here one CTA
+// per SM walks a static list of 128 x 256 output tiles (row tiles fastest, so
+// the CTAs in flight share a few weight tiles in L2); for each tile it forms
+// the K ranges one after another in two TMEM accumulators used in turn, and
+// eight epilogue warps fold each finished range into a running sum held in
+// registers while the tensor cores work on the next range (or the next
+// tile).  The sums are the same fp32 operations in the same order as
+// gemm_kernel's, and so are the epilogues (row scale, SwiGLU, residual add and
+// its sums of squares, bf16 / fp32 store), so a row has the same bits through
+// either kernel.
+//
+// Roles (320 threads): warps 0-7 fold and store (warp w reads TMEM lanes
+// 32 (w % 4) .. + 31 = tile rows, columns 128 (w / 4) .. + 127), warp 8 lane 0
+// issues the TMA loads, warp 9 lane 0 the MMAs (warp 9 also owns the TMEM
+// allocation: two accumulators of 256 columns).
+constexpr int kTilesBN = 256;
+constexpr int kTilesThreads = 320;
+constexpr int kTilesEpiWarps = 8;
+constexpr int kTilesABytes = BM * BK * 2;        // 16 KB
+constexpr int kTilesBBytes = kTilesBN * BK * 2;  // 32 KB
+constexpr int kTilesStage = kTilesABytes + kTilesBBytes;
+__host__ __device__ constexpr int tiles_bar_count(int stages) { return 2 * stages + 5; }
+
+// The push path's sum of squares of a 128-column tile (per warp a fixed xor
+// butterfly over 32 columns, then the four warps in order), formed by one
+// thread that holds the tile's 128 values: the same pairs in the same order.
+__device__ __forceinline__ float sumsq_butterfly128(const float (&v)[128]) {
+  float g4[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      t[i] = __fadd_rn(__fmul_rn(v[32 * g + i], v[32 * g + i]), __fmul_rn(v[32 * g + i + 16], v[32 * g + i + 16]));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t[i] = __fadd_rn(t[i], t[i + 8]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) t[i] = __fadd_rn(t[i], t[i + 4]);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) t[i] = __fadd_rn(t[i], t[i + 2]);
+    g4[g] = __fadd_rn(t[0], t[1]);
+  }
+  return __fadd_rn(__fadd_rn(__fadd_rn(g4[0], g4[1]), g4[2]), g4[3]);
+}
+
+template <int MMA_N>
+__global__ void __launch_bounds__(kTilesThreads, 1)
+    gemm_tiles_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                      const GemmArgs args) {
+  static_assert(MMA_N == 128 || MMA_N == 256, "one or two MMAs per 16-deep step");
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int stages = args.stages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + stages * kTilesStage);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + tiles_bar_count(stages));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto full_bar = [&](int st) { return smem_addr(bars + st); };
+  auto empty_bar = [&](int st) { return smem_addr(bars + stages + st); };
+  auto acc_full = [&](int b) { return smem_addr(bars + 2 * stages + b); };
+  auto acc_empty = [&](int b) { return smem_addr(bars + 2 * stages + 2 + b); };
+  const uint32_t done_bar = smem_addr(bars + 2 * stages + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles_m = args.tiles_m;
+  const int n_tiles = tiles_m * args.tiles_n;
+  const int splits = args.splits, kbs = args.kb_per_split;
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < stages; ++st) {
+      mbar_init(full_bar(st), 1);
+      mbar_init(empty_bar(st), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), kTilesEpiWarps);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) tmem_alloc(smem_addr(tmem_slot), 2 * kTilesBN);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // Dependent kernels may be scheduled only once every block of this grid
+  // holds its tensor memory: a dependent block that took the columns first
+  // would wait for this grid while this block waited for the columns.
+  pdl_launch_dependents();
+  // everything this kernel reads may come from the kernels before it
+  pdl_wait();
+
+  if (warp == 8) {
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+      const uint64_t pol_a = l2_policy_evict_last();
+      const uint64_t pol_w = l2_policy_evict_last();  // a weight tile serves every row tile
+      int it = 0;
+      bool stop = false;
+      for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
+        const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * kTilesBN;
+        for (int kb = 0; kb < splits * kbs; ++kb, ++it) {
+          const int st = it % stages;
+          const uint32_t ph = (it / stages) & 1u;
+          if (*abort_flag ||
+              !mbar_wait_bounded(empty_bar(st), ph ^ 1u, args.status, DEV_TIMEOUT_GEMM_PRODUCER)) {
+            *abort_flag = 1;
+            stop = true;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(st), kTilesStage);
+          unsigned char* sa = base + st * kTilesStage;
+          tma_load_3d(smem_addr(sa), &tmA, 0, m0, kb, full_bar(st), pol_a);
+          tma_load_3d(smem_addr(sa + kTilesABytes), &tmW, 0, n0, kb, full_bar(st), pol_w);
+        }
+      }
+      // loads still in flight (only after an abort) land before the block exits
+      for (int j = it - stages > 0 ? it - stages : 0; j < it; ++j)
+        mbar_wait_bounded(full_bar(j % stages), (j / stages) & 1u, nullptr, 0);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = instr_desc<MMA_N>();
+      int it = 0, seq = 0;
+      bool stop = false;
+      for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
+        for (int r = 0; r < splits && !stop; ++r, ++seq) {
+          const int b = seq & 1;
+          const uint32_t aph = (seq >> 1) & 1u;
+          if (*abort_flag ||
+              !mbar_wait_bounded(acc_empty(b), aph ^ 1u, args.status, DEV_TIMEOUT_GEMM_MMA)) {
+            *abort_flag = 1;
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + static_cast<uint32_t>(b * kTilesBN);
+          for (int k = 0; k < kbs; ++k, ++it) {
+            const int st = it % stages;
+            const uint32_t ph = (it / stages) & 1u;
+            if (*abort_flag || !mbar_wait_bounded(full_bar(st), ph, args.status, DEV_TIMEOUT_GEMM_MMA)) {
+              *abort_flag = 1;
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_addr(base + st * kTilesStage);
+            const uint32_t b_addr = a_addr + kTilesABytes;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint32_t accum = (k | kk) != 0 ? 1u : 0u;
+              const uint64_t adesc = sdesc_sw128(a_addr + kk * 32);
+              if constexpr (MMA_N == 256) {
+                umma_bf16(d, adesc, sdesc_sw128(b_addr + kk * 32), idesc, accum);
+              } else {
+                umma_bf16(d, adesc, sdesc_sw128(b_addr + kk * 32), idesc, accum);
+                umma_bf16(d + 128, adesc, sdesc_sw128(b_addr + 128 * 128 + kk * 32), idesc, accum);
+              }
+            }
+            umma_commit(empty_bar(st));
+          }
+          if (!stop) umma_commit(acc_full(b));
+        }
+      }
+      // every MMA issued has completed before the TMEM is released
+      umma_commit(done_bar);
+      mbar_wait_bounded(done_bar, 0, args.status, DEV_TIMEOUT_GEMM_MMA);
+    }
+    __syncwarp();
+  } else {
+    const int lg = warp & 3;       // TMEM lane group: tile rows 32 lg .. 32 lg + 31
+    const int half = warp >> 2;    // tile columns 128 half .. 128 half + 127
+    const int row = lg * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(lg * 32) << 16) + half * 128;
+    int seq = 0;
+    bool stop = false;
+    for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
+      const int m = (t % tiles_m) * BM + row;
+      const int nc0 = (t / tiles_m) * kTilesBN + half * 128;  // this thread's first column
+      float acc[128];
+      for (int r = 0; r < splits; ++r, ++seq) {
+        const int b = seq & 1;
+        const uint32_t aph = (seq >> 1) & 1u;
+        const bool ok = mbar_wait_bounded(acc_full(b), aph, args.status, DEV_TIMEOUT_GEMM_EPILOGUE);
+        if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
+          *abort_flag = 1;
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + b * kTilesBN + c * 32, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            acc[c * 32 + j] = r == 0 ? __uint_as_float(v[j]) : __fadd_rn(acc[c * 32 + j], __uint_as_float(v[j]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acc_empty(b)) : "memory");
+      }
+      if (stop || m >= args.M || nc0 >= args.N) continue;
+      if (args.row_ss) {
+        // 1 / rms of the row from its partial sums of squares, tiles in order
+        const float* ss = args.row_ss + static_cast<int64_t>(m) * args.row_ss_tiles;
+        float sacc = ss[0];
+        for (int q = 1; q < args.row_ss_tiles; ++q) sacc = __fadd_rn(sacc, ss[q]);
+        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(sacc, static_cast<float>(args.norm_dim)),
+                                                              args.eps)));
+#pragma unroll
+        for (int j = 0; j < 128; ++j) acc[j] = __fmul_rn(acc[j], inv);
+      }
+      if (args.swiglu) {
+        // columns 0..63 of this half are gate features nc0/2 .. nc0/2 + 63,
+        // columns 64..127 the up features for the same ids
+        __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(args.C) + m * args.ldc + nc0 / 2;
+#pragma unroll
+        for (int j = 0; j < 64; j += 8) {
+          uint4 o;
+          o.x = pack_bf16(silu_times(acc[j + 0], acc[64 + j + 0]), silu_times(acc[j + 1], acc[64 + j + 1]));
+          o.y = pack_bf16(silu_times(acc[j + 2], acc[64 + j + 2]), silu_times(acc[j + 3], acc[64 + j + 3]));
+          o.z = pack_bf16(silu_times(acc[j + 4], acc[64 + j + 4]), silu_times(acc[j + 5], acc[64 + j + 5]));
+          o.w = pack_bf16(silu_times(acc[j + 6], acc[64 + j + 6]), silu_times(acc[j + 7], acc[64 + j + 7]));
+          *reinterpret_cast<uint4*>(crow + j) = o;
+        }
+      } else if (args.resid) {
+        __nv_bfloat16* xrow = args.resid + m * args.ld_resid + nc0;
+        float ss_seq = 0.f;  // one range: the column-order FMA chain of the unsplit epilogue
+#pragma unroll
+        for (int j = 0; j < 128; j += 8) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xrow + j);
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+          uint32_t ow[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float s0 = residual_add(xw[q] & 0xFFFFu, acc[j + 2 * q]);
+            const float s1 = residual_add(xw[q] >> 16, acc[j + 2 * q + 1]);
+            acc[j + 2 * q] = s0;
+            acc[j + 2 * q + 1] = s1;
+            ss_seq = fmaf(s0, s0, ss_seq);
+            ss_seq = fmaf(s1, s1, ss_seq);
+            ow[q] = pack_bf16(s0, s1);
+          }
+          *reinterpret_cast<uint4*>(xrow + j) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        }
+        args.ss_out[static_cast<int64_t>(m) * (args.N / 128) + nc0 / 128] =
+            splits > 1 ? sumsq_butterfly128(acc) : ss_seq;
+      } else if (args.c_f32) {
+        float* crow = static_cast<float*>(args.C) + m * args.ldc + nc0;
+#pragma unroll
+        for (int j = 0; j < 128; j += 4)
+          if (nc0 + j < args.N)
+            *reinterpret_cast<float4*>(crow + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+      } else {
+        __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(args.C) + m * args.ldc + nc0;
+#pragma unroll
+        for (int j = 0; j < 128; j += 8) {
+          if (nc0 + j < args.N) {
+            uint4 o;
+            o.x = pack_bf16(acc[j + 0], acc[j + 1]);
+            o.y = pack_bf16(acc[j + 2], acc[j + 3]);
+            o.z = pack_bf16(acc[j + 4], acc[j + 5]);
+            o.w = pack_bf16(acc[j + 6], acc[j + 7]);
+            *reinterpret_cast<uint4*>(crow + j) = o;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * kTilesBN);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -889,6 +1185,37 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a
                        stream, static_cast<unsigned>(a.splits), ta, tw, a);
 }
 
+// The large-M schedule: one CTA per SM (at most one per tile), the stage ring
+// as deep as shared memory allows.
+template <int MMA_N>
+kinv_status launch_gemm_tiles(const void* A, int64_t lda, const void* W, int64_t ldw, int K, GemmArgs a,
+                              cudaStream_t stream) {
+  CUtensorMap ta, tw;
+  if (!make_map(&ta, A, a.M, K, lda, BM, 1) || !make_map(&tw, W, a.N, K, ldw, kTilesBN, 1))
+    return KINV_ERR_CUDA;
+  a.kb_per_split = K / BK / a.splits;
+  a.tiles_m = (a.M + BM - 1) / BM;
+  a.tiles_n = (a.N + kTilesBN - 1) / kTilesBN;
+  const int avail = max_smem_optin() - 1024 - 256;
+  int stages = avail / kTilesStage;
+  stages = stages > 6 ? 6 : stages;
+  if (stages < 2) return KINV_ERR_UNSUPPORTED;
+  a.stages = stages;
+  const size_t smem = 1024 + static_cast<size_t>(stages) * kTilesStage + tiles_bar_count(stages) * 8 + 16;
+  const kinv_status attr = ensure_smem(reinterpret_cast<const void*>(gemm_tiles_kernel<MMA_N>), smem);
+  if (attr != KINV_OK) return attr;
+  const long long tiles = static_cast<long long>(a.tiles_m) * a.tiles_n;
+  const int sms = sm_count() > 0 ? sm_count() : 1;
+  const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+  return launch_kernel(gemm_tiles_kernel<MMA_N>, dim3(grid), dim3(kTilesThreads), smem, stream, 1, ta, tw, a);
+}
+
+// Rows from which the tile schedule is used (the cluster split-K schedule
+// below it).  Either gives a row the same bits.
+constexpr int kTilesMinRows = 129;
+// MMA width of the tile schedule: one 128 x 256 instruction per 16-deep step.
+constexpr int kTilesMmaN = 256;
+
 }  // namespace
 }  // namespace kinv
 
@@ -906,8 +1233,8 @@ kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, vo
   if (fu && fu->row_ss && (fu->row_ss_tiles <= 0 || fu->norm_dim <= 0 || !(fu->eps >= 0.f)))
     return KINV_ERR_INVALID_ARG;
   if (resid) {
-    // the residual stream is the only output
-    if (!fu->ss_out || swiglu || rope || fu->ld_resid < N) return KINV_ERR_INVALID_ARG;
+    // the residual stream is the only output; a producing projection takes no row scale
+    if (!fu->ss_out || swiglu || rope || fu->ld_resid < N || fu->row_ss) return KINV_ERR_INVALID_ARG;
     if (N % 128) return KINV_ERR_UNSUPPORTED;
     if (!aligned16(fu->resid) || fu->ld_resid % 8) return KINV_ERR_ALIGNMENT;
     rope = nullptr;
@@ -962,6 +1289,10 @@ kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, vo
   a.resid = resid ? static_cast<__nv_bfloat16*>(fu->resid) : nullptr;
   a.ld_resid = resid ? fu->ld_resid : 0;
   a.ss_out = resid ? fu->ss_out : nullptr;
+  a.kb_per_split = 0;
+  a.tiles_m = a.tiles_n = 0;
+  if (!rope && M >= kTilesMinRows)
+    return launch_gemm_tiles<kTilesMmaN>(A, lda, W, ldw, K, a, stream);
   switch (p.bn) {
     case 128: return launch_gemm<128>(ta, tw, a, p.smem_budget, grid_y, grid_z, stream);
     default: return KINV_ERR_UNSUPPORTED;
