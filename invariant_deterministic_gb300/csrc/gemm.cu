@@ -1210,9 +1210,19 @@ kinv_status launch_gemm_tiles(const void* A, int64_t lda, const void* W, int64_t
   return launch_kernel(gemm_tiles_kernel<MMA_N>, dim3(grid), dim3(kTilesThreads), smem, stream, 1, ta, tw, a);
 }
 
-// Rows from which the tile schedule is used (the cluster split-K schedule
-// below it).  Either gives a row the same bits.
-constexpr int kTilesMinRows = 129;
+// Whether the tile schedule runs a call (else the cluster split-K schedule).
+// Either gives a row the same bits, so this is a speed choice.  Measured on
+// the GB300 (cold L2, per launch): with one K range per tile the tile
+// schedule is faster from 129 rows; with a K split, from 384 rows (768 for
+// K >= 8192, whose tiles' K loops are long and few at that size).
+#ifndef KINV_TILES_MIN_ROWS
+#define KINV_TILES_MIN_ROWS 129
+#endif
+bool use_tiles(int M, int K, int splits) {
+  if (M < KINV_TILES_MIN_ROWS) return false;
+  if (splits == 1) return true;
+  return M >= (K >= 8192 ? 768 : 384);
+}
 // MMA width of the tile schedule: one 128 x 256 instruction per 16-deep step.
 constexpr int kTilesMmaN = 256;
 
@@ -1291,7 +1301,7 @@ kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, vo
   a.ss_out = resid ? fu->ss_out : nullptr;
   a.kb_per_split = 0;
   a.tiles_m = a.tiles_n = 0;
-  if (!rope && M >= kTilesMinRows)
+  if (!rope && use_tiles(M, K, p.splits))
     return launch_gemm_tiles<kTilesMmaN>(A, lda, W, ldw, K, a, stream);
   switch (p.bn) {
     case 128: return launch_gemm<128>(ta, tw, a, p.smem_budget, grid_y, grid_z, stream);

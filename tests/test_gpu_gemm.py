@@ -60,14 +60,19 @@ MS = [1, 7, 16, 64, 128, 256]
 
 @pytest.mark.parametrize("n,k", SHAPES_8B)
 def test_8b_shapes_row_bits_independent_of_m(kinv, n, k):
-    """Row i's bits are the same for M in {1, 7, 16, 64, 128, 256} and for any
-    co-batched rows; sampled outputs match the oracle."""
+    """Row i's bits are the same for M in {1, 7, 16, 64, 128, 256, 512, 1024}
+    (the cluster split-K schedule below a few hundred rows, the tile schedule
+    above) and for any co-batched rows; every output of the M = 256 product
+    matches the oracle."""
     w = synth.normal_bf16((n, k), 0.02, 6).cuda()
-    a = synth.normal_bf16((256, k), 1.0, 7).cuda()
+    a_big = synth.normal_bf16((1024, k), 1.0, 7).cuda()
+    big = kinv.gemm(a_big, w)
+    a = a_big[:256].contiguous()
     full = kinv.gemm(a, w)
-    for m in MS:
-        part = kinv.gemm(a[:m].contiguous(), w)
-        assert_same_bits(part, full[:m], f"N={n} K={k} M={m}")
+    assert_same_bits(full, big[:256], f"N={n} K={k}: M=256 vs M=1024")
+    for m in MS + [512]:
+        part = kinv.gemm(a_big[:m].contiguous(), w)
+        assert_same_bits(part, big[:m], f"N={n} K={k} M={m}")
     # the same rows among different batch-mates, at other positions
     other = synth.normal_bf16((256, k), 1.0, 8).cuda()
     perm = torch.randperm(256, generator=synth.gen(9))
@@ -84,8 +89,11 @@ def test_8b_shapes_row_bits_independent_of_m(kinv, n, k):
 def test_lm_head_fp32_row_invariance(kinv):
     n, k = 151936, 4096
     w = synth.normal_bf16((n, k), 0.02, 11).cuda()
-    a = synth.normal_bf16((16, k), 1.0, 12).cuda()
-    full = kinv.gemm(a, w, out_dtype=torch.float32)
+    a_big = synth.normal_bf16((300, k), 1.0, 12).cuda()
+    big = kinv.gemm(a_big, w, out_dtype=torch.float32)   # the tile schedule
+    a = a_big[:16].contiguous()
+    full = kinv.gemm(a, w, out_dtype=torch.float32)      # the cluster schedule
+    assert_same_bits(full, big[:16], "LM head: 16 rows vs 300 rows")
     one = kinv.gemm(a[3:4].contiguous(), w, out_dtype=torch.float32)
     assert_same_bits(one, full[3:4], "LM head row 3")
     cols = torch.randint(0, n, (128,), generator=synth.gen(13)).numpy()
@@ -179,14 +187,15 @@ def test_gemm_swiglu_rejects_bad_f(kinv):
 
 
 # ---------------------------------------------------------------- folded RMSNorm epilogues
-@pytest.mark.parametrize("m", [64, 256])
+@pytest.mark.parametrize("m", [64, 256, 1024])
 def test_fused_epilogues_match_the_oracle_on_whole_rows(kinv, m):
     """The epilogues of kinv_gemm_fused / kinv_gemm_swiglu at 64 and 256 rows
-    (the owners of split-K rows pull the partials), against the oracle on every
-    element: the row scale 1/rms from per-tile sums of squares (QKV, gate/up),
-    the residual add with the new rows' sums of squares (O, down).  The same
-    rows computed in a 4-row call (partials pushed to their owners) have the
-    same bits."""
+    (the owners of split-K rows pull the partials) and at 1024 rows (the tile
+    schedule: one block folds every K range of a tile), against the oracle on
+    every element: the row scale 1/rms from per-tile sums of squares (QKV,
+    gate/up), the residual add with the new rows' sums of squares (O, down).
+    The same rows computed in a 4-row call (partials pushed to their owners)
+    have the same bits."""
     from oracle.gemm import matmul
     from oracle.rmsnorm import rmsnorm_f64
     d, f = 4096, 12288
