@@ -728,6 +728,62 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_case(spec: str, iters: int):
+    """One kernel on a small stand-alone case, `iters` launches after one
+    warm-up (for profiler captures): gemm:M:N:K (kinv_gemm, bf16 out),
+    attn_prefill:T (one sequence's T-row chunk at position 0, 32/8 heads of
+    128), attn_decode:B (B sequences, KV lengths U{1..32768}).  Prints the
+    mean launch time."""
+    import torch
+    from invariant_deterministic_gb300 import build, kinv, synth
+    build.build()
+    kind, *dims = spec.split(":")
+    dims = [int(x) for x in dims]
+    dev = torch.device("cuda", 0)
+    if kind == "gemm":
+        m, n, k = dims
+        w = synth.normal_bf16((n, k), 0.02, 6, dev)
+        a = synth.normal_bf16((m, k), 1.0, 7, dev)
+        c = torch.empty(m, n, dtype=torch.bfloat16, device=dev)
+        fn = lambda: kinv.gemm(a, w, out=c)
+    elif kind == "attn_prefill":
+        (t,) = dims
+        g = synth.gen(synth.SEED_ACT, dev)
+        kc = torch.empty(1, t, 8, 128, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+        vc = torch.empty_like(kc).normal_(generator=g)
+        q = synth.normal_bf16((t, 32, 128), 1.0, 32, dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        st, ln, off = torch.zeros(1, **i32), torch.tensor([t], **i32), torch.zeros(1, **i32)
+        out = torch.empty_like(q)
+        ws = torch.empty(kinv.attn_prefill_workspace(t, 32, 128, t), dtype=torch.uint8, device=dev)
+        fn = lambda: kinv.attn_prefill(q, kc, vc, st, ln, off, t, t, out=out, workspace=ws)
+    elif kind == "attn_decode":
+        (b,) = dims
+        g = synth.gen(synth.SEED_ACT, dev)
+        kc = torch.empty(b, 32768, 8, 128, dtype=torch.bfloat16, device=dev).normal_(generator=g)
+        vc = torch.empty_like(kc).normal_(generator=g)
+        q = synth.normal_bf16((b, 32, 128), 1.0, 32, dev)
+        lens = synth.uniform_int(b, 1, 32768, synth.SEED_LEN).to(dev)
+        out = torch.empty_like(q)
+        ws = torch.empty(kinv.attn_decode_workspace(b, 32, 128, 32768), dtype=torch.uint8, device=dev)
+        fn = lambda: kinv.attn_decode(q, kc, vc, lens, out=out, workspace=ws)
+    else:
+        raise SystemExit(f"unknown case {spec}")
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    status = kinv.last_device_status()
+    print(json.dumps({"case": spec, "iters": iters, "ms_per_launch": round(e0.elapsed_time(e1) / iters, 4),
+                      "device_status": status}), flush=True)
+    if status != 0:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -744,7 +800,12 @@ def main():
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
     ap.add_argument("--prefill-len", type=int, default=4096)
     ap.add_argument("--prefill-chunks", default="512,4096")
+    ap.add_argument("--case", default=None, help="run one kernel case (gemm:M:N:K, attn_prefill:T, attn_decode:B)")
+    ap.add_argument("--case-iters", type=int, default=3)
     args = ap.parse_args()
+    if args.case:
+        run_case(args.case, args.case_iters)
+        return
     if args.warmup < 3:
         args.warmup = 3
     args.prefill_chunks = [int(c) for c in str(args.prefill_chunks).split(",") if c]

@@ -33,6 +33,15 @@
 //  4. The draw: u = (Philox4x32-10(counter = (step lo, step hi, 0, 0),
 //     key = (seed lo, seed hi)).word0 >> 8) * 2^-24 (Salmon et al., SC'11,
 //     restated here from the published round function and constants).
+// Over the whole vocabulary (no top-k) nothing is gathered: every mass the
+// filters and the draw need -- the total, the entropy of typical-p, the mass
+// of the ids at or above a key -- is a masked sum over the whole row in one
+// fixed order (4 ids in order per lane of a 128-id block, a butterfly over the
+// lanes, a butterfly over the 32 blocks of a 4096-id group, the groups in
+// order), and the cuts are found by searching the 32-bit keys, seven
+// thresholds per pass, for where that mass crosses the target; ties at the cut
+// key are taken lowest id first (equal keys, equal weights).  Counts and
+// maxima are exact.
 #include <math.h>
 
 #include <mutex>
@@ -101,8 +110,14 @@ struct Smem {
   uint32_t n_cand;
   // this block's copy of the cluster-wide decisions
   float m_all;
-  float blk[kMaxBlocks];  // full vocabulary: sums of e over 128-id blocks (rank 0: every block)
-  float total_all;
+  // whole vocabulary: sums of one pass, per 128-id block of a group, per
+  // 4096-id group of this block's share, and (rank 0) every group's
+  float psum[16][32];
+  float gsum[16][kMaxBlocks / 32];
+  float gall[16][kMaxBlocks / 32];
+  float res[16];          // the pass results (rank 0's, copied to every block)
+  long long xi[2];        // this block's integer partials (counts, first ids)
+  long long ires[2];      // the cluster's (copied to every block)
   uint32_t eq_taken;
   uint32_t thresh;
   int k_rem;
@@ -234,8 +249,12 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
   const float* row = logits + b * ld;
   const kinv_sampling_params prm = params[b];
   const int words = (V + 31) >> 5;
-  // this block's ids: a multiple of 128 per rank (whole vectors, whole bitmap words)
-  const int chunk = ((V + C - 1) / C + 127) / 128 * 128;
+  // this block's ids: a multiple of 128 per rank (whole vectors, whole bitmap
+  // words); over the whole vocabulary a multiple of 4096 (whole groups of its
+  // sums)
+  const bool whole_row = (prm.top_k <= 0 || prm.top_k >= V) && V > kMaxTopK && prm.temperature > 0.f;
+  const int quantum = whole_row ? 4096 : 128;
+  const int chunk = ((V + C - 1) / C + quantum - 1) / quantum * quantum;
   const int v0 = min(V, rank * chunk), v1 = min(V, v0 + chunk);
   auto peer = [](const void* p, int q) { return map_to_rank(smem_addr(p), static_cast<uint32_t>(q)); };
 
@@ -368,6 +387,392 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
   };
 
   const float temp = prm.temperature;
+
+  // ---- the whole vocabulary (no top-k): masked sums and key searches
+  auto whole_vocabulary = [&]() {
+    constexpr int NS = 15;  // thresholds per search pass
+    // the row maximum (exact, any order)
+    {
+      float mx = -INFINITY;
+      visit([&](bool valid, int, float z) {
+        if (valid) mx = fmaxf(mx, z);
+      });
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0) sm.wmax[warp] = mx;
+      __syncthreads();
+      if (t == 0) {
+        float m = sm.wmax[0];
+        for (int w = 1; w < kWarps; ++w) m = fmaxf(m, sm.wmax[w]);
+        sm.x_max = m;
+      }
+      cluster_sync();
+      if (warp == 0) {
+        float m = lane < C ? ld_dsmem_f32(peer(&sm.x_max, lane)) : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) sm.m_all = m;
+      }
+      __syncthreads();
+    }
+    const float s0 = __fdiv_rn(sm.m_all, temp);
+    const uint32_t key_hi = ordered_key(sm.m_all);
+    auto weight = [&](float z) { return expf(__fsub_rn(__fdiv_rn(z, temp), s0)); };
+    const int groups = (V + 4095) / 4096;
+    const int g0 = v1 > v0 ? v0 / 4096 : 0, g1 = v1 > v0 ? (v1 + 4095) / 4096 : 0;
+
+    // nt sums of term(j, id, z, e) over the whole row in the fixed order (4
+    // ids per lane of a 128-id block, a butterfly over the lanes, a butterfly
+    // over the group's 32 blocks, the groups in order); every block gets
+    // them in sm.res
+    auto pass_sums = [&](int nt, auto&& term) {
+      for (int g = g0; g < g1; ++g) {
+        for (int bb = warp; bb < 32; bb += kWarps) {
+          float acc[NS];
+#pragma unroll
+          for (int j = 0; j < NS; ++j) acc[j] = 0.f;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int i = (32 * g + bb) * 128 + 4 * lane + q;
+            if (i < V) {
+              float z = penalised(row, i, pe);
+              if (isnan(z)) z = -INFINITY;
+              const float e = weight(z);
+#pragma unroll
+              for (int j = 0; j < NS; ++j)
+                if (j < nt) acc[j] = __fadd_rn(acc[j], term(j, i, z, e));
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < NS; ++j) {
+            if (j < nt) {
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) acc[j] = __fadd_rn(acc[j], __shfl_xor_sync(0xffffffffu, acc[j], o));
+              if (lane == 0) sm.psum[j][bb] = acc[j];
+            }
+          }
+        }
+        __syncthreads();
+        if (warp < nt) {
+          float v = sm.psum[warp][lane];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+          if (lane == 0) sm.gsum[warp][g - g0] = v;
+        }
+        __syncthreads();
+      }
+      cluster_sync();  // every block's group sums are in place
+      if (rank == 0) {
+        for (int idx = t; idx < nt * groups; idx += kThreadsS) {
+          const int j = idx / groups, g = idx % groups;
+          const int q = g * 4096 / chunk;  // the block holding group g
+          const int gl = g - q * (chunk / 4096);
+          sm.gall[j][g] = q == 0 ? sm.gsum[j][gl] : ld_dsmem_f32(peer(&sm.gsum[j][gl], q));
+        }
+        __syncthreads();
+        if (t < nt) {
+          float acc = 0.f;
+          for (int g = 0; g < groups; ++g) acc = __fadd_rn(acc, sm.gall[t][g]);
+          sm.res[t] = acc;
+        }
+      }
+      cluster_sync();  // rank 0's sums are in place
+      if (rank != 0 && t < nt) sm.res[t] = ld_dsmem_f32(peer(&sm.res[t], 0));
+      __syncthreads();
+    };
+    // over the ids with pred(id, z): the count (sm.ires[0]) and, with
+    // `largest` false, the smallest composite (key, id) (the last in
+    // candidate order), else the largest (the first), in sm.ires[1]
+    auto pass_count = [&](bool largest, auto&& pred) {
+      long long c = 0;
+      unsigned long long best = largest ? 0ull : ~0ull;
+      visit([&](bool valid, int i, float z) {
+        if (valid && pred(i, z)) {
+          ++c;
+          const unsigned long long x = composite(ordered_key(z), i);
+          best = largest ? (x > best ? x : best) : (x < best ? x : best);
+        }
+      });
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        c += __shfl_xor_sync(0xffffffffu, c, o);
+        const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+        best = largest ? (y > best ? y : best) : (y < best ? y : best);
+      }
+      if (lane == 0) {
+        sm.wcnt[warp][0] = static_cast<int>(c);
+        sm.wbest[warp] = best;
+      }
+      __syncthreads();
+      if (t == 0) {
+        long long tc = 0;
+        unsigned long long tb = largest ? 0ull : ~0ull;
+        for (int w = 0; w < kWarps; ++w) {
+          tc += sm.wcnt[w][0];
+          tb = largest ? (sm.wbest[w] > tb ? sm.wbest[w] : tb) : (sm.wbest[w] < tb ? sm.wbest[w] : tb);
+        }
+        sm.xi[0] = tc;
+        sm.xi[1] = static_cast<long long>(tb);
+      }
+      cluster_sync();
+      if (t == 0) {
+        long long tc = 0;
+        unsigned long long tb = largest ? 0ull : ~0ull;
+        for (int q = 0; q < C; ++q) {
+          tc += static_cast<long long>(ld_dsmem_u64(peer(&sm.xi[0], q)));
+          const unsigned long long y = ld_dsmem_u64(peer(&sm.xi[1], q));
+          tb = largest ? (y > tb ? y : tb) : (y < tb ? y : tb);
+        }
+        sm.ires[0] = tc;
+        sm.ires[1] = static_cast<long long>(tb);
+      }
+      cluster_sync();  // every block has read the partials
+    };
+    // the n-th smallest id (n >= 1) with pred(id, z), or -1
+    auto pass_nth = [&](long long n, auto&& pred) {
+      pass_count(true, pred);
+      // the ids per block are in sm.xi[0] of each block (kept until the next
+      // pass): the block holding the n-th one finds it by an ordered scan
+      long long before = 0;
+      int owner = -1;
+      for (int q = 0; q < C; ++q) {
+        const long long cq = static_cast<long long>(ld_dsmem_u64(peer(&sm.xi[0], q)));
+        if (owner < 0 && n <= before + cq) owner = q;
+        else if (owner < 0) before += cq;
+      }
+      __syncthreads();
+      if (t == 0) sm.thresh = 0xFFFFFFFFu;
+      __syncthreads();
+      if (owner == rank) {
+        long long run = before;
+        for (int base = v0; base < v1; base += kThreadsS) {
+          const int i = base + t;
+          bool hit = false;
+          if (i < v1) {
+            float z = penalised(row, i, pe);
+            if (isnan(z)) z = -INFINITY;
+            hit = pred(i, z);
+          }
+          const unsigned bal = __ballot_sync(0xffffffffu, hit);
+          if (lane == 0) sm.warp_cnt[warp] = __popc(bal);
+          __syncthreads();
+          long long r = run + __popc(bal & ((1u << lane) - 1u)) + 1;
+          for (int w2 = 0; w2 < warp; ++w2) r += sm.warp_cnt[w2];
+          if (hit && r == n) sm.thresh = static_cast<uint32_t>(i);
+          long long tot = 0;
+          for (int w2 = 0; w2 < kWarps; ++w2) tot += sm.warp_cnt[w2];
+          __syncthreads();
+          run += tot;
+          if (run >= n) break;
+        }
+      }
+      cluster_sync();
+      int id = -1;
+      if (owner >= 0) {
+        const uint32_t x = ld_dsmem_u32(peer(&sm.thresh, owner));
+        id = x == 0xFFFFFFFFu ? -1 : static_cast<int>(x);
+      }
+      cluster_sync();  // every block has read it
+      return id;
+    };
+    // the largest key k with F(k) >= target (strict: > target), F(k) the sum
+    // of e over the ids with in(id, z) and key >= k, F(0) meeting the target
+    auto search_max = [&](auto&& in, float target, bool strict) {
+      uint32_t lo = 0, hi = key_hi;
+      while (lo < hi) {
+        const unsigned long long span = static_cast<unsigned long long>(hi) - lo;
+        uint32_t th[NS];
+#pragma unroll
+        for (int j = 0; j < NS; ++j)
+          th[j] = lo + static_cast<uint32_t>((span * static_cast<unsigned long long>(j + 1) + NS) / (NS + 1));
+        pass_sums(NS, [&](int j, int i, float z, float e) {
+          return (ordered_key(z) >= th[j] && in(i, z)) ? e : 0.f;
+        });
+        int best = -1;
+        for (int j = 0; j < NS; ++j)
+          if (strict ? sm.res[j] > target : sm.res[j] >= target) best = j;
+        if (best < 0) {
+          hi = th[0] - 1;
+        } else {
+          lo = th[best];
+          if (best < NS - 1) hi = th[best + 1] - 1;
+        }
+      }
+      return lo;
+    };
+    // at the cut key kc (ties there have one weight e_t): how many of them,
+    // lowest id first, the kept prefix takes: the first j whose running sum
+    // from the mass above reaches the target (strict: passes it)
+    auto tie_take = [&](auto&& in, uint32_t kc, float target, bool strict) {
+      pass_sums(1, [&](int, int i, float z, float e) {
+        return (ordered_key(z) > kc && in(i, z)) ? e : 0.f;
+      });
+      float acc = sm.res[0];
+      pass_count(true, [&](int i, float z) { return ordered_key(z) == kc && in(i, z); });
+      const long long n_t = sm.ires[0];
+      const float e_t = weight(key_value(kc));
+      long long j = 0;
+      while (j < n_t) {
+        acc = __fadd_rn(acc, e_t);
+        ++j;
+        if (strict ? acc > target : acc >= target) break;
+      }
+      return pass_nth(j > 0 ? j : 1, [&](int i, float z) { return ordered_key(z) == kc && in(i, z); });
+    };
+
+    // the total
+    pass_sums(1, [&](int, int, float, float e) { return e; });
+    const float total = sm.res[0];
+    // typical-p: the shortest set by (|-log p - H|, candidate order) whose p
+    // reaches typical_p
+    const bool typical = prm.typical_p > 0.f && prm.typical_p < 1.0f;
+    float h = 0.f;
+    uint32_t th_eps = 0xFFFFFFFFu;
+    unsigned long long c_typ = 0ull;
+    auto eps_key = [&](float e) {
+      const float pi = __fdiv_rn(e, total);
+      return pi > 0.f ? ordered_key(fabsf(__fsub_rn(-logf(pi), h))) : ordered_key(INFINITY);
+    };
+    if (typical) {
+      pass_sums(1, [&](int, int, float, float e) {
+        const float pi = __fdiv_rn(e, total);
+        return pi > 0.f ? __fmul_rn(pi, logf(pi)) : 0.f;
+      });
+      h = -sm.res[0];
+      const float tp = prm.typical_p;
+      // the smallest eps key E with sum of p over the ids with eps key <= E
+      // reaching typical_p (every id if rounding keeps the sum below it)
+      uint32_t lo = 0, hi = 0xFFFFFFFFu;
+      while (lo < hi) {
+        const unsigned long long span = static_cast<unsigned long long>(hi) - lo;
+        uint32_t th[NS];
+#pragma unroll
+        for (int j = 0; j < NS; ++j)
+          th[j] = lo + static_cast<uint32_t>((span * static_cast<unsigned long long>(j + 1)) / (NS + 1));
+        pass_sums(NS, [&](int j, int, float, float e) {
+          return eps_key(e) <= th[j] ? __fdiv_rn(e, total) : 0.f;
+        });
+        int best = NS;
+        for (int j = NS - 1; j >= 0; --j)
+          if (sm.res[j] >= tp) best = j;
+        if (best == NS) {
+          lo = th[NS - 1] + 1;
+        } else {
+          hi = th[best];
+          if (best > 0) lo = th[best - 1] + 1;
+        }
+      }
+      th_eps = lo;
+      // ties at that eps key, in candidate order: the shortest prefix that
+      // reaches typical_p from the mass below
+      pass_sums(1, [&](int, int, float, float e) { return eps_key(e) < th_eps ? __fdiv_rn(e, total) : 0.f; });
+      const float below = sm.res[0];
+      pass_count(true, [&](int, float z) { return eps_key(weight(z)) == th_eps; });
+      const long long n_t = sm.ires[0];
+      if (n_t > kCap) {
+        if (rank == 0 && t == 0) {
+          out[b] = -1;
+          if (status) atomicExch(status, DEV_SAMPLER_UNSUPPORTED);
+        }
+        return;
+      }
+      if (t == 0) sm.n_cand = 0;
+      __syncthreads();
+      visit([&](bool valid, int i, float z) {
+        if (valid && eps_key(weight(z)) == th_eps) {
+          const uint32_t slot = atomicAdd(&sm.n_cand, 1u);  // parking slot only
+          sm.cand[slot] = composite(ordered_key(z), i);
+        }
+      });
+      cluster_sync();
+      if (rank == 0) {
+        if (t == 0) {
+          uint32_t off = sm.n_cand;
+          for (int q = 1; q < C; ++q) {
+            sm.offs[q] = off;
+            off += ld_dsmem_u32(peer(&sm.n_cand, q));
+          }
+          sm.offs[C] = off;
+          sm.offs[0] = 0;
+        }
+        __syncthreads();
+        for (int q = 1; q < C; ++q) {
+          const int n_q = static_cast<int>(sm.offs[q + 1] - sm.offs[q]);
+          const uint32_t src = peer(&sm.cand[0], q);
+          for (int i = t; i < n_q; i += kThreadsS) sm.cand[sm.offs[q] + i] = ld_dsmem_u64(src + 8u * i);
+        }
+        __syncthreads();
+        const int n = static_cast<int>(sm.offs[C]);
+        int n2 = 1;
+        while (n2 < n) n2 <<= 1;
+        for (int i = n + t; i < n2; i += kThreadsS) sm.cand[i] = 0ull;
+        __syncthreads();
+        bitonic_desc(sm.cand, n2);
+        if (t == 0) {
+          float acc = below;
+          unsigned long long last = sm.cand[0];
+          for (int j = 0; j < n; ++j) {
+            last = sm.cand[j];
+            acc = __fadd_rn(acc, __fdiv_rn(weight(key_value(static_cast<uint32_t>(last >> 32))), total));
+            if (acc >= tp) break;
+          }
+          sm.xi[1] = static_cast<long long>(last);
+        }
+      }
+      cluster_sync();
+      c_typ = ld_dsmem_u64(peer(&sm.xi[1], 0));
+      cluster_sync();  // every block has read it
+    }
+    auto in_typ = [&](int i, float z) {
+      if (!typical) return true;
+      const uint32_t ek = eps_key(weight(z));
+      return ek < th_eps || (ek == th_eps && composite(ordered_key(z), i) >= c_typ);
+    };
+    // top-p over the typical set, in candidate order
+    uint32_t k_tp = 0;
+    int tie_tp = V;
+    if (prm.top_p < 1.0f) {
+      float tot = total;
+      if (typical) {
+        pass_sums(1, [&](int, int i, float z, float e) { return in_typ(i, z) ? e : 0.f; });
+        tot = sm.res[0];
+      }
+      const float target = __fmul_rn(prm.top_p, tot);
+      k_tp = search_max(in_typ, target, false);
+      tie_tp = tie_take(in_typ, k_tp, target, false);
+    }
+    auto in_tp = [&](int i, float z) {
+      const uint32_t kz = ordered_key(z);
+      return in_typ(i, z) && (kz > k_tp || (kz == k_tp && i <= tie_tp));
+    };
+    // the first candidate of the typical set (it is always kept), and min-p
+    // relative to its weight
+    pass_count(true, in_typ);
+    const unsigned long long first_c = static_cast<unsigned long long>(sm.ires[1]);
+    const int first_id = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(first_c & 0xFFFFFFFFull));
+    const float thr = prm.min_p > 0.0f ? __fmul_rn(prm.min_p, weight(key_value(static_cast<uint32_t>(first_c >> 32))))
+                                       : -INFINITY;
+    auto in_kept = [&](int i, float z) { return i == first_id || (in_tp(i, z) && weight(z) >= thr); };
+    pass_sums(1, [&](int, int i, float z, float e) { return in_kept(i, z) ? e : 0.f; });
+    const float kept = sm.res[0];
+    // the draw: the first kept candidate whose running sum passes u * kept
+    const uint64_t stp = static_cast<uint64_t>(step[b]);
+    const Philox4 w = philox4x32_10(
+        Philox4{static_cast<uint32_t>(stp), static_cast<uint32_t>(stp >> 32), 0u, 0u},
+        static_cast<uint32_t>(prm.seed), static_cast<uint32_t>(prm.seed >> 32));
+    const float u = static_cast<float>(w.x >> 8) * (1.0f / 16777216.0f);
+    const float target = __fmul_rn(u, kept);
+    int pick;
+    if (kept > target) {
+      const uint32_t k_d = search_max(in_kept, target, true);
+      pick = tie_take(in_kept, k_d, target, true);
+    } else {
+      pass_count(false, in_kept);  // (u < 1 never gets here) the last kept candidate
+      pick = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(static_cast<unsigned long long>(sm.ires[1]) & 0xFFFFFFFFull));
+    }
+    if (rank == 0 && t == 0) out[b] = pick;
+  };
+
   if (!(temp > 0.f)) {
     // greedy: maximum of the strict total order
     unsigned long long best = 0ull;
@@ -399,9 +804,8 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
     cluster_sync();  // the peers stay until rank 0 has read them
     return;
   }
-  // Full vocabulary (no top-k) over more than kMaxTopK ids: the top kMaxTopK
-  // are gathered as candidates and the softmax total runs over the whole row;
-  // the top-p / min-p cut must fall inside those candidates.
+  // Whole vocabulary (no top-k) over more than kMaxTopK ids: the searches
+  // below; otherwise the top k are gathered and sorted.
   const bool full = (prm.top_k <= 0 || prm.top_k >= V) && V > kMaxTopK;
   const int k = full ? kMaxTopK : ((prm.top_k <= 0 || prm.top_k >= V) ? V : prm.top_k);
   if (k > kMaxTopK || (full && (V + 127) / 128 > kMaxBlocks)) {
@@ -409,6 +813,10 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
       out[b] = -1;
       if (status) atomicExch(status, DEV_SAMPLER_UNSUPPORTED);
     }
+    return;
+  }
+  if (full) {
+    whole_vocabulary();
     return;
   }
 
@@ -608,28 +1016,7 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
       __syncthreads();
     }
   }
-  if (full) {
-    // e = exp(z / T - z_max / T) summed over each 128-id block of this block's
-    // share: lane l takes ids 4l .. 4l + 3 of the block in order, then a fixed
-    // butterfly -- the same for any number of blocks per row
-    const float s0 = __fdiv_rn(sm.m_all, temp);
-    for (int blk = v0 / 128 + warp; blk * 128 < v1; blk += kWarps) {
-      float acc = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = blk * 128 + 4 * lane + e;
-        if (i < V) {
-          float z = penalised(row, i, pe);
-          if (isnan(z)) z = -INFINITY;
-          acc = __fadd_rn(acc, expf(__fsub_rn(__fdiv_rn(z, temp), s0)));
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
-      if (lane == 0) sm.blk[blk - v0 / 128] = acc;
-    }
-  }
-  cluster_sync();  // every block's candidates (and block sums) are parked
+  cluster_sync();  // every block's candidates are parked
   if (rank == 0) {
     // rank 0 appends the peers' candidates after its own
     if (t == 0) {
@@ -640,26 +1027,6 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
         off += ld_dsmem_u32(peer(&sm.n_cand, q));
       }
       sm.offs[C] = off;
-    }
-    if (full) {
-      // every block sum of the row, in block order (own blocks are in place)
-      const int nblk = (V + 127) / 128;
-      for (int q = 1; q < C && q * chunk < V; ++q) {
-        const int b0 = q * chunk / 128, b1 = min(nblk, (min(V, q * chunk + chunk) + 127) / 128);
-        const uint32_t src = peer(&sm.blk[0], q);
-        for (int i = b0 + t; i < b1; i += kThreadsS) sm.blk[i] = ld_dsmem_f32(src + 4u * (i - b0));
-      }
-    }
-    __syncthreads();
-    if (full && warp == 0) {
-      // the row's total: lane l adds blocks l, l + 32, ... in order, then a
-      // fixed butterfly (the shape depends on V only)
-      const int nblk = (V + 127) / 128;
-      float acc = 0.f;
-      for (int i = lane; i < nblk; i += 32) acc = __fadd_rn(acc, sm.blk[i]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
-      if (lane == 0) sm.total_all = acc;
     }
     __syncthreads();
     for (int q = 1; q < C; ++q) {
@@ -729,13 +1096,6 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
   const bool typical = prm.typical_p > 0.f && prm.typical_p < 1.0f;
   uint32_t* kmask = reinterpret_cast<uint32_t*>(sm.cand + 3072);  // kept candidates (typical-p)
   if (typical) {
-    if (full) {  // typical-p over the whole vocabulary: not supported
-      if (t == 0) {
-        out[b] = -1;
-        if (status) atomicExch(status, DEV_SAMPLER_UNSUPPORTED);
-      }
-      return;
-    }
     __syncthreads();  // P
     const float total = P[kk - 1];
     float* lp = reinterpret_cast<float*>(sm.cand + 2048);
@@ -806,29 +1166,18 @@ __global__ void __launch_bounds__(kThreadsS) sample_kernel(
     }
     return n;
   };
-  const float total = full ? sm.total_all : P[kk - 1];
+  const float total = P[kk - 1];
   int keep = kk;
-  bool cut = false;  // full vocabulary: did a filter end inside the candidates?
   if (prm.top_p < 1.0f) {
     const float target = __fmul_rn(prm.top_p, total);
     const int i = first(kk, [&](int j) { return P[j] >= target; });
     keep = i < kk ? i + 1 : kk;
-    cut = i < kk;
   }
   const int j0 = first(kk, kept_at);  // the first kept candidate (the largest kept e)
   if (prm.min_p > 0.0f) {
     const float thr = __fmul_rn(prm.min_p, sm.e[j0]);
     const int n = first(keep, [&](int j) { return kept_at(j) && !(sm.e[j] >= thr); });
-    cut = cut || n < keep;
     keep = n > j0 ? n : j0 + 1;
-  }
-  if (full && !cut) {
-    // the kept set may reach past the candidates: not supported
-    if (lane == 0) {
-      out[b] = -1;
-      if (status) atomicExch(status, DEV_SAMPLER_UNSUPPORTED);
-    }
-    return;
   }
   const float kept = P[keep - 1];
   const uint64_t st = static_cast<uint64_t>(step[b]);

@@ -279,6 +279,35 @@ class Decoder:
         return self.x[:rows]
 
 
+def run_requests(dec: Decoder, prompts, params, steps: int, chunk: int = 0):
+    """Serve requests together: request i takes slot i; its prompt, all but
+    the last token, is prefilled into the slot (chunks of `chunk` rows, 0 =
+    as large as the buffers allow), then every request decodes `steps` tokens
+    in one batch, starting from its last prompt token, with its own sampler
+    settings (repeat window over its prompt and output so far; Philox counter
+    = its own output index).  Returns each request's output ids.  A
+    request's tokens do not depend on the other requests, the slot or the
+    chunking, so a rerun alone reproduces them."""
+    bsz = len(prompts)
+    if bsz > dec.B:
+        raise ValueError("more requests than the decoder's slots")
+    for i, p in enumerate(prompts):
+        if len(p) < 1 or len(p) + steps > dec.Lmax:
+            raise ValueError("prompt empty or too long for the decoder's cache")
+        if len(p) > 1:
+            dec.prefill(i, torch.tensor(list(p[:-1]), dtype=torch.int32, device=dec.dev), chunk=chunk)
+    dec.set_sampling(params)
+    dec.set_history([list(p) for p in prompts])
+    dec.set_positions([len(p) - 1 for p in prompts])
+    dec.step[:bsz] = 0
+    dec.tokens[:bsz] = torch.tensor([int(p[-1]) for p in prompts], dtype=torch.int32, device=dec.dev)
+    out = torch.empty(bsz, steps, dtype=torch.int32, device=dec.dev)
+    for k in range(steps):
+        dec.decode_step(bsz)
+        out[:, k] = dec.tokens[:bsz]
+    return out.cpu().tolist()
+
+
 class _EventPair:
     def __init__(self, timer: dict, name: str):
         self.timer, self.name = timer, name

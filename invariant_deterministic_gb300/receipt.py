@@ -8,10 +8,12 @@ BLAKE3 over the ids as little-endian 32-bit integers.  *Verifying* reruns the
 recorded prompt tokens the plainest way (one request, alone) and reports
 "identical" or the first output token that differs.
 
-This module holds the host-side record: ``token_hash`` (BLAKE3 of LE int32
-ids), ``make_receipt`` and ``compare``.  The rerun itself is whatever decode
-loop the caller uses (see ``tests/test_gpu_receipt.py``).  Signing and
-model-file hashing are not part of it.
+This module holds the record: ``token_hash`` (BLAKE3 of LE int32 ids),
+``make_receipt``, ``compare`` and ``verify``, which rebuilds the model from
+the identity the record holds (shape and weight seed of the random-init
+model), prefills the recorded prompt ids in one slot alone, decodes as many
+tokens as were recorded with the recorded settings and seed, and compares.
+Signing and model-file hashing are not part of it.
 
 BLAKE3 is restated here from its published specification (O'Connor, Aumasson,
 Neves, Wilcox-O'Hearn, "BLAKE3: one function, fast everywhere", 2020): a
@@ -132,12 +134,14 @@ def token_hash(ids) -> str:
 
 
 def make_receipt(*, build_id: str, device_class: str, settings: dict, prompt_ids, sampling: dict,
-                 output_ids, finish: str = "length") -> dict:
+                 output_ids, finish: str = "length", model: dict | None = None) -> dict:
     """A run record in the spirit of a Kinetic receipt (unsigned, no model
-    file hash): enough to rerun the request and compare the tokens."""
+    file hash): enough to rerun the request and compare the tokens.  `model`
+    names the weights (here: the shape and seed of the random-init model)."""
     return {
         "receipt": 1,
         "kinv": {"build": build_id},
+        "model": dict(model) if model else None,
         "device": {"class": device_class, "settings": dict(settings)},
         "prompt": {"count": len(prompt_ids), "blake3": token_hash(prompt_ids),
                    "ids": [int(i) for i in prompt_ids]},
@@ -167,6 +171,48 @@ def compare(receipt: dict, rerun_ids, build_id: str, device_class: str) -> str:
     if len(want) != len(rerun_ids):
         return f"differs in length: receipt {len(want)}, rerun {len(rerun_ids)}{note}"
     return f"identical, {len(want)} of {len(want)} output tokens{note}"
+
+
+def model_identity(shape, weight_seed: int) -> dict:
+    """The model fields of a record: every ModelShape field and the seed the
+    random-init weights are drawn with."""
+    return {"shape": dict(shape.__dict__), "weight_seed": int(weight_seed),
+            "init": "projections ~N(0, 0.02) bf16, norm gains 1"}
+
+
+def settings_of(shape) -> dict:
+    """The settings that change bits: the KV split length, the RoPE base,
+    QK-norm, the RMSNorm eps and the prefill rule (all but the last prompt
+    token prefilled, the last one decoded)."""
+    from . import kinv
+    return {"split_len": kinv.SPLIT_LEN, "rope_base": shape.rope_base, "qk_norm": shape.qk_norm,
+            "eps": shape.eps, "prefill": "prompt[:-1], then decode from prompt[-1]"}
+
+
+def verify(record: dict, device="cuda", chunk: int = 0) -> str:
+    """Kinetic "Receipts", *Verifying*: rerun the recorded request the
+    plainest way -- one slot, alone, prefill chunk `chunk` (0: whole) -- and
+    report "identical" or the first differing output token.  Refuses a record
+    whose hashes do not match its ids, or whose settings are not this
+    library's."""
+    if not check_hashes(record):
+        return "refused: the recorded hashes do not match the recorded ids"
+    if not record.get("model"):
+        return "refused: the record does not identify the model"
+    from . import kinv, model as M
+    shape = M.ModelShape(**record["model"]["shape"])
+    if dict(record["device"]["settings"]) != settings_of(shape):
+        return "refused: the recorded settings are not this library's"
+    w = M.random_weights(shape, seed=record["model"]["weight_seed"], device=device)
+    prompt = record["prompt"]["ids"]
+    n_out = record["output"]["tokens"]["count"]
+    dec = M.Decoder(shape, w, max_batch=1, max_len=len(prompt) + n_out + 8,
+                    max_chunk=chunk or max(len(prompt) - 1, 1), device=device)
+    s = dict(record["sampling"])
+    if s.get("logit_bias"):
+        s["logit_bias"] = {int(k): float(v) for k, v in s["logit_bias"].items()}
+    out = M.run_requests(dec, [prompt], [kinv.SamplingParams(**s)], n_out, chunk=chunk)
+    return compare(record, out[0], kinv.build_id(), kinv.device_class())
 
 
 def dumps(receipt: dict) -> str:

@@ -48,10 +48,17 @@ not asserted for such a row.  The margin (relative to the sum) bounds the
 kernel's fp32 error: a sequential sum of k terms below 1 is off by at most
 k * 2^-24 relative, and each exponential by a few units in the last place, so
 ``tie_tol(k) = 1e-5 + k * 6e-8``.  Over the whole vocabulary (no top-k) the
-kernel still forms its running sums over at most 1024 ranked candidates, and
-the whole-row total per 128-id block and then in 32 strided runs of blocks,
-so k is the candidate count (at most 1024) and the total adds
-``whole_sum_tol(V)`` more.
+kernel forms every mass it compares (the total, the entropy, the mass at or
+above a key, the kept mass) as a sum over the whole row: 4 terms in order per
+lane of a 128-id block, a 32-lane butterfly, a butterfly over the 32 blocks of
+a 4096-id group, then the groups in order, each term exp(s_i - s_0) with its
+argument rounded once (|s_i - s_0| units in the last place, at most 60 for
+any term of weight above 1e-26, plus exp's own 2); the margin there is
+``whole_tol(V) = 4e-6 + whole_sum_tol(V)``.  Thousands of candidates then sit
+near a deep top-p or min-p cut, each with a tiny weight, so a cut there is a
+near tie only if it can move the token: the draw is made with the smallest and
+the largest kept prefix the margins allow, and the row is a near tie if the
+two picks differ or either draw falls within the margin of a boundary.
 """
 from __future__ import annotations
 
@@ -67,13 +74,17 @@ def tie_tol(k: int) -> float:
 
 
 def whole_sum_tol(v: int) -> float:
-    """Relative error bound of an fp32 sum of v terms taken as 128-term blocks
-    (4 in order per lane, then a 32-lane butterfly) and then 32 strided runs of
-    blocks added in order and by a butterfly: one rounding per addition along
-    the longest chain."""
-    blocks = (v + 127) // 128
-    chain = 4 + 5 + (blocks + 31) // 32 + 5
+    """Relative error bound of an fp32 sum of v nonnegative terms taken as
+    128-term blocks (4 in order per lane, then a 32-lane butterfly), 4096-term
+    groups (a butterfly over 32 blocks) and the groups in order: one rounding
+    per addition along the longest chain."""
+    groups = (v + 4095) // 4096
+    chain = 4 + 5 + 5 + groups
     return chain * 2.0 ** -24
+
+
+def whole_tol(v: int) -> float:
+    return 4e-6 + whole_sum_tol(v)
 
 
 @dataclass
@@ -120,8 +131,12 @@ def penalize(logits_f32: np.ndarray, history, p: SamplingParams) -> np.ndarray:
     return z
 
 
-def sample_row(logits_f32: np.ndarray, history, step: int, p: SamplingParams):
-    """Returns (token, near_tie)."""
+def sample_row(logits_f32: np.ndarray, history, step: int, p: SamplingParams, allowed=None):
+    """Returns (token, near_tie).  Over the whole vocabulary, a set passed as
+    `allowed` receives every token a draw within the margins can give (the
+    kept prefixes the margins allow, each with its draw target moved by the
+    margin either way); for a near tie the kernel's token must be one of
+    them."""
     z = penalize(bias_logits(logits_f32, p), history, p)
     v = z.shape[0]
     t = np.float32(p.temperature)
@@ -134,7 +149,7 @@ def sample_row(logits_f32: np.ndarray, history, step: int, p: SamplingParams):
     s = (z[order] / t).astype(np.float64)          # fp32 division, widened exactly
     e = np.exp(s - s[0])
     whole = len(order) > 1024
-    tol = tie_tol(min(len(order), 1024)) + (whole_sum_tol(v) if whole else 0.0)
+    tol = whole_tol(v) if whole else tie_tol(len(order))
     near = False
     n = len(order)
     kept = np.ones(n, dtype=bool)               # the set, in candidate order
@@ -157,37 +172,75 @@ def sample_row(logits_f32: np.ndarray, history, step: int, p: SamplingParams):
         kept[:] = False
         kept[torder[:m]] = True
     em = np.where(kept, e, 0.0)
+    cum_all = np.cumsum(em)
+    u = sampler_uniform(p.seed, step)
+    first = int(np.argmax(kept))                # the first kept candidate
+
+    def top_p_keep(target):
+        return max(1, min(int(np.searchsorted(cum_all, target, side="left")) + 1, n))
+
+    def min_p_keep(keep, thr):
+        """the first kept candidate before `keep` whose e is below thr, else keep"""
+        below = np.nonzero(kept[:keep] & ~(e[:keep] >= thr))[0]
+        return int(below[0]) if len(below) else keep
+
+    def draw(keep):
+        cum = cum_all[:keep]
+        target = u * cum[-1]
+        idx = int(np.searchsorted(cum, target, side="right"))
+        if idx >= keep:                               # (u < 1 never gets here) the last kept one
+            idx = max(j for j in range(keep) if kept[j])
+        # the pick moves if cum[idx] or cum[idx-1] sits at the target
+        at_edge = bool(np.any(np.abs(cum[max(0, idx - 1): idx + 1] - target) <= tol * cum[-1]))
+        return idx, at_edge
+
     keep = n
     if p.top_p < 1.0:
-        cum = np.cumsum(em)
-        target = float(np.float32(p.top_p)) * cum[-1]
-        keep = int(np.searchsorted(cum, target, side="left")) + 1
-        keep = max(1, min(keep, n))
+        target = float(np.float32(p.top_p)) * cum_all[-1]
+        keep = top_p_keep(target)
         # the cut moves if cum[keep-1] or cum[keep-2] sits at the target
-        if np.any(np.abs(cum[max(0, keep - 2): keep] - target) <= tol * cum[-1]):
+        if not whole and np.any(np.abs(cum_all[max(0, keep - 2): keep] - target) <= tol * cum_all[-1]):
             near = True
-    first = int(np.argmax(kept))                # the first kept candidate
+    keep_tp = keep
     if p.min_p > 0.0:
         thr = float(np.float32(p.min_p)) * e[first]
-        idx_k = [j for j in range(keep) if kept[j]]
-        ok = [j for j in idx_k if e[j] >= thr]
-        drop = [j for j in idx_k if not e[j] >= thr]
-        # the cut moves if the last kept or the first dropped e sits at the threshold
-        edge = ([ok[-1]] if ok else []) + ([drop[0]] if drop else [])
-        if any(abs(e[j] - thr) <= tol for j in edge):
-            near = True
-        keep = drop[0] if drop else keep
-        keep = max(keep, first + 1)
-    em = em[:keep]
-    cum = np.cumsum(em)
-    u = sampler_uniform(p.seed, step)
-    target = u * cum[-1]
-    idx = int(np.searchsorted(cum, target, side="right"))
-    if idx >= keep:                               # (u < 1 never gets here) the last kept one
-        idx = max(j for j in range(keep) if kept[j])
-    # the pick moves if cum[idx] or cum[idx-1] sits at the target
-    if np.any(np.abs(cum[max(0, idx - 1): idx + 1] - target) <= tol * cum[-1]):
-        near = True
+        if not whole:
+            idx_k = [j for j in range(keep) if kept[j]]
+            ok = [j for j in idx_k if e[j] >= thr]
+            drop = [j for j in idx_k if not e[j] >= thr]
+            # the cut moves if the last kept or the first dropped e sits at the threshold
+            edge = ([ok[-1]] if ok else []) + ([drop[0]] if drop else [])
+            if any(abs(e[j] - thr) <= tol for j in edge):
+                near = True
+        keep = max(min_p_keep(keep, thr), first + 1)
+    idx, at_edge = draw(keep)
+    near = near or at_edge
+    if whole and (p.top_p < 1.0 or p.min_p > 0.0):
+        # the smallest and the largest kept prefix within the margins
+        k_lo, k_hi = keep_tp, keep_tp
+        if p.top_p < 1.0:
+            target = float(np.float32(p.top_p)) * cum_all[-1]
+            k_lo = top_p_keep(target - tol * cum_all[-1])
+            k_hi = top_p_keep(target + tol * cum_all[-1])
+        if p.min_p > 0.0:
+            thr = float(np.float32(p.min_p)) * e[first]
+            k_lo = max(min_p_keep(k_lo, thr * (1.0 + tol)), first + 1)
+            k_hi = max(min_p_keep(k_hi, thr * (1.0 - tol)), first + 1)
+        for kk in (k_lo, k_hi):
+            j, edge = draw(kk)
+            if j != idx or edge:
+                near = True
+    if whole and allowed is not None:
+        ks = [keep]
+        if p.top_p < 1.0 or p.min_p > 0.0:
+            ks += [k_lo, k_hi]
+        for kk in ks:
+            cum = cum_all[:kk]
+            m = tol * cum[-1]
+            target = u * cum[-1]
+            lo = int(np.searchsorted(cum, target - m, side="right"))
+            hi = min(int(np.searchsorted(cum, target + m, side="right")), kk - 1)
+            allowed.update(int(order[j]) for j in range(min(lo, kk - 1), hi + 1) if kept[j])
     return int(order[idx]), near
 
 

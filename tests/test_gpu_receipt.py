@@ -1,6 +1,12 @@
-"""Receipt round trip (Kinetic "Receipts", *Verifying*): a tagged request's
-receipt made while it shares a busy batch verifies as identical when the
-request is rerun alone, the plainest way."""
+"""Receipt round trip (Kinetic "Receipts", *Verifying*): a request served in a
+busy batch of 64, from a real prompt prefill, gets a receipt that names the
+model (shape and weight seed), the settings, the prompt ids, the sampler
+settings and seed and the output ids; verify() rebuilds the model from the
+record and reruns the request alone, the plainest way, and finds it
+identical -- with any prefill chunking.  A record with a changed seed is
+reported at the first differing token, one with a wrong hash is refused."""
+import json
+
 import pytest
 import torch
 
@@ -18,23 +24,33 @@ def M():
 
 
 def test_receipt_from_busy_batch_verifies_alone(M):
-    from test_gpu_model import _decode_tokens
-    shape = M.ModelShape(**{**M.QWEN3_8B.__dict__, "n_layers": 4})
-    w = M.random_weights(shape, device="cuda")
-    lengths = synth.uniform_int(24, 16, 4096, synth.SEED_LEN + 5).tolist()
-    lmax = max(lengths) + 40
-    busy = [11, 3, 0, 17, 5, 23, 8, 1, 14, 20, 2, 9]
-    toks, _ = _decode_tokens(M, shape, w, busy, lengths, 32, lmax)
-    tag = busy.index(0)
     kinv = M.kinv
-    prompt_ids = synth.uniform_int(64, 0, shape.vocab - 1, 6000).tolist()   # request 0's recorded tail
-    p = kinv.SamplingParams(seed=1000)
+    shape = M.ModelShape(**{**M.QWEN3_8B.__dict__, "n_layers": 4})
+    seed = 0
+    w = M.random_weights(shape, seed=seed, device="cuda")
+    n_req, steps = 64, 24
+    lens = synth.uniform_int(n_req, 16, 600, synth.SEED_LEN + 11).tolist()
+    prompts = [synth.uniform_int(n, 0, shape.vocab - 1, 7000 + i).tolist() for i, n in enumerate(lens)]
+    params = [kinv.SamplingParams(seed=1000 + i) for i in range(n_req)]
+    dec = M.Decoder(shape, w, max_batch=n_req, max_len=max(lens) + steps + 8, max_chunk=256)
+    outs = M.run_requests(dec, prompts, params, steps, chunk=256)
+    assert kinv.last_device_status() == 0
+    del dec, w
+    torch.cuda.empty_cache()
+    tag = 37
     r = receipt.make_receipt(build_id=kinv.build_id(), device_class=kinv.device_class(),
-                             settings={"split_len": 256, "rope_base": shape.rope_base,
-                                       "qk_norm": shape.qk_norm, "layers": shape.n_layers},
-                             prompt_ids=prompt_ids, sampling=p.__dict__,
-                             output_ids=toks[tag].tolist())
+                             settings=receipt.settings_of(shape), prompt_ids=prompts[tag],
+                             sampling=params[tag].__dict__, output_ids=outs[tag],
+                             model=receipt.model_identity(shape, seed))
+    r = json.loads(receipt.dumps(r))      # the record as stored
     assert receipt.check_hashes(r)
-    alone, _ = _decode_tokens(M, shape, w, [0], lengths, 32, lmax)
-    verdict = receipt.compare(r, alone[0].tolist(), kinv.build_id(), kinv.device_class())
-    assert verdict.startswith("identical, 32 of 32"), verdict
+    assert receipt.verify(r).startswith(f"identical, {steps} of {steps}")
+    assert receipt.verify(r, chunk=7).startswith(f"identical, {steps} of {steps}")
+    # another seed draws other tokens: reported at the first difference
+    r2 = json.loads(json.dumps(r))
+    r2["sampling"]["seed"] += 1
+    assert receipt.verify(r2).startswith("differs at output token")
+    # a record whose ids do not match its hashes is refused
+    r3 = json.loads(json.dumps(r))
+    r3["prompt"]["ids"][0] ^= 1
+    assert receipt.verify(r3).startswith("refused")

@@ -193,8 +193,8 @@ def test_logit_bias(kinv):
 
 
 def test_typical_p(kinv):
-    """Typical-p with top-k, top-p, min-p and temperature against the oracle;
-    over the whole vocabulary it is not supported (token -1)."""
+    """Typical-p with top-k, top-p, min-p and temperature against the oracle,
+    and over the whole vocabulary (no top-k)."""
     vocab = 151936
     g = synth.gen(76)
     variants = [
@@ -219,11 +219,23 @@ def test_typical_p(kinv):
     top1 = z.argmax(axis=1)
     assert np.any(got[:8] != top1[:8])
     assert kinv.last_device_status() == 0
-    whole = [kinv.SamplingParams(temperature=1.0, top_k=0, top_p=0.9, min_p=0.0, typical_p=0.5,
-                                 repeat_penalty=1.0, repeat_last_n=0, seed=1)]
-    out = _run(kinv, logits[:1].contiguous(), whole, [[]], [0])
-    assert out[0] == -1
-    assert kinv.last_device_status() == kinv.ERR_UNSUPPORTED
+    # the whole vocabulary: typical set, then top-p and min-p over it
+    whole_v = [dict(temperature=1.0, top_k=0, top_p=0.9, min_p=0.0, typical_p=0.5),
+               dict(temperature=0.8, top_k=0, top_p=1.0, min_p=0.05, typical_p=0.9),
+               dict(temperature=1.2, top_k=-1, top_p=0.95, min_p=0.01, typical_p=0.3),
+               dict(temperature=0.9, top_k=0, top_p=1.0, min_p=0.0, typical_p=0.95)]
+    whole = [kinv.SamplingParams(**v, repeat_penalty=1.0, repeat_last_n=0, seed=31 + i)
+             for i, v in enumerate(whole_v) for _ in range(2)]
+    # rows with a few raised ids: the typical set's edge is not crowded
+    wl = _peaked(len(whole), vocab, 78)
+    wh, ws = [[] for _ in whole], list(range(len(whole)))
+    out = _run(kinv, wl, whole, wh, ws)
+    ref, ties = _oracle(wl, whole, wh, ws)
+    assert (out >= 0).all()
+    assert ties.sum() <= 2, f"{ties.sum()} near ties"
+    assert np.array_equal(out[~ties], ref[~ties]), np.nonzero(out != ref)
+    one = _run(kinv, wl[3:4].contiguous(), whole[3:4], wh[3:4], ws[3:4])
+    assert one[0] == out[3]
     assert kinv.last_device_status() == 0
 
 
@@ -301,15 +313,36 @@ def test_whole_vocabulary_top_p_min_p(kinv, top_k, top_p, min_p):
     assert kinv.last_device_status() == 0
 
 
-def test_whole_vocabulary_cut_beyond_the_candidates_is_unsupported(kinv):
-    """Flat logits: top-p 0.95 over the whole vocabulary would keep most of it,
-    past the 1024 ranked candidates -- token -1 and the unsupported status; the
-    peaked row beside it is sampled."""
-    vocab = 151936
-    logits = torch.cat([torch.zeros(1, vocab), _peaked(1, vocab, 81).cpu()]).cuda()
-    p = [kinv.SamplingParams(top_k=0, top_p=0.95, min_p=0.0, seed=1),
-         kinv.SamplingParams(top_k=0, top_p=0.95, min_p=0.0, seed=2)]
-    got = _run(kinv, logits, p, [[], []], [0, 0])
-    assert got[0] == -1 and got[1] >= 0
-    assert kinv.last_device_status() == kinv.ERR_UNSUPPORTED
+@pytest.mark.parametrize("temperature,top_p,min_p", [(0.8, 0.95, 0.0), (1.0, 0.5, 0.0), (0.6, 0.99, 0.0),
+                                                       (1.2, 1.0, 0.02), (0.9, 0.9, 0.001)])
+def test_whole_vocabulary_flat_rows(kinv, temperature, top_p, min_p):
+    """Un-peaked N(0, 1.3) logits over all 151936 ids: the top-p / min-p cut
+    lies tens of thousands of ids deep and most ids weigh less than the
+    oracle's margin, so many rows are near ties.  Away from near ties the token
+    is the oracle's; at a near tie it is one the oracle reaches within the
+    margins.  A row's token does not depend on the batch; an all-equal row
+    (every id tied) gives a valid token."""
+    vocab, bsz = 151936, 16
+    g = synth.gen(85)
+    logits = torch.randn(bsz, vocab, generator=g) * 1.3
+    logits[bsz - 1] = 0.0
+    logits = logits.cuda()
+    plist = [kinv.SamplingParams(temperature=temperature, top_k=0, top_p=top_p, min_p=min_p,
+                                 repeat_penalty=1.1, repeat_last_n=64, seed=700 + b) for b in range(bsz)]
+    hists = [list(range(100 * b, 100 * b + 40)) for b in range(bsz)]
+    steps = [3 * b for b in range(bsz)]
+    got = _run(kinv, logits, plist, hists, steps)
+    ref, ties = _oracle(logits, plist, hists, steps)
+    assert (got >= 0).all() and (got < vocab).all()
+    assert np.array_equal(got[~ties], ref[~ties]), np.nonzero(got != ref)
+    assert (~ties[: bsz - 1]).sum() >= 3, f"only {(~ties).sum()} rows away from near ties"
+    z = logits.cpu().numpy()
+    for b in np.nonzero(ties[: bsz - 1])[0]:
+        ok = set()
+        p = OParams(**{k: getattr(plist[b], k) for k in OParams.__dataclass_fields__})
+        sample_row(z[b], hists[b][-64:], steps[b], p, allowed=ok)
+        assert int(got[b]) in ok, (b, int(got[b]), sorted(ok)[:10])
+    for b in (0, 5, bsz - 1):
+        one = _run(kinv, logits[b: b + 1].contiguous(), plist[b: b + 1], hists[b: b + 1], steps[b: b + 1])
+        assert one[0] == got[b]
     assert kinv.last_device_status() == 0
