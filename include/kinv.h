@@ -269,8 +269,13 @@ kinv_status kinv_attn_decode_noalloc(const void* q, const void* k_cache, const v
  * sequence of length p + 1 (same splits at absolute offsets, same fold), so a
  * row's bits do not depend on the chunking, on p0, on the other rows, and a
  * decode step equals a one-row prefill bit for bit.
+ * The rows run on the tcgen05 tensor cores, 128 (row, head) pairs of one
+ * sequence and kv head per thread block, which folds the sequence's splits
+ * one after another in registers: kinv_attn_prefill_workspace() is 0 and
+ * `workspace` may be NULL.
  * q, out: device bf16 [total_rows][Hq][D].  q_start, q_len, q_offset: device
- * int32 [B].  Caches and strides as for decode.  max_q_len bounds q_len[b],
+ * int32 [B].  Caches and strides as for decode, the cache holding at least
+ * max_kv keys of each of the B sequences (seq_stride > 0 when B > 1).  max_q_len bounds q_len[b],
  * max_kv bounds q_start[b] + q_len[b] (both used to size the grid and the
  * workspace), and q_offset[b] + q_len[b] <= total_rows; a sequence whose
  * device-side values break one of these bounds (or is negative) is left out

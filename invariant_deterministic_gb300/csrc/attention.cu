@@ -4,36 +4,38 @@
 // than a fixed number of splits").
 //
 // A query row with L visible keys cuts them into splits of 256 keys at
-// absolute offsets 0, 256, 512, ...; the cut depends only on L.  Split kernel:
-// one thread block (eight warps) per (split, kv head, group of query rows of
-// one sequence); up to 16 (row, query head) pairs form the 16 rows of
-// warp-level tensor-core MMAs (m16n8k16, bf16 inputs, fp32 accumulation).
-// K, then V, arrive in shared memory through cp.async.  For every pair:
-//   s_t  = (q . k_t) * scale   warp w forms keys 32w..32w+31: eight 16-wide
-//                              k steps of d, ascending, accumulated in fp32
+// absolute offsets 0, 256, 512, ...; the cut depends only on L.  For every
+// (row, query head) pair and split:
+//   s_t  = (q . k_t) * scale   sixteen-deep tensor-core steps over d,
+//                              ascending, accumulated in fp32
 //   m    = max_t s_t           (max is exact in any order)
 //   e_t  = exp(s_t - m)        in fp32, then carried as the bf16 pair
 //   hi_t = bf16(e_t), lo_t = bf16(e_t - hi_t)   (about 16 significant bits)
-//   l    = sum_t (hi_t + lo_t) a lane's eight keys in order, a fixed
-//                              butterfly over four lanes, warps in order
+//   l    = sum_t (hi_t + lo_t) in 32-key groups: within a group key
+//                              8nb + 2tq + e is added to partial tq in (nb, e)
+//                              order, the partials (0 + 1) + (2 + 3), the
+//                              groups in order
 //   o[d] = sum_t hi_t v_t[d] + sum_t lo_t v_t[d]
-//                              each sum sixteen 16-key k steps, ascending,
-//                              in fp32; the two sums added once at the end
-// and (m, l, o) is stored as the split's fp32 partial.  The tensor cores take
-// P one bf16 half at a time: P's tile holds hi for the first pass and lo for
-// the second (the lo values wait in registers).  A key a pair cannot
-// see (beyond its count) gets p_t = 0; keys past the split's end read zero V.
-// An MMA row depends only on its own q row and weights, so a pair's bits are
-// the same whichever pairs share the block.
-// Merge kernel: per (row, query head), fold the partials in ascending split
-// order with the log-sum-exp update, then o / l -> bf16.
+//                              each sum sixteen 16-key steps, ascending, in
+//                              fp32; the two sums added once at the end
+// and the splits are folded in ascending order with the log-sum-exp update,
+// then o / l -> bf16.  A key a pair cannot see gets weight 0; keys past the
+// split's end read zero V.  A pair's bits depend only on its own q row and
+// its sequence's keys and values.
 //
-// Decode is the case of one row per block with L = kv_len[b]; prefill groups
-// up to 32 / (Hq/Hkv) consecutive rows of one sequence per block (they share
-// the split's K and V tiles in shared memory) with L = position + 1.  Both run
-// the same compiled kernels, so a decode step equals a one-row prefill bit for
-// bit, and a prompt's rows have the same bits for every chunking.
+// Decode (one new row per sequence): the split kernel, one block (eight
+// warps, warp-level mma.sync m16n8k16) per (split, kv head, sequence), stores
+// each split's (m, l, o) partial; the merge kernel folds them.  Prefill (rows
+// of a prompt chunk): one tcgen05 block per (sequence, kv head, 128 pairs)
+// folds the splits on chip.  A 16-deep tcgen05 step gives each element the
+// bits of the mma.sync step, and both take the sums above in the same order,
+// so a decode step equals a one-row prefill bit for bit and a prompt's rows
+// have the same bits for every chunking.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
+
+#include <mutex>
 
 #include "common.cuh"
 
@@ -44,7 +46,6 @@ constexpr int kSplit = 256;      // keys per split (the fixed split size)
 constexpr int kThreads = 256;    // eight warps, 32 keys each for the scores
 constexpr int kRowsMma = 16;     // (row, head) pairs of one block: the MMA's 16 rows
 constexpr int kMaxG = 8;         // query heads per kv head
-constexpr int kPrefillTiles = 4; // prefill: 16-row MMA tiles of (row, head) pairs per block
 
 struct AttnParams {
   const __nv_bfloat16* q;
@@ -392,281 +393,6 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   }
 }
 
-// The split kernel for prefill: MT 16-row MMA tiles of (row, head) pairs per
-// block, sharing the block's K and V tiles (so each tile load serves MT times
-// the rows).  Every pair is one MMA row and meets exactly the arithmetic of
-// attn_split_kernel (the same MMAs in the same order, the same softmax, sums
-// and rounding), so a prefill row has the bits of the decode row.
-template <int D, int MT>
-__global__ void __launch_bounds__(kThreads, 2) attn_split_tiles_kernel(const AttnParams p) {
-  constexpr int C8 = D / 8;               // 16-byte chunks per key row
-  constexpr int SUB = 64;                 // keys per load stage
-  constexpr int NSUB = kSplit / SUB;      // the K stages are reused for V
-  constexpr int KS = D / 16;              // 16-wide k steps of q . k
-  constexpr int PR = kRowsMma * MT;       // (row, head) pairs of a block
-  // Tiles in shared memory, rows of 16-byte chunks; chunk c of row r is
-  // stored at chunk c ^ (r & 7), so the eight row addresses of every ldmatrix
-  // phase fall in eight different bank groups.
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(smem_raw);                 // [256][D]
-  __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(smem_raw + kSplit * D * 2);  // P [PR][256]
-  // the block's q rows [PR][D] (swizzled like K) live where P goes, until the scores are done
-  __nv_bfloat16* qs = pt;
-  static_assert(kRowsMma * MT * D <= kRowsMma * MT * kSplit, "q rows fit in the P tile");
-  __shared__ float wmax[kThreads / 32][PR];
-  __shared__ float wsum[kThreads / 32][PR];
-
-  pdl_launch_dependents();
-  pdl_wait();
-  RowSet rs;
-  if (!block_rows(p, rs)) return;
-  // kv heads are the fastest grid index: the blocks reading the 256-byte
-  // slices of the same token rows run side by side
-  const int g = blockIdx.x;
-  const int s = blockIdx.y;
-  const int k0 = s * kSplit;
-  const int lenmax = rs.len0 + rs.nrows - 1;           // the last row sees the most keys
-  const int nmax = min(kSplit, lenmax - k0);
-  if (nmax <= 0) return;
-  const int G = p.G;
-  const int RG = rs.nrows * G;                         // (row, head) pairs: MMA rows 0..RG-1
-  const int t = threadIdx.x;
-  const int lane = t & 31, warp = t >> 5;
-  const int gq = lane >> 2, tq = lane & 3;             // fragment row / column group
-  const int64_t seq_off = rs.seq * p.seq_stride + static_cast<int64_t>(k0) * p.tok_stride + g * D;
-  const uint32_t kv_base = smem_addr(kv);
-  const uint32_t pt_base = smem_addr(pt);
-  auto count = [&](int r) { return r < RG ? min(kSplit, rs.len0 + r / G - k0) : 0; };
-
-  auto load_sub = [&](const __nv_bfloat16* src, int j) {
-    const int rows = min(SUB, nmax - j * SUB);
-    for (int idx = t; idx < rows * C8; idx += kThreads) {
-      const int r = idx / C8, c = idx % C8;
-      const int key = j * SUB + r;
-      cp_async16(kv_base + static_cast<uint32_t>(key * D * 2 + ((c ^ (key & 7)) << 4)),
-                 src + seq_off + static_cast<int64_t>(key) * p.tok_stride + c * 8);
-    }
-  };
-#pragma unroll
-  for (int j = 0; j < NSUB; ++j) load_sub(p.k, j);
-  cp_async_commit();
-
-  // the q rows of the block's pairs, once (pair r: row r / G, head g * G + r % G);
-  // rows of pairs past RG, in a tile that has pairs, read as zero
-  const uint32_t qs_base = smem_addr(qs);
-  const int tiles = (RG + kRowsMma - 1) / kRowsMma;
-  for (int idx = t; idx < tiles * kRowsMma * C8; idx += kThreads) {
-    const int r = idx / C8, c = idx % C8;
-    if (r < RG)
-      cp_async16(qs_base + static_cast<uint32_t>(r * D * 2 + ((c ^ (r & 7)) << 4)),
-                 p.q + (static_cast<int64_t>(rs.row0 + r / G) * p.Hq + g * G + r % G) * D + c * 8);
-    else
-      *reinterpret_cast<uint4*>(qs + r * D + ((c ^ (r & 7)) << 3)) = make_uint4(0, 0, 0, 0);
-  }
-  cp_async_commit();
-  uint32_t qa[KS][4];
-  cp_async_wait<0>();
-  __syncthreads();
-
-  // --- scores: warp w owns keys 32w .. 32w + 31 (four 8-key n blocks), for
-  // every tile of pairs
-  float sc[MT][4][4];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-    for (int nb = 0; nb < 4; ++nb)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) sc[mt][nb][i] = 0.f;
-    if (mt * kRowsMma >= RG) continue;  // (block-uniform)
-    // q fragments (A operand) of tile mt: lane l gives row mt * 16 + (l & 15),
-    // 8-column block 2 ks + (l >> 4) -- the MMA's a0..a3
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const int qrow = mt * kRowsMma + (lane & 15);
-      const int c = 2 * ks + (lane >> 4);
-      ldsm_x4(qs_base + static_cast<uint32_t>(qrow * D * 2 + ((c ^ (qrow & 7)) << 4)), qa[ks][0], qa[ks][1],
-              qa[ks][2], qa[ks][3]);
-    }
-#pragma unroll
-    for (int nb = 0; nb < 4; ++nb) {
-      const int key = warp * 32 + nb * 8 + (lane & 7);
-#pragma unroll
-      for (int kp = 0; kp < KS / 2; ++kp) {
-        const int c = kp * 4 + (lane >> 3);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kv_base + static_cast<uint32_t>(key * D * 2 + ((c ^ (key & 7)) << 4)), b0, b1, b2, b3);
-        mma_bf16_16816(sc[mt][nb], qa[2 * kp], b0, b1);
-        mma_bf16_16816(sc[mt][nb], qa[2 * kp + 1], b2, b3);
-      }
-    }
-  }
-  __syncthreads();  // every warp is done with K: the stages take V now
-#pragma unroll
-  for (int j = 0; j < NSUB; ++j) load_sub(p.v, j);
-  // keys the split does not hold read as zero (their weights are zero, and a
-  // stale NaN times zero would not be)
-  for (int idx = t; idx < (kSplit - nmax) * C8; idx += kThreads) {
-    const int key = nmax + idx / C8, c = idx % C8;
-    *reinterpret_cast<uint4*>(kv + key * D + ((c ^ (key & 7)) << 3)) = make_uint4(0, 0, 0, 0);
-  }
-  cp_async_commit();
-
-  // --- softmax statistics.  A lane holds rows gq and gq + 8 of each tile,
-  // keys 32w + 8nb + 2tq (+1).  Maxima: lane, then the four lanes of a row
-  // (exact), then the eight warps.  Weights are rounded to bf16 once; the sum
-  // adds the rounded weights: a lane's eight in (nb, pair) order, a fixed
-  // butterfly over the four lanes, the eight warps in ascending order.
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    if (mt * kRowsMma >= RG) continue;
-    const int r_lo = mt * kRowsMma + gq, r_hi = r_lo + 8;
-    const int cnt_lo = count(r_lo), cnt_hi = count(r_hi);
-    float mx_lo = -INFINITY, mx_hi = -INFINITY;
-#pragma unroll
-    for (int nb = 0; nb < 4; ++nb) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = warp * 32 + nb * 8 + 2 * tq + e;
-        sc[mt][nb][e] = key < cnt_lo ? __fmul_rn(sc[mt][nb][e], p.scale) : -INFINITY;
-        sc[mt][nb][2 + e] = key < cnt_hi ? __fmul_rn(sc[mt][nb][2 + e], p.scale) : -INFINITY;
-        mx_lo = fmaxf(mx_lo, sc[mt][nb][e]);
-        mx_hi = fmaxf(mx_hi, sc[mt][nb][2 + e]);
-      }
-    }
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, o));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, o));
-    }
-    if (tq == 0) {
-      wmax[warp][r_lo] = mx_lo;
-      wmax[warp][r_hi] = mx_hi;
-    }
-  }
-  __syncthreads();
-  // writes the weights held in w[nb][0..3] (rows gq and gq + 8 of tile mt)
-  // into P's tile
-  auto write_p = [&](int mt, const float (&w)[4][4]) {
-    const int r_lo = mt * kRowsMma + gq, r_hi = r_lo + 8;
-#pragma unroll
-    for (int nb = 0; nb < 4; ++nb) {
-      const int kc = warp * 4 + nb;                       // 8-key chunk of P
-      const uint32_t off_lo = static_cast<uint32_t>(r_lo * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
-      const uint32_t off_hi = static_cast<uint32_t>(r_hi * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
-      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_lo) = pack_bf16(w[nb][0], w[nb][1]);
-      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_hi) = pack_bf16(w[nb][2], w[nb][3]);
-    }
-  };
-  float m_lo[MT], m_hi[MT];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    m_lo[mt] = m_hi[mt] = -INFINITY;
-    if (mt * kRowsMma >= RG) continue;
-    const int r_lo = mt * kRowsMma + gq, r_hi = r_lo + 8;
-    m_lo[mt] = wmax[0][r_lo];
-    m_hi[mt] = wmax[0][r_hi];
-#pragma unroll
-    for (int w = 1; w < kThreads / 32; ++w) {
-      m_lo[mt] = fmaxf(m_lo[mt], wmax[w][r_lo]);
-      m_hi[mt] = fmaxf(m_hi[mt], wmax[w][r_hi]);
-    }
-    float sum_lo = 0.f, sum_hi = 0.f;
-    float hi[4][4];  // the high halves; sc keeps the low halves for the second pass
-#pragma unroll
-    for (int nb = 0; nb < 4; ++nb) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float xl = sc[mt][nb][e] == -INFINITY ? 0.f : expf(__fsub_rn(sc[mt][nb][e], m_lo[mt]));
-        const float xh = sc[mt][nb][2 + e] == -INFINITY ? 0.f : expf(__fsub_rn(sc[mt][nb][2 + e], m_hi[mt]));
-        split_bf16(xl, hi[nb][e], sc[mt][nb][e]);
-        split_bf16(xh, hi[nb][2 + e], sc[mt][nb][2 + e]);
-        sum_lo = __fadd_rn(sum_lo, __fadd_rn(hi[nb][e], sc[mt][nb][e]));
-        sum_hi = __fadd_rn(sum_hi, __fadd_rn(hi[nb][2 + e], sc[mt][nb][2 + e]));
-      }
-    }
-    write_p(mt, hi);
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-      sum_lo = __fadd_rn(sum_lo, __shfl_xor_sync(0xffffffffu, sum_lo, o));
-      sum_hi = __fadd_rn(sum_hi, __shfl_xor_sync(0xffffffffu, sum_hi, o));
-    }
-    if (tq == 0) {
-      wsum[warp][r_lo] = sum_lo;
-      wsum[warp][r_hi] = sum_hi;
-    }
-  }
-  cp_async_wait<0>();
-  __syncthreads();
-
-  // --- o = P . V: warp w owns columns 16w .. 16w + 15 (two 8-wide n
-  // blocks) over all 256 keys, sixteen k steps of 16 keys in ascending order;
-  // each V fragment serves every tile.  Once over the high halves of P, once
-  // over the low halves, the two sums added at the end.
-  auto pv = [&](float (&acc)[MT][2][4]) {
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[mt][nb][i] = 0.f;
-    if (warp >= D / 16) return;
-#pragma unroll 4
-    for (int kk = 0; kk < kSplit / 16; ++kk) {
-      uint32_t b0, b1, b2, b3;
-      {
-        const int key = kk * 16 + (lane & 15);
-        const int c = warp * 2 + (lane >> 4);
-        ldsm_x4_t(kv_base + static_cast<uint32_t>(key * D * 2 + ((c ^ (key & 7)) << 4)), b0, b1, b2, b3);
-      }
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        if (mt >= tiles) continue;
-        uint32_t a[4];
-        const int prow = mt * kRowsMma + (lane & 15);
-        const int kc = 2 * kk + (lane >> 4);
-        ldsm_x4(pt_base + static_cast<uint32_t>(prow * kSplit * 2 + ((kc ^ (prow & 7)) << 4)), a[0], a[1],
-                a[2], a[3]);
-        mma_bf16_16816(acc[mt][0], a, b0, b1);
-        mma_bf16_16816(acc[mt][1], a, b2, b3);
-      }
-    }
-  };
-  float oc[MT][2][4], ol[MT][2][4];
-  pv(oc);
-  __syncthreads();  // every warp is done with the high halves
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-    if (mt * kRowsMma < RG) write_p(mt, sc[mt]);
-  __syncthreads();
-  pv(ol);
-  if (warp < D / 16) {
-    // rows gq and gq + 8 of each tile, columns 16w + 8nb + 2tq (+1)
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = mt * kRowsMma + gq + 8 * h;
-        if (r < RG && count(r) > 0) {
-          const int row = r / G, i = r % G;
-          const int64_t base = (static_cast<int64_t>(rs.row0 + row) * p.Hq + g * G + i) * p.S + s;
-#pragma unroll
-          for (int nb = 0; nb < 2; ++nb)
-            *reinterpret_cast<float2*>(p.ws_o + base * D + warp * 16 + nb * 8 + 2 * tq) =
-                make_float2(__fadd_rn(oc[mt][nb][2 * h], ol[mt][nb][2 * h]),
-                            __fadd_rn(oc[mt][nb][2 * h + 1], ol[mt][nb][2 * h + 1]));
-          if (warp == 0 && tq == 0) {
-            float l = wsum[0][r];
-#pragma unroll
-            for (int w = 1; w < kThreads / 32; ++w) l = __fadd_rn(l, wsum[w][r]);
-            p.ws_ml[base * 2 + 0] = h ? m_hi[mt] : m_lo[mt];
-            p.ws_ml[base * 2 + 1] = l;
-          }
-        }
-      }
-    }
-  }
-}
-
 // One block per (query head, row); thread d folds column d.
 template <int D>
 __global__ void attn_merge_kernel(const AttnParams p) {
@@ -729,25 +455,453 @@ __global__ void attn_merge_kernel(const AttnParams p) {
   *dst = __float2bfloat16_rn(__fdiv_rn(o_acc, l_acc));
 }
 
-template <int D, int MT>
-size_t split_smem_bytes() {
-  return static_cast<size_t>(kSplit) * D * 2 + static_cast<size_t>(kRowsMma) * MT * kSplit * 2;
+// ---------------------------------------------------------------------------
+// Prefill on the tcgen05 tensor cores.  One block per (sequence, kv head,
+// tile of 128 (row, head) pairs: 128 / G consecutive rows, each with its G
+// query heads); it walks the 256-key splits the tile's rows can see in
+// ascending order and folds each split into a running (m, l, o) per pair in
+// registers with the merge kernel's arithmetic, so no partial goes to memory.
+// Per pair and split it computes what attn_split_kernel computes:
+//   S = Q . K^T         tcgen05 128 x 256 x 16 steps over the head dimension,
+//                       ascending, fp32 in tensor memory (the per-element
+//                       result of a 16-deep step equals mma.sync's)
+//   scores, max, e = exp(s - m), hi / lo split, l in the same order (a key's
+//   32-key group in the decode kernel's lane order, the groups in order)
+//   O = P_hi . V + P_lo . V, each sixteen 16-key steps ascending from zero
+// and then folds as the merge kernel does; out = bf16(o / l).  So a prompt
+// row has the bits of the decode step at its position.
+// Roles (192 threads): warps 0-3 take one pair per thread (TMEM lane = pair):
+// the softmax, the P tiles and the fold; warp 4 lane 0 issues the MMAs; warp
+// 5 issues the TMA loads of Q, K and V and zeroes V rows past the tile's last
+// visible key.  Tensor memory: S in columns 0-255, O_hi and O_lo after it.
+constexpr int kTcThreads = 192;
+constexpr int kTcPairs = 128;
+
+struct PrefillTcArgs {
+  const int32_t* q_start;
+  const int32_t* q_len;
+  const int32_t* q_offset;
+  __nv_bfloat16* out;
+  int Hq, Hkv, G, RT;  // RT rows per tile (128 / G)
+  int tiles_per_seq;
+  int max_len, max_q_len, total_rows;
+  float scale;
+  int* status;
+};
+
+// tcgen05 instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B,
+// A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), N, M = 128.
+__host__ __device__ constexpr uint32_t tc_idesc(int n, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(b_mn) << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+}
+// Shared-memory descriptors, 128-byte swizzle, version 1.  K-major: rows of
+// 128 bytes (64 bf16 of K), 8-row groups 1024 bytes apart.  MN-major: rows of
+// 128 bytes along MN (64 bf16) per K index, 8 K rows 1024 bytes apart (stride
+// field), the next 64 MN elements `mn_stride` bytes further (leading field).
+__device__ __forceinline__ uint64_t desc_k_sw128(uint32_t addr) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (1ull << 16) | (64ull << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t addr, uint32_t mn_stride) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16) |
+         (64ull << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// MT == 1: attn_split_kernel (decode); otherwise attn_split_tiles_kernel.
-template <int D, int MT>
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV, const PrefillTcArgs a) {
+  constexpr int DS = D / 64;                   // 64-wide slices of the head dimension
+  constexpr int Q_BYTES = DS * kTcPairs * 128; // [slice][128 pairs][64]
+  constexpr int KV_SLICE = kSplit * 128;       // [256 keys][64] per slice
+  constexpr int KV_BYTES = DS * KV_SLICE;
+  constexpr int P_BYTES = kTcPairs * 128;      // [128 pairs][64 keys]
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* q_s = base;
+  unsigned char* k_s = q_s + Q_BYTES;
+  unsigned char* v_s = k_s + KV_BYTES;
+  unsigned char* p_s = v_s + KV_BYTES;         // [2 slots][hi, lo][P_BYTES]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(p_s + 4 * P_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t q_full = smem_addr(bars + 0), k_full = smem_addr(bars + 1), k_empty = smem_addr(bars + 2);
+  const uint32_t v_full = smem_addr(bars + 3), v_ready = smem_addr(bars + 4), v_empty = smem_addr(bars + 5);
+  const uint32_t s_full = smem_addr(bars + 6), s_empty = smem_addr(bars + 7);
+  const uint32_t o_full = smem_addr(bars + 8), o_empty = smem_addr(bars + 9);
+  auto p_full = [&](int slot) { return smem_addr(bars + 10 + slot); };
+  auto p_empty = [&](int slot) { return smem_addr(bars + 12 + slot); };
+  const uint32_t done_bar = smem_addr(bars + 14);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
+  const int g = blockIdx.y;
+  const int b = blockIdx.z;
+  const int tile = a.tiles_per_seq - 1 - static_cast<int>(blockIdx.x);  // the longest tiles first
+  pdl_wait();
+  // the sequence's device-side lengths within the stated bounds, else left out
+  const int n = a.q_len[b], st0 = a.q_start[b], off = a.q_offset[b];
+  if (!(n >= 0 && n <= a.max_q_len && st0 >= 0 && st0 <= a.max_len - n && off >= 0 && off <= a.total_rows - n)) {
+    if (t == 0 && tile == 0 && a.status) atomicExch(a.status, DEV_ATTN_BAD_LENGTH);
+    return;
+  }
+  const int first = tile * a.RT;
+  if (first >= n) return;
+  const int nrows = min(a.RT, n - first);
+  const int row0 = off + first;           // q / out row of the tile's first row
+  const int len0 = st0 + first + 1;       // keys the first row sees (row r: len0 + r)
+  const int len_last = len0 + nrows - 1;
+  const int ns = (len_last + kSplit - 1) / kSplit;
+
+  if (t == 0) {
+    // the softmax threads' signals take one arrival per pair, the rest one
+    for (int i = 0; i < 15; ++i) {
+      const uint32_t bar = smem_addr(bars + i);
+      const bool per_pair = bar == s_empty || bar == o_empty || bar == p_full(0) || bar == p_full(1);
+      mbar_init(bar, per_pair ? kTcPairs : 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) tmem_alloc(smem_addr(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();  // after the TMEM allocation (see the GEMM kernels)
+  int* status = a.status;
+
+  if (warp == 5) {
+    // ---- TMA: Q once, then K and V of each split; V rows past the tile's
+    // last visible key are zeroed (stale cache rows may hold anything, and
+    // their weight 0 times a NaN would not be 0)
+    const uint64_t pol = l2_policy_evict_last();
+    bool stop = false;
+    int k_issued = 0, v_issued = 0;  // splits whose K / V loads were issued
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
+      mbar_arrive_expect_tx(q_full, Q_BYTES);
+      for (int ds = 0; ds < DS; ++ds)
+        tma_load_3d(smem_addr(q_s + ds * kTcPairs * 128), &tmQ, 64 * ds, g * a.G, row0, q_full, pol);
+    }
+    for (int s = 0; s < ns && !stop; ++s) {
+      const uint32_t ph = s & 1;
+      if (lane == 0) {
+        bool ok = !*abort_flag && mbar_wait_bounded(k_empty, ph ^ 1u, status, DEV_TIMEOUT_ATTN);
+        if (ok) {
+          mbar_arrive_expect_tx(k_full, KV_BYTES);
+          for (int ds = 0; ds < DS; ++ds)
+            tma_load_4d(smem_addr(k_s + ds * KV_SLICE), &tmK, 64 * ds, g, s * kSplit, b, k_full, pol);
+          k_issued = s + 1;
+          ok = !*abort_flag && mbar_wait_bounded(v_empty, ph ^ 1u, status, DEV_TIMEOUT_ATTN);
+        }
+        if (ok) {
+          mbar_arrive_expect_tx(v_full, KV_BYTES);
+          for (int ds = 0; ds < DS; ++ds)
+            tma_load_4d(smem_addr(v_s + ds * KV_SLICE), &tmV, 64 * ds, g, s * kSplit, b, v_full, pol);
+          v_issued = s + 1;
+          ok = mbar_wait_bounded(v_full, ph, status, DEV_TIMEOUT_ATTN);
+        }
+        if (!ok) *abort_flag = 1;
+      }
+      stop = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
+      if (stop) break;
+      const int nmax = min(kSplit, len_last - s * kSplit);
+      for (int idx = lane; idx < (kSplit - nmax) * DS * 8; idx += 32) {
+        const int key = nmax + idx / (DS * 8), rest = idx % (DS * 8);
+        *reinterpret_cast<uint4*>(v_s + (rest / 8) * KV_SLICE + key * 128 + (rest % 8) * 16) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(v_ready);
+    }
+    if (lane == 0) {
+      // loads still in flight (only after an abort) land before the block exits
+      mbar_wait_bounded(q_full, 0, nullptr, 0);
+      if (k_issued > 0) mbar_wait_bounded(k_full, (k_issued - 1) & 1u, nullptr, 0);
+      if (v_issued > 0) mbar_wait_bounded(v_full, (v_issued - 1) & 1u, nullptr, 0);
+    }
+    __syncwarp();
+  } else if (warp == 4) {
+    // ---- MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = tc_idesc(kSplit, 0);
+      constexpr uint32_t idesc_o = tc_idesc(D, 1);
+      bool ok = mbar_wait_bounded(q_full, 0, status, DEV_TIMEOUT_ATTN);
+      const uint32_t qa = smem_addr(q_s), ka = smem_addr(k_s), va = smem_addr(v_s), pa = smem_addr(p_s);
+      int gc = 0;  // P chunks issued so far
+      for (int s = 0; s < ns && ok; ++s) {
+        const uint32_t ph = s & 1;
+        ok = !*abort_flag && mbar_wait_bounded(k_full, ph, status, DEV_TIMEOUT_ATTN) &&
+             mbar_wait_bounded(s_empty, ph ^ 1u, status, DEV_TIMEOUT_ATTN);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ds = 0; ds < DS; ++ds)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem, desc_k_sw128(qa + ds * kTcPairs * 128 + kk * 32),
+                      desc_k_sw128(ka + ds * KV_SLICE + kk * 32), idesc_s, (ds | kk) != 0 ? 1u : 0u);
+        umma_commit(k_empty);
+        umma_commit(s_full);
+        ok = !*abort_flag && mbar_wait_bounded(v_ready, ph, status, DEV_TIMEOUT_ATTN) &&
+             mbar_wait_bounded(o_empty, ph ^ 1u, status, DEV_TIMEOUT_ATTN);
+        if (!ok) break;
+        tc_fence_after();
+        for (int j = 0; j < 4 && ok; ++j, ++gc) {
+          const int slot = gc & 1;
+          ok = !*abort_flag && mbar_wait_bounded(p_full(slot), (gc >> 1) & 1u, status, DEV_TIMEOUT_ATTN);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t phi = pa + slot * 2 * P_BYTES, plo = phi + P_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t vdesc = desc_mn_sw128(va + (4 * j + kk) * 2048, KV_SLICE);
+            const uint32_t acc = (j | kk) != 0 ? 1u : 0u;
+            umma_bf16(tmem + 256, desc_k_sw128(phi + kk * 32), vdesc, idesc_o, acc);
+            umma_bf16(tmem + 256 + D, desc_k_sw128(plo + kk * 32), vdesc, idesc_o, acc);
+          }
+          umma_commit(p_empty(slot));
+        }
+        if (!ok) break;
+        umma_commit(v_empty);
+        umma_commit(o_full);
+      }
+      if (!ok) *abort_flag = 1;
+      umma_commit(done_bar);
+      mbar_wait_bounded(done_bar, 0, status, DEV_TIMEOUT_ATTN);
+    }
+    __syncwarp();
+  } else {
+    // ---- one (row, head) pair per thread
+    const int pr = t;                                    // pair = TMEM lane
+    const int r = pr / a.G, hi_head = g * a.G + pr % a.G;
+    const int len = len0 + r;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float o_acc[D];
+#pragma unroll
+    for (int d = 0; d < D; ++d) o_acc[d] = 0.f;
+    float m_acc = -INFINITY, l_acc = 0.f;
+    int gc = 0;
+    bool ok = true;
+    for (int s = 0; s < ns; ++s) {
+      const uint32_t ph = s & 1;
+      const int cnt = min(kSplit, len - s * kSplit);
+      ok = mbar_wait_bounded(s_full, ph, status, DEV_TIMEOUT_ATTN);
+      if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // the maximum (exact in any order)
+      float m = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + 32 * c, v);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj)
+          m = fmaxf(m, 32 * c + jj < cnt ? __fmul_rn(__uint_as_float(v[jj]), a.scale) : -INFINITY);
+      }
+      // weights, their sum, and the P tiles, 64 keys at a time
+      float l = 0.f;
+      for (int j = 0; j < 4; ++j, ++gc) {
+        const int slot = gc & 1;
+        ok = mbar_wait_bounded(p_empty(slot), ((gc >> 1) & 1u) ^ 1u, status, DEV_TIMEOUT_ATTN);
+        if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        unsigned char* phi = p_s + slot * 2 * P_BYTES;
+        unsigned char* plo = phi + P_BYTES;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = 2 * j + h;  // 32-key group c: the decode kernel's warp c
+          uint32_t v[32];
+          tmem_ld32(lane_base + 32 * c, v);
+          float ph_[32], pl_[32];
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const float sc = 32 * c + jj < cnt ? __fmul_rn(__uint_as_float(v[jj]), a.scale) : -INFINITY;
+            const float x = sc == -INFINITY ? 0.f : expf(__fsub_rn(sc, m));
+            split_bf16(x, ph_[jj], pl_[jj]);
+          }
+          // lane tq of the decode kernel adds keys 8nb + 2tq + e in (nb, e)
+          // order; a butterfly over tq; then the groups in order
+          float sq[4];
+#pragma unroll
+          for (int tq = 0; tq < 4; ++tq) {
+            float acc = 0.f;
+#pragma unroll
+            for (int nb = 0; nb < 4; ++nb)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int k = 8 * nb + 2 * tq + e;
+                acc = __fadd_rn(acc, __fadd_rn(ph_[k], pl_[k]));
+              }
+            sq[tq] = acc;
+          }
+          const float w = __fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3]));
+          l = c == 0 ? w : __fadd_rn(l, w);
+          // this pair's row of the two P tiles (keys 32h .. 32h + 31 of the chunk)
+          const uint32_t row_off = static_cast<uint32_t>((pr >> 3) * 1024 + (pr & 7) * 128);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int unit = 4 * h + u;  // 16-byte unit of the 128-byte row
+            const uint32_t off = row_off + static_cast<uint32_t>(((unit ^ (pr & 7)) & 7) * 16);
+            *reinterpret_cast<uint4*>(phi + off) =
+                make_uint4(pack_bf16(ph_[8 * u + 0], ph_[8 * u + 1]), pack_bf16(ph_[8 * u + 2], ph_[8 * u + 3]),
+                           pack_bf16(ph_[8 * u + 4], ph_[8 * u + 5]), pack_bf16(ph_[8 * u + 6], ph_[8 * u + 7]));
+            *reinterpret_cast<uint4*>(plo + off) =
+                make_uint4(pack_bf16(pl_[8 * u + 0], pl_[8 * u + 1]), pack_bf16(pl_[8 * u + 2], pl_[8 * u + 3]),
+                           pack_bf16(pl_[8 * u + 4], pl_[8 * u + 5]), pack_bf16(pl_[8 * u + 6], pl_[8 * u + 7]));
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(p_full(slot));
+      }
+      if (!ok) break;
+      tc_fence_before();
+      mbar_arrive(s_empty);  // the scores have been read
+      // fold this split's (m, l, o) into the running state (the merge kernel's arithmetic)
+      ok = mbar_wait_bounded(o_full, ph, status, DEV_TIMEOUT_ATTN);
+      if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool in = cnt > 0;
+      const float m_new = fmaxf(m_acc, m);
+      const float fa = expf(__fsub_rn(m_acc, m_new));
+      const float fc = expf(__fsub_rn(m, m_new));
+      if (in) {
+        l_acc = __fadd_rn(__fmul_rn(l_acc, fa), __fmul_rn(l, fc));
+      }
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t vh[32], vl[32];
+        tmem_ld32(lane_base + 256 + 32 * c, vh);
+        tmem_ld32(lane_base + 256 + D + 32 * c, vl);
+        if (in) {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const float os = __fadd_rn(__uint_as_float(vh[jj]), __uint_as_float(vl[jj]));
+            o_acc[32 * c + jj] = __fadd_rn(__fmul_rn(o_acc[32 * c + jj], fa), __fmul_rn(os, fc));
+          }
+        }
+      }
+      if (in) m_acc = m_new;
+      tc_fence_before();
+      mbar_arrive(o_empty);
+    }
+    if (ok && r < nrows) {
+      __nv_bfloat16* dst = a.out + (static_cast<int64_t>(row0 + r) * a.Hq + hi_head) * D;
+#pragma unroll
+      for (int d = 0; d < D; d += 8) {
+        uint4 o;
+        o.x = pack_bf16(__fdiv_rn(o_acc[d + 0], l_acc), __fdiv_rn(o_acc[d + 1], l_acc));
+        o.y = pack_bf16(__fdiv_rn(o_acc[d + 2], l_acc), __fdiv_rn(o_acc[d + 3], l_acc));
+        o.z = pack_bf16(__fdiv_rn(o_acc[d + 4], l_acc), __fdiv_rn(o_acc[d + 5], l_acc));
+        o.w = pack_bf16(__fdiv_rn(o_acc[d + 6], l_acc), __fdiv_rn(o_acc[d + 7], l_acc));
+        *reinterpret_cast<uint4*>(dst + d) = o;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+size_t prefill_tc_smem_bytes() {
+  return 1024 + static_cast<size_t>(D / 64) * kTcPairs * 128 + 2 * static_cast<size_t>(D / 64) * kSplit * 128 +
+         4 * static_cast<size_t>(kTcPairs) * 128 + 16 * 8 + 16;
+}
+
+template <int D>
+size_t split_smem_bytes() {
+  return static_cast<size_t>(kSplit) * D * 2 + static_cast<size_t>(kRowsMma) * kSplit * 2;
+}
+
+// Decode: attn_split_kernel, then the merge.
+template <int D>
 kinv_status launch(const AttnParams& p, dim3 split_grid, dim3 merge_grid, cudaStream_t stream) {
-  void (*kernel)(const AttnParams);
-  if constexpr (MT == 1)
-    kernel = attn_split_kernel<D>;
-  else
-    kernel = attn_split_tiles_kernel<D, MT>;
-  const size_t smem = split_smem_bytes<D, MT>();
+  void (*kernel)(const AttnParams) = attn_split_kernel<D>;
+  const size_t smem = split_smem_bytes<D>();
   const kinv_status attr = ensure_smem(reinterpret_cast<const void*>(kernel), smem);
   if (attr != KINV_OK) return attr;
   const kinv_status st = launch_kernel(kernel, split_grid, dim3(kThreads), smem, stream, 1, p);
   if (st != KINV_OK) return st;
   return launch_kernel(attn_merge_kernel<D>, merge_grid, dim3(D), 0, stream, 1, p);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tma_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// A bf16 tensor of rank `r` (dims innermost first, byte strides of dims 1..),
+// boxes of `box` elements, 128-byte swizzle, out-of-range elements zero.
+bool encode_map(CUtensorMap* map, const void* ptr, int r, const uint64_t* dims, const uint64_t* strides,
+                const uint32_t* box) {
+  auto fn = tma_encoder();
+  if (!fn) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < r; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < r) st[i] = strides[i];
+  }
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, r, const_cast<void*>(ptr), d, st, bx, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Prefill with the tcgen05 kernel: one block per (sequence, kv head, tile of
+// 128 (row, head) pairs).
+template <int D>
+kinv_status launch_prefill_tc(const void* q, const void* k_cache, const void* v_cache, int64_t seq_stride,
+                              int64_t tok_stride, PrefillTcArgs a, int B, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  const uint64_t qd[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.Hq), static_cast<uint64_t>(a.total_rows)};
+  const uint64_t qs[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a.Hq) * D * 2};
+  const uint32_t qb[3] = {64, static_cast<uint32_t>(a.G), static_cast<uint32_t>(a.RT)};
+  const uint64_t kd[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.Hkv), static_cast<uint64_t>(a.max_len),
+                          static_cast<uint64_t>(B)};
+  // one sequence: any sequence stride describes it (the coordinate is 0)
+  const int64_t sst = B > 1 ? seq_stride : static_cast<int64_t>(a.max_len) * tok_stride;
+  const uint64_t ks[3] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(tok_stride) * 2,
+                          static_cast<uint64_t>(sst) * 2};
+  const uint32_t kb[4] = {64, 1, static_cast<uint32_t>(kSplit), 1};
+  if (!encode_map(&mq, q, 3, qd, qs, qb) || !encode_map(&mk, k_cache, 4, kd, ks, kb) ||
+      !encode_map(&mv, v_cache, 4, kd, ks, kb))
+    return KINV_ERR_UNSUPPORTED;
+  const size_t smem = prefill_tc_smem_bytes<D>();
+  if (smem > static_cast<size_t>(max_smem_optin())) return KINV_ERR_UNSUPPORTED;
+  const kinv_status attr = ensure_smem(reinterpret_cast<const void*>(attn_prefill_tc_kernel<D>), smem);
+  if (attr != KINV_OK) return attr;
+  return launch_kernel(attn_prefill_tc_kernel<D>, dim3(a.tiles_per_seq, a.Hkv, B), dim3(kTcThreads), smem, stream, 1,
+                       mq, mk, mv, a);
 }
 
 kinv_status check_common(const void* q, const void* k, const void* v, int64_t seq_stride,
@@ -832,8 +986,8 @@ kinv_status decode_launch(const void* q, const void* k_cache, const void* v_cach
   p.total_rows = B;
   p.status = device_status_word();
   const dim3 split_grid(Hkv, S, B), merge_grid(Hq, B, 1);
-  return D == 128 ? launch<128, 1>(p, split_grid, merge_grid, stream)
-                  : launch<64, 1>(p, split_grid, merge_grid, stream);
+  return D == 128 ? launch<128>(p, split_grid, merge_grid, stream)
+                  : launch<64>(p, split_grid, merge_grid, stream);
 }
 }  // namespace
 }  // namespace kinv
@@ -852,8 +1006,13 @@ extern "C" kinv_status kinv_attn_decode(const void* q, const void* k_cache, cons
 
 extern "C" size_t kinv_attn_prefill_workspace(int total_rows, int Hq, int D, int max_kv,
                                               int split_len) {
-  if (total_rows <= 0 || Hq <= 0 || D <= 0 || max_kv <= 0 || split_len <= 0) return 0;
-  return workspace_bytes(total_rows, Hq, D, (max_kv + split_len - 1) / split_len);
+  // the splits are folded on chip: no workspace
+  (void)total_rows;
+  (void)Hq;
+  (void)D;
+  (void)max_kv;
+  (void)split_len;
+  return 0;
 }
 
 extern "C" kinv_status kinv_attn_prefill(const void* q, const void* k_cache, const void* v_cache,
@@ -863,45 +1022,34 @@ extern "C" kinv_status kinv_attn_prefill(const void* q, const void* k_cache, con
                                          int total_rows, int max_q_len, int max_kv, int Hq,
                                          int Hkv, int D, int split_len, float scale,
                                          void* workspace, size_t ws_bytes, kinv_stream stream) {
+  (void)ws_bytes;
   if (B < 0 || total_rows < 0 || max_q_len < 0 || max_kv < 0) return KINV_ERR_INVALID_ARG;
   if (B == 0 || total_rows == 0 || max_q_len == 0) return KINV_OK;
   if (!q_start || !q_len || !q_offset || max_kv <= 0) return KINV_ERR_INVALID_ARG;
-  kinv_status st = check_common(q, k_cache, v_cache, seq_stride, tok_stride, out, Hq, Hkv, D,
-                                split_len, workspace);
+  // no workspace is used; an aligned stand-in keeps the shared checks
+  const void* aligned_placeholder = reinterpret_cast<const void*>(static_cast<uintptr_t>(256));
+  kinv_status st = check_common(q, k_cache, v_cache, seq_stride, tok_stride, out, Hq, Hkv, D, split_len,
+                                workspace ? workspace : aligned_placeholder);
   if (st != KINV_OK) return st;
-  const int S = (max_kv + kSplit - 1) / kSplit;
-  if (ws_bytes < workspace_bytes(total_rows, Hq, D, S)) return KINV_ERR_WORKSPACE;
-  AttnParams p{};
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k = static_cast<const __nv_bfloat16*>(k_cache);
-  p.v = static_cast<const __nv_bfloat16*>(v_cache);
-  p.seq_stride = seq_stride;
-  p.tok_stride = tok_stride;
-  p.q_start = q_start;
-  p.q_len = q_len;
-  p.q_offset = q_offset;
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.ws_o = static_cast<float*>(workspace);
-  const size_t o_bytes = static_cast<size_t>(total_rows) * Hq * S * D * 4;
-  p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
-  p.prefill = 1;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.G = Hq / Hkv;
-  p.R = kRowsMma * kPrefillTiles / p.G;
-  p.S = S;
-  p.groups_per_seq = (max_q_len + p.R - 1) / p.R;
-  p.rg_cap = p.R * p.G;
-  p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
-  p.max_len = max_kv;
-  p.max_q_len = max_q_len;
-  p.total_rows = total_rows;
-  p.status = device_status_word();
-  const int64_t groups = static_cast<int64_t>(B) * p.groups_per_seq;
-  if (groups > 65535 || max_q_len > 65535 || B > 65535) return KINV_ERR_UNSUPPORTED;
-  const dim3 split_grid(Hkv, S, static_cast<unsigned>(groups)), merge_grid(Hq, max_q_len, B);
-  return D == 128 ? launch<128, kPrefillTiles>(p, split_grid, merge_grid, stream)
-                  : launch<64, kPrefillTiles>(p, split_grid, merge_grid, stream);
+  PrefillTcArgs a{};
+  a.q_start = q_start;
+  a.q_len = q_len;
+  a.q_offset = q_offset;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = Hq / Hkv;
+  a.RT = kTcPairs / a.G;
+  a.tiles_per_seq = (max_q_len + a.RT - 1) / a.RT;
+  a.max_len = max_kv;
+  a.max_q_len = max_q_len;
+  a.total_rows = total_rows;
+  a.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
+  a.status = device_status_word();
+  if (a.tiles_per_seq > 65535 || B > 65535) return KINV_ERR_UNSUPPORTED;
+  if (B > 1 && seq_stride <= 0) return KINV_ERR_INVALID_ARG;
+  return D == 128 ? launch_prefill_tc<128>(q, k_cache, v_cache, seq_stride, tok_stride, a, B, stream)
+                  : launch_prefill_tc<64>(q, k_cache, v_cache, seq_stride, tok_stride, a, B, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -45,6 +45,7 @@ enum : int {
   DEV_SAMPLER_UNSUPPORTED = dev_code(4, KINV_ERR_UNSUPPORTED),
   DEV_TIMEOUT_TEST = dev_code(5, KINV_ERR_TIMEOUT),
   DEV_ATTN_BAD_LENGTH = dev_code(6, KINV_ERR_INVALID_ARG),
+  DEV_TIMEOUT_ATTN = dev_code(7, KINV_ERR_TIMEOUT),
 };
 
 // ---------------------------------------------------------------- device side
@@ -133,6 +134,28 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
       ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// 4-D tiled TMA load: coordinates (x, y, z, w), x innermost.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int x, int y, int z, int w,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Arrive once on a barrier of this CTA.
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Shared-memory writes of this thread become visible to the asynchronous
+// proxy (the tensor cores' operand reads) once the reader has synchronised
+// with it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
