@@ -470,11 +470,14 @@ __global__ void attn_merge_kernel(const AttnParams p) {
 //   O = P_hi . V + P_lo . V, each sixteen 16-key steps ascending from zero
 // and then folds as the merge kernel does; out = bf16(o / l).  So a prompt
 // row has the bits of the decode step at its position.
-// Roles (192 threads): warps 0-3 take one pair per thread (TMEM lane = pair):
-// the softmax, the P tiles and the fold; warp 4 lane 0 issues the MMAs; warp
-// 5 issues the TMA loads of Q, K and V and zeroes V rows past the tile's last
-// visible key.  Tensor memory: S in columns 0-255, O_hi and O_lo after it.
-constexpr int kTcThreads = 192;
+// Roles (320 threads): warps 0-7 take the pairs (TMEM lane = pair), two
+// threads per pair: warp w handles keys 128 (w / 4) .. + 127 of each split
+// and output columns D/2 (w / 4) .. + D/2 - 1 of the fold; the two exchange
+// their maxima and 32-key group sums through shared memory, so the sums keep
+// their order.  Warp 8 lane 0 issues the MMAs; warp 9 issues the TMA loads of
+// Q, K and V and zeroes V rows past the tile's last visible key.  Tensor
+// memory: S in columns 0-255, O_hi and O_lo after it.
+constexpr int kTcThreads = 320;
 constexpr int kTcPairs = 128;
 
 struct PrefillTcArgs {
@@ -526,6 +529,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   unsigned char* p_s = v_s + KV_BYTES;         // [2 slots][hi, lo][P_BYTES]
   uint64_t* bars = reinterpret_cast<uint64_t*>(p_s + 4 * P_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  // the two threads of a pair exchange their maxima [2][128] and the running
+  // sum of l [128] (the first half's four groups, then the whole split's)
+  float* x_max = reinterpret_cast<float*>(tmem_slot + 4);
+  float* x_l = x_max + 2 * kTcPairs;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t q_full = smem_addr(bars + 0), k_full = smem_addr(bars + 1), k_empty = smem_addr(bars + 2);
   const uint32_t v_full = smem_addr(bars + 3), v_ready = smem_addr(bars + 4), v_empty = smem_addr(bars + 5);
@@ -558,13 +565,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // the softmax threads' signals take one arrival per pair, the rest one
     for (int i = 0; i < 15; ++i) {
       const uint32_t bar = smem_addr(bars + i);
-      const bool per_pair = bar == s_empty || bar == o_empty || bar == p_full(0) || bar == p_full(1);
-      mbar_init(bar, per_pair ? kTcPairs : 1);
+      // s_empty, o_empty: every softmax thread; p_full: the half that writes the chunk
+      const int count = (bar == s_empty || bar == o_empty) ? 2 * kTcPairs
+                        : (bar == p_full(0) || bar == p_full(1)) ? kTcPairs : 1;
+      mbar_init(bar, count);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4) tmem_alloc(smem_addr(tmem_slot), 512);
+  if (warp == 8) tmem_alloc(smem_addr(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -572,7 +581,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_launch_dependents();  // after the TMEM allocation (see the GEMM kernels)
   int* status = a.status;
 
-  if (warp == 5) {
+  if (warp == 9) {
     // ---- TMA: Q once, then K and V of each split; V rows past the tile's
     // last visible key are zeroed (stale cache rows may hold anything, and
     // their weight 0 times a NaN would not be 0)
@@ -625,7 +634,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (v_issued > 0) mbar_wait_bounded(v_full, (v_issued - 1) & 1u, nullptr, 0);
     }
     __syncwarp();
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ---- MMA issue
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc_idesc(kSplit, 0);
@@ -676,63 +685,103 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---- one (row, head) pair per thread
-    const int pr = t;                                    // pair = TMEM lane
+    // ---- two threads per (row, head) pair
+    const int pr = t & (kTcPairs - 1);                   // pair = TMEM lane
+    const int half = t >> 7;                             // keys 128 half .., columns D/2 half ..
     const int r = pr / a.G, hi_head = g * a.G + pr % a.G;
     const int len = len0 + r;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    float o_acc[D];
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    constexpr int DH = D / 2;
+    float o_acc[DH];
 #pragma unroll
-    for (int d = 0; d < D; ++d) o_acc[d] = 0.f;
+    for (int d = 0; d < DH; ++d) o_acc[d] = 0.f;
     float m_acc = -INFINITY, l_acc = 0.f;
-    int gc = 0;
     bool ok = true;
+    auto softmax_sync = []() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
     for (int s = 0; s < ns; ++s) {
       const uint32_t ph = s & 1;
       const int cnt = min(kSplit, len - s * kSplit);
+      // every pair of the tile sees the whole split: no key is masked
+      const bool whole = len0 - s * kSplit >= kSplit;
       ok = mbar_wait_bounded(s_full, ph, status, DEV_TIMEOUT_ATTN);
       if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
         *abort_flag = 1;
         ok = false;
+      }
+      softmax_sync();
+      if (*abort_flag) {
+        ok = false;
         break;
       }
       tc_fence_after();
-      // the maximum (exact in any order)
+      // the maximum (exact in any order): this thread's 128 keys, then the pair's
       float m = -INFINITY;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + 32 * c, v);
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          m = fmaxf(m, 32 * c + jj < cnt ? __fmul_rn(__uint_as_float(v[jj]), a.scale) : -INFINITY);
-      }
-      // weights, their sum, and the P tiles, 64 keys at a time
-      float l = 0.f;
-      for (int j = 0; j < 4; ++j, ++gc) {
-        const int slot = gc & 1;
-        ok = mbar_wait_bounded(p_empty(slot), ((gc >> 1) & 1u) ^ 1u, status, DEV_TIMEOUT_ATTN);
-        if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
-          *abort_flag = 1;
-          ok = false;
-          break;
-        }
-        unsigned char* phi = p_s + slot * 2 * P_BYTES;
-        unsigned char* plo = phi + P_BYTES;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c = 2 * j + h;  // 32-key group c: the decode kernel's warp c
-          uint32_t v[32];
-          tmem_ld32(lane_base + 32 * c, v);
-          float ph_[32], pl_[32];
+      for (int c = 4 * half; c < 4 * half + 4; c += 2) {
+        uint32_t v[32], w[32];
+        tmem_ld32_nowait(lane_base + 32 * c, v);
+        tmem_ld32_nowait(lane_base + 32 * c + 32, w);
+        tmem_ld_wait(v);
+        tmem_ld_wait(w);
+        if (whole) {
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
-            const float sc = 32 * c + jj < cnt ? __fmul_rn(__uint_as_float(v[jj]), a.scale) : -INFINITY;
-            const float x = sc == -INFINITY ? 0.f : expf(__fsub_rn(sc, m));
-            split_bf16(x, ph_[jj], pl_[jj]);
+            m = fmaxf(m, __fmul_rn(__uint_as_float(v[jj]), a.scale));
+            m = fmaxf(m, __fmul_rn(__uint_as_float(w[jj]), a.scale));
           }
-          // lane tq of the decode kernel adds keys 8nb + 2tq + e in (nb, e)
-          // order; a butterfly over tq; then the groups in order
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            m = fmaxf(m, 32 * c + jj < cnt ? __fmul_rn(__uint_as_float(v[jj]), a.scale) : -INFINITY);
+            m = fmaxf(m, 32 * c + 32 + jj < cnt ? __fmul_rn(__uint_as_float(w[jj]), a.scale) : -INFINITY);
+          }
+        }
+      }
+      x_max[half * kTcPairs + pr] = m;
+      softmax_sync();
+      m = fmaxf(x_max[pr], x_max[kTcPairs + pr]);
+      // weights, their group sums and this half's two P chunks
+      float wsum[4];
+      for (int jh = 0; jh < 2; ++jh) {
+        const int j = 2 * half + jh;                       // 64-key chunk of the split
+        const int gc = 4 * s + j;
+        const int slot = gc & 1;
+        unsigned char* phi = p_s + slot * 2 * P_BYTES;
+        unsigned char* plo = phi + P_BYTES;
+        uint32_t vv[2][32];
+        tmem_ld32_nowait(lane_base + 64 * j, vv[0]);
+        tmem_ld32_nowait(lane_base + 64 * j + 32, vv[1]);
+        tmem_ld_wait(vv[0]);
+        tmem_ld_wait(vv[1]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = 2 * j + h;  // 32-key group c
+          const uint32_t (&v)[32] = vv[h];
+          uint32_t hp[16], lp[16];  // bf16 pairs of the high and the low halves
+          float wl[32];             // hi + lo of each key
+#pragma unroll
+          for (int jj = 0; jj < 32; jj += 2) {
+            float x[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              if (whole) {
+                // every score finite or -inf with a finite maximum: exp gives the 0 the mask would
+                x[e] = expf(__fsub_rn(__fmul_rn(__uint_as_float(v[jj + e]), a.scale), m));
+              } else {
+                const float sc = 32 * c + jj + e < cnt ? __fmul_rn(__uint_as_float(v[jj + e]), a.scale) : -INFINITY;
+                x[e] = sc == -INFINITY ? 0.f : expf(__fsub_rn(sc, m));
+              }
+            }
+            const __nv_bfloat162 h2 = __float22bfloat162_rn(make_float2(x[0], x[1]));
+            const float h0 = __low2float(h2), h1 = __high2float(h2);
+            const __nv_bfloat162 l2 = __float22bfloat162_rn(make_float2(__fsub_rn(x[0], h0), __fsub_rn(x[1], h1)));
+            wl[jj] = __fadd_rn(h0, __low2float(l2));
+            wl[jj + 1] = __fadd_rn(h1, __high2float(l2));
+            hp[jj / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+            lp[jj / 2] = *reinterpret_cast<const uint32_t*>(&l2);
+          }
+          // the decode kernel's order: key 8nb + 2tq + e into partial tq in
+          // (nb, e) order, then (0 + 1) + (2 + 3)
           float sq[4];
 #pragma unroll
           for (int tq = 0; tq < 4; ++tq) {
@@ -740,54 +789,64 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int nb = 0; nb < 4; ++nb)
 #pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int k = 8 * nb + 2 * tq + e;
-                acc = __fadd_rn(acc, __fadd_rn(ph_[k], pl_[k]));
-              }
+              for (int e = 0; e < 2; ++e) acc = __fadd_rn(acc, wl[8 * nb + 2 * tq + e]);
             sq[tq] = acc;
           }
-          const float w = __fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3]));
-          l = c == 0 ? w : __fadd_rn(l, w);
+          wsum[2 * jh + h] = __fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3]));
+          if (h == 0) {
+            // the slot is free once the MMAs of the chunk two before have read it
+            ok = mbar_wait_bounded(p_empty(slot), ((gc >> 1) & 1u) ^ 1u, status, DEV_TIMEOUT_ATTN);
+            if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
+              *abort_flag = 1;
+              ok = false;
+            }
+          }
           // this pair's row of the two P tiles (keys 32h .. 32h + 31 of the chunk)
           const uint32_t row_off = static_cast<uint32_t>((pr >> 3) * 1024 + (pr & 7) * 128);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int unit = 4 * h + u;  // 16-byte unit of the 128-byte row
-            const uint32_t off = row_off + static_cast<uint32_t>(((unit ^ (pr & 7)) & 7) * 16);
-            *reinterpret_cast<uint4*>(phi + off) =
-                make_uint4(pack_bf16(ph_[8 * u + 0], ph_[8 * u + 1]), pack_bf16(ph_[8 * u + 2], ph_[8 * u + 3]),
-                           pack_bf16(ph_[8 * u + 4], ph_[8 * u + 5]), pack_bf16(ph_[8 * u + 6], ph_[8 * u + 7]));
-            *reinterpret_cast<uint4*>(plo + off) =
-                make_uint4(pack_bf16(pl_[8 * u + 0], pl_[8 * u + 1]), pack_bf16(pl_[8 * u + 2], pl_[8 * u + 3]),
-                           pack_bf16(pl_[8 * u + 4], pl_[8 * u + 5]), pack_bf16(pl_[8 * u + 6], pl_[8 * u + 7]));
+            const uint32_t off = row_off + static_cast<uint32_t>((((4 * h + u) ^ (pr & 7)) & 7) * 16);
+            *reinterpret_cast<uint4*>(phi + off) = make_uint4(hp[4 * u], hp[4 * u + 1], hp[4 * u + 2], hp[4 * u + 3]);
+            *reinterpret_cast<uint4*>(plo + off) = make_uint4(lp[4 * u], lp[4 * u + 1], lp[4 * u + 2], lp[4 * u + 3]);
           }
         }
         fence_proxy_async_smem();
         mbar_arrive(p_full(slot));
       }
-      if (!ok) break;
+      // l: the groups 0 .. 7 in order -- the first half adds its four, the
+      // second half continues with its four and hands the total back
+      if (half == 0) x_l[pr] = __fadd_rn(__fadd_rn(__fadd_rn(wsum[0], wsum[1]), wsum[2]), wsum[3]);
       tc_fence_before();
       mbar_arrive(s_empty);  // the scores have been read
-      // fold this split's (m, l, o) into the running state (the merge kernel's arithmetic)
+      softmax_sync();
+      if (half == 1) {
+        float lt = x_l[pr];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) lt = __fadd_rn(lt, wsum[q]);
+        x_l[pr] = lt;
+      }
+      softmax_sync();
+      const float l = x_l[pr];
+      // fold this split's (m, l, o) into the running state (the merge
+      // kernel's arithmetic), this thread's D/2 output columns
       ok = mbar_wait_bounded(o_full, ph, status, DEV_TIMEOUT_ATTN);
       if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
         *abort_flag = 1;
         ok = false;
-        break;
       }
       tc_fence_after();
       const bool in = cnt > 0;
       const float m_new = fmaxf(m_acc, m);
       const float fa = expf(__fsub_rn(m_acc, m_new));
       const float fc = expf(__fsub_rn(m, m_new));
-      if (in) {
-        l_acc = __fadd_rn(__fmul_rn(l_acc, fa), __fmul_rn(l, fc));
-      }
+      if (in) l_acc = __fadd_rn(__fmul_rn(l_acc, fa), __fmul_rn(l, fc));
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < DH / 32; ++c) {
         uint32_t vh[32], vl[32];
-        tmem_ld32(lane_base + 256 + 32 * c, vh);
-        tmem_ld32(lane_base + 256 + D + 32 * c, vl);
+        tmem_ld32_nowait(lane_base + 256 + half * DH + 32 * c, vh);
+        tmem_ld32_nowait(lane_base + 256 + D + half * DH + 32 * c, vl);
+        tmem_ld_wait(vh);
+        tmem_ld_wait(vl);
         if (in) {
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
@@ -801,9 +860,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_arrive(o_empty);
     }
     if (ok && r < nrows) {
-      __nv_bfloat16* dst = a.out + (static_cast<int64_t>(row0 + r) * a.Hq + hi_head) * D;
+      __nv_bfloat16* dst = a.out + (static_cast<int64_t>(row0 + r) * a.Hq + hi_head) * D + half * DH;
 #pragma unroll
-      for (int d = 0; d < D; d += 8) {
+      for (int d = 0; d < DH; d += 8) {
         uint4 o;
         o.x = pack_bf16(__fdiv_rn(o_acc[d + 0], l_acc), __fdiv_rn(o_acc[d + 1], l_acc));
         o.y = pack_bf16(__fdiv_rn(o_acc[d + 2], l_acc), __fdiv_rn(o_acc[d + 3], l_acc));
@@ -815,7 +874,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -824,7 +883,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 template <int D>
 size_t prefill_tc_smem_bytes() {
   return 1024 + static_cast<size_t>(D / 64) * kTcPairs * 128 + 2 * static_cast<size_t>(D / 64) * kSplit * 128 +
-         4 * static_cast<size_t>(kTcPairs) * 128 + 16 * 8 + 16;
+         4 * static_cast<size_t>(kTcPairs) * 128 + 16 * 8 + 16 + 3 * kTcPairs * 4;
 }
 
 template <int D>
