@@ -198,17 +198,20 @@ kinv_status kinv_rmsnorm(void* x, int64_t ldx, const void* residual,
 /* ------------------------------------------------------ decode attention
  * out[b][h] = sum_{j < L_b} softmax_j(scale * q[b][h] . k[b][j][g]) v[b][j][g],
  * g = h / (Hq / Hkv)  ("Deterministic and bit-exact inference", *technical*:
- * batch-invariant attention with a fixed split size of the key/value
- * dimension rather than a fixed number of splits).
+ * attention is batch-invariant when the keys are cut into splits of one fixed
+ * length, whatever their number).
  *
  * Keys of sequence b are cut into splits of `split_len` keys at absolute
  * offsets 0, split_len, 2 split_len, ...; each split yields an fp32 partial
  * (max, sum of exponentials, unnormalised output) and the partials are folded
  * in ascending split order.  The cut depends only on L_b, so a sequence's bits
  * do not depend on its batch-mates or their lengths.  L_b == 0 gives zeros.
- * Within a split the softmax weights e = exp(s - max) are formed in fp32 and
- * enter the tensor cores as the bf16 pair hi = bf16(e), lo = bf16(e - hi)
- * (P.V = hi.V + lo.V, each in fp32), so they keep about 16 significant bits.
+ * Within a split the softmax is taken in base 2: with r = q . k (fp32) and
+ * c = fp32(scale * log2 e), m = fp32(max r * c) and the weights
+ * e = 2^fma(r, c, -m) (the hardware's approximate exp2) are formed in fp32,
+ * summed in fp32, and enter the tensor cores as the bf16 pair hi = bf16(e),
+ * lo = bf16(e - hi), so they keep about 16 significant bits; P.V is one fp32
+ * chain over 16-key steps, each adding its hi . V, then its lo . V.
  *
  * q, out: device bf16 [B][Hq][D] (contiguous).  k_cache, v_cache: device bf16;
  *   element (b, j, g, d) is at b*seq_stride + j*tok_stride + g*D + d
@@ -220,7 +223,8 @@ kinv_status kinv_rmsnorm(void* x, int64_t ldx, const void* residual,
  * workspace: device, at least kinv_attn_decode_workspace(B, Hq, D, Lmax,
  *   split_len) bytes, 16-byte aligned.
  * Requirements: D in {64, 128}; Hq % Hkv == 0; Hq / Hkv in {1, 2, 4, 8};
- * split_len == 256; strides multiples of 8.  scale <= 0 means 1/sqrt(D). */
+ * split_len == 256; strides multiples of 8.  A scale that is not a positive
+ * finite number means 1/sqrt(D). */
 size_t kinv_attn_decode_workspace(int B, int Hq, int D, int Lmax, int split_len);
 kinv_status kinv_attn_decode(const void* q, const void* k_cache, const void* v_cache,
                              int64_t seq_stride, int64_t tok_stride,

@@ -100,13 +100,18 @@ int* device_status_word() {
 }
 
 kinv_status ensure_smem(const void* kernel, size_t bytes) {
-  if (bytes <= 48 * 1024) return KINV_OK;
+  // without the attribute a block may hold 48 KB of static and dynamic
+  // shared memory together
+  if (bytes == 0) return KINV_OK;
   std::lock_guard<std::mutex> lock(g_ctx_mu);
   const auto key = std::make_pair(context_id(), kernel);
   auto it = g_smem_by_ctx.find(key);
   if (key.first != 0 && it != g_smem_by_ctx.end() && it->second >= bytes) return KINV_OK;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
-      cudaSuccess)
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return KINV_ERR_CUDA;
+  if (bytes + fa.sharedSizeBytes > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
+          cudaSuccess)
     return KINV_ERR_CUDA;
   if (key.first != 0) g_smem_by_ctx[key] = bytes;
   return KINV_OK;

@@ -1,27 +1,28 @@
 // Batch-invariant split-KV attention for decode and prefill
-// ("Deterministic and bit-exact inference", *technical*: attention made
-// batch-invariant "with a fixed split size for the key-value dimension rather
-// than a fixed number of splits").
+// ("Deterministic and bit-exact inference", *technical*: attention is made
+// batch-invariant by cutting the keys into splits of one fixed length, not
+// into a fixed number of splits).
 //
 // A query row with L visible keys cuts them into splits of 256 keys at
-// absolute offsets 0, 256, 512, ...; the cut depends only on L.  For every
-// (row, query head) pair and split:
-//   s_t  = (q . k_t) * scale   sixteen-deep tensor-core steps over d,
+// absolute offsets 0, 256, 512, ...; the cut depends only on L.  The softmax
+// is taken in base 2 (2^(x log2 e) = e^x, the form FlashAttention uses), with
+// c = fp32(scale * log2 e).  For every (row, query head) pair and split:
+//   r_t  = q . k_t             sixteen-deep tensor-core steps over d,
 //                              ascending, accumulated in fp32
-//   m    = max_t s_t           (max is exact in any order)
-//   e_t  = exp(s_t - m)        in fp32, then carried as the bf16 pair
+//   m    = fp32(max_t r_t * c) (max is exact in any order, and rounding a
+//                              product by c > 0 keeps the order)
+//   e_t  = 2^fma(r_t, c, -m)   ex2.approx; then carried as the bf16 pair
 //   hi_t = bf16(e_t), lo_t = bf16(e_t - hi_t)   (about 16 significant bits)
-//   l    = sum_t (hi_t + lo_t) in 32-key groups: within a group key
+//   l    = sum_t e_t           in 32-key groups: within a group key
 //                              8nb + 2tq + e is added to partial tq in (nb, e)
 //                              order, the partials (0 + 1) + (2 + 3), the
 //                              groups in order
-//   o[d] = sum_t hi_t v_t[d] + sum_t lo_t v_t[d]
-//                              each sum sixteen 16-key steps, ascending, in
-//                              fp32; the two sums added once at the end
-// and the splits are folded in ascending order with the log-sum-exp update,
-// then o / l -> bf16.  A key a pair cannot see gets weight 0; keys past the
-// split's end read zero V.  A pair's bits depend only on its own q row and
-// its sequence's keys and values.
+//   o[d] = one fp32 chain over sixteen 16-key steps, ascending; each step
+//          adds its hi . v, then its lo . v
+// and the splits are folded in ascending order with the log-sum-exp update
+// (factors 2^(m_old - m_new), 2^(m_split - m_new)), then o / l -> bf16.  A key
+// a pair cannot see gets weight 0; keys past the split's end read zero V.  A
+// pair's bits depend only on its own q row and its sequence's keys and values.
 //
 // Decode (one new row per sequence): the split kernel, one block (eight
 // warps, warp-level mma.sync m16n8k16) per (split, kv head, sequence), stores
@@ -34,6 +35,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
+
+#include <cmath>
 
 #include <mutex>
 
@@ -64,7 +67,7 @@ struct AttnParams {
   int S;                    // splits per row in the workspace
   int groups_per_seq;       // prefill: ceil(max_q_len / R)
   int rg_cap;               // R * G: sizes the query and weight buffers
-  float scale;
+  float c2;                 // fp32(scale * log2 e) > 0
   // bounds the device-side lengths must keep (the host cannot read them):
   // decode 0 <= kv_len[b] <= max_len; prefill 0 <= q_len[b] <= max_q_len,
   // 0 <= q_start[b] <= max_len - q_len[b], 0 <= q_offset[b] <= total_rows - q_len[b]
@@ -177,7 +180,8 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   // phase fall in eight different bank groups.
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(smem_raw);                 // [256][D]
-  __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(smem_raw + kSplit * D * 2);  // P [16][256]
+  __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(smem_raw + kSplit * D * 2);  // P_hi [16][256]
+  __nv_bfloat16* pt_lo = pt + kRowsMma * kSplit;                                      // P_lo [16][256]
   __shared__ float wmax[kThreads / 32][kRowsMma];
   __shared__ float wsum[kThreads / 32][kRowsMma];
 
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   const int gq = lane >> 2, tq = lane & 3;             // fragment row / column group
   const int64_t seq_off = rs.seq * p.seq_stride + static_cast<int64_t>(k0) * p.tok_stride + g * D;
   const uint32_t kv_base = smem_addr(kv);
-  const uint32_t pt_base = smem_addr(pt);
+  const uint32_t pt_base = smem_addr(pt), pt_lo_base = smem_addr(pt_lo);
   auto count = [&](int r) { return r < RG ? min(kSplit, rs.len0 + r / G - k0) : 0; };
 
   auto load_sub = [&](const __nv_bfloat16* src, int j) {
@@ -264,10 +268,10 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   cp_async_commit();
 
   // --- softmax statistics.  A lane holds rows gq and gq + 8, keys
-  // 32w + 8nb + 2tq (+1).  Maxima: lane, then the four lanes of a row
-  // (exact), then the eight warps.  Weights are rounded to bf16 once; the sum
-  // adds the rounded weights: a lane's eight in (nb, pair) order, a fixed
-  // butterfly over the four lanes, the eight warps in ascending order.
+  // 32w + 8nb + 2tq (+1).  Maxima of the raw scores: lane, then the four
+  // lanes of a row (exact), then the eight warps; m = fp32(max * c).  The sum
+  // adds the weights e: a lane's eight in (nb, pair) order, a fixed butterfly
+  // over the four lanes, the eight warps in ascending order.
   const int cnt_lo = count(gq), cnt_hi = count(gq + 8);
   float mx_lo = -INFINITY, mx_hi = -INFINITY;
 #pragma unroll
@@ -275,10 +279,8 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int key = warp * 32 + nb * 8 + 2 * tq + e;
-      sc[nb][e] = key < cnt_lo ? __fmul_rn(sc[nb][e], p.scale) : -INFINITY;
-      sc[nb][2 + e] = key < cnt_hi ? __fmul_rn(sc[nb][2 + e], p.scale) : -INFINITY;
-      mx_lo = fmaxf(mx_lo, sc[nb][e]);
-      mx_hi = fmaxf(mx_hi, sc[nb][2 + e]);
+      if (key < cnt_lo) mx_lo = fmaxf(mx_lo, sc[nb][e]);
+      if (key < cnt_hi) mx_hi = fmaxf(mx_hi, sc[nb][2 + e]);
     }
   }
 #pragma unroll
@@ -297,32 +299,36 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
     m_lo = fmaxf(m_lo, wmax[w][gq]);
     m_hi = fmaxf(m_hi, wmax[w][gq + 8]);
   }
+  m_lo = __fmul_rn(m_lo, p.c2);
+  m_hi = __fmul_rn(m_hi, p.c2);
   float sum_lo = 0.f, sum_hi = 0.f;
-  // writes the weights held in w[nb][0..3] (rows gq and gq + 8) into P's tile
-  auto write_p = [&](const float (&w)[4][4]) {
+  // writes the weights held in w[nb][0..3] (rows gq and gq + 8) into a P tile
+  auto write_p = [&](__nv_bfloat16* tile, const float (&w)[4][4]) {
 #pragma unroll
     for (int nb = 0; nb < 4; ++nb) {
       const int kc = warp * 4 + nb;                       // 8-key chunk of P
       const uint32_t off_lo = static_cast<uint32_t>(gq * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
       const uint32_t off_hi = static_cast<uint32_t>((gq + 8) * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
-      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_lo) = pack_bf16(w[nb][0], w[nb][1]);
-      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off_hi) = pack_bf16(w[nb][2], w[nb][3]);
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(tile) + off_lo) = pack_bf16(w[nb][0], w[nb][1]);
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(tile) + off_hi) = pack_bf16(w[nb][2], w[nb][3]);
     }
   };
-  float hi[4][4];  // the high halves; sc keeps the low halves for the second pass
+  float hi[4][4];  // the high halves; sc takes the low halves
 #pragma unroll
   for (int nb = 0; nb < 4; ++nb) {
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const float xl = sc[nb][e] == -INFINITY ? 0.f : expf(__fsub_rn(sc[nb][e], m_lo));
-      const float xh = sc[nb][2 + e] == -INFINITY ? 0.f : expf(__fsub_rn(sc[nb][2 + e], m_hi));
+      const int key = warp * 32 + nb * 8 + 2 * tq + e;
+      const float xl = key < cnt_lo ? ex2_approx(__fmaf_rn(sc[nb][e], p.c2, -m_lo)) : 0.f;
+      const float xh = key < cnt_hi ? ex2_approx(__fmaf_rn(sc[nb][2 + e], p.c2, -m_hi)) : 0.f;
       split_bf16(xl, hi[nb][e], sc[nb][e]);
       split_bf16(xh, hi[nb][2 + e], sc[nb][2 + e]);
-      sum_lo = __fadd_rn(sum_lo, __fadd_rn(hi[nb][e], sc[nb][e]));
-      sum_hi = __fadd_rn(sum_hi, __fadd_rn(hi[nb][2 + e], sc[nb][2 + e]));
+      sum_lo = __fadd_rn(sum_lo, xl);
+      sum_hi = __fadd_rn(sum_hi, xh);
     }
   }
-  write_p(hi);
+  write_p(pt, hi);
+  write_p(pt_lo, sc);
 #pragma unroll
   for (int o = 1; o <= 2; o <<= 1) {
     sum_lo = __fadd_rn(sum_lo, __shfl_xor_sync(0xffffffffu, sum_lo, o));
@@ -336,22 +342,23 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   __syncthreads();
 
   // --- o = P . V: warp w owns columns 16w .. 16w + 15 (two 8-wide n
-  // blocks) over all 256 keys, sixteen k steps of 16 keys in ascending order;
-  // once over the high halves of P, once over the low halves.
-  auto pv = [&](float (&acc)[2][4]) {
+  // blocks) over all 256 keys: sixteen k steps of 16 keys in ascending order,
+  // each adding its high halves, then its low halves, to one fp32 chain.
+  float oc[2][4];
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb)
+  for (int nb = 0; nb < 2; ++nb)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[nb][i] = 0.f;
-    if (warp >= D / 16) return;
+    for (int i = 0; i < 4; ++i) oc[nb][i] = 0.f;
+  if (warp < D / 16) {
 #pragma unroll 4
     for (int kk = 0; kk < kSplit / 16; ++kk) {
-      uint32_t a[4];
+      uint32_t ah[4], al[4];
       {
         const int prow = lane & 15;
         const int kc = 2 * kk + (lane >> 4);
-        ldsm_x4(pt_base + static_cast<uint32_t>(prow * kSplit * 2 + ((kc ^ (prow & 7)) << 4)), a[0], a[1],
-                a[2], a[3]);
+        const uint32_t off = static_cast<uint32_t>(prow * kSplit * 2 + ((kc ^ (prow & 7)) << 4));
+        ldsm_x4(pt_base + off, ah[0], ah[1], ah[2], ah[3]);
+        ldsm_x4(pt_lo_base + off, al[0], al[1], al[2], al[3]);
       }
       uint32_t b0, b1, b2, b3;
       {
@@ -359,16 +366,12 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
         const int c = warp * 2 + (lane >> 4);
         ldsm_x4_t(kv_base + static_cast<uint32_t>(key * D * 2 + ((c ^ (key & 7)) << 4)), b0, b1, b2, b3);
       }
-      mma_bf16_16816(acc[0], a, b0, b1);
-      mma_bf16_16816(acc[1], a, b2, b3);
+      mma_bf16_16816(oc[0], ah, b0, b1);
+      mma_bf16_16816(oc[1], ah, b2, b3);
+      mma_bf16_16816(oc[0], al, b0, b1);
+      mma_bf16_16816(oc[1], al, b2, b3);
     }
-  };
-  float oc[2][4], ol[2][4];
-  pv(oc);
-  __syncthreads();  // every warp is done with the high halves
-  write_p(sc);
-  __syncthreads();
-  pv(ol);
+  }
   if (warp < D / 16) {
     // rows gq and gq + 8, columns 16w + 8nb + 2tq (+1)
 #pragma unroll
@@ -380,7 +383,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
 #pragma unroll
         for (int nb = 0; nb < 2; ++nb)
           *reinterpret_cast<float2*>(p.ws_o + base * D + warp * 16 + nb * 8 + 2 * tq) =
-              make_float2(__fadd_rn(oc[nb][2 * h], ol[nb][2 * h]), __fadd_rn(oc[nb][2 * h + 1], ol[nb][2 * h + 1]));
+              make_float2(oc[nb][2 * h], oc[nb][2 * h + 1]);
         if (warp == 0 && tq == 0) {
           float l = wsum[0][r];
 #pragma unroll
@@ -444,8 +447,8 @@ __global__ void attn_merge_kernel(const AttnParams p) {
     for (int i = 0; i < CH; ++i) {
       if (s0 + i < ns) {
         const float m_new = fmaxf(m_acc, mv[i]);
-        const float a = expf(__fsub_rn(m_acc, m_new));
-        const float c = expf(__fsub_rn(mv[i], m_new));
+        const float a = ex2_approx(__fsub_rn(m_acc, m_new));
+        const float c = ex2_approx(__fsub_rn(mv[i], m_new));
         l_acc = __fadd_rn(__fmul_rn(l_acc, a), __fmul_rn(lv[i], c));
         o_acc = __fadd_rn(__fmul_rn(o_acc, a), __fmul_rn(ov[i], c));
         m_acc = m_new;
@@ -462,23 +465,33 @@ __global__ void attn_merge_kernel(const AttnParams p) {
 // ascending order and folds each split into a running (m, l, o) per pair in
 // registers with the merge kernel's arithmetic, so no partial goes to memory.
 // Per pair and split it computes what attn_split_kernel computes:
-//   S = Q . K^T         tcgen05 128 x 256 x 16 steps over the head dimension,
+//   R = Q . K^T         tcgen05 128 x 64 x 16 steps over the head dimension,
 //                       ascending, fp32 in tensor memory (the per-element
-//                       result of a 16-deep step equals mma.sync's)
-//   scores, max, e = exp(s - m), hi / lo split, l in the same order (a key's
-//   32-key group in the decode kernel's lane order, the groups in order)
-//   O = P_hi . V + P_lo . V, each sixteen 16-key steps ascending from zero
+//                       result of a 16-deep step equals mma.sync's), four
+//                       64-key chunks
+//   max, e = 2^fma(r, c, -m), hi / lo, l in the decode kernel's order
+//   O = P . V           one chain of sixteen 16-key steps, each the hi step
+//                       then the lo step, P read from tensor memory
 // and then folds as the merge kernel does; out = bf16(o / l).  So a prompt
 // row has the bits of the decode step at its position.
 // Roles (320 threads): warps 0-7 take the pairs (TMEM lane = pair), two
 // threads per pair: warp w handles keys 128 (w / 4) .. + 127 of each split
-// and output columns D/2 (w / 4) .. + D/2 - 1 of the fold; the two exchange
-// their maxima and 32-key group sums through shared memory, so the sums keep
-// their order.  Warp 8 lane 0 issues the MMAs; warp 9 issues the TMA loads of
-// Q, K and V and zeroes V rows past the tile's last visible key.  Tensor
-// memory: S in columns 0-255, O_hi and O_lo after it.
+// (chunks 2 (w / 4) and 2 (w / 4) + 1) and output columns D/2 (w / 4) ..
+// + D/2 - 1 of the fold; the two exchange their maxima and 32-key group sums
+// through shared memory, so the sums keep their order.  Warp 8 lane 0 issues
+// the MMAs; warp 9 issues the TMA loads of Q, K and V and zeroes V rows past
+// the tile's last visible key.
+// Tensor memory: R of a split in columns 0-255 (chunk j at 64 j); once a
+// thread has read its chunk it writes the chunk's P there as packed bf16
+// pairs (32-key group h of the chunk: hi at 64 j + 32 h, lo 16 columns
+// further), which the PV MMAs read as their A operand; O in two buffers after
+// it, so split s + 1's PV runs while split s is folded.  The MMA thread
+// issues split s + 1's R chunk j right after split s's PV chunk j (the MMAs
+// run in issue order, so the chunk's P is read before R overwrites it), and
+// the softmax threads fold split s after writing split s + 1's P.
 constexpr int kTcThreads = 320;
 constexpr int kTcPairs = 128;
+constexpr int kTcBars = 17;
 
 struct PrefillTcArgs {
   const int32_t* q_start;
@@ -488,7 +501,7 @@ struct PrefillTcArgs {
   int Hq, Hkv, G, RT;  // RT rows per tile (128 / G)
   int tiles_per_seq;
   int max_len, max_q_len, total_rows;
-  float scale;
+  float c2;            // fp32(scale * log2 e) > 0
   int* status;
 };
 
@@ -516,31 +529,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const PrefillTcArgs a) {
   constexpr int DS = D / 64;                   // 64-wide slices of the head dimension
-  constexpr int Q_BYTES = DS * kTcPairs * 128; // [slice][128 pairs][64]
+  constexpr int Q_SLICE = kTcPairs * 128;      // [128 pairs][64]
+  constexpr int Q_BYTES = DS * Q_SLICE;
   constexpr int KV_SLICE = kSplit * 128;       // [256 keys][64] per slice
   constexpr int KV_BYTES = DS * KV_SLICE;
-  constexpr int P_BYTES = kTcPairs * 128;      // [128 pairs][64 keys]
+  constexpr int DH = D / 2;                    // output columns per thread
   extern __shared__ __align__(16) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char* q_s = base;
   unsigned char* k_s = q_s + Q_BYTES;
   unsigned char* v_s = k_s + KV_BYTES;
-  unsigned char* p_s = v_s + KV_BYTES;         // [2 slots][hi, lo][P_BYTES]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(p_s + 4 * P_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-  // the two threads of a pair exchange their maxima [2][128] and the running
-  // sum of l [128] (the first half's four groups, then the whole split's)
-  float* x_max = reinterpret_cast<float*>(tmem_slot + 4);
-  float* x_l = x_max + 2 * kTcPairs;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(v_s + KV_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kTcBars + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // the two threads of a pair exchange their raw maxima [2][128] and their
+  // 32-key group sums [8][128]
+  float* x_max = reinterpret_cast<float*>(tmem_slot + 4);
+  float* x_w = x_max + 2 * kTcPairs;
   const uint32_t q_full = smem_addr(bars + 0), k_full = smem_addr(bars + 1), k_empty = smem_addr(bars + 2);
   const uint32_t v_full = smem_addr(bars + 3), v_ready = smem_addr(bars + 4), v_empty = smem_addr(bars + 5);
-  const uint32_t s_full = smem_addr(bars + 6), s_empty = smem_addr(bars + 7);
-  const uint32_t o_full = smem_addr(bars + 8), o_empty = smem_addr(bars + 9);
-  auto p_full = [&](int slot) { return smem_addr(bars + 10 + slot); };
-  auto p_empty = [&](int slot) { return smem_addr(bars + 12 + slot); };
-  const uint32_t done_bar = smem_addr(bars + 14);
+  auto s_full = [&](int h) { return smem_addr(bars + 6 + h); };     // R chunks 2h, 2h + 1 written
+  auto p_full = [&](int j) { return smem_addr(bars + 8 + j); };     // P chunk j written
+  auto o_full = [&](int i) { return smem_addr(bars + 12 + i); };    // O buffer i complete
+  auto o_empty = [&](int i) { return smem_addr(bars + 14 + i); };   // O buffer i read
+  const uint32_t done_bar = smem_addr(bars + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
   const int g = blockIdx.y;
@@ -562,13 +575,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int ns = (len_last + kSplit - 1) / kSplit;
 
   if (t == 0) {
-    // the softmax threads' signals take one arrival per pair, the rest one
-    for (int i = 0; i < 15; ++i) {
-      const uint32_t bar = smem_addr(bars + i);
-      // s_empty, o_empty: every softmax thread; p_full: the half that writes the chunk
-      const int count = (bar == s_empty || bar == o_empty) ? 2 * kTcPairs
-                        : (bar == p_full(0) || bar == p_full(1)) ? kTcPairs : 1;
-      mbar_init(bar, count);
+    for (int i = 0; i < kTcBars; ++i) {
+      // p_full: the 128 threads of the half that writes the chunk; o_empty:
+      // all 256 softmax threads; the rest one arrival (a thread or a commit)
+      const int count = (i >= 8 && i < 12) ? kTcPairs : (i == 14 || i == 15) ? 2 * kTcPairs : 1;
+      mbar_init(smem_addr(bars + i), count);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -582,38 +593,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   int* status = a.status;
 
   if (warp == 9) {
-    // ---- TMA: Q once, then K and V of each split; V rows past the tile's
-    // last visible key are zeroed (stale cache rows may hold anything, and
-    // their weight 0 times a NaN would not be 0)
+    // ---- TMA: Q once; K of split s + 1 as soon as split s's R MMAs are
+    // done, V of split s + 1 as soon as split s's PV MMAs are done.  V rows
+    // past the tile's last visible key are zeroed (stale cache rows may hold
+    // anything, and their weight 0 times a NaN would not be 0).
     const uint64_t pol = l2_policy_evict_last();
     bool stop = false;
     int k_issued = 0, v_issued = 0;  // splits whose K / V loads were issued
+    auto load_k = [&](int s) {
+      mbar_arrive_expect_tx(k_full, KV_BYTES);
+      for (int ds = 0; ds < DS; ++ds)
+        tma_load_4d(smem_addr(k_s + ds * KV_SLICE), &tmK, 64 * ds, g, s * kSplit, b, k_full, pol);
+      k_issued = s + 1;
+    };
+    auto load_v = [&](int s) {
+      mbar_arrive_expect_tx(v_full, KV_BYTES);
+      for (int ds = 0; ds < DS; ++ds)
+        tma_load_4d(smem_addr(v_s + ds * KV_SLICE), &tmV, 64 * ds, g, s * kSplit, b, v_full, pol);
+      v_issued = s + 1;
+    };
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
       mbar_arrive_expect_tx(q_full, Q_BYTES);
       for (int ds = 0; ds < DS; ++ds)
-        tma_load_3d(smem_addr(q_s + ds * kTcPairs * 128), &tmQ, 64 * ds, g * a.G, row0, q_full, pol);
+        tma_load_3d(smem_addr(q_s + ds * Q_SLICE), &tmQ, 64 * ds, g * a.G, row0, q_full, pol);
+      load_k(0);
+      load_v(0);
     }
     for (int s = 0; s < ns && !stop; ++s) {
       const uint32_t ph = s & 1;
       if (lane == 0) {
-        bool ok = !*abort_flag && mbar_wait_bounded(k_empty, ph ^ 1u, status, DEV_TIMEOUT_ATTN);
-        if (ok) {
-          mbar_arrive_expect_tx(k_full, KV_BYTES);
-          for (int ds = 0; ds < DS; ++ds)
-            tma_load_4d(smem_addr(k_s + ds * KV_SLICE), &tmK, 64 * ds, g, s * kSplit, b, k_full, pol);
-          k_issued = s + 1;
-          ok = !*abort_flag && mbar_wait_bounded(v_empty, ph ^ 1u, status, DEV_TIMEOUT_ATTN);
+        bool ok = true;
+        if (s + 1 < ns) {
+          ok = !*abort_flag && mbar_wait_bounded(k_empty, ph, status, DEV_TIMEOUT_ATTN);
+          if (ok) load_k(s + 1);
         }
-        if (ok) {
-          mbar_arrive_expect_tx(v_full, KV_BYTES);
-          for (int ds = 0; ds < DS; ++ds)
-            tma_load_4d(smem_addr(v_s + ds * KV_SLICE), &tmV, 64 * ds, g, s * kSplit, b, v_full, pol);
-          v_issued = s + 1;
-          ok = mbar_wait_bounded(v_full, ph, status, DEV_TIMEOUT_ATTN);
-        }
+        if (ok) ok = mbar_wait_bounded(v_full, ph, status, DEV_TIMEOUT_ATTN);
         if (!ok) *abort_flag = 1;
       }
       stop = __shfl_sync(0xffffffffu, *abort_flag, 0) != 0;
@@ -625,7 +642,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(v_ready);
+      if (lane == 0) {
+        mbar_arrive(v_ready);
+        if (s + 1 < ns) {
+          const bool ok = !*abort_flag && mbar_wait_bounded(v_empty, ph, status, DEV_TIMEOUT_ATTN);
+          if (ok) load_v(s + 1);
+          else *abort_flag = 1;
+        }
+      }
     }
     if (lane == 0) {
       // loads still in flight (only after an abort) land before the block exits
@@ -635,49 +659,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else if (warp == 8) {
-    // ---- MMA issue
+    // ---- MMA issue: iteration s issues split s - 1's PV chunks and split
+    // s's R chunks, interleaved
     if (lane == 0) {
-      constexpr uint32_t idesc_s = tc_idesc(kSplit, 0);
+      constexpr uint32_t idesc_r = tc_idesc(64, 0);
       constexpr uint32_t idesc_o = tc_idesc(D, 1);
       bool ok = mbar_wait_bounded(q_full, 0, status, DEV_TIMEOUT_ATTN);
-      const uint32_t qa = smem_addr(q_s), ka = smem_addr(k_s), va = smem_addr(v_s), pa = smem_addr(p_s);
-      int gc = 0;  // P chunks issued so far
-      for (int s = 0; s < ns && ok; ++s) {
-        const uint32_t ph = s & 1;
-        ok = !*abort_flag && mbar_wait_bounded(k_full, ph, status, DEV_TIMEOUT_ATTN) &&
-             mbar_wait_bounded(s_empty, ph ^ 1u, status, DEV_TIMEOUT_ATTN);
+      const uint32_t qa = smem_addr(q_s), ka = smem_addr(k_s), va = smem_addr(v_s);
+      for (int s = 0; s <= ns && ok; ++s) {
+        const bool has_r = s < ns, has_pv = s > 0;
+        const int sp = s - 1;
+        const uint32_t o_col = tmem + 256 + static_cast<uint32_t>((sp & 1) * D);
+        if (has_pv)
+          ok = !*abort_flag && mbar_wait_bounded(v_ready, sp & 1, status, DEV_TIMEOUT_ATTN) &&
+               mbar_wait_bounded(o_empty(sp & 1), ((sp >> 1) & 1) ^ 1, status, DEV_TIMEOUT_ATTN);
+        if (ok && has_r) ok = !*abort_flag && mbar_wait_bounded(k_full, s & 1, status, DEV_TIMEOUT_ATTN);
         if (!ok) break;
         tc_fence_after();
+        for (int j = 0; j < 4; ++j) {
+          if (has_pv) {
+            ok = !*abort_flag && mbar_wait_bounded(p_full(j), sp & 1, status, DEV_TIMEOUT_ATTN);
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
-        for (int ds = 0; ds < DS; ++ds)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem, desc_k_sw128(qa + ds * kTcPairs * 128 + kk * 32),
-                      desc_k_sw128(ka + ds * KV_SLICE + kk * 32), idesc_s, (ds | kk) != 0 ? 1u : 0u);
-        umma_commit(k_empty);
-        umma_commit(s_full);
-        ok = !*abort_flag && mbar_wait_bounded(v_ready, ph, status, DEV_TIMEOUT_ATTN) &&
-             mbar_wait_bounded(o_empty, ph ^ 1u, status, DEV_TIMEOUT_ATTN);
-        if (!ok) break;
-        tc_fence_after();
-        for (int j = 0; j < 4 && ok; ++j, ++gc) {
-          const int slot = gc & 1;
-          ok = !*abort_flag && mbar_wait_bounded(p_full(slot), (gc >> 1) & 1u, status, DEV_TIMEOUT_ATTN);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t phi = pa + slot * 2 * P_BYTES, plo = phi + P_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t vdesc = desc_mn_sw128(va + (4 * j + kk) * 2048, KV_SLICE);
-            const uint32_t acc = (j | kk) != 0 ? 1u : 0u;
-            umma_bf16(tmem + 256, desc_k_sw128(phi + kk * 32), vdesc, idesc_o, acc);
-            umma_bf16(tmem + 256 + D, desc_k_sw128(plo + kk * 32), vdesc, idesc_o, acc);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t vdesc = desc_mn_sw128(va + (4 * j + kk) * 2048, KV_SLICE);
+              const uint32_t p_hi = tmem + static_cast<uint32_t>(64 * j + 32 * (kk >> 1) + 8 * (kk & 1));
+              umma_bf16_tmem_a(o_col, p_hi, vdesc, idesc_o, (j | kk) != 0 ? 1u : 0u);
+              umma_bf16_tmem_a(o_col, p_hi + 16, vdesc, idesc_o, 1u);
+            }
           }
-          umma_commit(p_empty(slot));
+          if (has_r) {
+#pragma unroll
+            for (int ds = 0; ds < DS; ++ds)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(tmem + static_cast<uint32_t>(64 * j), desc_k_sw128(qa + ds * Q_SLICE + kk * 32),
+                          desc_k_sw128(ka + ds * KV_SLICE + j * 64 * 128 + kk * 32), idesc_r,
+                          (ds | kk) != 0 ? 1u : 0u);
+            if (j & 1) umma_commit(s_full(j >> 1));
+          }
         }
         if (!ok) break;
-        umma_commit(v_empty);
-        umma_commit(o_full);
+        if (has_pv) {
+          umma_commit(v_empty);
+          umma_commit(o_full(sp & 1));
+        }
+        if (has_r) umma_commit(k_empty);
       }
       if (!ok) *abort_flag = 1;
       umma_commit(done_bar);
@@ -691,95 +719,120 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int r = pr / a.G, hi_head = g * a.G + pr % a.G;
     const int len = len0 + r;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    constexpr int DH = D / 2;
+    const float c2 = a.c2;
     float o_acc[DH];
 #pragma unroll
     for (int d = 0; d < DH; ++d) o_acc[d] = 0.f;
     float m_acc = -INFINITY, l_acc = 0.f;
     bool ok = true;
     auto softmax_sync = []() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
+    auto check = [&](bool waited) {
+      if (__any_sync(0xffffffffu, !waited || *abort_flag)) {
+        *abort_flag = 1;
+        ok = false;
+      }
+    };
+    // folds split sf (maximum mf, sum lf, visible keys or not) into the
+    // running state, this thread's D/2 output columns of O buffer sf & 1
+    auto fold = [&](int sf, float mf, float lf, bool in) {
+      check(mbar_wait_bounded(o_full(sf & 1), (sf >> 1) & 1, status, DEV_TIMEOUT_ATTN));
+      tc_fence_after();
+      const float m_new = fmaxf(m_acc, mf);
+      const float fa = ex2_approx(__fsub_rn(m_acc, m_new));
+      const float fc = ex2_approx(__fsub_rn(mf, m_new));
+      // o * 1 = o exactly: where no pair of the warp moves its maximum the
+      // update drops that product
+      const bool unit = __all_sync(0xffffffffu, !in || fa == 1.f);
+      if (in) l_acc = __fadd_rn(__fmul_rn(l_acc, fa), __fmul_rn(lf, fc));
+      const uint32_t col = lane_base + 256 + static_cast<uint32_t>((sf & 1) * D + half * DH);
+#pragma unroll
+      for (int c = 0; c < DH / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(col + 32 * c, v);
+        if (in) {
+          if (unit) {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+              o_acc[32 * c + jj] = __fadd_rn(o_acc[32 * c + jj], __fmul_rn(__uint_as_float(v[jj]), fc));
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+              o_acc[32 * c + jj] =
+                  __fadd_rn(__fmul_rn(o_acc[32 * c + jj], fa), __fmul_rn(__uint_as_float(v[jj]), fc));
+          }
+        }
+      }
+      if (in) m_acc = m_new;
+      tc_fence_before();
+      mbar_arrive(o_empty(sf & 1));
+    };
+    float m_prev = 0.f, l_prev = 0.f;
+    bool in_prev = false;
     for (int s = 0; s < ns; ++s) {
       const uint32_t ph = s & 1;
       const int cnt = min(kSplit, len - s * kSplit);
       // every pair of the tile sees the whole split: no key is masked
       const bool whole = len0 - s * kSplit >= kSplit;
-      ok = mbar_wait_bounded(s_full, ph, status, DEV_TIMEOUT_ATTN);
-      if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
-        *abort_flag = 1;
-        ok = false;
-      }
+      check(mbar_wait_bounded(s_full(half), ph, status, DEV_TIMEOUT_ATTN));
       softmax_sync();
       if (*abort_flag) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // the maximum (exact in any order): this thread's 128 keys, then the pair's
-      float m = -INFINITY;
+      // the raw maximum (exact in any order): this thread's 128 keys, four
+      // chains, then the pair's
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-      for (int c = 4 * half; c < 4 * half + 4; c += 2) {
-        uint32_t v[32], w[32];
-        tmem_ld32_nowait(lane_base + 32 * c, v);
-        tmem_ld32_nowait(lane_base + 32 * c + 32, w);
-        tmem_ld_wait(v);
-        tmem_ld_wait(w);
+      for (int c = 4 * half; c < 4 * half + 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + 32 * c, v);
         if (whole) {
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            m = fmaxf(m, __fmul_rn(__uint_as_float(v[jj]), a.scale));
-            m = fmaxf(m, __fmul_rn(__uint_as_float(w[jj]), a.scale));
+          for (int jj = 0; jj < 32; jj += 4) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) mx[e] = fmaxf(mx[e], __uint_as_float(v[jj + e]));
           }
         } else {
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            m = fmaxf(m, 32 * c + jj < cnt ? __fmul_rn(__uint_as_float(v[jj]), a.scale) : -INFINITY);
-            m = fmaxf(m, 32 * c + 32 + jj < cnt ? __fmul_rn(__uint_as_float(w[jj]), a.scale) : -INFINITY);
+          for (int jj = 0; jj < 32; jj += 4) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (32 * c + jj + e < cnt) mx[e] = fmaxf(mx[e], __uint_as_float(v[jj + e]));
           }
         }
       }
-      x_max[half * kTcPairs + pr] = m;
+      x_max[half * kTcPairs + pr] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       softmax_sync();
-      m = fmaxf(x_max[pr], x_max[kTcPairs + pr]);
-      // weights, their group sums and this half's two P chunks
-      float wsum[4];
+      const float m = __fmul_rn(fmaxf(x_max[pr], x_max[kTcPairs + pr]), c2);
+      // weights, their group sums (to x_w), and this half's two P chunks in place of R
+#pragma unroll 1
       for (int jh = 0; jh < 2; ++jh) {
-        const int j = 2 * half + jh;                       // 64-key chunk of the split
-        const int gc = 4 * s + j;
-        const int slot = gc & 1;
-        unsigned char* phi = p_s + slot * 2 * P_BYTES;
-        unsigned char* plo = phi + P_BYTES;
-        uint32_t vv[2][32];
-        tmem_ld32_nowait(lane_base + 64 * j, vv[0]);
-        tmem_ld32_nowait(lane_base + 64 * j + 32, vv[1]);
-        tmem_ld_wait(vv[0]);
-        tmem_ld_wait(vv[1]);
+        const int j = 2 * half + jh;  // 64-key chunk of the split
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int c = 2 * j + h;  // 32-key group c
-          const uint32_t (&v)[32] = vv[h];
+          uint32_t v[32];
+          tmem_ld32(lane_base + 32 * c, v);
           uint32_t hp[16], lp[16];  // bf16 pairs of the high and the low halves
-          float wl[32];             // hi + lo of each key
 #pragma unroll
           for (int jj = 0; jj < 32; jj += 2) {
             float x[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              if (whole) {
-                // every score finite or -inf with a finite maximum: exp gives the 0 the mask would
-                x[e] = expf(__fsub_rn(__fmul_rn(__uint_as_float(v[jj + e]), a.scale), m));
-              } else {
-                const float sc = 32 * c + jj + e < cnt ? __fmul_rn(__uint_as_float(v[jj + e]), a.scale) : -INFINITY;
-                x[e] = sc == -INFINITY ? 0.f : expf(__fsub_rn(sc, m));
-              }
+              const float y = ex2_approx(__fmaf_rn(__uint_as_float(v[jj + e]), c2, -m));
+              x[e] = whole || 32 * c + jj + e < cnt ? y : 0.f;
             }
             const __nv_bfloat162 h2 = __float22bfloat162_rn(make_float2(x[0], x[1]));
-            const float h0 = __low2float(h2), h1 = __high2float(h2);
-            const __nv_bfloat162 l2 = __float22bfloat162_rn(make_float2(__fsub_rn(x[0], h0), __fsub_rn(x[1], h1)));
-            wl[jj] = __fadd_rn(h0, __low2float(l2));
-            wl[jj + 1] = __fadd_rn(h1, __high2float(l2));
+            const __nv_bfloat162 l2 = __float22bfloat162_rn(
+                make_float2(__fsub_rn(x[0], __low2float(h2)), __fsub_rn(x[1], __high2float(h2))));
             hp[jj / 2] = *reinterpret_cast<const uint32_t*>(&h2);
             lp[jj / 2] = *reinterpret_cast<const uint32_t*>(&l2);
+            v[jj] = __float_as_uint(x[0]);
+            v[jj + 1] = __float_as_uint(x[1]);
           }
+          tmem_st16(lane_base + 64 * j + 32 * h, hp);
+          tmem_st16(lane_base + 64 * j + 32 * h + 16, lp);
           // the decode kernel's order: key 8nb + 2tq + e into partial tq in
           // (nb, e) order, then (0 + 1) + (2 + 3)
           float sq[4];
@@ -789,76 +842,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int nb = 0; nb < 4; ++nb)
 #pragma unroll
-              for (int e = 0; e < 2; ++e) acc = __fadd_rn(acc, wl[8 * nb + 2 * tq + e]);
+              for (int e = 0; e < 2; ++e) acc = __fadd_rn(acc, __uint_as_float(v[8 * nb + 2 * tq + e]));
             sq[tq] = acc;
           }
-          wsum[2 * jh + h] = __fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3]));
-          if (h == 0) {
-            // the slot is free once the MMAs of the chunk two before have read it
-            ok = mbar_wait_bounded(p_empty(slot), ((gc >> 1) & 1u) ^ 1u, status, DEV_TIMEOUT_ATTN);
-            if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
-              *abort_flag = 1;
-              ok = false;
-            }
-          }
-          // this pair's row of the two P tiles (keys 32h .. 32h + 31 of the chunk)
-          const uint32_t row_off = static_cast<uint32_t>((pr >> 3) * 1024 + (pr & 7) * 128);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t off = row_off + static_cast<uint32_t>((((4 * h + u) ^ (pr & 7)) & 7) * 16);
-            *reinterpret_cast<uint4*>(phi + off) = make_uint4(hp[4 * u], hp[4 * u + 1], hp[4 * u + 2], hp[4 * u + 3]);
-            *reinterpret_cast<uint4*>(plo + off) = make_uint4(lp[4 * u], lp[4 * u + 1], lp[4 * u + 2], lp[4 * u + 3]);
-          }
+          x_w[(2 * j + h) * kTcPairs + pr] = __fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3]));
         }
-        fence_proxy_async_smem();
-        mbar_arrive(p_full(slot));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full(j));
       }
-      // l: the groups 0 .. 7 in order -- the first half adds its four, the
-      // second half continues with its four and hands the total back
-      if (half == 0) x_l[pr] = __fadd_rn(__fadd_rn(__fadd_rn(wsum[0], wsum[1]), wsum[2]), wsum[3]);
-      tc_fence_before();
-      mbar_arrive(s_empty);  // the scores have been read
+      // l: the groups 0 .. 7 in order
       softmax_sync();
-      if (half == 1) {
-        float lt = x_l[pr];
+      float l = x_w[pr];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) lt = __fadd_rn(lt, wsum[q]);
-        x_l[pr] = lt;
-      }
-      softmax_sync();
-      const float l = x_l[pr];
-      // fold this split's (m, l, o) into the running state (the merge
-      // kernel's arithmetic), this thread's D/2 output columns
-      ok = mbar_wait_bounded(o_full, ph, status, DEV_TIMEOUT_ATTN);
-      if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
-        *abort_flag = 1;
-        ok = false;
-      }
-      tc_fence_after();
-      const bool in = cnt > 0;
-      const float m_new = fmaxf(m_acc, m);
-      const float fa = expf(__fsub_rn(m_acc, m_new));
-      const float fc = expf(__fsub_rn(m, m_new));
-      if (in) l_acc = __fadd_rn(__fmul_rn(l_acc, fa), __fmul_rn(l, fc));
-#pragma unroll
-      for (int c = 0; c < DH / 32; ++c) {
-        uint32_t vh[32], vl[32];
-        tmem_ld32_nowait(lane_base + 256 + half * DH + 32 * c, vh);
-        tmem_ld32_nowait(lane_base + 256 + D + half * DH + 32 * c, vl);
-        tmem_ld_wait(vh);
-        tmem_ld_wait(vl);
-        if (in) {
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const float os = __fadd_rn(__uint_as_float(vh[jj]), __uint_as_float(vl[jj]));
-            o_acc[32 * c + jj] = __fadd_rn(__fmul_rn(o_acc[32 * c + jj], fa), __fmul_rn(os, fc));
-          }
-        }
-      }
-      if (in) m_acc = m_new;
-      tc_fence_before();
-      mbar_arrive(o_empty);
+      for (int q = 1; q < 8; ++q) l = __fadd_rn(l, x_w[q * kTcPairs + pr]);
+      if (s > 0) fold(s - 1, m_prev, l_prev, in_prev);
+      m_prev = m;
+      l_prev = l;
+      in_prev = cnt > 0;
     }
+    if (ok && ns > 0) fold(ns - 1, m_prev, l_prev, in_prev);
     if (ok && r < nrows) {
       __nv_bfloat16* dst = a.out + (static_cast<int64_t>(row0 + r) * a.Hq + hi_head) * D + half * DH;
 #pragma unroll
@@ -883,12 +886,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 template <int D>
 size_t prefill_tc_smem_bytes() {
   return 1024 + static_cast<size_t>(D / 64) * kTcPairs * 128 + 2 * static_cast<size_t>(D / 64) * kSplit * 128 +
-         4 * static_cast<size_t>(kTcPairs) * 128 + 16 * 8 + 16 + 3 * kTcPairs * 4;
+         (kTcBars + 1) * 8 + 16 + 10 * kTcPairs * 4;
 }
 
 template <int D>
 size_t split_smem_bytes() {
-  return static_cast<size_t>(kSplit) * D * 2 + static_cast<size_t>(kRowsMma) * kSplit * 2;
+  return static_cast<size_t>(kSplit) * D * 2 + 2 * static_cast<size_t>(kRowsMma) * kSplit * 2;
 }
 
 // Decode: attn_split_kernel, then the merge.
@@ -961,6 +964,13 @@ kinv_status launch_prefill_tc(const void* q, const void* k_cache, const void* v_
   if (attr != KINV_OK) return attr;
   return launch_kernel(attn_prefill_tc_kernel<D>, dim3(a.tiles_per_seq, a.Hkv, B), dim3(kTcThreads), smem, stream, 1,
                        mq, mk, mv, a);
+}
+
+// c = fp32(scale * log2 e), the scores' factor in the base-2 softmax; a
+// scale that is not a positive finite number means 1 / sqrt(D).
+float base2_factor(float scale, int D) {
+  const float s = (scale > 0.f && std::isfinite(scale)) ? scale : 1.0f / sqrtf(static_cast<float>(D));
+  return static_cast<float>(static_cast<double>(s) * 1.4426950408889634074);
 }
 
 kinv_status check_common(const void* q, const void* k, const void* v, int64_t seq_stride,
@@ -1039,7 +1049,7 @@ kinv_status decode_launch(const void* q, const void* k_cache, const void* v_cach
   p.S = S;
   p.groups_per_seq = 1;
   p.rg_cap = ((p.G + 3) / 4) * 4;
-  p.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
+  p.c2 = base2_factor(scale, D);
   p.max_len = Lmax;
   p.max_q_len = 0;
   p.total_rows = B;
@@ -1103,7 +1113,7 @@ extern "C" kinv_status kinv_attn_prefill(const void* q, const void* k_cache, con
   a.max_len = max_kv;
   a.max_q_len = max_q_len;
   a.total_rows = total_rows;
-  a.scale = scale > 0.f ? scale : 1.0f / sqrtf(static_cast<float>(D));
+  a.c2 = base2_factor(scale, D);
   a.status = device_status_word();
   if (a.tiles_per_seq > 65535 || B > 65535) return KINV_ERR_UNSUPPORTED;
   if (B > 1 && seq_stride <= 0) return KINV_ERR_INVALID_ARG;

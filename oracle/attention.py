@@ -1,8 +1,8 @@
 """Softmax attention for decode and causal prefill (test infrastructure only).
 
 Follows "Deterministic and bit-exact inference" (M-0002), *technical*:
-attention is made batch-invariant "with a fixed split size for the key-value
-dimension rather than a fixed number of splits".  The split is how the GPU
+attention is made batch-invariant by cutting the keys into splits of one fixed
+length, not into a fixed number of splits.  The split is how the GPU
 schedules the sum; the quantity itself is plain softmax attention, so the
 oracle computes it unsplit, in fp64:
 
