@@ -47,47 +47,30 @@ namespace {
 
 constexpr int kSplit = 256;      // keys per split (the fixed split size)
 constexpr int kThreads = 256;    // eight warps, 32 keys each for the scores
-constexpr int kRowsMma = 16;     // (row, head) pairs of one block: the MMA's 16 rows
 constexpr int kMaxG = 8;         // query heads per kv head
+constexpr int kRowsP = 8;        // P rows kept in shared memory (G <= 8); the rest read a zero row
 
 struct AttnParams {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
   int64_t seq_stride, tok_stride;
-  const int32_t* kv_len;    // decode
-  const int32_t* q_start;   // prefill
-  const int32_t* q_len;
-  const int32_t* q_offset;
+  const int32_t* kv_len;
   __nv_bfloat16* out;
-  float* ws_o;              // [rows][Hq][S][D]
-  float* ws_ml;             // [rows][Hq][S][2]
-  int prefill;
-  int Hq, Hkv, G, R;
+  float* ws_o;              // [B][Hq][S][D]
+  float* ws_ml;             // [B][Hq][S][2]
+  int Hq, Hkv, G;
   int S;                    // splits per row in the workspace
-  int groups_per_seq;       // prefill: ceil(max_q_len / R)
-  int rg_cap;               // R * G: sizes the query and weight buffers
   float c2;                 // fp32(scale * log2 e) > 0
-  // bounds the device-side lengths must keep (the host cannot read them):
-  // decode 0 <= kv_len[b] <= max_len; prefill 0 <= q_len[b] <= max_q_len,
-  // 0 <= q_start[b] <= max_len - q_len[b], 0 <= q_offset[b] <= total_rows - q_len[b]
-  int max_len;              // decode: Lmax; prefill: max_kv
-  int max_q_len;
-  int total_rows;
-  int* status;              // device status word (a sequence outside the bounds)
+  int max_len;              // Lmax: the bound 0 <= kv_len[b] <= Lmax (the host cannot read kv_len)
+  int* status;              // device status word (a sequence outside the bound)
 };
 
-// A sequence whose device-side lengths break the bounds above is left out
-// (decode writes zeros for it, prefill leaves its rows untouched) and the call
-// records DEV_ATTN_BAD_LENGTH, so no access leaves the caller's buffers.
+// A sequence whose kv_len breaks the bound gets zeros and the call records
+// DEV_ATTN_BAD_LENGTH, so no access leaves the caller's buffers.
 __device__ __forceinline__ bool seq_ok(const AttnParams& p, int b) {
-  if (!p.prefill) {
-    const int n = p.kv_len[b];
-    return n >= 0 && n <= p.max_len;
-  }
-  const int n = p.q_len[b], st = p.q_start[b], off = p.q_offset[b];
-  return n >= 0 && n <= p.max_q_len && st >= 0 && st <= p.max_len - n && off >= 0 &&
-         off <= p.total_rows - n;
+  const int n = p.kv_len[b];
+  return n >= 0 && n <= p.max_len;
 }
 
 __device__ __forceinline__ void report_bad_length(const AttnParams& p) {
@@ -103,40 +86,6 @@ __device__ __forceinline__ void cp_async_commit() {
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Rows handled by this block: their q/out row indices and visible key counts.
-struct RowSet {
-  int nrows;
-  int seq;
-  int row0;     // q/out row of the first row (rows are consecutive)
-  int len0;     // visible keys of the first row (row r sees len0 + r)
-};
-
-__device__ __forceinline__ bool block_rows(const AttnParams& p, RowSet& rs) {
-  const int bq = p.prefill ? static_cast<int>(blockIdx.z) / p.groups_per_seq : static_cast<int>(blockIdx.z);
-  if (!seq_ok(p, bq)) {
-    report_bad_length(p);
-    return false;
-  }
-  if (!p.prefill) {
-    const int b = blockIdx.z;
-    rs.nrows = 1;
-    rs.seq = b;
-    rs.row0 = b;
-    rs.len0 = p.kv_len[b];
-    return rs.len0 > 0;
-  }
-  const int b = blockIdx.z / p.groups_per_seq;
-  const int j = blockIdx.z % p.groups_per_seq;
-  const int first = j * p.R;
-  const int n = p.q_len[b];
-  if (first >= n) return false;
-  rs.nrows = min(p.R, n - first);
-  rs.seq = b;
-  rs.row0 = p.q_offset[b] + first;
-  rs.len0 = p.q_start[b] + first + 1;
-  return true;
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -180,32 +129,36 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   // phase fall in eight different bank groups.
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __nv_bfloat16* kv = reinterpret_cast<__nv_bfloat16*>(smem_raw);                 // [256][D]
-  __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(smem_raw + kSplit * D * 2);  // P_hi [16][256]
-  __nv_bfloat16* pt_lo = pt + kRowsMma * kSplit;                                      // P_lo [16][256]
-  __shared__ float wmax[kThreads / 32][kRowsMma];
-  __shared__ float wsum[kThreads / 32][kRowsMma];
+  // P_hi and P_lo [8][256]: the MMA's rows 8-15 (no (row, head) pair when
+  // G <= 8) read a row of zeros
+  __nv_bfloat16* pt = reinterpret_cast<__nv_bfloat16*>(smem_raw + kSplit * D * 2);
+  __nv_bfloat16* pt_lo = pt + kRowsP * kSplit;
+  unsigned char* zrow = reinterpret_cast<unsigned char*>(pt_lo + kRowsP * kSplit);  // [256] zeros
+  __shared__ float wmax[kThreads / 32][kRowsP];
+  __shared__ float wsum[kThreads / 32][kRowsP];
 
   pdl_launch_dependents();
   pdl_wait();
-  RowSet rs;
-  if (!block_rows(p, rs)) return;
   // kv heads are the fastest grid index: the blocks reading the 256-byte
   // slices of the same token rows run side by side
   const int g = blockIdx.x;
   const int s = blockIdx.y;
+  const int b = blockIdx.z;
+  if (!seq_ok(p, b)) {
+    report_bad_length(p);
+    return;
+  }
+  const int len = p.kv_len[b];
   const int k0 = s * kSplit;
-  const int lenmax = rs.len0 + rs.nrows - 1;           // the last row sees the most keys
-  const int nmax = min(kSplit, lenmax - k0);
+  const int nmax = min(kSplit, len - k0);              // keys of this split
   if (nmax <= 0) return;
-  const int G = p.G;
-  const int RG = rs.nrows * G;                         // (row, head) pairs: MMA rows 0..RG-1
+  const int G = p.G;                                   // (row, head) pairs: MMA rows 0..G-1
   const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
   const int gq = lane >> 2, tq = lane & 3;             // fragment row / column group
-  const int64_t seq_off = rs.seq * p.seq_stride + static_cast<int64_t>(k0) * p.tok_stride + g * D;
+  const int64_t seq_off = b * p.seq_stride + static_cast<int64_t>(k0) * p.tok_stride + g * D;
   const uint32_t kv_base = smem_addr(kv);
-  const uint32_t pt_base = smem_addr(pt), pt_lo_base = smem_addr(pt_lo);
-  auto count = [&](int r) { return r < RG ? min(kSplit, rs.len0 + r / G - k0) : 0; };
+  const uint32_t pt_base = smem_addr(pt), pt_lo_base = smem_addr(pt_lo), zrow_base = smem_addr(zrow);
 
   auto load_sub = [&](const __nv_bfloat16* src, int j) {
     const int rows = min(SUB, nmax - j * SUB);
@@ -224,10 +177,8 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   uint32_t qa[KS][4];
   {
     const int r_lo = gq, r_hi = gq + 8;
-    const __nv_bfloat16* q_lo = r_lo < RG
-        ? p.q + (static_cast<int64_t>(rs.row0 + r_lo / G) * p.Hq + g * G + r_lo % G) * D : nullptr;
-    const __nv_bfloat16* q_hi = r_hi < RG
-        ? p.q + (static_cast<int64_t>(rs.row0 + r_hi / G) * p.Hq + g * G + r_hi % G) * D : nullptr;
+    const __nv_bfloat16* q_lo = r_lo < G ? p.q + (static_cast<int64_t>(b) * p.Hq + g * G + r_lo) * D : nullptr;
+    const __nv_bfloat16* q_hi = r_hi < G ? p.q + (static_cast<int64_t>(b) * p.Hq + g * G + r_hi) * D : nullptr;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       const int d0 = ks * 16 + 2 * tq;
@@ -267,77 +218,54 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   }
   cp_async_commit();
 
-  // --- softmax statistics.  A lane holds rows gq and gq + 8, keys
-  // 32w + 8nb + 2tq (+1).  Maxima of the raw scores: lane, then the four
-  // lanes of a row (exact), then the eight warps; m = fp32(max * c).  The sum
-  // adds the weights e: a lane's eight in (nb, pair) order, a fixed butterfly
-  // over the four lanes, the eight warps in ascending order.
-  const int cnt_lo = count(gq), cnt_hi = count(gq + 8);
-  float mx_lo = -INFINITY, mx_hi = -INFINITY;
+  // --- softmax statistics.  A lane holds row gq (pair gq < G; the
+  // fragment's rows gq + 8 hold no pair), keys 32w + 8nb + 2tq (+1).  Maxima
+  // of the raw scores: lane, then the four lanes of a row (exact), then the
+  // eight warps; m = fp32(max * c).  The sum adds the weights e: a lane's
+  // eight in (nb, pair) order, a fixed butterfly over the four lanes, the
+  // eight warps in ascending order.
+  const int cnt = gq < G ? nmax : 0;
+  float mx = -INFINITY;
 #pragma unroll
   for (int nb = 0; nb < 4; ++nb) {
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int key = warp * 32 + nb * 8 + 2 * tq + e;
-      if (key < cnt_lo) mx_lo = fmaxf(mx_lo, sc[nb][e]);
-      if (key < cnt_hi) mx_hi = fmaxf(mx_hi, sc[nb][2 + e]);
-    }
+    for (int e = 0; e < 2; ++e)
+      if (warp * 32 + nb * 8 + 2 * tq + e < cnt) mx = fmaxf(mx, sc[nb][e]);
   }
 #pragma unroll
-  for (int o = 1; o <= 2; o <<= 1) {
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, o));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, o));
-  }
-  if (tq == 0) {
-    wmax[warp][gq] = mx_lo;
-    wmax[warp][gq + 8] = mx_hi;
-  }
+  for (int o = 1; o <= 2; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (tq == 0) wmax[warp][gq] = mx;
   __syncthreads();
-  float m_lo = wmax[0][gq], m_hi = wmax[0][gq + 8];
+  float m = wmax[0][gq];
 #pragma unroll
-  for (int w = 1; w < kThreads / 32; ++w) {
-    m_lo = fmaxf(m_lo, wmax[w][gq]);
-    m_hi = fmaxf(m_hi, wmax[w][gq + 8]);
-  }
-  m_lo = __fmul_rn(m_lo, p.c2);
-  m_hi = __fmul_rn(m_hi, p.c2);
-  float sum_lo = 0.f, sum_hi = 0.f;
-  // writes the weights held in w[nb][0..3] (rows gq and gq + 8) into a P tile
-  auto write_p = [&](__nv_bfloat16* tile, const float (&w)[4][4]) {
-#pragma unroll
-    for (int nb = 0; nb < 4; ++nb) {
-      const int kc = warp * 4 + nb;                       // 8-key chunk of P
-      const uint32_t off_lo = static_cast<uint32_t>(gq * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
-      const uint32_t off_hi = static_cast<uint32_t>((gq + 8) * kSplit * 2 + ((kc ^ (gq & 7)) << 4) + 4 * tq);
-      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(tile) + off_lo) = pack_bf16(w[nb][0], w[nb][1]);
-      *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(tile) + off_hi) = pack_bf16(w[nb][2], w[nb][3]);
-    }
-  };
-  float hi[4][4];  // the high halves; sc takes the low halves
+  for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, wmax[w][gq]);
+  m = __fmul_rn(m, p.c2);
+  float sum = 0.f;
+  uint32_t hp[4], lp[4];  // bf16 pairs of the high and the low halves
 #pragma unroll
   for (int nb = 0; nb < 4; ++nb) {
+    float x[2], h[2], l[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int key = warp * 32 + nb * 8 + 2 * tq + e;
-      const float xl = key < cnt_lo ? ex2_approx(__fmaf_rn(sc[nb][e], p.c2, -m_lo)) : 0.f;
-      const float xh = key < cnt_hi ? ex2_approx(__fmaf_rn(sc[nb][2 + e], p.c2, -m_hi)) : 0.f;
-      split_bf16(xl, hi[nb][e], sc[nb][e]);
-      split_bf16(xh, hi[nb][2 + e], sc[nb][2 + e]);
-      sum_lo = __fadd_rn(sum_lo, xl);
-      sum_hi = __fadd_rn(sum_hi, xh);
+      x[e] = warp * 32 + nb * 8 + 2 * tq + e < cnt ? ex2_approx(__fmaf_rn(sc[nb][e], p.c2, -m)) : 0.f;
+      split_bf16(x[e], h[e], l[e]);
+      sum = __fadd_rn(sum, x[e]);
     }
+    hp[nb] = pack_bf16(h[0], h[1]);
+    lp[nb] = pack_bf16(l[0], l[1]);
   }
-  write_p(pt, hi);
-  write_p(pt_lo, sc);
+  // row gq of the P tiles (8-key chunk kc at chunk kc ^ gq)
 #pragma unroll
-  for (int o = 1; o <= 2; o <<= 1) {
-    sum_lo = __fadd_rn(sum_lo, __shfl_xor_sync(0xffffffffu, sum_lo, o));
-    sum_hi = __fadd_rn(sum_hi, __shfl_xor_sync(0xffffffffu, sum_hi, o));
+  for (int nb = 0; nb < 4; ++nb) {
+    const int kc = warp * 4 + nb;
+    const uint32_t off = static_cast<uint32_t>(gq * kSplit * 2 + ((kc ^ gq) << 4) + 4 * tq);
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt) + off) = hp[nb];
+    *reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(pt_lo) + off) = lp[nb];
   }
-  if (tq == 0) {
-    wsum[warp][gq] = sum_lo;
-    wsum[warp][gq + 8] = sum_hi;
-  }
+  if (t < kSplit * 2 / 16) *reinterpret_cast<uint4*>(zrow + 16 * t) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, o));
+  if (tq == 0) wsum[warp][gq] = sum;
   cp_async_wait<0>();
   __syncthreads();
 
@@ -350,15 +278,16 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
 #pragma unroll
     for (int i = 0; i < 4; ++i) oc[nb][i] = 0.f;
   if (warp < D / 16) {
+    const int prow = lane & 15;
 #pragma unroll 4
     for (int kk = 0; kk < kSplit / 16; ++kk) {
       uint32_t ah[4], al[4];
       {
-        const int prow = lane & 15;
         const int kc = 2 * kk + (lane >> 4);
-        const uint32_t off = static_cast<uint32_t>(prow * kSplit * 2 + ((kc ^ (prow & 7)) << 4));
-        ldsm_x4(pt_base + off, ah[0], ah[1], ah[2], ah[3]);
-        ldsm_x4(pt_lo_base + off, al[0], al[1], al[2], al[3]);
+        const uint32_t chunk = static_cast<uint32_t>((kc ^ (prow & 7)) << 4);
+        const uint32_t off = static_cast<uint32_t>(prow * kSplit * 2) + chunk;
+        ldsm_x4(prow < kRowsP ? pt_base + off : zrow_base + chunk, ah[0], ah[1], ah[2], ah[3]);
+        ldsm_x4(prow < kRowsP ? pt_lo_base + off : zrow_base + chunk, al[0], al[1], al[2], al[3]);
       }
       uint32_t b0, b1, b2, b3;
       {
@@ -371,26 +300,19 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
       mma_bf16_16816(oc[0], al, b0, b1);
       mma_bf16_16816(oc[1], al, b2, b3);
     }
-  }
-  if (warp < D / 16) {
-    // rows gq and gq + 8, columns 16w + 8nb + 2tq (+1)
+    // row gq = query head g G + gq of sequence b, columns 16w + 8nb + 2tq (+1)
+    if (gq < G) {
+      const int64_t base = (static_cast<int64_t>(b) * p.Hq + g * G + gq) * p.S + s;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int r = gq + 8 * h;
-      if (r < RG && count(r) > 0) {
-        const int row = r / G, i = r % G;
-        const int64_t base = (static_cast<int64_t>(rs.row0 + row) * p.Hq + g * G + i) * p.S + s;
+      for (int nb = 0; nb < 2; ++nb)
+        *reinterpret_cast<float2*>(p.ws_o + base * D + warp * 16 + nb * 8 + 2 * tq) =
+            make_float2(oc[nb][0], oc[nb][1]);
+      if (warp == 0 && tq == 0) {
+        float l = wsum[0][gq];
 #pragma unroll
-        for (int nb = 0; nb < 2; ++nb)
-          *reinterpret_cast<float2*>(p.ws_o + base * D + warp * 16 + nb * 8 + 2 * tq) =
-              make_float2(oc[nb][2 * h], oc[nb][2 * h + 1]);
-        if (warp == 0 && tq == 0) {
-          float l = wsum[0][r];
-#pragma unroll
-          for (int w = 1; w < kThreads / 32; ++w) l = __fadd_rn(l, wsum[w][r]);
-          p.ws_ml[base * 2 + 0] = h ? m_hi : m_lo;
-          p.ws_ml[base * 2 + 1] = l;
-        }
+        for (int w = 1; w < kThreads / 32; ++w) l = __fadd_rn(l, wsum[w][gq]);
+        p.ws_ml[base * 2 + 0] = m;
+        p.ws_ml[base * 2 + 1] = l;
       }
     }
   }
@@ -401,26 +323,12 @@ template <int D>
 __global__ void attn_merge_kernel(const AttnParams p) {
   pdl_launch_dependents();
   pdl_wait();
-  int row, len;
-  if (!p.prefill) {
-    row = blockIdx.y;
-    if (!seq_ok(p, row)) {
-      report_bad_length(p);
-      len = 0;  // zeros
-    } else {
-      len = p.kv_len[row];
-    }
-  } else {
-    const int b = blockIdx.z;
-    const int i = blockIdx.y;
-    if (!seq_ok(p, b)) {
-      if (i == 0) report_bad_length(p);
-      return;
-    }
-    if (i >= p.q_len[b]) return;
-    row = p.q_offset[b] + i;
-    len = p.q_start[b] + i + 1;
-  }
+  const int row = blockIdx.y;
+  int len = 0;  // a sequence outside the bound gets zeros
+  if (!seq_ok(p, row))
+    report_bad_length(p);
+  else
+    len = p.kv_len[row];
   const int h = blockIdx.x;
   const int d = threadIdx.x;
   __nv_bfloat16* dst = p.out + (static_cast<int64_t>(row) * p.Hq + h) * D + d;
@@ -891,7 +799,7 @@ size_t prefill_tc_smem_bytes() {
 
 template <int D>
 size_t split_smem_bytes() {
-  return static_cast<size_t>(kSplit) * D * 2 + 2 * static_cast<size_t>(kRowsMma) * kSplit * 2;
+  return static_cast<size_t>(kSplit) * D * 2 + (2 * kRowsP + 1) * static_cast<size_t>(kSplit) * 2;
 }
 
 // Decode: attn_split_kernel, then the merge.
@@ -1041,18 +949,12 @@ kinv_status decode_launch(const void* q, const void* k_cache, const void* v_cach
   p.ws_o = static_cast<float*>(workspace);
   const size_t o_bytes = static_cast<size_t>(B) * Hq * S * D * 4;
   p.ws_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) / 256) * 256);
-  p.prefill = 0;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.G = Hq / Hkv;
-  p.R = 1;
   p.S = S;
-  p.groups_per_seq = 1;
-  p.rg_cap = ((p.G + 3) / 4) * 4;
   p.c2 = base2_factor(scale, D);
   p.max_len = Lmax;
-  p.max_q_len = 0;
-  p.total_rows = B;
   p.status = device_status_word();
   const dim3 split_grid(Hkv, S, B), merge_grid(Hq, B, 1);
   return D == 128 ? launch<128>(p, split_grid, merge_grid, stream)
