@@ -39,6 +39,7 @@
 #include <cmath>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -634,6 +635,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float m_acc = -INFINITY, l_acc = 0.f;
     bool ok = true;
     auto softmax_sync = []() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
+    // named barrier 1 over the 256 softmax threads, returning whether `v`
+    // holds for any of them
+    auto softmax_sync_or = [](bool v) {
+      uint32_t r;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+          "bar.red.or.pred p, 1, 256, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(r)
+          : "r"(static_cast<uint32_t>(v))
+          : "memory");
+      return r != 0;
+    };
     auto check = [&](bool waited) {
       if (__any_sync(0xffffffffu, !waited || *abort_flag)) {
         *abort_flag = 1;
@@ -682,11 +695,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // every pair of the tile sees the whole split: no key is masked
       const bool whole = len0 - s * kSplit >= kSplit;
       check(mbar_wait_bounded(s_full(half), ph, status, DEV_TIMEOUT_ATTN));
-      softmax_sync();
-      if (*abort_flag) {
-        ok = false;
-        break;
-      }
       tc_fence_after();
       // the raw maximum (exact in any order): this thread's 128 keys, four
       // chains, then the pair's
@@ -711,7 +719,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       x_max[half * kTcPairs + pr] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      softmax_sync();
+      // the exchange's barrier also takes one decision for all 256 threads:
+      // leave if any of them has given up (a flag read after a plain barrier
+      // could change between two threads' reads)
+      if (softmax_sync_or(!ok || *abort_flag)) {
+        ok = false;
+        break;
+      }
       const float m = __fmul_rn(fmaxf(x_max[pr], x_max[kTcPairs + pr]), c2);
       // weights, their group sums (to x_w), and this half's two P chunks in place of R
 #pragma unroll 1
@@ -723,22 +737,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           uint32_t v[32];
           tmem_ld32(lane_base + 32 * c, v);
           uint32_t hp[16], lp[16];  // bf16 pairs of the high and the low halves
+          // (two copies of the loop: without and with the mask test)
+          auto weights = [&](auto masked) {
 #pragma unroll
-          for (int jj = 0; jj < 32; jj += 2) {
-            float x[2];
+            for (int jj = 0; jj < 32; jj += 2) {
+              float x[2];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const float y = ex2_approx(__fmaf_rn(__uint_as_float(v[jj + e]), c2, -m));
-              x[e] = whole || 32 * c + jj + e < cnt ? y : 0.f;
+              for (int e = 0; e < 2; ++e) {
+                const float y = ex2_approx(__fmaf_rn(__uint_as_float(v[jj + e]), c2, -m));
+                x[e] = !decltype(masked)::value || 32 * c + jj + e < cnt ? y : 0.f;
+              }
+              const __nv_bfloat162 h2 = __float22bfloat162_rn(make_float2(x[0], x[1]));
+              const __nv_bfloat162 l2 = __float22bfloat162_rn(
+                  make_float2(__fsub_rn(x[0], __low2float(h2)), __fsub_rn(x[1], __high2float(h2))));
+              hp[jj / 2] = *reinterpret_cast<const uint32_t*>(&h2);
+              lp[jj / 2] = *reinterpret_cast<const uint32_t*>(&l2);
+              v[jj] = __float_as_uint(x[0]);
+              v[jj + 1] = __float_as_uint(x[1]);
             }
-            const __nv_bfloat162 h2 = __float22bfloat162_rn(make_float2(x[0], x[1]));
-            const __nv_bfloat162 l2 = __float22bfloat162_rn(
-                make_float2(__fsub_rn(x[0], __low2float(h2)), __fsub_rn(x[1], __high2float(h2))));
-            hp[jj / 2] = *reinterpret_cast<const uint32_t*>(&h2);
-            lp[jj / 2] = *reinterpret_cast<const uint32_t*>(&l2);
-            v[jj] = __float_as_uint(x[0]);
-            v[jj + 1] = __float_as_uint(x[1]);
-          }
+          };
+          if (whole)
+            weights(std::false_type{});
+          else
+            weights(std::true_type{});
           tmem_st16(lane_base + 64 * j + 32 * h, hp);
           tmem_st16(lane_base + 64 * j + 32 * h + 16, lp);
           // the decode kernel's order: key 8nb + 2tq + e into partial tq in
