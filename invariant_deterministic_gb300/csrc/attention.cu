@@ -670,16 +670,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int c = 0; c < DH / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(col + 32 * c, v);
+        // the same roundings on pairs of columns (packed fp32x2 multiply and add)
         if (in) {
-          if (unit) {
+          const float2 fc2 = make_float2(fc, fc), fa2 = make_float2(fa, fa);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-              o_acc[32 * c + jj] = __fadd_rn(o_acc[32 * c + jj], __fmul_rn(__uint_as_float(v[jj]), fc));
-          } else {
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-              o_acc[32 * c + jj] =
-                  __fadd_rn(__fmul_rn(o_acc[32 * c + jj], fa), __fmul_rn(__uint_as_float(v[jj]), fc));
+          for (int jj = 0; jj < 32; jj += 2) {
+            float2 o = make_float2(o_acc[32 * c + jj], o_acc[32 * c + jj + 1]);
+            const float2 t = __fmul2_rn(make_float2(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])), fc2);
+            o = __fadd2_rn(unit ? o : __fmul2_rn(o, fa2), t);
+            o_acc[32 * c + jj] = o.x;
+            o_acc[32 * c + jj + 1] = o.y;
           }
         }
       }
@@ -705,9 +705,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_ld32(lane_base + 32 * c, v);
         if (whole) {
 #pragma unroll
-          for (int jj = 0; jj < 32; jj += 4) {
+          for (int jj = 0; jj < 32; jj += 8) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) mx[e] = fmaxf(mx[e], __uint_as_float(v[jj + e]));
+            for (int e = 0; e < 4; ++e)
+              mx[e] = fmax3(mx[e], __uint_as_float(v[jj + 2 * e]), __uint_as_float(v[jj + 2 * e + 1]));
           }
         } else {
 #pragma unroll
@@ -727,6 +728,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       const float m = __fmul_rn(fmaxf(x_max[pr], x_max[kTcPairs + pr]), c2);
+      const float2 c2x2 = make_float2(c2, c2), neg_m2 = make_float2(-m, -m);
       // weights, their group sums (to x_w), and this half's two P chunks in place of R
 #pragma unroll 1
       for (int jh = 0; jh < 2; ++jh) {
@@ -741,15 +743,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           auto weights = [&](auto masked) {
 #pragma unroll
             for (int jj = 0; jj < 32; jj += 2) {
-              float x[2];
+              // fma(r, c, -m) and x - hi on pairs (packed fp32x2; x - hi as
+              // fma(hi, -1, x), the same single rounding)
+              const float2 arg = __ffma2_rn(make_float2(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1])), c2x2,
+                                            neg_m2);
+              float x[2] = {ex2_approx(arg.x), ex2_approx(arg.y)};
+              if (decltype(masked)::value) {
 #pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const float y = ex2_approx(__fmaf_rn(__uint_as_float(v[jj + e]), c2, -m));
-                x[e] = !decltype(masked)::value || 32 * c + jj + e < cnt ? y : 0.f;
+                for (int e = 0; e < 2; ++e) x[e] = 32 * c + jj + e < cnt ? x[e] : 0.f;
               }
               const __nv_bfloat162 h2 = __float22bfloat162_rn(make_float2(x[0], x[1]));
               const __nv_bfloat162 l2 = __float22bfloat162_rn(
-                  make_float2(__fsub_rn(x[0], __low2float(h2)), __fsub_rn(x[1], __high2float(h2))));
+                  __ffma2_rn(__bfloat1622float2(h2), make_float2(-1.f, -1.f), make_float2(x[0], x[1])));
               hp[jj / 2] = *reinterpret_cast<const uint32_t*>(&h2);
               lp[jj / 2] = *reinterpret_cast<const uint32_t*>(&l2);
               v[jj] = __float_as_uint(x[0]);

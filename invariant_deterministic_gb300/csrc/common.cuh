@@ -216,6 +216,13 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// max(a, b, c) in one three-input instruction (exact, as two fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // 2^x by the hardware's approximate base-2 exponential (ex2.approx, flushing
 // subnormal results to zero); 2^-inf = 0.
 __device__ __forceinline__ float ex2_approx(float x) {
