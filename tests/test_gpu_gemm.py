@@ -241,3 +241,23 @@ def test_fused_epilogues_match_the_oracle_on_whole_rows(kinv, m):
     acts = kinv.gemm_swiglu(x1[:4].contiguous(), w_il, fusion=kinv.norm_in(ss1[:4].contiguous(), d, 1e-6))
     assert_same_bits(acts, act[:4], "gate/up: 4 rows vs in the larger call")
     assert kinv.last_device_status() == 0
+
+
+def test_tile_schedule_partial_last_tile(kinv):
+    """The tile schedule (400 rows, a K split) on widths that end in half a
+    256-column tile: SwiGLU (F = 320, N = 640) and an fp32 output match the
+    oracle, and their rows keep the bits of the same rows in a 4-row call
+    (the cluster schedule)."""
+    a = synth.normal_bf16((400, 512), 1.0, 95).cuda()
+    w_gu = synth.normal_bf16((640, 512), 0.05, 96).cuda()
+    w_il = kinv.interleave_gate_up(w_gu)
+    act = kinv.gemm_swiglu(a, w_il)
+    assert_close(f64(act), obf.to_f64(_swiglu_ref(a, w_gu)), "SwiGLU, 400 rows")
+    assert_same_bits(kinv.gemm_swiglu(a[:4].contiguous(), w_il), act[:4], "SwiGLU: 4 rows vs 400")
+    a2 = synth.normal_bf16((400, 256), 1.0, 97).cuda()
+    w2 = synth.normal_bf16((1024, 256), 0.05, 98).cuda()
+    c = kinv.gemm(a2, w2, out_dtype=torch.float32)
+    assert_same_bits(kinv.gemm(a2[:4].contiguous(), w2, out_dtype=torch.float32), c[:4], "fp32: 4 rows vs 400")
+    ref = ogemm(synth.bits(a2), synth.bits(w2), out="f64")
+    assert np.allclose(c.double().cpu().numpy(), ref, rtol=1e-5, atol=1e-4)
+    assert kinv.last_device_status() == 0
