@@ -374,10 +374,10 @@ __global__ void attn_merge_kernel(const AttnParams p) {
 // ascending order and folds each split into a running (m, l, o) per pair in
 // registers with the merge kernel's arithmetic, so no partial goes to memory.
 // Per pair and split it computes what attn_split_kernel computes:
-//   R = Q . K^T         tcgen05 128 x 64 x 16 steps over the head dimension,
+//   R = Q . K^T         tcgen05 128 x 128 x 16 steps over the head dimension,
 //                       ascending, fp32 in tensor memory (the per-element
-//                       result of a 16-deep step equals mma.sync's), four
-//                       64-key chunks
+//                       result of a 16-deep step equals mma.sync's), two
+//                       128-key halves
 //   max, e = 2^fma(r, c, -m), hi / lo, l in the decode kernel's order
 //   O = P . V           one chain of sixteen 16-key steps, each the hi step
 //                       then the lo step, P read from tensor memory
@@ -395,9 +395,10 @@ __global__ void attn_merge_kernel(const AttnParams p) {
 // pairs (32-key group h of the chunk: hi at 64 j + 32 h, lo 16 columns
 // further), which the PV MMAs read as their A operand; O in two buffers after
 // it, so split s + 1's PV runs while split s is folded.  The MMA thread
-// issues split s + 1's R chunk j right after split s's PV chunk j (the MMAs
-// run in issue order, so the chunk's P is read before R overwrites it), and
-// the softmax threads fold split s after writing split s + 1's P.
+// issues split s + 1's R half h right after split s's PV chunks 2h and
+// 2h + 1 (the MMAs run in issue order, so their P is read before R
+// overwrites it), and the softmax threads fold split s after writing split
+// s + 1's P.
 constexpr int kTcThreads = 320;
 constexpr int kTcPairs = 128;
 constexpr int kTcBars = 17;
@@ -571,7 +572,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---- MMA issue: iteration s issues split s - 1's PV chunks and split
     // s's R chunks, interleaved
     if (lane == 0) {
-      constexpr uint32_t idesc_r = tc_idesc(64, 0);
+      constexpr uint32_t idesc_r = tc_idesc(128, 0);
       constexpr uint32_t idesc_o = tc_idesc(D, 1);
       bool ok = mbar_wait_bounded(q_full, 0, status, DEV_TIMEOUT_ATTN);
       const uint32_t qa = smem_addr(q_s), ka = smem_addr(k_s), va = smem_addr(v_s);
@@ -598,15 +599,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               umma_bf16_tmem_a(o_col, p_hi + 16, vdesc, idesc_o, 1u);
             }
           }
-          if (has_r) {
+          if (has_r && (j & 1)) {
+            // R of chunks j - 1 and j (keys 128 h .. + 127, h = j / 2): one
+            // 128 x 128 MMA per 16-deep step
+            const int h = j >> 1;
 #pragma unroll
             for (int ds = 0; ds < DS; ++ds)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                umma_bf16(tmem + static_cast<uint32_t>(64 * j), desc_k_sw128(qa + ds * Q_SLICE + kk * 32),
-                          desc_k_sw128(ka + ds * KV_SLICE + j * 64 * 128 + kk * 32), idesc_r,
+                umma_bf16(tmem + static_cast<uint32_t>(128 * h), desc_k_sw128(qa + ds * Q_SLICE + kk * 32),
+                          desc_k_sw128(ka + ds * KV_SLICE + h * 128 * 128 + kk * 32), idesc_r,
                           (ds | kk) != 0 ? 1u : 0u);
-            if (j & 1) umma_commit(s_full(j >> 1));
+            umma_commit(s_full(h));
           }
         }
         if (!ok) break;
