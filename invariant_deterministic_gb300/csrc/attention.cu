@@ -575,7 +575,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t idesc_r = tc_idesc(128, 0);
       constexpr uint32_t idesc_o = tc_idesc(D, 1);
       bool ok = mbar_wait_bounded(q_full, 0, status, DEV_TIMEOUT_ATTN);
-      const uint32_t qa = smem_addr(q_s), ka = smem_addr(k_s), va = smem_addr(v_s);
+      // base descriptors; an operand at byte offset b from a base adds b / 16
+      // to the start-address field (shared addresses stay below 256 KB, so
+      // the field never carries into the next)
+      const uint64_t qd = desc_k_sw128(smem_addr(q_s)), kd = desc_k_sw128(smem_addr(k_s));
+      const uint64_t vd = desc_mn_sw128(smem_addr(v_s), KV_SLICE);
       for (int s = 0; s <= ns && ok; ++s) {
         const bool has_r = s < ns, has_pv = s > 0;
         const int sp = s - 1;
@@ -586,6 +590,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (ok && has_r) ok = !*abort_flag && mbar_wait_bounded(k_full, s & 1, status, DEV_TIMEOUT_ATTN);
         if (!ok) break;
         tc_fence_after();
+#pragma unroll
         for (int j = 0; j < 4; ++j) {
           if (has_pv) {
             ok = !*abort_flag && mbar_wait_bounded(p_full(j), sp & 1, status, DEV_TIMEOUT_ATTN);
@@ -593,7 +598,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t vdesc = desc_mn_sw128(va + (4 * j + kk) * 2048, KV_SLICE);
+              const uint64_t vdesc = vd + static_cast<uint64_t>(((4 * j + kk) * 2048) >> 4);
               const uint32_t p_hi = tmem + static_cast<uint32_t>(64 * j + 32 * (kk >> 1) + 8 * (kk & 1));
               umma_bf16_tmem_a(o_col, p_hi, vdesc, idesc_o, (j | kk) != 0 ? 1u : 0u);
               umma_bf16_tmem_a(o_col, p_hi + 16, vdesc, idesc_o, 1u);
@@ -607,8 +612,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int ds = 0; ds < DS; ++ds)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                umma_bf16(tmem + static_cast<uint32_t>(128 * h), desc_k_sw128(qa + ds * Q_SLICE + kk * 32),
-                          desc_k_sw128(ka + ds * KV_SLICE + h * 128 * 128 + kk * 32), idesc_r,
+                umma_bf16(tmem + static_cast<uint32_t>(128 * h),
+                          qd + static_cast<uint64_t>((ds * Q_SLICE + kk * 32) >> 4),
+                          kd + static_cast<uint64_t>((ds * KV_SLICE + h * 128 * 128 + kk * 32) >> 4), idesc_r,
                           (ds | kk) != 0 ? 1u : 0u);
             umma_commit(s_full(h));
           }
