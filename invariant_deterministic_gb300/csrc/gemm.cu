@@ -833,11 +833,10 @@ __device__ __forceinline__ float sumsq_butterfly128(const float (&v)[128]) {
   return __fadd_rn(__fadd_rn(__fadd_rn(g4[0], g4[1]), g4[2]), g4[3]);
 }
 
-template <int MMA_N, int J>
+template <int J>
 __global__ void __launch_bounds__(kTilesThreads, 1)
     gemm_tiles_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                       const GemmArgs args) {
-  static_assert(MMA_N == 128 || MMA_N == 256, "one or two MMAs per 16-deep step");
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -917,7 +916,7 @@ __global__ void __launch_bounds__(kTilesThreads, 1)
     __syncwarp();
   } else if (warp == 9) {
     if (lane == 0) {
-      constexpr uint32_t idesc = instr_desc<MMA_N>();
+      constexpr uint32_t idesc = instr_desc<kTilesBN>();  // one 128 x 256 MMA per 16-deep step
       int it = 0, seq = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
@@ -949,13 +948,7 @@ __global__ void __launch_bounds__(kTilesThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < BK / 16; ++kk) {
                 const uint32_t accum = (k | h | kk) != 0 ? 1u : 0u;
-                const uint64_t adesc = sdesc_sw128(a_addr + kk * 32);
-                if constexpr (MMA_N == 256) {
-                  umma_bf16(d, adesc, sdesc_sw128(b_addr + kk * 32), idesc, accum);
-                } else {
-                  umma_bf16(d, adesc, sdesc_sw128(b_addr + kk * 32), idesc, accum);
-                  umma_bf16(d + 128, adesc, sdesc_sw128(b_addr + 128 * 128 + kk * 32), idesc, accum);
-                }
+                umma_bf16(d, sdesc_sw128(a_addr + kk * 32), sdesc_sw128(b_addr + kk * 32), idesc, accum);
               }
             }
             umma_commit(empty_bar(st));
@@ -1195,7 +1188,7 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a
 
 // The large-M schedule: one CTA per SM (at most one per tile), the stage ring
 // as deep as shared memory allows.
-template <int MMA_N, int J>
+template <int J>
 kinv_status launch_gemm_tiles_j(const void* A, int64_t lda, const void* W, int64_t ldw, int K, GemmArgs a,
                               cudaStream_t stream) {
   a.kb_per_split = K / BK / a.splits;
@@ -1212,24 +1205,23 @@ kinv_status launch_gemm_tiles_j(const void* A, int64_t lda, const void* W, int64
   if (stages < 2) return KINV_ERR_UNSUPPORTED;
   a.stages = stages;
   const size_t smem = 1024 + static_cast<size_t>(stages) * stage + tiles_bar_count(stages) * 8 + 16;
-  const kinv_status attr = ensure_smem(reinterpret_cast<const void*>(gemm_tiles_kernel<MMA_N, J>), smem);
+  const kinv_status attr = ensure_smem(reinterpret_cast<const void*>(gemm_tiles_kernel<J>), smem);
   if (attr != KINV_OK) return attr;
   const long long tiles = static_cast<long long>(a.tiles_m) * a.tiles_n;
   const int sms = sm_count() > 0 ? sm_count() : 1;
   const int grid = static_cast<int>(tiles < sms ? tiles : sms);
-  return launch_kernel(gemm_tiles_kernel<MMA_N, J>, dim3(grid), dim3(kTilesThreads), smem, stream, 1, ta, tw, a);
+  return launch_kernel(gemm_tiles_kernel<J>, dim3(grid), dim3(kTilesThreads), smem, stream, 1, ta, tw, a);
 }
 
 // Two K blocks per TMA copy for tall products: a CTA keeps only a few copies
 // in flight, and larger copies took the 4096-row projections 7-12 % faster
 // (measured; at 512 rows the deeper ring of single blocks did better).  The
 // MMAs keep their order.
-template <int MMA_N>
 kinv_status launch_gemm_tiles(const void* A, int64_t lda, const void* W, int64_t ldw, int K, GemmArgs a,
                               cudaStream_t stream) {
   const bool tall = (a.M + BM - 1) / BM >= 16 && (K / BK / a.splits) % 2 == 0;
-  return tall ? launch_gemm_tiles_j<MMA_N, 2>(A, lda, W, ldw, K, a, stream)
-              : launch_gemm_tiles_j<MMA_N, 1>(A, lda, W, ldw, K, a, stream);
+  return tall ? launch_gemm_tiles_j<2>(A, lda, W, ldw, K, a, stream)
+              : launch_gemm_tiles_j<1>(A, lda, W, ldw, K, a, stream);
 }
 
 // Whether the tile schedule runs a call (else the cluster split-K schedule).
@@ -1245,8 +1237,6 @@ bool use_tiles(int M, int K, int splits) {
   if (splits == 1) return true;
   return M >= (K >= 8192 ? 768 : 384);
 }
-// MMA width of the tile schedule: one 128 x 256 instruction per 16-deep step.
-constexpr int kTilesMmaN = 256;
 
 }  // namespace
 }  // namespace kinv
@@ -1324,7 +1314,7 @@ kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, vo
   a.kb_per_split = 0;
   a.tiles_m = a.tiles_n = 0;
   if (!rope && use_tiles(M, K, p.splits))
-    return launch_gemm_tiles<kTilesMmaN>(A, lda, W, ldw, K, a, stream);
+    return launch_gemm_tiles(A, lda, W, ldw, K, a, stream);
   switch (p.bn) {
     case 128: return launch_gemm<128>(ta, tw, a, p.smem_budget, grid_y, grid_z, stream);
     default: return KINV_ERR_UNSUPPORTED;
