@@ -107,7 +107,8 @@ def test_prefill_sized_m(kinv):
     w = synth.normal_bf16((n, k), 0.02, 14).cuda()
     a = synth.normal_bf16((4096, k), 1.0, 15).cuda()
     full = kinv.gemm(a, w)
-    for m0, m in [(0, 1), (4095, 1), (512, 512), (1000, 64)]:
+    # (2000 rows: the tile schedule with two K blocks per stage and a ragged last tile)
+    for m0, m in [(0, 1), (4095, 1), (512, 512), (1000, 64), (1000, 2000)]:
         part = kinv.gemm(a[m0: m0 + m].contiguous(), w)
         assert_same_bits(part, full[m0: m0 + m], f"rows {m0}..{m0 + m}")
 
