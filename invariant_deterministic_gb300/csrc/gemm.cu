@@ -1213,15 +1213,20 @@ kinv_status launch_gemm_tiles_j(const void* A, int64_t lda, const void* W, int64
   return launch_kernel(gemm_tiles_kernel<J>, dim3(grid), dim3(kTilesThreads), smem, stream, 1, ta, tw, a);
 }
 
-// Two K blocks per TMA copy for tall products: a CTA keeps only a few copies
-// in flight, and larger copies took the 4096-row projections 7-12 % faster
-// (measured; at 512 rows the deeper ring of single blocks did better).  The
-// MMAs keep their order.
+// Two K blocks per TMA copy: a CTA keeps only a few copies in flight, and
+// larger copies (measured, per launch) took the 4096-row projections 7-12 %
+// faster, and the shapes with at most about one tile per CTA (QKV and O at
+// 512-1024 rows) 9-14 %; with a few tiles per CTA at 512-1024 rows (gate/up,
+// and down with K = 12288) the deeper ring of single blocks was 2-5 %
+// faster.  The MMAs keep their order.
 kinv_status launch_gemm_tiles(const void* A, int64_t lda, const void* W, int64_t ldw, int K, GemmArgs a,
                               cudaStream_t stream) {
-  const bool tall = (a.M + BM - 1) / BM >= 16 && (K / BK / a.splits) % 2 == 0;
-  return tall ? launch_gemm_tiles_j<2>(A, lda, W, ldw, K, a, stream)
-              : launch_gemm_tiles_j<1>(A, lda, W, ldw, K, a, stream);
+  const long long tiles_m = (a.M + BM - 1) / BM;
+  const long long tiles = tiles_m * ((a.N + kTilesBN - 1) / kTilesBN);
+  const int sms = sm_count() > 0 ? sm_count() : 1;
+  const bool two = (K / BK / a.splits) % 2 == 0 && (tiles_m >= 16 || (2 * tiles <= 3LL * sms && K < 8192));
+  return two ? launch_gemm_tiles_j<2>(A, lda, W, ldw, K, a, stream)
+             : launch_gemm_tiles_j<1>(A, lda, W, ldw, K, a, stream);
 }
 
 // Whether the tile schedule runs a call (else the cluster split-K schedule).
