@@ -134,6 +134,7 @@ struct GemmArgs {
   // the large-M tile kernel's schedule
   int kb_per_split;  // 64-wide K blocks of one K range
   int tiles_m, tiles_n;
+  int n_tail;        // the last n_tail tiles (M fastest) run as two 128-wide halves each
 };
 
 // Rows [0, n) of a staged tile (bf16, row stride BN) are rows row_of(r) of the
@@ -836,7 +837,7 @@ __device__ __forceinline__ float sumsq_butterfly128(const float (&v)[128]) {
 template <int J>
 __global__ void __launch_bounds__(kTilesThreads, 1)
     gemm_tiles_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                      const GemmArgs args) {
+                      const __grid_constant__ CUtensorMap tmW_half, const GemmArgs args) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -856,7 +857,22 @@ __global__ void __launch_bounds__(kTilesThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles_m = args.tiles_m;
-  const int n_tiles = tiles_m * args.tiles_n;
+  // the work list: whole 128 x 256 tiles, then the last n_tail tiles as
+  // 128 x 128 halves, so the last round over the SMs is a short one (a
+  // 128 x 128 MMA gives each element the bits of the 128 x 256 one)
+  const int tiles_full = tiles_m * args.tiles_n - args.n_tail;
+  const int n_tiles = tiles_full + 2 * args.n_tail;
+  auto tile_at = [&](int v, int& m0, int& n0) -> bool {  // true: a 128-wide half
+    int t = v, hf = 0;
+    const bool narrow = v >= tiles_full;
+    if (narrow) {
+      t = tiles_full + ((v - tiles_full) >> 1);
+      hf = (v - tiles_full) & 1;
+    }
+    m0 = (t % tiles_m) * BM;
+    n0 = (t / tiles_m) * kTilesBN + hf * 128;
+    return narrow;
+  };
   const int splits = args.splits, kbs = args.kb_per_split;
 
   if (threadIdx.x == 0) {
@@ -888,12 +904,14 @@ __global__ void __launch_bounds__(kTilesThreads, 1)
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmW_half)) : "memory");
       const uint64_t pol_a = l2_policy_evict_last();
       const uint64_t pol_w = l2_policy_evict_last();  // a weight tile serves every row tile
       int it = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
-        const int m0 = (t % tiles_m) * BM, n0 = (t / tiles_m) * kTilesBN;
+        int m0, n0;
+        const bool narrow = tile_at(t, m0, n0);
         for (int kb = 0; kb < splits * kbs; kb += j, ++it) {
           const int st = it % stages;
           const uint32_t ph = (it / stages) & 1u;
@@ -903,10 +921,10 @@ __global__ void __launch_bounds__(kTilesThreads, 1)
             stop = true;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(st), stage_bytes);
+          mbar_arrive_expect_tx(full_bar(st), narrow ? J * (kTilesABytes + kTilesBBytes / 2) : stage_bytes);
           unsigned char* sa = base + st * stage_bytes;
           tma_load_3d(smem_addr(sa), &tmA, 0, m0, kb, full_bar(st), pol_a);
-          tma_load_3d(smem_addr(sa + j * kTilesABytes), &tmW, 0, n0, kb, full_bar(st), pol_w);
+          tma_load_3d(smem_addr(sa + j * kTilesABytes), narrow ? &tmW_half : &tmW, 0, n0, kb, full_bar(st), pol_w);
         }
       }
       // loads still in flight (only after an abort) land before the block exits
@@ -916,10 +934,15 @@ __global__ void __launch_bounds__(kTilesThreads, 1)
     __syncwarp();
   } else if (warp == 9) {
     if (lane == 0) {
-      constexpr uint32_t idesc = instr_desc<kTilesBN>();  // one 128 x 256 MMA per 16-deep step
       int it = 0, seq = 0;
       bool stop = false;
       for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
+        int m0, n0;
+        // one 128 x 256 MMA per 16-deep step, or 128 x 128 for a half tile
+        // (whose W blocks, 128 rows each, lie 16 KB apart in the stage)
+        const bool narrow = tile_at(t, m0, n0);
+        const uint32_t idesc = narrow ? instr_desc<128>() : instr_desc<kTilesBN>();
+        const uint32_t w_blk = narrow ? kTilesBBytes / 2 : kTilesBBytes;
         for (int r = 0; r < splits && !stop; ++r, ++seq) {
           const int b = seq & 1;
           const uint32_t aph = (seq >> 1) & 1u;
@@ -944,7 +967,7 @@ __global__ void __launch_bounds__(kTilesThreads, 1)
             const uint32_t b0 = a0 + j * kTilesABytes;
 #pragma unroll
             for (int h = 0; h < J; ++h) {  // the stage's K blocks, ascending
-              const uint32_t a_addr = a0 + h * kTilesABytes, b_addr = b0 + h * kTilesBBytes;
+              const uint32_t a_addr = a0 + h * kTilesABytes, b_addr = b0 + h * w_blk;
 #pragma unroll
               for (int kk = 0; kk < BK / 16; ++kk) {
                 const uint32_t accum = (k | h | kk) != 0 ? 1u : 0u;
@@ -969,8 +992,11 @@ __global__ void __launch_bounds__(kTilesThreads, 1)
     int seq = 0;
     bool stop = false;
     for (int t = blockIdx.x; t < n_tiles && !stop; t += gridDim.x) {
-      const int m = (t % tiles_m) * BM + row;
-      const int nc0 = (t / tiles_m) * kTilesBN + half * 128;  // this thread's first column
+      int m0, n0;
+      const bool narrow = tile_at(t, m0, n0);
+      const int m = m0 + row;
+      const int nc0 = n0 + half * 128;  // this thread's first column
+      const bool cols = !narrow || half == 0;  // a half tile has columns for warps 0-3 only
       float acc[128];
       for (int r = 0; r < splits; ++r, ++seq) {
         const int b = seq & 1;
@@ -982,19 +1008,21 @@ __global__ void __launch_bounds__(kTilesThreads, 1)
           break;
         }
         tc_fence_after();
+        if (cols) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + b * kTilesBN + c * 32, v);
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld32(lane_base + b * kTilesBN + c * 32, v);
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            acc[c * 32 + j] = r == 0 ? __uint_as_float(v[j]) : __fadd_rn(acc[c * 32 + j], __uint_as_float(v[j]));
+            for (int j = 0; j < 32; ++j)
+              acc[c * 32 + j] = r == 0 ? __uint_as_float(v[j]) : __fadd_rn(acc[c * 32 + j], __uint_as_float(v[j]));
+          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acc_empty(b)) : "memory");
       }
-      if (stop || m >= args.M || nc0 >= args.N) continue;
+      if (stop || !cols || m >= args.M || nc0 >= args.N) continue;
       if (args.row_ss) {
         // 1 / rms of the row from its partial sums of squares, tiles in order
         const float* ss = args.row_ss + static_cast<int64_t>(m) * args.row_ss_tiles;
@@ -1195,8 +1223,9 @@ kinv_status launch_gemm_tiles_j(const void* A, int64_t lda, const void* W, int64
   a.tiles_m = (a.M + BM - 1) / BM;
   a.tiles_n = (a.N + kTilesBN - 1) / kTilesBN;
   a.j = J;
-  CUtensorMap ta, tw;
-  if (!make_map(&ta, A, a.M, K, lda, BM, a.j) || !make_map(&tw, W, a.N, K, ldw, kTilesBN, a.j))
+  CUtensorMap ta, tw, tw_half;
+  if (!make_map(&ta, A, a.M, K, lda, BM, a.j) || !make_map(&tw, W, a.N, K, ldw, kTilesBN, a.j) ||
+      !make_map(&tw_half, W, a.N, K, ldw, kTilesBN / 2, a.j))
     return KINV_ERR_CUDA;
   const int stage = a.j * kTilesStage;
   const int avail = max_smem_optin() - 1024 - 256;
@@ -1209,8 +1238,15 @@ kinv_status launch_gemm_tiles_j(const void* A, int64_t lda, const void* W, int64
   if (attr != KINV_OK) return attr;
   const long long tiles = static_cast<long long>(a.tiles_m) * a.tiles_n;
   const int sms = sm_count() > 0 ? sm_count() : 1;
-  const int grid = static_cast<int>(tiles < sms ? tiles : sms);
-  return launch_kernel(gemm_tiles_kernel<J>, dim3(grid), dim3(kTilesThreads), smem, stream, 1, ta, tw, a);
+  // a partial last round over the SMs (at least one full round before it)
+  // runs its tiles as halves when they fit one round: it then takes about
+  // as long as half a tile's operands take to stream in
+  const long long rem = tiles % sms;
+  a.n_tail = tiles >= sms && rem > 0 && 2 * rem <= sms ? static_cast<int>(rem) : 0;
+  const long long work = tiles + a.n_tail;
+  const int grid = static_cast<int>(work < sms ? work : sms);
+  return launch_kernel(gemm_tiles_kernel<J>, dim3(grid), dim3(kTilesThreads), smem, stream, 1, ta, tw, tw_half,
+                       a);
 }
 
 // Two K blocks per TMA copy: a CTA keeps only a few copies in flight, and
@@ -1318,6 +1354,7 @@ kinv_status gemm_impl(const void* A, int64_t lda, const void* W, int64_t ldw, vo
   a.ss_out = resid ? fu->ss_out : nullptr;
   a.kb_per_split = 0;
   a.tiles_m = a.tiles_n = 0;
+  a.n_tail = 0;
   if (!rope && use_tiles(M, K, p.splits))
     return launch_gemm_tiles(A, lda, W, ldw, K, a, stream);
   switch (p.bn) {
