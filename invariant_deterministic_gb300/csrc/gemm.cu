@@ -33,6 +33,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "rope.cuh"
@@ -567,19 +568,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       cluster_sync();  // every rank's partials are staged
       const int owned = rank < rows_here ? (rows_here - rank + splits - 1) / splits : 0;
       __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(part + args.a_rows * LDP);  // rope rows
-      for (int i = warp; i < owned && good; i += kGemmThreads / 32) {
+      // The output of owned row i from a4, its sum over the ranks (warp-wide:
+      // lane l holds columns 4l .. 4l + 3).
+      auto emit = [&](int i, float (&a4)[4]) {
         const int ml = i * splits + rank;
         const int mm = m0 + ml;
-        const uint32_t off = smem_addr(part + ml * LDP + 4 * lane);
-        float4 acc = ld_dsmem_v4(map_to_rank(off, 0));
-        for (int q = 1; q < splits; ++q) {
-          const float4 v = ld_dsmem_v4(map_to_rank(off, q));
-          acc.x = __fadd_rn(acc.x, v.x);
-          acc.y = __fadd_rn(acc.y, v.y);
-          acc.z = __fadd_rn(acc.z, v.z);
-          acc.w = __fadd_rn(acc.w, v.w);
-        }
-        float a4[4] = {acc.x, acc.y, acc.z, acc.w};
         if (args.row_ss) {
           const float inv = row_inv[ml];
 #pragma unroll
@@ -638,7 +631,47 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(args.C) + mm * args.ldc + n0 + 4 * lane) =
                 make_uint2(pack_bf16(a4[0], a4[1]), pack_bf16(a4[2], a4[3]));
         }
-      }
+      };
+      // Warp w takes the owned rows i = w (mod 4).  DSMEM reads are long
+      // latency, so a warp requests the partials of a batch of rows (16 reads
+      // per lane) before it adds any; each row's sum is still formed in rank
+      // order.  The split count is a power of two up to kMaxSplits.
+      auto pull_rows = [&](auto splits_c) {
+        constexpr int S = decltype(splits_c)::value;
+        constexpr int RB = 16 / S;  // rows per batch
+        for (int i0 = warp; i0 < owned && good; i0 += 4 * RB) {
+          float4 v[RB][S];
+#pragma unroll
+          for (int u = 0; u < RB; ++u) {
+            if (i0 + 4 * u < owned) {
+              const uint32_t off = smem_addr(part + ((i0 + 4 * u) * S + rank) * LDP + 4 * lane);
+#pragma unroll
+              for (int q = 0; q < S; ++q) v[u][q] = ld_dsmem_v4(map_to_rank(off, q));
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < RB; ++u) {
+            if (i0 + 4 * u < owned) {
+              float4 acc = v[u][0];
+#pragma unroll
+              for (int q = 1; q < S; ++q) {
+                acc.x = __fadd_rn(acc.x, v[u][q].x);
+                acc.y = __fadd_rn(acc.y, v[u][q].y);
+                acc.z = __fadd_rn(acc.z, v[u][q].z);
+                acc.w = __fadd_rn(acc.w, v[u][q].w);
+              }
+              float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+              emit(i0 + 4 * u, a4);
+            }
+          }
+        }
+      };
+      if (splits == 2)
+        pull_rows(std::integral_constant<int, 2>{});
+      else if (splits == 4)
+        pull_rows(std::integral_constant<int, 4>{});
+      else
+        pull_rows(std::integral_constant<int, kMaxSplits>{});
       __syncthreads();  // this rank's reads of the peers' rows are done
       if (warp == 0 && lane < splits) mbar_arrive_cluster_relaxed(map_to_rank(read_bar, lane));
       if (args.rope.on && good) {
