@@ -85,7 +85,7 @@ def fold_gain(w: torch.Tensor, g: torch.Tensor) -> torch.Tensor:
 # kinv_rope_append (measured faster at one row and at many).  Both give the
 # same bits, so the choice never changes a result.
 FUSED_ROPE_MIN_ROWS = 2
-FUSED_ROPE_MAX_ROWS = 32
+FUSED_ROPE_MAX_ROWS = 64
 
 
 class Decoder:
