@@ -46,7 +46,7 @@ constexpr int BK = 64;  // one 128-byte swizzle row of bf16
 constexpr int kGemmThreads = 128;
 constexpr int A_STAGE = BM * BK * 2;
 constexpr int kRopeTabRows = 4;  // owned rows up to which the RoPE angles are formed ahead
-constexpr int kPushMaxRows = 32;  // split-K tiles of more rows have the owners pull the partials
+constexpr int kPushMaxRows = 8;  // split-K tiles of more rows have the owners pull the partials
 constexpr int kMaxSplits = 8;     // K splits (cluster size) at most
 // mbarriers after the ring: full and empty per stage, done, recv, one
 // "ready" per K-split rank (push path), "read" (pull path) and a spare that

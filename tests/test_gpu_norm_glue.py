@@ -108,6 +108,7 @@ def test_decode_advance(kinv):
 
 
 @pytest.mark.parametrize("d,hq,hkv,base,qk,k,m", [(64, 4, 2, 1e4, False, 256, 5), (128, 32, 8, 1e6, True, 4096, 1),
+                                                  (128, 32, 8, 1e6, True, 4096, 8),
                                                   (128, 32, 8, 1e6, True, 4096, 16),
                                                   (128, 32, 8, 1e6, True, 4096, 64),
                                                   (128, 32, 8, 1e6, True, 4096, 200)])
