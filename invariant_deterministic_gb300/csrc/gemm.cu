@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // split-K RoPE epilogue with few owned rows (decode): what it needs is
   // gathered by the otherwise idle warps 2 and 3 while the weights stream
-  const bool use_pre = args.rope.on && args.splits > 1 && !args.pull && args.own_rows <= kRopeTabRows;
+  const bool use_pre = args.rope.on && args.splits > 1 && args.own_rows <= kRopeTabRows;
   RopePre pre{};
   // the tables after the barriers take 16-byte vector accesses
   unsigned char* tail = reinterpret_cast<unsigned char*>(
@@ -253,9 +253,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (args.row_ss) tail += BM * 4;
   float* red4 = reinterpret_cast<float*>(tail);     // [own_rows][4] for the split residual
   const bool push = args.splits > 1 && !args.pull;
-  // the residual rows a rank owns in the push path ([own_rows][BN] bf16),
-  // read while the weights stream
-  const bool use_resid_pre = push && args.resid != nullptr;
+  // the residual rows a rank owns ([own_rows][BN] bf16, either split-K
+  // path), read while the weights stream
+  const bool use_resid_pre = args.splits > 1 && args.resid != nullptr;
   uint16_t* resid_pre = reinterpret_cast<uint16_t*>(red4 + (use_resid_pre ? args.own_rows * 4 : 0));
   auto full_bar = [&](int s) { return smem_addr(bars + s); };
   auto empty_bar = [&](int s) { return smem_addr(bars + stages + s); };
@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         } else if (args.resid) {
           __nv_bfloat16* xp = args.resid + mm * args.ld_resid + n0 + 4 * lane;
-          const uint2 xv = *reinterpret_cast<const uint2*>(xp);
+          const uint2 xv = *reinterpret_cast<const uint2*>(resid_pre + i * BN + 4 * lane);
           float sv[4];
           sv[0] = residual_add(xv.x & 0xFFFFu, a4[0]);
           sv[1] = residual_add(xv.x >> 16, a4[1]);
@@ -676,7 +676,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (warp == 0 && lane < splits) mbar_arrive_cluster_relaxed(map_to_rank(read_bar, lane));
       if (args.rope.on && good) {
         auto row_of = [&](int r) { return m0 + r * splits + rank; };
-        rope_dispatch<BN>(stage, nullptr, owned, n0, args.M, args.rope, row_of);
+        rope_dispatch<BN>(stage, use_pre ? &pre : nullptr, owned, n0, args.M, args.rope, row_of);
       }
     }
   } else {
@@ -1223,12 +1223,12 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a
                                         : (a.rope.on ? a.a_rows * BN * 2 : 0);
   // what the block keeps after the ring and its barriers: the RoPE inputs,
   // 1/rms per row, the split residual's partial sums and its residual rows
-  const bool push = a.splits > 1 && !a.pull;
-  const int tab_bytes = (a.rope.on && push && a.own_rows <= kRopeTabRows
+  const bool split = a.splits > 1;
+  const int tab_bytes = (a.rope.on && split && a.own_rows <= kRopeTabRows
                              ? rope_pre_bytes(a.own_rows, a.rope.D, BN)
                              : 0) +
                         (a.row_ss ? BM * 4 : 0) +
-                        (a.resid && push ? a.own_rows * 16 + a.own_rows * BN * 2 : 0);
+                        (a.resid && split ? a.own_rows * 16 + a.own_rows * BN * 2 : 0);
   const int cap = ring_cap(static_cast<long long>(a.splits) * grid_y * grid_z) - tab_bytes;
   const int limit = budget < cap ? budget : cap;
   const int stage = a.a_blk * a.j + BN * BK * 2 * a.j;
