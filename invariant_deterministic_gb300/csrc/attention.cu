@@ -78,8 +78,10 @@ __device__ __forceinline__ void report_bad_length(const AttnParams& p) {
   if (threadIdx.x == 0 && p.status) atomicExch(p.status, DEV_ATTN_BAD_LENGTH);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// A 16-byte cp.async with an L2 eviction policy (createpolicy).
+__device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+               : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -161,13 +163,16 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnParams p
   const uint32_t kv_base = smem_addr(kv);
   const uint32_t pt_base = smem_addr(pt), pt_lo_base = smem_addr(pt_lo), zrow_base = smem_addr(zrow);
 
+  // each K/V row is read once per step: it should not push the partials
+  // (read back by the merge) out of L2
+  const uint64_t kv_policy = l2_policy_evict_first();
   auto load_sub = [&](const __nv_bfloat16* src, int j) {
     const int rows = min(SUB, nmax - j * SUB);
     for (int idx = t; idx < rows * C8; idx += kThreads) {
       const int r = idx / C8, c = idx % C8;
       const int key = j * SUB + r;
-      cp_async16(kv_base + static_cast<uint32_t>(key * D * 2 + ((c ^ (key & 7)) << 4)),
-                 src + seq_off + static_cast<int64_t>(key) * p.tok_stride + c * 8);
+      cp_async16_hint(kv_base + static_cast<uint32_t>(key * D * 2 + ((c ^ (key & 7)) << 4)),
+                      src + seq_off + static_cast<int64_t>(key) * p.tok_stride + c * 8, kv_policy);
     }
   };
 #pragma unroll
