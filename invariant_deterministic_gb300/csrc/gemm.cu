@@ -14,11 +14,12 @@
 //    each brought by a single 3-D TMA copy (a CTA keeps only a few copies in
 //    flight, so each copy must be large for the weight stream to keep up);
 //  * K is cut into `splits` equal, contiguous ranges (splits depends on N and
-//    K only); the CTAs of one cluster compute one range each.  Each rank
-//    pushes its fp32 partial rows into the shared memory of the rank that
-//    owns them (row m belongs to rank m % splits), and the owner adds the
-//    partials in rank order p0 + p1 + ... -- no atomics, no batch-dependent
-//    split;
+//    K only); the CTAs of one cluster compute one range each.  Row m belongs
+//    to rank m % splits, which adds the fp32 partials of its rows in rank
+//    order p0 + p1 + ...: for tiles of up to kPushMaxRows rows every rank
+//    pushes them into the owner's shared memory, for taller tiles every rank
+//    stages its own and the owners read them over DSMEM -- no atomics, no
+//    batch-dependent split;
 //  * TMA brings in the rows of A that exist (M rounded up to 8, at most 128);
 //    the tile rows beyond them feed accumulator rows that are never stored.
 // Row i therefore meets the same instructions in the same order for every M,
@@ -117,7 +118,7 @@ struct GemmArgs {
   int stages;
   int splits;
   int own_rows;  // split-K: rows a rank owns at most (ceil(a_rows / splits))
-  int pull;      // split-K with many rows: owners read the partials (coalesced) instead of receiving them
+  int pull;      // split-K with more than kPushMaxRows rows: owners read the partials instead of receiving them
   int ring_bytes;  // the stage ring, or more when the epilogue's receive slots need it
   int* status;
   RopeEpilogue rope;
@@ -544,7 +545,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (args.pull) {
-    // Constant split-K, many rows: every rank stages its fp32 partial rows in
+    // Constant split-K, more than kPushMaxRows rows: every rank stages its fp32 partial rows in
     // its own (idle) ring; after a cluster barrier the owner of row m (rank
     // m % splits) reads that row from every rank -- a warp per row, lane l
     // taking columns 4l .. 4l + 3 -- and adds them in rank order.  The
@@ -1212,7 +1213,7 @@ kinv_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tw, GemmArgs a
   // it), and the 128 rows one MMA reads from the start of the last A block
   // must stay inside the block's shared memory.
   a.own_rows = (a.a_rows + a.splits - 1) / a.splits;
-  // split-K with many rows: owners pull the partials (coalesced reads) from
+  // split-K with more than kPushMaxRows rows: owners pull the partials (coalesced reads) from
   // rows staged in each rank's ring; otherwise ranks push into receive slots
   a.pull = a.splits > 1 && a.a_rows > kPushMaxRows && BN == kGemmThreads ? 1 : 0;
   // split-K receive slots (or the staged partial rows), plus the staged bf16
