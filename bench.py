@@ -32,10 +32,10 @@ UNIT = "tokens/s"
 # from one `ncu --set full` capture (profiles/gemm_kernel_qwen3_8b_decode_b16.md).
 # Reported only while the GEMM's sources still hash to `src`.
 NCU_GEMM_TRAFFIC = {
-    "src": "5a713c160e3ea401",
+    "src": "6bb866ca61d7c8c9",
     "batch": 16,
-    "bytes": {"gemm_qkv": 50.593e6, "gemm_o": 33.898e6, "gemm_gate_up": 204.527e6,
-              "gemm_down": 104.052e6, "gemm_lm_head": 1251.753e6},
+    "bytes": {"gemm_qkv": 50.590e6, "gemm_o": 33.899e6, "gemm_gate_up": 204.416e6,
+              "gemm_down": 104.013e6, "gemm_lm_head": 1251.766e6},
 }
 
 
