@@ -5,7 +5,7 @@ SwiGLU, down GEMM), an untied LM head and the seeded sampler.
 Every arithmetic step is a kinv kernel; this module only owns buffers and
 issues the calls in order on the current CUDA stream, so a whole decode step
 can be captured into a CUDA graph.  Kernels per layer: the QKV projection
-(with RoPE and the KV append for 2..32 rows), split-KV attention (split and
+(with RoPE and the KV append for 2..64 rows), split-KV attention (split and
 merge), the O projection, the gate/up projection with SwiGLU, the down
 projection.  The RMSNorms are folded into the projections (kinv_gemm_fusion):
 the O and down projections add their output to the residual stream x and
