@@ -238,8 +238,12 @@ def run_kinv(args):
     dev = torch.device("cuda", local)
     sweep = sorted(set([args.batch] + [int(x) for x in args.sweep.split(",") if x]))
     bmax = max(sweep)
+    # decode steps a row may take: per sweep batch two eager warm-ups, the
+    # graph's warm-up and timed replays; then the instrumented pass and the
+    # end-to-end warm-up and timed steps
     per_b = args.warmup + args.steps + 3
-    shape, w, dec, lens0 = build_workload(bmax, per_b * len(sweep) + 8, args.layers, rank, dev,
+    steps_total = per_b * len(sweep) + args.prof_steps + args.warmup + args.steps + 8
+    shape, w, dec, lens0 = build_workload(bmax, steps_total, args.layers, rank, dev,
                                           max_chunk=max(args.prefill_chunks) if args.prefill else 0)
     hbm_peak, tc_peak, tc_sustained, peak_kind = _peaks()
     # per layer: QKV (+ RoPE/append for M.FUSED_ROPE_MIN_ROWS .. MAX rows, else
@@ -358,23 +362,34 @@ def run_kinv(args):
                 "step_share": {k: round(v / sum(total.values()), 4) for k, v in
                                sorted(total.items(), key=lambda kv: -kv[1])}}
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers: every step
+    # copies the input token ids from pinned host memory, runs the step and
+    # copies the sampled ids back (the copies are nodes of the step's graph),
+    # and the host reads them before it feeds them to the next step
     head = results[bsz]
-    graph = head["graph"]
     tok_host = torch.empty(bsz, dtype=torch.int32, pin_memory=True)
     out_host = torch.empty(bsz, dtype=torch.int32, pin_memory=True)
     tok_host.copy_(dec.tokens[:bsz].cpu())
     with torch.cuda.stream(stream):
+        io_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(io_graph, stream=stream):
+            dec.tokens[:bsz].copy_(tok_host, non_blocking=True)
+            dec.decode_step(bsz)
+            out_host.copy_(dec.tokens[:bsz], non_blocking=True)
+        for _ in range(args.warmup):
+            io_graph.replay()
+            stream.synchronize()
+            tok_host.copy_(out_host)
         barrier()
         stream.synchronize()
         t_start = time.perf_counter()
         for _ in range(args.steps):
-            dec.tokens[:bsz].copy_(tok_host, non_blocking=True)
-            graph.replay()
-            out_host.copy_(dec.tokens[:bsz], non_blocking=True)
+            io_graph.replay()
             stream.synchronize()
             tok_host.copy_(out_host)
         e2e_s = max_over_ranks(time.perf_counter() - t_start, dev)
+        if kinv.last_device_status(stream) != 0:
+            raise RuntimeError("device status after the end-to-end steps")
     e2e = {"value": round(bsz * ws * args.steps / e2e_s, 2), "unit": UNIT,
            "h2d_bytes_per_step": bsz * 4, "d2h_bytes_per_step": bsz * 4}
 
